@@ -1,0 +1,179 @@
+"""Seeded synthetic inputs, shared by the CUDA path's tests and benchmark and
+by the CPU oracle.  This module only draws and lays out random numbers.  It
+holds none of the attention arithmetic.
+
+Recipe (the same for every workload)
+------------------------------------
+* Use a CPU ``torch.Generator`` seeded with ``manual_seed(seed)``.
+* Draw fp32 ``randn`` in this order: Q ``[N, Hq, d]``, K ``[N, Hkv, d]``,
+  V ``[N, Hkv, d]``.  The layout is token-major with batch 1.
+* The workload's extra draws are the row picks for scaled or planted keys,
+  each a ``randperm`` of the block length.  They come from a second CPU
+  generator seeded with ``seed + 1000``, in the order given below.  The
+  picks can then be found again without redrawing the big tensors.
+* Apply the multiplications in fp32.
+* Last, cast to the workload dtype (``.to(torch.bfloat16)`` rounds to
+  nearest even).  The oracle and the GPU both read the cast tensors.
+
+The five workloads, with sizes as the pages' long-context discussion
+motivates them, are listed in ``WORKLOADS``.  Blocks are contiguous:
+virtual rank i holds tokens [i*c, (i+1)*c).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    seed: int
+    heads: int
+    kv_heads: int
+    d: int
+    N: int
+    P: int
+    dtype: str  # "f32" or "bf16"
+    causal: bool
+    recipe: str = "iid"  # iid | scaled_keys | half | planted
+    notes: str = ""
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def c(self) -> int:
+        return self.N // self.P
+
+    @property
+    def torch_dtype(self):
+        return torch.float32 if self.dtype == "f32" else torch.bfloat16
+
+    def flops_causal_adjusted(self) -> float:
+        """4*d FLOPs per allowed (q, k) pair per query head, with the causal
+        pair count taken as N^2/2 (the metric's convention)."""
+        pairs = self.N * self.N / (2.0 if self.causal else 1.0)
+        return 4.0 * self.d * self.heads * pairs
+
+    def flops_exact(self) -> float:
+        """Same convention, exact pair count N(N+1)/2 under causal masking."""
+        pairs = self.N * (self.N + 1) / 2.0 if self.causal else float(self.N) * self.N
+        return 4.0 * self.d * self.heads * pairs
+
+
+WORKLOADS = {
+    "tiny-exact": Workload(
+        "tiny-exact", seed=0, heads=1, kv_heads=1, d=64, N=1024, P=4, dtype="f32",
+        causal=False, notes="fp32 exactness case, non-causal"),
+    "mha-8k": Workload(
+        "mha-8k", seed=1, heads=8, kv_heads=8, d=64, N=8192, P=8, dtype="bf16", causal=True),
+    "mha-32k-scaled-keys": Workload(
+        "mha-32k-scaled-keys", seed=2, heads=32, kv_heads=32, d=128, N=32768, P=8,
+        dtype="bf16", causal=True, recipe="scaled_keys",
+        notes="1% of key rows of blocks P/2..P-1 scaled x8",
+        extra={"frac": 0.01, "factor": 8.0}),
+    "gqa-128k": Workload(
+        "gqa-128k", seed=3, heads=32, kv_heads=8, d=128, N=131072, P=16, dtype="bf16",
+        causal=True, recipe="half", notes="GQA 32/8, values N(0,1)*0.5"),
+    "mha-1m-planted": Workload(
+        "mha-1m-planted", seed=4, heads=8, kv_heads=8, d=128, N=1048576, P=64,
+        dtype="bf16", causal=True, recipe="planted",
+        notes="blocks j = 0 mod 8 carry 16 keys scaled x20",
+        extra={"every": 8, "count": 16, "factor": 20.0}),
+}
+
+
+def scaled_key_rows(w: Workload, g: torch.Generator):
+    """Row picks for the scaled-keys recipe.  For each block j in [P/2, P)
+    (the outer loop) and each KV head (the inner loop), take round(frac*c)
+    distinct rows from randperm(c)."""
+    c = w.c
+    count = int(round(w.extra["frac"] * c))
+    picks = []
+    for j in range(w.P // 2, w.P):
+        for h in range(w.kv_heads):
+            idx = torch.randperm(c, generator=g)[:count]
+            picks.append((j, h, idx + j * c))
+    return picks
+
+
+def planted_key_rows(w: Workload, g: torch.Generator):
+    """Row picks for the planted-keys recipe.  For each block j with
+    j % every == 0 (the outer loop) and each KV head (the inner loop), take
+    ``count`` distinct rows from randperm(c)."""
+    c = w.c
+    picks = []
+    for j in range(0, w.P, w.extra["every"]):
+        for h in range(w.kv_heads):
+            idx = torch.randperm(c, generator=g)[: w.extra["count"]]
+            picks.append((j, h, idx + j * c))
+    return picks
+
+
+def pick_generator(w: Workload) -> torch.Generator:
+    return torch.Generator().manual_seed(w.seed + 1000)
+
+
+def make_workload(w: Workload | str):
+    """Return (q, k, v) CPU tensors of the workload's dtype, token-major."""
+    if isinstance(w, str):
+        w = WORKLOADS[w]
+    g = torch.Generator().manual_seed(w.seed)
+    q = torch.randn((w.N, w.heads, w.d), generator=g, dtype=torch.float32)
+    k = torch.randn((w.N, w.kv_heads, w.d), generator=g, dtype=torch.float32)
+    v = torch.randn((w.N, w.kv_heads, w.d), generator=g, dtype=torch.float32)
+    if w.recipe == "scaled_keys":
+        for _, h, rows in scaled_key_rows(w, pick_generator(w)):
+            k[rows, h, :] *= w.extra["factor"]
+    elif w.recipe == "planted":
+        for _, h, rows in planted_key_rows(w, pick_generator(w)):
+            k[rows, h, :] *= w.extra["factor"]
+    elif w.recipe == "half":
+        q *= 0.5
+        k *= 0.5
+        v *= 0.5
+    elif w.recipe != "iid":
+        raise ValueError(f"unknown recipe {w.recipe}")
+    dt = w.torch_dtype
+    return q.to(dt), k.to(dt), v.to(dt)
+
+
+def make_random(N: int, heads: int, kv_heads: int, d: int, *, dtype=torch.bfloat16,
+                seed: int = 0, scale: float = 1.0):
+    """Small iid N(0,1)*scale case: Q [N,Hq,d], K and V [N,Hkv,d], drawn in that order."""
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn((N, heads, d), generator=g) * scale
+    k = torch.randn((N, kv_heads, d), generator=g) * scale
+    v = torch.randn((N, kv_heads, d), generator=g) * scale
+    return q.to(dtype), k.to(dtype), v.to(dtype)
+
+
+def sample_rows(w: Workload | str, *, random_per_block: int = 16, seed: int = 12345,
+                after_planted: int = 8) -> np.ndarray:
+    """Query rows to check at full size.  Per block i: local rows {0, 1, 127,
+    128, c/2, c-1}, plus ``random_per_block`` seeded random rows.  For the
+    scaled or planted recipes, add the ``after_planted`` rows that follow
+    the first picked key row of one block per picked block.  Returns sorted
+    unique global row indices."""
+    if isinstance(w, str):
+        w = WORKLOADS[w]
+    c = w.c
+    rng = np.random.default_rng(seed)
+    rows = []
+    for i in range(w.P):
+        base = i * c
+        fixed = [0, 1, 127, 128, c // 2, c - 1]
+        rows.extend(base + r for r in fixed if 0 <= r < c)
+        rows.extend((base + rng.integers(0, c, size=random_per_block)).tolist())
+    if w.recipe in ("scaled_keys", "planted") and after_planted > 0:
+        g = pick_generator(w)
+        picks = scaled_key_rows(w, g) if w.recipe == "scaled_keys" else planted_key_rows(w, g)
+        seen = set()
+        for j, h, idx in picks:
+            if j in seen:
+                continue
+            seen.add(j)
+            r0 = int(idx.min())
+            rows.extend(r for r in range(r0, min(r0 + after_planted, w.N)))
+    return np.unique(np.asarray(rows, dtype=np.int64))

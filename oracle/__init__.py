@@ -1,0 +1,158 @@
+"""CPU oracle for blockwise online-softmax attention -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA library and its Python
+binding never import it, and nothing here imports them.  The two sides share
+only the seeded input generator, which holds none of the method's arithmetic.
+
+Contents
+--------
+* ``attention.c`` is the dense fp64 definition (see its header), built with
+  gcc into ``liboracle.so`` and loaded through ctypes.  ``partial_state`` and
+  ``attention`` below wrap it.
+* ``online.py`` restates, in fp64 numpy, the pages' own blockwise recurrence,
+  merge and finalize.  The invariant tests use it, and it serves as the
+  oracle for the state-level calls (block update, merge, finalize).
+
+Pins
+----
+``tests/test_oracle.py`` pins every function here to facts other than the
+code itself: the worked example the pages print, special cases that reduce
+to library routines, closed forms, brute force and invariants.  No function
+is unpinned.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attention.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+F32 = 0
+BF16 = 1
+
+
+def build_library(force: bool = False) -> str:
+    """Compile ``attention.c`` with gcc into ``liboracle.so`` next to it."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fPIC", "-shared", "-pthread", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build_library()
+            lib = ctypes.CDLL(_LIB_PATH)
+            f = lib.oracle_partial_state
+            P = ctypes.c_void_p
+            LL = ctypes.c_longlong
+            f.argtypes = [P, P, P, ctypes.c_int, LL, LL, ctypes.c_int, ctypes.c_int,
+                          ctypes.c_int, ctypes.c_double, ctypes.c_int, P, P, P, LL, P, P, P,
+                          ctypes.c_int]
+            f.restype = ctypes.c_int
+            lib.oracle_abi_version.restype = ctypes.c_int
+            if lib.oracle_abi_version() != 1:
+                raise RuntimeError("liboracle.so is stale; rebuild it")
+            _lib = lib
+    return _lib
+
+
+def _as_input(x):
+    """Accept a numpy float32 array, a numpy uint16 array of bf16 bit
+    patterns, or a CPU torch tensor (float32 or bfloat16)."""
+    if not isinstance(x, np.ndarray):
+        import torch  # local import: only needed for tensor inputs
+
+        t = x.detach().cpu().contiguous()
+        if t.dtype == torch.bfloat16:
+            x = t.view(torch.int16).numpy().view(np.uint16)
+        elif t.dtype == torch.float32:
+            x = t.numpy()
+        else:
+            raise TypeError(f"oracle takes float32 or bfloat16, got {t.dtype}")
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.float32:
+        return x, F32
+    if x.dtype == np.uint16:
+        return x, BF16
+    raise TypeError(f"oracle takes float32 or bf16 bit patterns (uint16), got {x.dtype}")
+
+
+def partial_state(q, k, v, *, causal: bool, q_pos=None, k_pos=None, rows=None,
+                  scale: float | None = None, threads: int | None = None):
+    """Partial online-softmax state of query rows against a key set, in fp64.
+
+    q: [nq, hq, d]; k, v: [nk, hkv, d] (token-major).  ``q_pos``/``k_pos``
+    are global token positions (default: the index).  ``rows`` selects the
+    query rows (default: all).  Returns ``(m, l, o)`` of shapes
+    ``[nrows, hq]``, ``[nrows, hq]`` and ``[nrows, hq, d]``, as defined in
+    ``attention.c``.  The default scale is 1/sqrt(d).
+    """
+    qa, dt = _as_input(q)
+    ka, dk = _as_input(k)
+    va, dv = _as_input(v)
+    if not (dt == dk == dv):
+        raise TypeError("q, k and v must share one dtype")
+    if qa.ndim != 3 or ka.ndim != 3 or va.ndim != 3:
+        raise ValueError("q, k, v must be 3-D token-major arrays")
+    nq, hq, d = qa.shape
+    nk, hkv, dk_ = ka.shape
+    if va.shape != ka.shape or dk_ != d:
+        raise ValueError("shape mismatch between q, k and v")
+    if rows is None:
+        rows = np.arange(nq, dtype=np.int64)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    qp = None if q_pos is None else np.ascontiguousarray(np.asarray(q_pos, dtype=np.int64))
+    kp = None if k_pos is None else np.ascontiguousarray(np.asarray(k_pos, dtype=np.int64))
+    if qp is not None and qp.shape != (nq,):
+        raise ValueError("q_pos must have one entry per query row")
+    if kp is not None and kp.shape != (nk,):
+        raise ValueError("k_pos must have one entry per key")
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    if threads is None:
+        threads = os.cpu_count() or 1
+    nr = rows.shape[0]
+    m = np.empty((nr, hq), dtype=np.float64)
+    l = np.empty((nr, hq), dtype=np.float64)
+    o = np.empty((nr, hq, d), dtype=np.float64)
+
+    def ptr(a):
+        return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+    rc = _load().oracle_partial_state(
+        ptr(qa), ptr(ka), ptr(va), dt, nq, nk, hq, hkv, d, float(scale), int(bool(causal)),
+        ptr(qp), ptr(kp), ptr(rows), nr, ptr(m), ptr(l), ptr(o), int(threads))
+    if rc != 0:
+        raise ValueError(f"oracle_partial_state failed with code {rc}")
+    return m, l, o
+
+
+def attention(q, k, v, *, causal: bool, q_pos=None, k_pos=None, rows=None,
+              scale: float | None = None, threads: int | None = None):
+    """Dense attention O = softmax(q k^T * scale) v and its row log-sum-exp.
+
+    Returns ``(O [nrows, hq, d], LSE [nrows, hq])`` in fp64.  A row with no
+    allowed key gets O = 0 and LSE = -inf.
+    """
+    m, l, o = partial_state(q, k, v, causal=causal, q_pos=q_pos, k_pos=k_pos, rows=rows,
+                            scale=scale, threads=threads)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        out = np.where(l[..., None] > 0, o / np.where(l > 0, l, 1.0)[..., None], 0.0)
+        lse = np.where(l > 0, m + np.log(np.where(l > 0, l, 1.0)), -np.inf)
+    return out, lse

@@ -1,0 +1,368 @@
+"""Pins for the CPU oracle.  These tests run on CPU only.
+
+Each test ties the oracle to a fact that does not come from the oracle
+itself:
+* the worked example the pages print,
+* special cases that reduce to library routines (scipy softmax and
+  logsumexp),
+* closed forms,
+* brute force in exact arithmetic,
+* invariants.
+Each test is chosen so that a plausible slip fails it: a dropped scale, a
+wrong sign, a wrong head or row index, an off-by-one in the causal mask, or
+a transposed operand.
+"""
+import itertools
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import oracle
+from oracle import online
+from blockwise_online_softmax_gb300 import inputs
+
+
+def _example(golden):
+    g = golden("worked_example.txt")
+    s = np.array(g["block_A.s"] + g["block_B.s"], dtype=np.float32)
+    v = np.array(g["block_A.v"] + g["block_B.v"], dtype=np.float32)
+    # d = 1, q = 1, scale = 1: the score of key t is exactly k_t.
+    q = np.ones((1, 1, 1), dtype=np.float32)
+    k = s.reshape(4, 1, 1)
+    vv = v.reshape(4, 1, 1)
+    return g, q, k, vv
+
+
+# --- the worked example ("Ring Attention Math Deep", "A worked numeric example")
+
+def test_worked_example_dense_output(golden):
+    g, q, k, v = _example(golden)
+    out, lse = oracle.attention(q, k, v, causal=False, scale=1.0)
+    assert abs(out[0, 0, 0] - g["out"]) <= g["tol"]
+    assert abs(out[0, 0, 0] - g["direct"]) <= g["tol"]
+    # the full-set state equals the page's state after block B
+    m, l, o = oracle.partial_state(q, k, v, causal=False, scale=1.0)
+    assert m[0, 0] == g["after_B.m"]
+    assert abs(l[0, 0] - g["after_B.l"]) <= g["tol"]
+    assert abs(o[0, 0, 0] - g["after_B.o"]) <= g["tol"]
+    # LSE is consistent with the state: ln of the sum of exp(scores)
+    assert abs(lse[0, 0] - (m[0, 0] + math.log(l[0, 0]))) < 1e-12
+
+
+def test_worked_example_block_A_state(golden):
+    g, q, k, v = _example(golden)
+    m, l, o = oracle.partial_state(q, k[:2], v[:2], causal=False, scale=1.0)
+    assert m[0, 0] == g["after_A.m"]
+    assert abs(l[0, 0] - g["after_A.l"]) <= g["tol"]
+    assert abs(o[0, 0, 0] - g["after_A.o"]) <= g["tol"]
+
+
+def test_worked_example_online_intermediates(golden):
+    g, q, k, v = _example(golden)
+    st = online.identity_state(1, 1, 1)
+    pos = np.arange(4)
+    st, alpha, p = online.block_update(st, q, k[:2], v[:2], causal=False, q_pos=[0],
+                                       k_pos=pos[:2], scale=1.0, return_terms=True)
+    assert st[0][0, 0] == g["after_A.m"] and alpha[0, 0] == g["after_A.alpha"]
+    np.testing.assert_allclose(p[0, 0], g["after_A.p"], atol=g["tol"])
+    assert abs(st[1][0, 0] - g["after_A.l"]) <= g["tol"]
+    assert abs(st[2][0, 0, 0] - g["after_A.o"]) <= g["tol"]
+    st, alpha, p = online.block_update(st, q, k[2:], v[2:], causal=False, q_pos=[0],
+                                       k_pos=pos[2:], scale=1.0, return_terms=True)
+    assert st[0][0, 0] == g["after_B.m"]
+    assert abs(alpha[0, 0] - g["after_B.alpha"]) <= g["tol"]
+    np.testing.assert_allclose(p[0, 0], g["after_B.p"], atol=g["tol"])
+    assert abs(st[1][0, 0] - g["after_B.l"]) <= g["tol"]
+    assert abs(st[2][0, 0, 0] - g["after_B.o"]) <= g["tol"]
+    out, _ = online.finalize(st)
+    assert abs(out[0, 0, 0] - g["out"]) <= g["tol"]
+
+
+def test_worked_example_merge_and_finalize(golden):
+    g, q, k, v = _example(golden)
+    a = oracle.partial_state(q, k[:2], v[:2], causal=False, scale=1.0)
+    b = oracle.partial_state(q, k[2:], v[2:], causal=False, scale=1.0)
+    for x, y in ((a, b), (b, a)):
+        m, l, o = online.merge(x, y)
+        assert m[0, 0] == g["after_B.m"]
+        assert abs(l[0, 0] - g["after_B.l"]) <= g["tol"]
+        assert abs(o[0, 0, 0] - g["after_B.o"]) <= g["tol"]
+        out, _ = online.finalize((m, l, o))
+        assert abs(out[0, 0, 0] - g["out"]) <= g["tol"]
+
+
+# --- special cases that reduce to library routines
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_onehot_values_return_softmax_rows(causal, dtype):
+    """With v_t = e_t (one-hot), row r of O is row r of softmax(S).  It is
+    checked against scipy.special.softmax of a numpy matmul, per head,
+    with GQA.  The shapes are non-square (nq != nk, d != nk) so a transposed
+    operand cannot pass."""
+    nq, nk, hq, hkv, d = 7, 12, 4, 2, 16
+    g = torch.Generator().manual_seed(3)
+    q = torch.randn(nq, hq, d, generator=g).to(dtype)
+    k = torch.randn(nk, hkv, d, generator=g).to(dtype)
+    v = torch.zeros(nk, hkv, d, dtype=dtype)
+    for t in range(nk):
+        v[t, :, t] = 1.0
+    q_pos = np.arange(nq) + 3  # queries sit at positions 3..9, keys at 0..11
+    out, lse = oracle.attention(q, k, v, causal=causal, q_pos=q_pos)
+    qd = q.to(torch.float64).numpy()
+    kd = k.to(torch.float64).numpy()
+    for h in range(hq):
+        s = qd[:, h, :] @ kd[:, h // (hq // hkv), :].T / math.sqrt(d)
+        if causal:
+            s = np.where(np.arange(nk)[None, :] <= q_pos[:, None], s, -np.inf)
+        ref = scipy.special.softmax(s, axis=1)
+        np.testing.assert_allclose(out[:, h, :nk], ref, rtol=0, atol=1e-13)
+        np.testing.assert_allclose(out[:, h, nk:], 0.0, atol=0)
+        np.testing.assert_allclose(lse[:, h], scipy.special.logsumexp(s, axis=1), atol=1e-12)
+
+
+def test_gqa_equals_repeated_kv_heads():
+    """Query head h reads KV head h // (hq/hkv): the same as MHA with each
+    KV head repeated hq/hkv times in a row (np.repeat)."""
+    q, k, v = inputs.make_random(40, 6, 2, 8, dtype=torch.float32, seed=5)
+    o1, l1 = oracle.attention(q, k, v, causal=True)
+    kr = np.repeat(k.numpy(), 3, axis=1)
+    vr = np.repeat(v.numpy(), 3, axis=1)
+    o2, l2 = oracle.attention(q, kr, vr, causal=True)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+    # and not the interleaved convention h % hkv
+    kt = np.tile(k.numpy(), (1, 3, 1))
+    vt = np.tile(v.numpy(), (1, 3, 1))
+    o3, _ = oracle.attention(q, kt, vt, causal=True)
+    assert np.abs(o1 - o3).max() > 1e-2
+
+
+# --- closed forms
+
+def test_equal_keys_give_running_mean():
+    """If every key is the same vector, every allowed score is equal.  The
+    weights are then uniform: causal row r gets mean(v_0..v_r), and the
+    non-causal rows get the global mean."""
+    n, h, d = 33, 2, 8
+    g = torch.Generator().manual_seed(7)
+    q = torch.randn(n, h, d, generator=g)
+    k = torch.randn(1, h, d, generator=g).expand(n, h, d).contiguous()
+    v = torch.randn(n, h, d, generator=g)
+    out, lse = oracle.attention(q, k, v, causal=True)
+    vd = v.double().numpy()
+    running_mean = np.cumsum(vd, axis=0) / np.arange(1, n + 1)[:, None, None]
+    np.testing.assert_allclose(out, running_mean, atol=1e-13)
+    s = (q.double() * k.double()).sum(-1).numpy() / math.sqrt(d)
+    np.testing.assert_allclose(lse, s + np.log(np.arange(1, n + 1))[:, None], atol=1e-12)
+    out_nc, _ = oracle.attention(q, k, v, causal=False)
+    np.testing.assert_allclose(out_nc, np.broadcast_to(vd.mean(0), out_nc.shape), atol=1e-13)
+
+
+def test_causal_row_zero_is_its_own_value():
+    q, k, v = inputs.make_random(16, 3, 3, 8, dtype=torch.float32, seed=2)
+    out, lse = oracle.attention(q, k, v, causal=True)
+    np.testing.assert_array_equal(out[0], v[0].double().numpy())
+    s00 = (q[0].double() * k[0].double()).sum(-1).numpy() / math.sqrt(8)
+    np.testing.assert_allclose(lse[0], s00, atol=1e-14)
+
+
+def test_dominant_key_large_logits():
+    """Scores scaled by 100 (|s| up to ~1e3): no overflow, and the output is
+    the value of the arg-max key to machine precision."""
+    q, k, v = inputs.make_random(20, 2, 2, 8, dtype=torch.float32, seed=11, scale=1.0)
+    q = q * 100.0
+    out, lse = oracle.attention(q, k, v, causal=False)
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+    s = np.einsum("rhx,thx->rht", q.double().numpy(), k.double().numpy()) / math.sqrt(8)
+    top = s.argmax(axis=2)
+    srt = np.sort(s, axis=2)
+    gap = srt[:, :, -1] - srt[:, :, -2]
+    for r in range(20):
+        for h in range(2):
+            if gap[r, h] > 40:  # runner-up weight < e^-40
+                np.testing.assert_allclose(out[r, h], v[top[r, h], h].double().numpy(),
+                                           atol=1e-15)
+                np.testing.assert_allclose(lse[r, h], srt[r, h, -1], atol=1e-15)
+
+
+def test_values_all_one_give_one():
+    q, k, _ = inputs.make_random(50, 4, 2, 16, dtype=torch.bfloat16, seed=4)
+    v = torch.ones(50, 2, 16, dtype=torch.bfloat16)
+    for causal in (False, True):
+        out, _ = oracle.attention(q, k, v, causal=causal)
+        np.testing.assert_allclose(out, 1.0, atol=1e-14)
+
+
+# --- brute force in exact arithmetic
+
+def test_brute_force_exact_rationals_tiny():
+    """Tiny inputs with integer scores: sum_t e^{s_t} v_t / sum_t e^{s_t} with
+    no max shift.  Evaluated as exact rationals in x = e (scores in 0..3 give
+    powers of e, a polynomial ratio), then turned to float once.  This needs
+    no exp() and no floating-point order."""
+    # d = 1, scale = 1: score(r, t) = q_r * k_t, integers in [-3, 3]
+    qv = [1, -1, 2, 0, 1]
+    kv = [0, 1, -1, 1, 2, -2]
+    # values exactly representable in float32, so the inputs are exact too
+    vv = [Fraction(1), Fraction(-2), Fraction(3, 2), Fraction(5), Fraction(-3, 8), Fraction(2)]
+    q = np.array(qv, dtype=np.float32).reshape(5, 1, 1)
+    k = np.array(kv, dtype=np.float32).reshape(6, 1, 1)
+    v = np.array([float(x) for x in vv], dtype=np.float32).reshape(6, 1, 1)
+    for causal in (False, True):
+        out, lse = oracle.attention(q, k, v, causal=causal, scale=1.0)
+        for r in range(5):
+            allowed = [t for t in range(6) if not causal or t <= r]
+            # ratio of polynomials in e with exponents s + 8 (all >= 0)
+            num = {}
+            den = {}
+            for t in allowed:
+                p = qv[r] * kv[t] + 8
+                num[p] = num.get(p, Fraction(0)) + vv[t]
+                den[p] = den.get(p, Fraction(0)) + 1
+
+            def ev(poly):
+                return math.fsum(float(c) * math.e ** p for p, c in poly.items())
+            assert abs(out[r, 0, 0] - ev(num) / ev(den)) < 1e-13
+            assert abs(lse[r, 0] - (math.log(ev(den)) - 8)) < 1e-13
+
+
+def test_brute_force_pairs_no_max_shift():
+    """Explicit (r, t) loops in pure Python with math.fsum, no max shift,
+    on random tiny inputs with causal and GQA."""
+    nq, hq, hkv, d = 9, 4, 2, 4
+    g = torch.Generator().manual_seed(21)
+    q = torch.randn(nq, hq, d, generator=g)
+    k = torch.randn(nq, hkv, d, generator=g)
+    v = torch.randn(nq, hkv, d, generator=g)
+    out, lse = oracle.attention(q, k, v, causal=True)
+    qd, kd, vd = q.tolist(), k.tolist(), v.tolist()
+    for r in range(nq):
+        for h in range(hq):
+            kh = h // 2
+            w = []
+            for t in range(r + 1):
+                s = math.fsum(qd[r][h][x] * kd[t][kh][x] for x in range(d)) / math.sqrt(d)
+                w.append(math.exp(s))
+            den = math.fsum(w)
+            for x in range(d):
+                num = math.fsum(w[t] * vd[t][kh][x] for t in range(r + 1))
+                assert abs(out[r, h, x] - num / den) < 1e-13
+            assert abs(lse[r, h] - math.log(den)) < 1e-13
+
+
+# --- invariants
+
+def test_permutation_equivariance():
+    """Non-causal: permuting key/value rows together leaves O unchanged, and
+    permuting the query rows permutes the output rows."""
+    q, k, v = inputs.make_random(24, 2, 1, 8, dtype=torch.float32, seed=9)
+    out, lse = oracle.attention(q, k, v, causal=False)
+    perm = np.random.default_rng(0).permutation(24)
+    out_k, lse_k = oracle.attention(q, k[perm], v[perm], causal=False)
+    np.testing.assert_allclose(out_k, out, atol=1e-14)
+    np.testing.assert_allclose(lse_k, lse, atol=1e-14)
+    out_q, _ = oracle.attention(q[perm], k, v, causal=False)
+    np.testing.assert_array_equal(out_q, out[perm])
+
+
+def test_linear_in_values_and_shift_in_scores():
+    q, k, v = inputs.make_random(16, 2, 2, 8, dtype=torch.float32, seed=13)
+    out, lse = oracle.attention(q, k, v, causal=True)
+    out3, lse3 = oracle.attention(q, k, v * 4.0, causal=True)
+    np.testing.assert_allclose(out3, 4.0 * out, atol=1e-13)
+    np.testing.assert_array_equal(lse3, lse)
+    # Append a constant coordinate (1 in q, c in k).  Every score of row r
+    # moves by c / sqrt(d'), so O stays and LSE shifts by the same amount.
+    c = 3.0
+    q2 = torch.cat([q, torch.ones(16, 2, 1)], dim=2)
+    k2 = torch.cat([k, torch.full((16, 2, 1), c)], dim=2)
+    v2 = torch.cat([v, torch.zeros(16, 2, 1)], dim=2)
+    sc = 1.0 / math.sqrt(8)
+    out2, lse2 = oracle.attention(q2, k2, v2, causal=True, scale=sc)
+    np.testing.assert_allclose(out2[..., :8], out, atol=1e-13)
+    np.testing.assert_allclose(lse2, lse + c * sc, atol=1e-13)
+
+
+def test_rows_subset_positions_and_threads():
+    q, k, v = inputs.make_random(30, 2, 1, 8, dtype=torch.bfloat16, seed=17)
+    full, full_lse = oracle.attention(q, k, v, causal=True, threads=1)
+    rows = np.array([29, 0, 7, 7, 15])
+    sub, sub_lse = oracle.attention(q, k, v, causal=True, rows=rows, threads=4)
+    np.testing.assert_array_equal(sub, full[rows])
+    np.testing.assert_array_equal(sub_lse, full_lse[rows])
+    pos = np.arange(30)
+    exp_, exp_lse = oracle.attention(q, k, v, causal=True, q_pos=pos, k_pos=pos)
+    np.testing.assert_array_equal(exp_, full)
+    # bf16 bit patterns are widened exactly: same as passing float32 values
+    f32, _ = oracle.attention(q.float(), k.float(), v.float(), causal=True)
+    np.testing.assert_array_equal(f32, full)
+
+
+def test_row_without_allowed_key():
+    q, k, v = inputs.make_random(4, 1, 1, 8, dtype=torch.float32, seed=1)
+    m, l, o = oracle.partial_state(q, k, v, causal=True, q_pos=[0, 1, 5, 9],
+                                   k_pos=[2, 3, 4, 5])
+    assert np.isneginf(m[0, 0]) and l[0, 0] == 0 and not o[0].any()
+    assert np.isneginf(m[1, 0]) and l[1, 0] == 0
+    out, lse = oracle.attention(q, k, v, causal=True, q_pos=[0, 1, 5, 9], k_pos=[2, 3, 4, 5])
+    assert np.isneginf(lse[0, 0]) and not out[0].any()
+    assert np.isfinite(lse[2:]).all()
+
+
+def test_online_ring_equals_dense():
+    """The pages' blockwise ring (fp64 recurrence) equals the dense definition."""
+    q, k, v = inputs.make_random(64, 4, 2, 8, dtype=torch.bfloat16, seed=23)
+    for causal in (False, True):
+        ref, ref_lse = oracle.attention(q, k, v, causal=causal)
+        out, lse = online.ring_forward(q, k, v, P=4, causal=causal)
+        np.testing.assert_allclose(out, ref, atol=1e-12)
+        np.testing.assert_allclose(lse, ref_lse, atol=1e-12)
+
+
+def test_ring_order_and_merge_order_independence():
+    """Any order of visiting the blocks, and any order of merging the block
+    states, gives the same result (all 4! orders, within 1e-12)."""
+    q, k, v = inputs.make_random(32, 2, 2, 8, dtype=torch.float32, seed=29)
+    ref, ref_lse = oracle.attention(q, k, v, causal=False)
+    for perm in itertools.permutations(range(4)):
+        out, lse = online.ring_forward(q, k, v, P=4, causal=False, order=[list(perm)] * 4)
+        np.testing.assert_allclose(out, ref, atol=1e-12)
+        np.testing.assert_allclose(lse, ref_lse, atol=1e-12)
+    # merge of block partial states, from the C oracle, in every order
+    parts = [oracle.partial_state(q, k[j * 8:(j + 1) * 8], v[j * 8:(j + 1) * 8], causal=False)
+             for j in range(4)]
+    for perm in itertools.permutations(range(4)):
+        st = online.identity_state(32, 2, 8)
+        for j in perm:
+            st = online.merge(st, parts[j])
+        out, lse = online.finalize(st)
+        np.testing.assert_allclose(out, ref, atol=1e-12)
+        np.testing.assert_allclose(lse, ref_lse, atol=1e-12)
+
+
+def test_identity_state_is_neutral():
+    q, k, v = inputs.make_random(8, 2, 2, 4, dtype=torch.float32, seed=31)
+    st = oracle.partial_state(q, k, v, causal=True)
+    e = online.identity_state(8, 2, 4)
+    for a, b in ((st, e), (e, st)):
+        m, l, o = online.merge(a, b)
+        np.testing.assert_array_equal(m, st[0])
+        np.testing.assert_array_equal(l, st[1])
+        np.testing.assert_array_equal(o, st[2])
+
+
+def test_normalize_then_average_is_wrong():
+    """Normalizing each block on its own and then averaging is not attention
+    ("Ring Attention Math Deep", "Causal masking, load balance, and other
+    wrinkles").  The oracle tells the two apart."""
+    q, k, v = inputs.make_random(32, 2, 2, 8, dtype=torch.float32, seed=37)
+    ref, _ = oracle.attention(q, k, v, causal=False)
+    blocks = [oracle.attention(q, k[j * 8:(j + 1) * 8], v[j * 8:(j + 1) * 8], causal=False)[0]
+              for j in range(4)]
+    wrong = sum(blocks) / 4
+    assert np.abs(wrong - ref).max() > 1e-2
