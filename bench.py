@@ -1,0 +1,404 @@
+#!/usr/bin/env python3
+"""Ring Attention forward benchmark on GB300.
+
+It reports causal-adjusted attention TFLOP/s, and the fraction of dense
+BF16 tensor peak, for ``ra_ring_forward``.  One step is one full forward:
+state init, the P ring steps (every virtual rank folds its visiting K/V
+block), and the finalize.  A step runs over one batch of the workload, with
+the inputs resident in HBM.
+
+FLOP convention: 4*d FLOPs per allowed (query, key) pair per query head
+(QK^T and PV, two each).  The causal pair count is N^2/2 ("causal-adjusted").
+The exact count N(N+1)/2 is reported as well.
+
+The JSON line also carries:
+  e2e           the same metric through ra_ring_forward_host.  That call
+                copies pinned host Q/K/V to the device, runs, and copies O
+                and LSE back, every step.
+  roofline      the block-update kernel's achieved TFLOP/s against the
+                measured dense BF16 peak, timed by the library's per-launch
+                CUDA events on the launching stream.
+  cpu_baseline  the fp64 CPU oracle on a bounded sample of the same
+                workload, on this host's cores.
+  clocks        SM clocks and throttle reasons sampled during the timed
+                region.
+
+--impl reference times the CPU oracle alone: a bounded sample per step, on
+the same workload, metric and unit.
+
+Multi-GPU (torchrun): each rank runs an independent replica of the
+workload on its own GPU.  The per-GPU work is fixed, the time is the max
+over ranks, and the value is the sum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+METRIC = "causal-adjusted attention TFLOP/s on 1 GB300 and % of dense BF16 tensor peak"
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(x: float, ws: int) -> float:
+    """Max of a host float over ranks (identity at world size 1)."""
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" \
+        else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu)], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sms.append(float(parts[1]))
+                    maxes.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(nm)
+        if not sms:
+            return None
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes),
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+# ------------------------------------------------------------------ traffic record
+def kernel_digest() -> str:
+    h = hashlib.sha256()
+    for f in ("umma_kernel.cu", "ptx.cuh", "ra_internal.h"):
+        with open(os.path.join(ROOT, "blockwise_online_softmax_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per block-update launch from the committed ncu summary, if
+    it was taken on the current kernel source (digest match), else None."""
+    p = os.path.join(ROOT, "profiles", "block_update_bf16_traffic.md")
+    try:
+        text = open(p).read()
+    except OSError:
+        return None
+    dig = re.search(r"kernel_digest:\s*([0-9a-f]+)", text)
+    val = re.search(rf"traffic_bytes_per_launch\[{re.escape(workload)}\]:\s*([0-9.eE+]+)", text)
+    if not dig or not val or dig.group(1) != kernel_digest():
+        return None
+    return float(val.group(1))
+
+
+# ------------------------------------------------------------------ CPU oracle sample
+def oracle_sample(w, q, k, v, target_s: float, seed: int = 7):
+    """Time the fp64 oracle on sampled query rows (all heads, full key
+    range), sized to take about ``target_s`` seconds.  Returns (TFLOP/s,
+    cores, description)."""
+    import numpy as np
+
+    import oracle
+
+    cores = os.cpu_count() or 1
+    rng = np.random.default_rng(seed)
+
+    def flops(rows):
+        keys = (rows + 1) if w.causal else np.full_like(rows, w.N)
+        return float(4.0 * w.d * w.heads * keys.sum())
+
+    # calibrate on a few rows
+    probe = np.sort(rng.integers(w.N // 2, w.N, size=max(2, cores // w.heads + 1)))
+    t0 = time.perf_counter()
+    oracle.partial_state(q, k, v, causal=w.causal, rows=probe, threads=cores)
+    dt = time.perf_counter() - t0
+    rate = flops(probe) / max(dt, 1e-6)
+    # rows drawn uniformly over the sequence; expected FLOPs per row
+    per_row = 4.0 * w.d * w.heads * (w.N / 2 if w.causal else w.N)
+    n_rows = int(max(1, min(w.N, target_s * rate / per_row)))
+    rows = np.sort(rng.choice(w.N, size=n_rows, replace=False))
+    t0 = time.perf_counter()
+    oracle.partial_state(q, k, v, causal=w.causal, rows=rows, threads=cores)
+    dt = time.perf_counter() - t0
+    f = flops(rows)
+    desc = (f"{n_rows} query rows drawn uniformly from {w.N}, all {w.heads} heads, each over its "
+            f"full causal key range ({f:.3e} FLOPs, {dt:.1f} s)")
+    return f / dt / 1e12, cores, desc, dt
+
+
+# ------------------------------------------------------------------ arms
+def run_reference(args, w, ws, rank):
+    if rank != 0:
+        return
+    from blockwise_online_softmax_gb300 import inputs
+
+    q, k, v = inputs.make_workload(w)
+    per_step = args.ref_step_seconds
+    for _ in range(args.warmup):
+        oracle_sample(w, q, k, v, per_step / 4)
+    vals, secs, desc, cores = [], [], "", 1
+    for s in range(args.steps):
+        val, cores, desc, dt = oracle_sample(w, q, k, v, per_step, seed=100 + s)
+        vals.append(val)
+        secs.append(dt)
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * statistics.median(secs), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "N": w.N, "P": w.P, "heads": w.heads,
+                   "kv_heads": w.kv_heads, "d": w.d, "causal": w.causal,
+                   "input_dtype": w.dtype},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": "per step: " + desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w, ws, rank, local):
+    import torch
+
+    import blockwise_online_softmax_gb300 as ra
+    from blockwise_online_softmax_gb300 import binding, inputs
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    binding.lib()
+    peaks, peak_src = load_peaks()
+
+    q, k, v = inputs.make_workload(w)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    out = torch.empty((w.N, w.heads, w.d), dtype=torch.float32, device=dev)
+    lse = torch.empty((w.N, w.heads), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ra.ra_ring_forward(qd, kd, vd, P=w.P, causal=w.causal, out=out, lse=lse, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    ra.ra_device_status(stream)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+
+    gpu_index = local
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    if vis and "," not in vis and vis.strip().isdigit():
+        gpu_index = int(vis)
+    clocks = ClockSampler(gpu_index)
+    clocks.start()
+    ra.ra_trace_reset()
+    ra.ra_trace_enable(True)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    ra.ra_trace_enable(False)
+    clk = clocks.stop()
+    ra.ra_device_status(stream)
+    ms_total = ev0.elapsed_time(ev1)
+    n_upd, ms_upd = ra.ra_trace_query("block_update_bf16" if w.dtype == "bf16"
+                                      else "block_update_f32")
+    n_init, ms_init = ra.ra_trace_query("state_init")
+    n_fin, ms_fin = ra.ra_trace_query("finalize")
+    ra.ra_trace_reset()
+
+    ms_max = reduce_max(ms_total, ws)
+    ms_step = ms_max / args.steps
+    f_adj = w.flops_causal_adjusted()
+    value = ws * f_adj / (ms_step * 1e-3) / 1e12
+
+    # roofline of the dominant kernel (block update): algorithmic FLOPs of
+    # all its launches (exact allowed-pair count) over their summed time.
+    f_exact = w.flops_exact()
+    achieved = (f_exact * args.steps) / (ms_upd * 1e-3) / 1e12 if ms_upd > 0 else None
+    peak = peaks["bf16_tflops_sustained"]
+    traffic = recorded_traffic(w.name)
+
+    # end to end through the host-buffer entry point
+    qp, kp, vp = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    out_h = torch.empty((w.N, w.heads, w.d), dtype=torch.float32, pin_memory=True)
+    lse_h = torch.empty((w.N, w.heads), dtype=torch.float32, pin_memory=True)
+    ra.ra_ring_forward_host(qp, kp, vp, P=w.P, causal=w.causal, out=out_h, lse=lse_h,
+                            stream=stream)
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    barrier(ws)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        ra.ra_ring_forward_host(qp, kp, vp, P=w.P, causal=w.causal, out=out_h, lse=lse_h,
+                                stream=stream)
+    e2e_s = reduce_max(time.perf_counter() - t0, ws) / e2e_steps
+    h2d = sum(t.numel() * t.element_size() for t in (q, k, v))
+    d2h = out_h.numel() * 4 + lse_h.numel() * 4
+    e2e_value = ws * f_adj / e2e_s / 1e12
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        val, cores, desc, _ = oracle_sample(w, q, k, v, args.cpu_seconds)
+        cpu = {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": desc}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic",
+        "frac_of_dense_bf16_peak": value / ws / peaks["bf16_tflops"],
+        "frac_of_dense_bf16_peak_sustained": value / ws / peaks["bf16_tflops_sustained"],
+        "peak_source": peak_src,
+        "config": {
+            "workload": w.name, "N": w.N, "P": w.P, "c": w.c, "heads": w.heads,
+            "kv_heads": w.kv_heads, "d": w.d, "causal": w.causal, "recipe": w.recipe,
+            "seed": w.seed, "parallelism": f"replicas{ws}",
+            "flops_per_step_causal_adjusted": f_adj, "flops_per_step_exact": f_exact,
+            "l2": "inputs larger than L2 (Q alone exceeds 129 MB); no flush",
+        },
+        "clocks": clk,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": n_upd + n_init + n_fin,
+        "kernel_ms": {"block_update": ms_upd / args.steps, "state_init": ms_init / args.steps,
+                      "finalize": ms_fin / args.steps},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": (achieved / peak) if achieved else None, "traffic": traffic,
+                     "kernel": "block update (tcgen05)", "peak_kind":
+                     f"bf16_tflops_sustained ({peak_src})",
+                     "frac_of_burst": (achieved / peaks["bf16_tflops"]) if achieved else None},
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    from blockwise_online_softmax_gb300.inputs import WORKLOADS
+
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gqa-128k", choices=sorted(WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=6.0)
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+    ws, rank, local = dist_info()
+    w = WORKLOADS[args.workload]
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+
+        backend = "nccl" if (torch.cuda.is_available() and args.impl == "ours") else "gloo"
+        if args.impl == "ours" and torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, w, ws, rank)
+        else:
+            run_ours(args, w, ws, rank, local)
+    finally:
+        if ws > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -5,3 +5,19 @@ CUDA kernels.  ``binding`` marshals torch tensors into it.  Importing this
 package does not load the library.  The first call of a binding function
 loads it, and raises if it has not been built.
 """
+
+from .binding import (  # noqa: E402,F401
+    RaError,
+    ra_block_update,
+    ra_device_status,
+    ra_finalize,
+    ra_merge,
+    ra_ring_forward,
+    ra_ring_forward_host,
+    ra_ring_step,
+    ra_selftest_wait_timeout,
+    ra_state_init,
+    ra_trace_enable,
+    ra_trace_query,
+    ra_trace_reset,
+)

@@ -1,0 +1,247 @@
+"""Thin Python binding over ``libra.so``.  The functions carry the C ABI's
+names (include/ra.h).  This module only marshals arguments: it takes torch
+tensors, passes raw pointers, sizes and the stream, and turns status codes
+into exceptions.  Every step of the computation runs in the library's CUDA
+kernels.  There is no fallback.  If ``libra.so`` is missing, the first call
+raises ``RaError``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libra.so")
+
+RA_OK = 0
+RA_ERR_INVALID = -1
+RA_ERR_UNSUPPORTED = -2
+RA_ERR_CUDA = -3
+RA_ERR_TIMEOUT = -4
+RA_ERR_ALLOC = -5
+RA_F32 = 0
+RA_BF16 = 1
+KERNEL_KINDS = {
+    "state_init": 0,
+    "block_update_bf16": 1,
+    "block_update_f32": 2,
+    "merge": 3,
+    "finalize": 4,
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class RaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{message} [{status}]")
+        self.status = status
+
+
+_SIGNATURES = {
+    # name: (argtypes, restype)
+    "ra_state_init": ("PPPLiiP", "i"),
+    "ra_block_update": ("PPPPPPLiiiLLiiP", "i"),
+    "ra_merge": ("PPPPPPLiiP", "i"),
+    "ra_finalize": ("PPPPPLiiP", "i"),
+    "ra_ring_step": ("PPPPPPLiiiiiiiP", "i"),
+    "ra_ring_forward": ("PPPPPLiiiiiiP", "i"),
+    "ra_ring_forward_host": ("PPPPPLiiiiiiP", "i"),
+    "ra_device_status": ("P", "i"),
+    "ra_selftest_wait_timeout": ("LP", "i"),
+    "ra_trace_enable": ("i", "i"),
+    "ra_trace_reset": ("", "i"),
+    "ra_trace_query": ("iPP", "i"),
+    "ra_status_string": ("i", "s"),
+    "ra_last_error": ("", "s"),
+    "ra_abi_version": ("", "i"),
+}
+_CT = {"P": ctypes.c_void_p, "L": ctypes.c_longlong, "i": ctypes.c_int, "s": ctypes.c_char_p}
+
+
+def lib():
+    """Load libra.so once.  Raise RaError if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RaError(RA_ERR_UNSUPPORTED,
+                              f"{LIB_PATH} is not built; run __graft_entry__.build() "
+                              "(nvcc, sm_103a)")
+            L = ctypes.CDLL(LIB_PATH)
+            for name, (args, res) in _SIGNATURES.items():
+                f = getattr(L, name)
+                f.argtypes = [_CT[c] for c in args]
+                f.restype = _CT[res]
+            if L.ra_abi_version() != 1:
+                raise RaError(RA_ERR_UNSUPPORTED, "libra.so ABI version mismatch; rebuild it")
+            _lib = L
+    return _lib
+
+
+def _check(rc: int):
+    if rc != RA_OK:
+        L = lib()
+        raise RaError(rc, f"{L.ra_status_string(rc).decode()}: {L.ra_last_error().decode()}")
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous (token-major)")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _qkv_dtype(q: torch.Tensor) -> int:
+    if q.dtype == torch.bfloat16:
+        return RA_BF16
+    if q.dtype == torch.float32:
+        return RA_F32
+    raise TypeError(f"q/k/v must be bfloat16 or float32, got {q.dtype}")
+
+
+def _shapes(q, k, v):
+    if q.dim() != 3 or k.dim() != 3 or v.dim() != 3:
+        raise ValueError("q, k, v must be [rows, heads, d] (token-major)")
+    if k.shape != v.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("k and v must match in shape, and q, k, v in dtype")
+    if q.shape[2] != k.shape[2]:
+        raise ValueError("q and k must share the head dim")
+    return q.shape[0], q.shape[1], k.shape[1], q.shape[2]
+
+
+def _state_shapes(m, l, o, rows, heads, d):
+    for name, t, shp in (("m", m, (rows, heads)), ("l", l, (rows, heads)),
+                         ("o", o, (rows, heads, d))):
+        if tuple(t.shape) != shp:
+            raise ValueError(f"{name} must have shape {shp}, got {tuple(t.shape)}")
+
+
+def ra_state_init(m, l, o, stream=None):
+    rows, heads, d = o.shape
+    _state_shapes(m, l, o, rows, heads, d)
+    _check(lib().ra_state_init(_dev(m, "m", torch.float32), _dev(l, "l", torch.float32),
+                               _dev(o, "o", torch.float32), rows, d, heads, _stream(stream)))
+
+
+def ra_block_update(q, k, v, m, l, o, *, q_off: int = 0, kv_off: int = 0, causal: bool = False,
+                    stream=None):
+    c, heads, kv_heads, d = _shapes(q, k, v)
+    if k.shape[0] != c:
+        raise ValueError("the query block and the K/V block must have the same length c")
+    _state_shapes(m, l, o, c, heads, d)
+    _check(lib().ra_block_update(
+        _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(m, "m", torch.float32),
+        _dev(l, "l", torch.float32), _dev(o, "o", torch.float32), c, d, heads, kv_heads,
+        int(q_off), int(kv_off), int(bool(causal)), _qkv_dtype(q), _stream(stream)))
+
+
+def ra_merge(m_a, l_a, o_a, m_b, l_b, o_b, stream=None):
+    rows, heads, d = o_a.shape
+    _state_shapes(m_a, l_a, o_a, rows, heads, d)
+    _state_shapes(m_b, l_b, o_b, rows, heads, d)
+    _check(lib().ra_merge(_dev(m_a, "m_a", torch.float32), _dev(l_a, "l_a", torch.float32),
+                          _dev(o_a, "o_a", torch.float32), _dev(m_b, "m_b", torch.float32),
+                          _dev(l_b, "l_b", torch.float32), _dev(o_b, "o_b", torch.float32),
+                          rows, d, heads, _stream(stream)))
+
+
+def ra_finalize(m, l, o, out=None, lse=None, stream=None):
+    rows, heads, d = o.shape
+    _state_shapes(m, l, o, rows, heads, d)
+    if out is None:
+        out = torch.empty_like(o)
+    if lse is None:
+        lse = torch.empty_like(m)
+    _state_shapes(lse, lse, out, rows, heads, d)
+    _check(lib().ra_finalize(_dev(m, "m", torch.float32), _dev(l, "l", torch.float32),
+                             _dev(o, "o", torch.float32), _dev(out, "out", torch.float32),
+                             _dev(lse, "lse", torch.float32), rows, d, heads, _stream(stream)))
+    return out, lse
+
+
+def ra_ring_step(q, k, v, m, l, o, *, P: int, s: int, causal: bool, stream=None):
+    N, heads, kv_heads, d = _shapes(q, k, v)
+    if k.shape[0] != N:
+        raise ValueError("q, k and v must cover the same N tokens")
+    _state_shapes(m, l, o, N, heads, d)
+    _check(lib().ra_ring_step(
+        _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(m, "m", torch.float32),
+        _dev(l, "l", torch.float32), _dev(o, "o", torch.float32), N, int(P), int(s),
+        int(bool(causal)), d, heads, kv_heads, _qkv_dtype(q), _stream(stream)))
+
+
+def ra_ring_forward(q, k, v, *, P: int, causal: bool, out=None, lse=None, stream=None):
+    """Returns (out [N, heads, d] fp32, lse [N, heads] fp32)."""
+    N, heads, kv_heads, d = _shapes(q, k, v)
+    if k.shape[0] != N:
+        raise ValueError("q, k and v must cover the same N tokens")
+    if out is None:
+        out = torch.empty((N, heads, d), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((N, heads), dtype=torch.float32, device=q.device)
+    _state_shapes(lse, lse, out, N, heads, d)
+    _check(lib().ra_ring_forward(
+        _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(out, "out", torch.float32),
+        _dev(lse, "lse", torch.float32), N, int(P), int(bool(causal)), d, heads, kv_heads,
+        _qkv_dtype(q), _stream(stream)))
+    return out, lse
+
+
+def ra_ring_forward_host(q, k, v, *, P: int, causal: bool, out=None, lse=None, stream=None):
+    """ra_ring_forward on CPU tensors.  Pinned memory makes the copies
+    asynchronous DMA.  The call returns when out and lse are on the host."""
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CPU tensor")
+    N, heads, kv_heads, d = _shapes(q, k, v)
+    if out is None:
+        out = torch.empty((N, heads, d), dtype=torch.float32, pin_memory=q.is_pinned())
+    if lse is None:
+        lse = torch.empty((N, heads), dtype=torch.float32, pin_memory=q.is_pinned())
+    _check(lib().ra_ring_forward_host(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), N, int(P),
+        int(bool(causal)), d, heads, kv_heads, _qkv_dtype(q), _stream(stream)))
+    return out, lse
+
+
+def ra_device_status(stream=None):
+    _check(lib().ra_device_status(_stream(stream)))
+
+
+def ra_selftest_wait_timeout(limit_cycles: int, stream=None) -> int:
+    return lib().ra_selftest_wait_timeout(int(limit_cycles), _stream(stream))
+
+
+def ra_trace_enable(on: bool = True):
+    _check(lib().ra_trace_enable(int(bool(on))))
+
+
+def ra_trace_reset():
+    _check(lib().ra_trace_reset())
+
+
+def ra_trace_query(kind) -> tuple[int, float]:
+    """Returns (launches, total device ms) of one kernel kind since the last reset."""
+    k = KERNEL_KINDS[kind] if isinstance(kind, str) else int(kind)
+    n = ctypes.c_longlong(0)
+    ms = ctypes.c_double(0.0)
+    _check(lib().ra_trace_query(k, ctypes.addressof(n), ctypes.addressof(ms)))
+    return n.value, ms.value

@@ -1,0 +1,465 @@
+// Host side of the C ABI declared in include/ra.h: argument checks, TMA
+// tensor-map encoding, the ring schedule, stream-ordered scratch, tracing
+// and device status.  Host code only; the kernels live in the other units.
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "ra.h"
+#include "ra_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int status, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return status;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(RA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Default wait bound for the kernels' mbarrier waits: 2^31 SM cycles,
+// about one second at the maximum SM clock.
+constexpr long long kWaitLimit = 1LL << 31;
+
+// ----------------------------------------------------------------- tracing
+struct TraceRec {
+  int kind;
+  cudaEvent_t start;
+  cudaEvent_t stop;
+};
+std::mutex g_trace_mu;
+bool g_trace_on = false;
+std::vector<TraceRec> g_trace;       // recorded since the last reset
+std::vector<cudaEvent_t> g_ev_pool;  // spare events
+
+cudaEvent_t take_event() {
+  if (!g_ev_pool.empty()) {
+    cudaEvent_t e = g_ev_pool.back();
+    g_ev_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Brackets one kernel launch with an event pair on its stream while
+// tracing is on.
+struct TraceScope {
+  int kind;
+  cudaStream_t st;
+  cudaEvent_t a = nullptr, b = nullptr;
+  bool on = false;
+  TraceScope(int k, cudaStream_t s) : kind(k), st(s) {
+    std::lock_guard<std::mutex> g(g_trace_mu);
+    if (!g_trace_on) return;
+    a = take_event();
+    b = take_event();
+    if (a && b && cudaEventRecord(a, st) == cudaSuccess) on = true;
+  }
+  void done(bool launched) {
+    std::lock_guard<std::mutex> g(g_trace_mu);
+    if (!on) {
+      if (a) g_ev_pool.push_back(a);
+      if (b) g_ev_pool.push_back(b);
+      return;
+    }
+    if (launched && cudaEventRecord(b, st) == cudaSuccess) {
+      g_trace.push_back({kind, a, b});
+    } else {
+      g_ev_pool.push_back(a);
+      g_ev_pool.push_back(b);
+    }
+  }
+};
+
+// ----------------------------------------------------------------- TMA maps
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+int get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  return RA_OK;
+}
+
+// 3-D map over a token-major bf16 tensor [rows, heads, d]: dims (d, heads,
+// rows).  The box is 64 elements (128 B, one swizzle span) x 1 head x 128
+// rows, with 128-byte swizzle.  Rows past the end read as zero.
+int encode_map(CUtensorMap* map, const void* base, long long rows, int heads, int d) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
+                              static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(heads) * d * 2};
+  const cuuint32_t box[3] = {64, 1, 128};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+  return RA_OK;
+}
+
+// ----------------------------------------------------------------- checks
+int check_common(int d, int heads, int dtype) {
+  if (dtype != RA_F32 && dtype != RA_BF16) return fail(RA_ERR_INVALID, "dtype %d is not RA_F32 or RA_BF16", dtype);
+  if (d != 64 && d != 128) return fail(RA_ERR_UNSUPPORTED, "head dim d=%d (supported: 64, 128)", d);
+  if (heads < 1 || heads > 65535) return fail(RA_ERR_INVALID, "heads=%d out of range [1, 65535]", heads);
+  return RA_OK;
+}
+
+int check_heads(int heads, int kv_heads) {
+  if (kv_heads < 1) return fail(RA_ERR_INVALID, "kv_heads=%d must be >= 1", kv_heads);
+  if (heads % kv_heads != 0) return fail(RA_ERR_INVALID, "heads=%d is not a multiple of kv_heads=%d", heads, kv_heads);
+  return RA_OK;
+}
+
+int check_ptrs(std::initializer_list<const void*> ps) {
+  int i = 0;
+  for (const void* p : ps) {
+    if (!p) return fail(RA_ERR_INVALID, "pointer argument %d is NULL", i);
+    if (!aligned16(p)) return fail(RA_ERR_INVALID, "pointer argument %d is not 16-byte aligned", i);
+    ++i;
+  }
+  return RA_OK;
+}
+
+// Run one block-update launch (mode 0 or 1), picking the kernel by dtype.
+int run_update(ra::FwdArgs& a, int d, int dtype, cudaStream_t st) {
+  a.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
+  a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+  a.wait_limit = kWaitLimit;
+  if (a.nwork == 0 || a.c == 0) return RA_OK;
+  cudaError_t e;
+  if (dtype == RA_BF16) {
+    int rc = get_encoder();
+    if (rc != RA_OK) return rc;
+    CUtensorMap tq, tk, tv;
+    if ((rc = encode_map(&tq, a.q, a.q_rows, a.heads, d)) != RA_OK) return rc;
+    if ((rc = encode_map(&tk, a.k, a.kv_rows, a.kv_heads, d)) != RA_OK) return rc;
+    if ((rc = encode_map(&tv, a.v, a.kv_rows, a.kv_heads, d)) != RA_OK) return rc;
+    TraceScope ts(RA_KERNEL_BLOCK_UPDATE_BF16, st);
+    e = ra::launch_umma_update(a, d, tq, tk, tv, st);
+    ts.done(e == cudaSuccess);
+  } else {
+    TraceScope ts(RA_KERNEL_BLOCK_UPDATE_F32, st);
+    e = ra::launch_simt_update(a, d, st);
+    ts.done(e == cudaSuccess);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "block-update launch");
+  return RA_OK;
+}
+
+int ring_args_check(const void* q, const void* k, const void* v, long long N, int P, int s,
+                    int d, int heads, int kv_heads, int dtype) {
+  int rc;
+  if ((rc = check_common(d, heads, dtype)) != RA_OK) return rc;
+  if ((rc = check_heads(heads, kv_heads)) != RA_OK) return rc;
+  if (N < 0) return fail(RA_ERR_INVALID, "N=%lld is negative", N);
+  if (P < 1 || P > 65535) return fail(RA_ERR_INVALID, "P=%d out of range [1, 65535]", P);
+  if (N % P != 0) return fail(RA_ERR_INVALID, "N=%lld is not a multiple of P=%d", N, P);
+  if (s < 0 || s >= P) return fail(RA_ERR_INVALID, "ring step s=%d out of range [0, P)", s);
+  if (N > (1LL << 31) - 256) return fail(RA_ERR_UNSUPPORTED, "N=%lld exceeds the 32-bit TMA row coordinate", N);
+  (void)q; (void)k; (void)v;
+  return RA_OK;
+}
+
+int ring_step_impl(const void* q, const void* k, const void* v, float* m, float* l, float* o,
+                   long long N, int P, int s, int causal, int d, int heads, int kv_heads,
+                   int dtype, cudaStream_t st) {
+  ra::FwdArgs a{};
+  a.q = q; a.k = k; a.v = v; a.m = m; a.l = l; a.o = o;
+  a.c = N / P;
+  a.q_rows = N;
+  a.kv_rows = N;
+  a.heads = heads;
+  a.kv_heads = kv_heads;
+  a.causal = causal ? 1 : 0;
+  a.mode = 1;
+  a.P = P;
+  a.s = s;
+  a.nwork = causal ? P - s : P;  // causal: ranks i < s would fold a future block
+  return run_update(a, d, dtype, st);
+}
+
+int ring_forward_impl(const void* q, const void* k, const void* v, float* out, float* lse,
+                      long long N, int P, int causal, int d, int heads, int kv_heads, int dtype,
+                      cudaStream_t st, float* l_scratch) {
+  const long long rows = N;
+  TraceScope t0(RA_KERNEL_STATE_INIT, st);
+  cudaError_t e = ra::launch_state_init(lse, l_scratch, out, rows, heads, d, st);
+  t0.done(e == cudaSuccess);
+  if (e != cudaSuccess) return cuda_fail(e, "state-init launch");
+  for (int s = 0; s < P; ++s) {
+    int rc = ring_step_impl(q, k, v, lse, l_scratch, out, N, P, s, causal, d, heads, kv_heads,
+                            dtype, st);
+    if (rc != RA_OK) return rc;
+  }
+  TraceScope t1(RA_KERNEL_FINALIZE, st);
+  e = ra::launch_finalize(lse, l_scratch, out, out, lse, rows, heads, d, st);
+  t1.done(e == cudaSuccess);
+  if (e != cudaSuccess) return cuda_fail(e, "finalize launch");
+  return RA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ra_abi_version(void) { return 1; }
+
+const char* ra_status_string(int status) {
+  switch (status) {
+    case RA_OK: return "RA_OK";
+    case RA_ERR_INVALID: return "RA_ERR_INVALID";
+    case RA_ERR_UNSUPPORTED: return "RA_ERR_UNSUPPORTED";
+    case RA_ERR_CUDA: return "RA_ERR_CUDA";
+    case RA_ERR_TIMEOUT: return "RA_ERR_TIMEOUT";
+    case RA_ERR_ALLOC: return "RA_ERR_ALLOC";
+    default: return "RA_ERR_UNKNOWN";
+  }
+}
+
+const char* ra_last_error(void) { return g_last_error.c_str(); }
+
+int ra_state_init(float* m, float* l, float* o, long long c, int d, int heads, void* stream) {
+  int rc;
+  if ((rc = check_common(d, heads, RA_F32)) != RA_OK) return rc;
+  if (c < 0) return fail(RA_ERR_INVALID, "c=%lld is negative", c);
+  if (c == 0) return RA_OK;
+  if ((rc = check_ptrs({m, l, o})) != RA_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  TraceScope ts(RA_KERNEL_STATE_INIT, st);
+  cudaError_t e = ra::launch_state_init(m, l, o, c, heads, d, st);
+  ts.done(e == cudaSuccess);
+  if (e != cudaSuccess) return cuda_fail(e, "state-init launch");
+  return RA_OK;
+}
+
+int ra_block_update(const void* q, const void* k, const void* v, float* m, float* l, float* o,
+                    long long c, int d, int heads, int kv_heads, long long q_off,
+                    long long kv_off, int causal, int dtype, void* stream) {
+  int rc;
+  if ((rc = check_common(d, heads, dtype)) != RA_OK) return rc;
+  if ((rc = check_heads(heads, kv_heads)) != RA_OK) return rc;
+  if (c < 0) return fail(RA_ERR_INVALID, "c=%lld is negative", c);
+  if (c > (1LL << 31) - 256) return fail(RA_ERR_UNSUPPORTED, "c=%lld exceeds the 32-bit TMA row coordinate", c);
+  if (c == 0) return RA_OK;
+  if ((rc = check_ptrs({q, k, v, m, l, o})) != RA_OK) return rc;
+  ra::FwdArgs a{};
+  a.q = q; a.k = k; a.v = v; a.m = m; a.l = l; a.o = o;
+  a.c = c;
+  a.q_rows = c;
+  a.kv_rows = c;
+  a.q_off = q_off;
+  a.kv_off = kv_off;
+  a.heads = heads;
+  a.kv_heads = kv_heads;
+  a.causal = causal ? 1 : 0;
+  a.mode = 0;
+  a.P = 1;
+  a.s = 0;
+  a.nwork = 1;
+  return run_update(a, d, dtype, static_cast<cudaStream_t>(stream));
+}
+
+int ra_merge(float* m_a, float* l_a, float* o_a, const float* m_b, const float* l_b,
+             const float* o_b, long long c, int d, int heads, void* stream) {
+  int rc;
+  if ((rc = check_common(d, heads, RA_F32)) != RA_OK) return rc;
+  if (c < 0) return fail(RA_ERR_INVALID, "c=%lld is negative", c);
+  if (c == 0) return RA_OK;
+  if ((rc = check_ptrs({m_a, l_a, o_a, m_b, l_b, o_b})) != RA_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  TraceScope ts(RA_KERNEL_MERGE, st);
+  cudaError_t e = ra::launch_merge(m_a, l_a, o_a, m_b, l_b, o_b, c, heads, d, st);
+  ts.done(e == cudaSuccess);
+  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  return RA_OK;
+}
+
+int ra_finalize(const float* m, const float* l, const float* o, float* out, float* lse,
+                long long c, int d, int heads, void* stream) {
+  int rc;
+  if ((rc = check_common(d, heads, RA_F32)) != RA_OK) return rc;
+  if (c < 0) return fail(RA_ERR_INVALID, "c=%lld is negative", c);
+  if (c == 0) return RA_OK;
+  if ((rc = check_ptrs({m, l, o, out, lse})) != RA_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  TraceScope ts(RA_KERNEL_FINALIZE, st);
+  cudaError_t e = ra::launch_finalize(m, l, o, out, lse, c, heads, d, st);
+  ts.done(e == cudaSuccess);
+  if (e != cudaSuccess) return cuda_fail(e, "finalize launch");
+  return RA_OK;
+}
+
+int ra_ring_step(const void* q, const void* k, const void* v, float* m, float* l, float* o,
+                 long long N, int P, int s, int causal, int d, int heads, int kv_heads,
+                 int dtype, void* stream) {
+  int rc = ring_args_check(q, k, v, N, P, s, d, heads, kv_heads, dtype);
+  if (rc != RA_OK) return rc;
+  if (N == 0) return RA_OK;
+  if ((rc = check_ptrs({q, k, v, m, l, o})) != RA_OK) return rc;
+  return ring_step_impl(q, k, v, m, l, o, N, P, s, causal, d, heads, kv_heads, dtype,
+                        static_cast<cudaStream_t>(stream));
+}
+
+int ra_ring_forward(const void* q, const void* k, const void* v, float* out, float* lse,
+                    long long N, int P, int causal, int d, int heads, int kv_heads, int dtype,
+                    void* stream) {
+  int rc = ring_args_check(q, k, v, N, P, 0, d, heads, kv_heads, dtype);
+  if (rc != RA_OK) return rc;
+  if (N == 0) return RA_OK;
+  if ((rc = check_ptrs({q, k, v, out, lse})) != RA_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  float* l_scratch = nullptr;
+  const size_t l_bytes = static_cast<size_t>(N) * heads * sizeof(float);
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&l_scratch), l_bytes, st);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(RA_ERR_ALLOC, "cudaMallocAsync of %zu bytes for the l state failed: %s", l_bytes,
+                cudaGetErrorString(e));
+  }
+  rc = ring_forward_impl(q, k, v, out, lse, N, P, causal, d, heads, kv_heads, dtype, st, l_scratch);
+  e = cudaFreeAsync(l_scratch, st);
+  if (rc == RA_OK && e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync");
+  return rc;
+}
+
+int ra_ring_forward_host(const void* q_host, const void* k_host, const void* v_host,
+                         float* out_host, float* lse_host, long long N, int P, int causal, int d,
+                         int heads, int kv_heads, int dtype, void* stream) {
+  int rc = ring_args_check(q_host, k_host, v_host, N, P, 0, d, heads, kv_heads, dtype);
+  if (rc != RA_OK) return rc;
+  if (N == 0) return RA_OK;
+  if (!q_host || !k_host || !v_host || !out_host || !lse_host)
+    return fail(RA_ERR_INVALID, "a host pointer is NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t esz = dtype == RA_BF16 ? 2 : 4;
+  const size_t q_bytes = static_cast<size_t>(N) * heads * d * esz;
+  const size_t kv_bytes = static_cast<size_t>(N) * kv_heads * d * esz;
+  const size_t out_bytes = static_cast<size_t>(N) * heads * d * sizeof(float);
+  const size_t rh_bytes = static_cast<size_t>(N) * heads * sizeof(float);
+  void *dq = nullptr, *dk = nullptr, *dv = nullptr;
+  float *dout = nullptr, *dlse = nullptr, *dl = nullptr;
+  cudaError_t e = cudaSuccess;
+  auto alloc = [&](void** p, size_t n) {
+    if (e == cudaSuccess) e = cudaMallocAsync(p, n, st);
+  };
+  alloc(&dq, q_bytes);
+  alloc(&dk, kv_bytes);
+  alloc(&dv, kv_bytes);
+  alloc(reinterpret_cast<void**>(&dout), out_bytes);
+  alloc(reinterpret_cast<void**>(&dlse), rh_bytes);
+  alloc(reinterpret_cast<void**>(&dl), rh_bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    rc = fail(RA_ERR_ALLOC, "cudaMallocAsync of device staging failed: %s", cudaGetErrorString(e));
+  } else {
+    e = cudaMemcpyAsync(dq, q_host, q_bytes, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dk, k_host, kv_bytes, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dv, v_host, kv_bytes, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) {
+      rc = cuda_fail(e, "host-to-device copy");
+    } else {
+      rc = ring_forward_impl(dq, dk, dv, dout, dlse, N, P, causal, d, heads, kv_heads, dtype, st, dl);
+      if (rc == RA_OK) {
+        e = cudaMemcpyAsync(out_host, dout, out_bytes, cudaMemcpyDeviceToHost, st);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(lse_host, dlse, rh_bytes, cudaMemcpyDeviceToHost, st);
+        if (e != cudaSuccess) rc = cuda_fail(e, "device-to-host copy");
+      }
+    }
+  }
+  void* bufs[6] = {dq, dk, dv, dout, dlse, dl};
+  for (void* p : bufs)
+    if (p) cudaFreeAsync(p, st);
+  const int st_rc = ra_device_status(stream);
+  if (rc != RA_OK) return rc;
+  return st_rc;
+}
+
+int ra_device_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int a = 0, b = 0;
+  if ((e = ra::take_umma_status(&a)) != cudaSuccess) return cuda_fail(e, "reading the tcgen05 kernel status");
+  if ((e = ra::take_simt_status(&b)) != cudaSuccess) return cuda_fail(e, "reading the fp32 kernel status");
+  if (a != 0 || b != 0)
+    return fail(RA_ERR_TIMEOUT, "a kernel gave up a bounded wait (codes 0x%x, 0x%x)", a, b);
+  return RA_OK;
+}
+
+int ra_selftest_wait_timeout(long long limit_cycles, void* stream) {
+  if (limit_cycles < 0) return fail(RA_ERR_INVALID, "limit_cycles must be >= 0");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = ra::launch_wait_selftest(limit_cycles, st);
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  return ra_device_status(stream);
+}
+
+int ra_trace_enable(int on) {
+  std::lock_guard<std::mutex> g(g_trace_mu);
+  g_trace_on = on != 0;
+  return RA_OK;
+}
+
+int ra_trace_reset(void) {
+  std::lock_guard<std::mutex> g(g_trace_mu);
+  for (auto& r : g_trace) {
+    g_ev_pool.push_back(r.start);
+    g_ev_pool.push_back(r.stop);
+  }
+  g_trace.clear();
+  return RA_OK;
+}
+
+int ra_trace_query(int kind, long long* launches, double* total_ms) {
+  if (kind < 0 || kind >= RA_KERNEL_KINDS) return fail(RA_ERR_INVALID, "unknown kernel kind %d", kind);
+  if (!launches || !total_ms) return fail(RA_ERR_INVALID, "NULL output pointer");
+  std::lock_guard<std::mutex> g(g_trace_mu);
+  long long n = 0;
+  double ms = 0.0;
+  for (auto& r : g_trace) {
+    if (r.kind != kind) continue;
+    cudaError_t e = cudaEventSynchronize(r.stop);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize");
+    float x = 0.f;
+    e = cudaEventElapsedTime(&x, r.start, r.stop);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventElapsedTime");
+    ms += x;
+    ++n;
+  }
+  *launches = n;
+  *total_ms = ms;
+  return RA_OK;
+}
+
+}  // extern "C"

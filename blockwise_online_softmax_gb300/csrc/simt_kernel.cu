@@ -1,0 +1,243 @@
+// fp32 block update on the FFMA pipes.  fp32 inputs are held to 1e-5,
+// which tf32 tensor cores cannot meet.  It follows the same recurrence as
+// the tcgen05 kernel, in natural-log units.
+//
+// A CTA owns 64 query rows of one head.  It stages 64-key K/V tiles in
+// shared memory and loops over the tiles of the K/V block:
+//   S = Q K^T * scale   (4x4 register tile per thread),
+//   mask,               (causal on global positions, ragged tail)
+//   row max / sum       (one warp per 8 rows, warp shuffles),
+//   O = alpha O + P V   (O in registers, 4 rows x d/16 columns per thread).
+// Key tiles wholly in the future are not visited.
+#include <cmath>
+#include <cstdint>
+
+#include "ra_internal.h"
+
+namespace ra {
+
+__device__ int g_simt_status = 0;
+
+namespace {
+
+constexpr int BQ = 64;
+constexpr int BK = 64;
+constexpr int NT = 256;
+
+template <int D>
+struct SimtSmem {
+  float q[BQ][D + 1];
+  float k[BK][D + 1];
+  float v[BK][D + 1];
+  float s[BQ][BK + 1];
+  float m[BQ];
+  float l[BQ];
+  float alpha[BQ];
+};
+
+template <int D>
+__global__ void __launch_bounds__(NT) simt_update_kernel(const FwdArgs a) {
+  extern __shared__ float4 smem_f4[];
+  SimtSmem<D>& sm = *reinterpret_cast<SimtSmem<D>*>(smem_f4);
+  const int tid = threadIdx.x;
+  const int tx = tid & 15, ty = tid >> 4;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int h = blockIdx.y;
+  const int kh = h / (a.heads / a.kv_heads);
+  const Work wk = decode_work(a, blockIdx.z);
+  const long long q_tile0 = static_cast<long long>(blockIdx.x) * BQ;
+  if (q_tile0 >= a.c) return;
+
+  const float* __restrict__ Q = static_cast<const float*>(a.q);
+  const float* __restrict__ K = static_cast<const float*>(a.k);
+  const float* __restrict__ V = static_cast<const float*>(a.v);
+
+  // Number of key tiles with at least one allowed key for this query tile.
+  const long long kv_tiles = (a.c + BK - 1) / BK;
+  long long nt = kv_tiles;
+  if (a.causal) {
+    const long long last_row = (q_tile0 + BQ - 1 < a.c - 1) ? q_tile0 + BQ - 1 : a.c - 1;
+    const long long last_key = wk.q_pos0 + last_row - wk.kv_pos0;  // local index
+    nt = (last_key < 0) ? 0 : (last_key / BK + 1 < kv_tiles ? last_key / BK + 1 : kv_tiles);
+  }
+  if (nt == 0) return;  // state unchanged
+
+  // Q tile and state in.
+  for (int i = tid; i < BQ * D / 4; i += NT) {
+    const int r = i / (D / 4), c4 = i % (D / 4);
+    const long long gr = q_tile0 + r;
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (gr < a.c)
+      x = reinterpret_cast<const float4*>(Q + ((wk.q_base + gr) * a.heads + h) * D)[c4];
+    sm.q[r][4 * c4 + 0] = x.x;
+    sm.q[r][4 * c4 + 1] = x.y;
+    sm.q[r][4 * c4 + 2] = x.z;
+    sm.q[r][4 * c4 + 3] = x.w;
+  }
+  if (tid < BQ) {
+    const long long gr = q_tile0 + tid;
+    float mm = -INFINITY, ll = 0.f;
+    if (gr < a.c) {
+      const long long si = (wk.state_base + gr) * a.heads + h;
+      mm = a.m[si];
+      ll = a.l[si];
+    }
+    sm.m[tid] = mm;
+    sm.l[tid] = ll;
+  }
+  constexpr int OC = D / 16;  // output columns per thread: tx + 16 * j
+  float acc[4][OC];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const long long gr = q_tile0 + ty + 16 * i;
+    const float* src = a.o + ((wk.state_base + gr) * a.heads + h) * D;
+#pragma unroll
+    for (int j = 0; j < OC; ++j) acc[i][j] = (gr < a.c) ? src[tx + 16 * j] : 0.f;
+  }
+  __syncthreads();
+
+  for (long long t = 0; t < nt; ++t) {
+    const long long k0 = t * BK;
+    for (int i = tid; i < BK * D / 4; i += NT) {
+      const int r = i / (D / 4), c4 = i % (D / 4);
+      float4 x = make_float4(0.f, 0.f, 0.f, 0.f), y = x;
+      if (k0 + r < a.c) {
+        const long long off = ((wk.kv_base + k0 + r) * a.kv_heads + kh) * D;
+        x = reinterpret_cast<const float4*>(K + off)[c4];
+        y = reinterpret_cast<const float4*>(V + off)[c4];
+      }
+      sm.k[r][4 * c4 + 0] = x.x; sm.k[r][4 * c4 + 1] = x.y;
+      sm.k[r][4 * c4 + 2] = x.z; sm.k[r][4 * c4 + 3] = x.w;
+      sm.v[r][4 * c4 + 0] = y.x; sm.v[r][4 * c4 + 1] = y.y;
+      sm.v[r][4 * c4 + 2] = y.z; sm.v[r][4 * c4 + 3] = y.w;
+    }
+    __syncthreads();
+
+    // S = Q K^T * scale, masked.
+    float sacc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) sacc[i][j] = 0.f;
+#pragma unroll 8
+    for (int x = 0; x < D; ++x) {
+      float qa[4], kb[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) qa[i] = sm.q[ty + 16 * i][x];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) kb[j] = sm.k[tx + 16 * j][x];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sacc[i][j] = fmaf(qa[i], kb[j], sacc[i][j]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = ty + 16 * i;
+      const long long qpos = wk.q_pos0 + q_tile0 + r;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int cidx = tx + 16 * j;
+        const long long kl = k0 + cidx;
+        const bool ok = (kl < a.c) && (!a.causal || wk.kv_pos0 + kl <= qpos);
+        sm.s[r][cidx] = ok ? sacc[i][j] * a.scale : -INFINITY;
+      }
+    }
+    __syncthreads();
+
+    // Row statistics: warp w takes rows 8w .. 8w+7, two columns per lane.
+#pragma unroll
+    for (int rr = 0; rr < BQ / 8; ++rr) {
+      const int r = warp * (BQ / 8) + rr;
+      const float s0 = sm.s[r][lane], s1 = sm.s[r][lane + 32];
+      float mx = fmaxf(s0, s1);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      const float m_old = sm.m[r];
+      const float m_new = fmaxf(m_old, mx);
+      const float mref = (m_new == -INFINITY) ? 0.f : m_new;
+      const float p0 = expf(s0 - mref), p1 = expf(s1 - mref);
+      float sum = p0 + p1;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+      // alpha = exp(m_old - m_new); a still-empty row keeps its state.
+      const float alpha = (m_new == -INFINITY) ? 1.f : expf(m_old - mref);
+      sm.s[r][lane] = p0;
+      sm.s[r][lane + 32] = p1;
+      __syncwarp();
+      if (lane == 0) {
+        sm.alpha[r] = alpha;
+        sm.l[r] = alpha * sm.l[r] + sum;
+        sm.m[r] = m_new;
+      }
+    }
+    __syncthreads();
+
+    // O = alpha O + P V.
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float al = sm.alpha[ty + 16 * i];
+#pragma unroll
+      for (int j = 0; j < OC; ++j) acc[i][j] *= al;
+    }
+#pragma unroll 4
+    for (int kk = 0; kk < BK; ++kk) {
+      float p[4], vv[OC];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) p[i] = sm.s[ty + 16 * i][kk];
+#pragma unroll
+      for (int j = 0; j < OC; ++j) vv[j] = sm.v[kk][tx + 16 * j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < OC; ++j) acc[i][j] = fmaf(p[i], vv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+
+  // State out.
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const long long gr = q_tile0 + ty + 16 * i;
+    if (gr < a.c) {
+      float* dst = a.o + ((wk.state_base + gr) * a.heads + h) * D;
+#pragma unroll
+      for (int j = 0; j < OC; ++j) dst[tx + 16 * j] = acc[i][j];
+    }
+  }
+  if (tid < BQ) {
+    const long long gr = q_tile0 + tid;
+    if (gr < a.c) {
+      const long long si = (wk.state_base + gr) * a.heads + h;
+      a.m[si] = sm.m[tid];
+      a.l[si] = sm.l[tid];
+    }
+  }
+}
+
+template <int D>
+cudaError_t launch_d(const FwdArgs& a, cudaStream_t st) {
+  const size_t smem = sizeof(SimtSmem<D>);
+  cudaError_t e = cudaFuncSetAttribute(simt_update_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  dim3 grid(static_cast<unsigned>((a.c + BQ - 1) / BQ), a.heads, a.nwork);
+  simt_update_kernel<D><<<grid, NT, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_simt_update(const FwdArgs& a, int d, cudaStream_t st) {
+  return d == 128 ? launch_d<128>(a, st) : launch_d<64>(a, st);
+}
+
+cudaError_t take_simt_status(int* code) {
+  int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(code, g_simt_status, sizeof(int));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(g_simt_status, &zero, sizeof(int));
+}
+
+}  // namespace ra

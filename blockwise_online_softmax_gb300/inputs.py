@@ -4,9 +4,13 @@ holds none of the attention arithmetic.
 
 Recipe (the same for every workload)
 ------------------------------------
-* Use a CPU ``torch.Generator`` seeded with ``manual_seed(seed)``.
-* Draw fp32 ``randn`` in this order: Q ``[N, Hq, d]``, K ``[N, Hkv, d]``,
-  V ``[N, Hkv, d]``.  The layout is token-major with batch 1.
+* Tensors are Q ``[N, Hq, d]``, K ``[N, Hkv, d]`` and V ``[N, Hkv, d]``,
+  token-major with batch 1.  Each gets a tensor id: Q = 0, K = 1, V = 2.
+* Each tensor is filled with fp32 standard normals in flat (row-major)
+  order, in chunks of 2^22 elements.  Chunk b of tensor t comes from its
+  own CPU ``torch.Generator`` seeded with ``(seed << 20) | (t << 16) | b``,
+  using ``torch.randn``.  The chunks are independent, so they are drawn in
+  parallel, and the result does not depend on the thread count.
 * The workload's extra draws are the row picks for scaled or planted keys,
   each a ``randperm`` of the block length.  They come from a second CPU
   generator seeded with ``seed + 1000``, in the order given below.  The
@@ -21,10 +25,37 @@ virtual rank i holds tokens [i*c, (i+1)*c).
 """
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass, field
 
 import numpy as np
 import torch
+
+CHUNK = 1 << 22
+
+
+def randn_chunked(shape, seed: int, tensor_id: int, threads: int | None = None) -> torch.Tensor:
+    """fp32 standard normals, filled chunk by chunk (see the module recipe)."""
+    out = torch.empty(shape, dtype=torch.float32)
+    flat = out.view(-1)
+    n = flat.numel()
+    nchunks = (n + CHUNK - 1) // CHUNK
+    if nchunks >= (1 << 16) or not (0 <= tensor_id < 16) or seed < 0:
+        raise ValueError("tensor too large or bad seed / tensor id for the chunked recipe")
+
+    def fill(b):
+        g = torch.Generator().manual_seed((seed << 20) | (tensor_id << 16) | b)
+        part = flat[b * CHUNK:(b + 1) * CHUNK]
+        torch.randn(part.shape, generator=g, out=part)
+
+    if nchunks <= 1:
+        for b in range(nchunks):
+            fill(b)
+    else:
+        with ThreadPoolExecutor(max_workers=threads or os.cpu_count() or 1) as ex:
+            list(ex.map(fill, range(nchunks)))
+    return out
 
 
 @dataclass(frozen=True)
@@ -116,36 +147,44 @@ def pick_generator(w: Workload) -> torch.Generator:
 
 
 def make_workload(w: Workload | str):
-    """Return (q, k, v) CPU tensors of the workload's dtype, token-major."""
+    """Return (q, k, v) CPU tensors of the workload's dtype, token-major.
+
+    Each tensor is drawn, modified and cast before the next one, so only
+    one fp32 tensor is alive at a time."""
     if isinstance(w, str):
         w = WORKLOADS[w]
-    g = torch.Generator().manual_seed(w.seed)
-    q = torch.randn((w.N, w.heads, w.d), generator=g, dtype=torch.float32)
-    k = torch.randn((w.N, w.kv_heads, w.d), generator=g, dtype=torch.float32)
-    v = torch.randn((w.N, w.kv_heads, w.d), generator=g, dtype=torch.float32)
+    if w.recipe not in ("iid", "scaled_keys", "half", "planted"):
+        raise ValueError(f"unknown recipe {w.recipe}")
+    dt = w.torch_dtype
+    half = w.recipe == "half"
+
+    q = randn_chunked((w.N, w.heads, w.d), w.seed, 0)
+    if half:
+        q *= 0.5
+    q = q.to(dt)
+    k = randn_chunked((w.N, w.kv_heads, w.d), w.seed, 1)
     if w.recipe == "scaled_keys":
         for _, h, rows in scaled_key_rows(w, pick_generator(w)):
             k[rows, h, :] *= w.extra["factor"]
     elif w.recipe == "planted":
         for _, h, rows in planted_key_rows(w, pick_generator(w)):
             k[rows, h, :] *= w.extra["factor"]
-    elif w.recipe == "half":
-        q *= 0.5
+    elif half:
         k *= 0.5
+    k = k.to(dt)
+    v = randn_chunked((w.N, w.kv_heads, w.d), w.seed, 2)
+    if half:
         v *= 0.5
-    elif w.recipe != "iid":
-        raise ValueError(f"unknown recipe {w.recipe}")
-    dt = w.torch_dtype
-    return q.to(dt), k.to(dt), v.to(dt)
+    v = v.to(dt)
+    return q, k, v
 
 
 def make_random(N: int, heads: int, kv_heads: int, d: int, *, dtype=torch.bfloat16,
                 seed: int = 0, scale: float = 1.0):
-    """Small iid N(0,1)*scale case: Q [N,Hq,d], K and V [N,Hkv,d], drawn in that order."""
-    g = torch.Generator().manual_seed(seed)
-    q = torch.randn((N, heads, d), generator=g) * scale
-    k = torch.randn((N, kv_heads, d), generator=g) * scale
-    v = torch.randn((N, kv_heads, d), generator=g) * scale
+    """iid N(0,1)*scale case: Q [N,Hq,d], K and V [N,Hkv,d] (module recipe)."""
+    q = randn_chunked((N, heads, d), seed, 0) * scale
+    k = randn_chunked((N, kv_heads, d), seed, 1) * scale
+    v = randn_chunked((N, kv_heads, d), seed, 2) * scale
     return q.to(dtype), k.to(dtype), v.to(dtype)
 
 

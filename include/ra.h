@@ -1,0 +1,224 @@
+/*
+ * ra.h -- C ABI of the GB300 blockwise online-softmax library (libra.so).
+ *
+ * The library computes the per-device hot path of Ring Attention on one
+ * GPU.  Virtual rank i keeps its query block Q_i.  At ring step s it folds
+ * in the K/V block j = (i - s) mod P by the online-softmax rescale.  The
+ * running state (m, l, O~) stays in HBM between steps.  Then comes a merge
+ * or a finalize.
+ *
+ * Sources, by page title and section:
+ *  [MATH]  "Ring Attention Math Deep -- Belgavi.AI Lab": "The online-softmax
+ *          identity that makes streaming legal", "The ring schedule:
+ *          passing K/V around", "Accumulation math, step by step", "A worked
+ *          numeric example".
+ *  [PB]    "Ring Attention Paper Breakdown: Blockwise Distributed
+ *          Transformers for Near-Infinite Context": "2. Ring Topology &
+ *          Asynchronous Double-Buffered KV Circulation", "3. Cross-Device
+ *          Online Softmax Accumulator Math", "4. Zero-Overhead Overlapping
+ *          Condition & Roofline Analysis".
+ *  [XF]    xf_ring_attention (aicassindra.com): "The architecture: every
+ *          piece explained", "End-to-end flow".
+ *  [SP]    "Ring Attention：把超长序列沿设备环流动": "环是怎样工作的",
+ *          "局部 Softmax 为什么不能直接相加", "Causal Attention
+ *          让环不再完全对称", "位置编码必须使用全局位置".
+ *  [GUIDE] "RingAttention: Scaling LLM Context to 10M Tokens": "1.
+ *          Incremental Online Softmax Accumulation".
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Layout.  All tensors are token-major and dense, with batch 1:
+ *   Q:  [rows, heads, d]       (bf16 or fp32, as `dtype` says)
+ *   K, V: [rows, kv_heads, d]
+ *   m, l: [rows, heads] fp32   (running max, running sum of exp)
+ *   o (O~): [rows, heads, d] fp32 (unnormalized running output)
+ * Query head h reads KV head h / (heads / kv_heads), so consecutive groups
+ * of query heads share one KV head (GQA; heads % kv_heads must be 0).
+ *
+ * Scores.  s = (q . k) / sqrt(d), with 1/sqrt(d) rounded to fp32 [MATH],
+ * [PB] step 1.  The state is in natural-log units: m = max s, l = sum
+ * exp(s - m), o = sum exp(s - m) v.
+ *
+ * Causal mask.  Key t is allowed for query r when kv_off + t <= q_off + r,
+ * on global token positions [SP] "位置编码必须使用全局位置".
+ *
+ * Types.  dtype RA_BF16 runs the tcgen05 tensor-core path: bf16 operands,
+ * fp32 accumulation, and P rounded to bf16 before the P V product.  dtype
+ * RA_F32 runs an fp32 FFMA path.  d must be 64 or 128.
+ *
+ * Pointers.  All pointers are device pointers, except for the *_host
+ * call.  Each pointer must be 16-byte aligned.  The caller owns every
+ * buffer.  No call keeps a pointer after it returns.
+ *
+ * Streams.  `stream` is a cudaStream_t (NULL = legacy default stream).
+ * Compute calls only enqueue work and return.  A call returns RA_OK once
+ * its launches are enqueued.  A launch failure returns RA_ERR_CUDA.
+ * Device-side wait timeouts are reported by ra_device_status().
+ *
+ * Errors.  Every call returns an ra_status.  Arguments are checked before
+ * any launch, and a bad argument returns RA_ERR_INVALID without touching
+ * memory.  ra_last_error() returns a message for the calling thread's last
+ * failure.  Zero-size work (c == 0 or N == 0) is RA_OK and launches
+ * nothing.
+ */
+#ifndef RA_H
+#define RA_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  RA_OK = 0,
+  RA_ERR_INVALID = -1,     /* bad argument: null/misaligned pointer, shape, dtype */
+  RA_ERR_UNSUPPORTED = -2, /* well-formed but outside what the kernels handle */
+  RA_ERR_CUDA = -3,        /* a CUDA runtime/driver call failed */
+  RA_ERR_TIMEOUT = -4,     /* a kernel gave up a bounded wait (see ra_device_status) */
+  RA_ERR_ALLOC = -5        /* stream-ordered allocation of scratch failed */
+} ra_status;
+
+typedef enum { RA_F32 = 0, RA_BF16 = 1 } ra_dtype;
+
+/* Kernel kinds for the tracing calls. */
+typedef enum {
+  RA_KERNEL_STATE_INIT = 0,
+  RA_KERNEL_BLOCK_UPDATE_BF16 = 1, /* tcgen05 / TMEM / TMA kernel */
+  RA_KERNEL_BLOCK_UPDATE_F32 = 2,  /* fp32 FFMA kernel */
+  RA_KERNEL_MERGE = 3,
+  RA_KERNEL_FINALIZE = 4,
+  RA_KERNEL_KINDS = 5
+} ra_kernel_kind;
+
+/*
+ * ra_state_init -- set c rows of state to the merge identity (m, l, O~) =
+ * (-inf, 0, 0) [XF] "End-to-end flow", [MATH] "Accumulation math, step by
+ * step".
+ *   m, l: [c, heads] fp32 ; o: [c, heads, d] fp32 (written).
+ */
+int ra_state_init(float* m, float* l, float* o, long long c, int d, int heads, void* stream);
+
+/*
+ * ra_block_update -- fold one K/V block into the running state of one query
+ * block.  This is [PB] section 3, steps 1-7, also [MATH] "Accumulation math,
+ * step by step" and [GUIDE] section 1, in the unnormalized-O~ form:
+ *   S = Q K^T / sqrt(d);  m' = max(m, rowmax S);  alpha = exp(m - m');
+ *   P = exp(S - m');  l' = alpha l + rowsum P;  O~' = alpha O~ + P V.
+ *   q: [c, heads, d], the first row of Q_i (global position q_off).
+ *   k, v: [c, kv_heads, d], the first row of K_j, V_j (global position kv_off).
+ *   m, l, o: the state of Q_i's c rows, updated in place.  On return, m is
+ *           the exact running max of the allowed scores (-inf for a row
+ *           with none yet).  l and o are taken relative to that m.
+ *   causal: nonzero applies the causal mask on global positions.  The
+ *           kernel skips key tiles that lie wholly in the future and masks
+ *           elementwise only the tiles that cross the diagonal [SP] "Causal
+ *           Attention 让环不再完全对称".  A row with no allowed key keeps
+ *           its state.
+ *   dtype: RA_BF16 (q, k, v are bf16) or RA_F32 (q, k, v are fp32).
+ */
+int ra_block_update(const void* q, const void* k, const void* v, float* m, float* l, float* o,
+                    long long c, int d, int heads, int kv_heads, long long q_off,
+                    long long kv_off, int causal, int dtype, void* stream);
+
+/*
+ * ra_merge -- a <- a (+) b on c rows of two partial states: m = max(m_a,
+ * m_b), then each side is rescaled by exp(m_side - m) and the two are added
+ * [XF] "The architecture: every piece explained" (online softmax
+ * accumulator), [SP] "局部 Softmax 为什么不能直接相加".  The identity
+ * state is neutral.  m_a/l_a/o_a are updated in place.  b is read only and
+ * must not overlap a.
+ */
+int ra_merge(float* m_a, float* l_a, float* o_a, const float* m_b, const float* l_b,
+             const float* o_b, long long c, int d, int heads, void* stream);
+
+/*
+ * ra_finalize -- out = O~ / l and lse = m + ln l ([MATH] "After the final
+ * block: out = o / l").  The log-sum-exp is kept for backward recompute
+ * ([SP] "Backward 需要让梯度也沿环传播").  A row with l = 0 gets out = 0
+ * and lse = -inf.
+ *   out: [c, heads, d] fp32 and lse: [c, heads] fp32 (written).  `out` may
+ *   be the same buffer as `o`, and `lse` may be the same buffer as `m`
+ *   (in place).  Any other overlap is not allowed.
+ */
+int ra_finalize(const float* m, const float* l, const float* o, float* out, float* lse,
+                long long c, int d, int heads, void* stream);
+
+/*
+ * ra_ring_step -- one step s of the ring schedule for all P virtual ranks
+ * at once ([MATH] "The ring schedule: passing K/V around", [PB] section 2).
+ * Virtual rank i folds block j = (i - s) mod P of K/V into its state.
+ * Under `causal`, ranks whose block j lies in the future (j > i) are
+ * skipped at launch granularity.  Each rank's diagonal block (s = 0) is
+ * masked elementwise.  The "hop" is the block index advancing on the
+ * device.  No bytes move.
+ *   q: [N, heads, d]; k, v: [N, kv_heads, d]; m, l: [N, heads]; o: [N, heads, d].
+ *   N = P * c, 0 <= s < P.  Block i holds tokens [i*c, (i+1)*c).
+ */
+int ra_ring_step(const void* q, const void* k, const void* v, float* m, float* l, float* o,
+                 long long N, int P, int s, int causal, int d, int heads, int kv_heads,
+                 int dtype, void* stream);
+
+/*
+ * ra_ring_forward -- the whole per-device forward loop of [MATH]
+ * "Accumulation math, step by step" for all P virtual ranks.  It runs the
+ * state init, ring steps s = 0 .. P-1, then the finalize.
+ *   out: [N, heads, d] fp32.  It is used as the O~ state during the ring,
+ *        then finalized in place.
+ *   lse: [N, heads] fp32.  It is used as the m state, then holds LSE =
+ *        m + ln l.
+ * Scratch: the l state ([N, heads] fp32) is the only scratch.  It is
+ * allocated with cudaMallocAsync on `stream` and freed the same way.  A
+ * failed allocation returns RA_ERR_ALLOC.
+ */
+int ra_ring_forward(const void* q, const void* k, const void* v, float* out, float* lse,
+                    long long N, int P, int causal, int d, int heads, int kv_heads, int dtype,
+                    void* stream);
+
+/*
+ * ra_ring_forward_host -- ra_ring_forward on HOST buffers.  It copies q, k
+ * and v to stream-ordered device buffers, runs the ring, copies out and
+ * lse back, frees the buffers, and synchronizes `stream` before it
+ * returns.  Pinned host memory makes the copies asynchronous DMA.  Device
+ * wait timeouts are checked before return and give RA_ERR_TIMEOUT.
+ */
+int ra_ring_forward_host(const void* q_host, const void* k_host, const void* v_host,
+                         float* out_host, float* lse_host, long long N, int P, int causal, int d,
+                         int heads, int kv_heads, int dtype, void* stream);
+
+/*
+ * ra_device_status -- synchronize `stream`, then read and clear the
+ * library's device-side error words.  Every mbarrier wait in the kernels is
+ * bounded.  A wait that runs out records a code and makes its CTA leave
+ * cleanly.  The call returns RA_ERR_TIMEOUT if any code was recorded since
+ * the last call, RA_ERR_CUDA if the synchronize failed, else RA_OK.  While
+ * a code is recorded, block-update CTAs that start do no work (so one
+ * failed wait cannot turn into a long cascade).  Results of launches made
+ * since the failure are therefore invalid until this call clears the code.
+ */
+int ra_device_status(void* stream);
+
+/*
+ * ra_selftest_wait_timeout -- failure-detection self test.  It launches one
+ * CTA that waits, with a bound of `limit_cycles` SM cycles, on an mbarrier
+ * that nothing arrives on.  It then returns what ra_device_status returns
+ * (RA_ERR_TIMEOUT when the bounded wait works).  Nothing faults and nothing
+ * hangs.
+ */
+int ra_selftest_wait_timeout(long long limit_cycles, void* stream);
+
+/* Tracing.  When enabled, the library records a CUDA event pair on the
+ * launching stream around every kernel it launches.  ra_trace_query then
+ * synchronizes those events.  It returns the number of launches of `kind`
+ * and their summed device time in milliseconds since the last reset. */
+int ra_trace_enable(int on);
+int ra_trace_reset(void);
+int ra_trace_query(int kind, long long* launches, double* total_ms);
+
+const char* ra_status_string(int status);
+const char* ra_last_error(void);
+int ra_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RA_H */

@@ -1,0 +1,63 @@
+"""Tolerances and comparison helpers for the GPU-vs-oracle parity tests.
+
+The stated bars:
+* bf16 inputs with fp32 accumulation: max |O - O_ref| <= 1e-2, and
+  |LSE - LSE_ref| <= 1e-3 * max(1, |LSE_ref|).  The floor keeps the relative
+  bound meaningful near LSE = 0.
+* fp32 inputs: max |O - O_ref| <= 1e-5, and the same floored form with 1e-5
+  for LSE.
+
+States (m, l, O~) are compared in their canonical form, relative to the
+exact running max:
+* |m - m_ref| <= tol_lse * max(1, |m_ref|)
+* |l - l_ref| <= tol_l * l_ref
+* |O~ - O~_ref| <= tol_o * l_ref, elementwise.  O~ is a weighted sum with
+  total weight l, so its error scales with l.
+"""
+import numpy as np
+
+TOL = {
+    "bf16": {"o": 1e-2, "lse": 1e-3, "l": 2e-3},
+    "f32": {"o": 1e-5, "lse": 1e-5, "l": 1e-5},
+}
+
+
+def _np(x):
+    import torch
+
+    if isinstance(x, torch.Tensor):
+        return x.detach().cpu().to(torch.float64).numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+def check_output(out, lse, ref_out, ref_lse, kind):
+    """max |O - O_ref| and the floored relative LSE error against the bars."""
+    t = TOL[kind]
+    out, lse = _np(out), _np(lse)
+    assert out.shape == ref_out.shape and lse.shape == ref_lse.shape
+    assert np.isfinite(out).all(), "non-finite output"
+    err_o = np.abs(out - ref_out).max() if out.size else 0.0
+    fin = np.isfinite(ref_lse)
+    assert (np.isneginf(lse) == ~fin).all(), "LSE -inf pattern differs"
+    err_l = (np.abs(lse[fin] - ref_lse[fin]) / np.maximum(1.0, np.abs(ref_lse[fin]))).max() \
+        if fin.any() else 0.0
+    assert err_o <= t["o"], f"max |O - O_ref| = {err_o:.3e} > {t['o']}"
+    assert err_l <= t["lse"], f"LSE rel err = {err_l:.3e} > {t['lse']}"
+    return err_o, err_l
+
+
+def check_state(m, l, o, ref, kind):
+    t = TOL[kind]
+    m, l, o = _np(m), _np(l), _np(o)
+    mr, lr, orf = ref
+    assert (np.isneginf(m) == np.isneginf(mr)).all(), "m -inf pattern differs"
+    fin = np.isfinite(mr)
+    if fin.any():
+        em = (np.abs(m[fin] - mr[fin]) / np.maximum(1.0, np.abs(mr[fin]))).max()
+        assert em <= t["lse"], f"m err {em:.3e}"
+        el = (np.abs(l[fin] - lr[fin]) / lr[fin]).max()
+        assert el <= t["l"], f"l rel err {el:.3e}"
+        eo = (np.abs(o - orf)[fin] / lr[fin][:, None]).max()
+        assert eo <= t["o"], f"O~ err / l = {eo:.3e}"
+    # rows with no allowed key keep the identity state
+    assert (l[~fin] == 0).all() and (o[~fin] == 0).all()

@@ -1,0 +1,198 @@
+"""GPU parity of the ring forward (init, P ring steps, finalize) against the
+CPU oracle.  The five named workloads are checked, in the launch
+configuration the benchmark times: the two small ones on every output, the
+three large ones on sampled rows over each row's full key range.  Ragged
+and degenerate shapes, invariants, resume from a saved state, and the
+host-buffer entry point are covered too."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity import TOL, check_output
+
+import blockwise_online_softmax_gb300 as ra
+from blockwise_online_softmax_gb300 import binding, inputs
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from blockwise_online_softmax_gb300 import build
+
+    build.build()
+    binding.lib()
+    yield
+    torch.cuda.empty_cache()
+
+
+def kind_of(dtype):
+    return "bf16" if dtype == torch.bfloat16 else "f32"
+
+
+def run_ring(q, k, v, P, causal):
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    out, lse = ra.ra_ring_forward(qd, kd, vd, P=P, causal=causal)
+    ra.ra_device_status()
+    return out, lse
+
+
+@pytest.mark.parametrize("name", ["tiny-exact", "mha-8k"])
+def test_small_workloads_every_output(name):
+    w = inputs.WORKLOADS[name]
+    q, k, v = inputs.make_workload(w)
+    out, lse = run_ring(q, k, v, w.P, w.causal)
+    ref_out, ref_lse = oracle.attention(q, k, v, causal=w.causal)
+    check_output(out, lse, ref_out, ref_lse, w.dtype)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,random_rows", [("mha-32k-scaled-keys", 16), ("gqa-128k", 16),
+                                              ("mha-1m-planted", 4)])
+def test_large_workloads_sampled_rows(name, random_rows):
+    w = inputs.WORKLOADS[name]
+    q, k, v = inputs.make_workload(w)
+    rows = inputs.sample_rows(w, random_per_block=random_rows)
+    out, lse = run_ring(q, k, v, w.P, w.causal)
+    idx = torch.from_numpy(rows).to(DEV)
+    got_out = out.index_select(0, idx).cpu()
+    got_lse = lse.index_select(0, idx).cpu()
+    del out, lse
+    torch.cuda.empty_cache()
+    ref_out, ref_lse = oracle.attention(q, k, v, causal=w.causal, rows=rows)
+    check_output(got_out, got_lse, ref_out, ref_lse, w.dtype)
+
+
+SHAPES = [
+    # N, P, heads, kv_heads, d, dtype, causal
+    (600, 3, 4, 2, 128, torch.bfloat16, True),    # c = 200: ragged tail tile
+    (600, 3, 4, 2, 128, torch.bfloat16, False),
+    (1000, 5, 2, 1, 64, torch.bfloat16, True),    # MQA, d = 64
+    (256, 1, 2, 2, 128, torch.bfloat16, True),    # P = 1: a single block
+    (130, 2, 1, 1, 128, torch.bfloat16, True),    # c = 65 < one tile
+    (8, 8, 1, 1, 64, torch.bfloat16, True),       # c = 1
+    (1536, 6, 3, 1, 64, torch.float32, True),     # fp32 path, GQA 3:1
+    (768, 2, 2, 2, 128, torch.float32, False),    # fp32, d = 128
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+def test_ring_shapes_match_oracle(shape):
+    N, P, heads, kv_heads, d, dtype, causal = shape
+    q, k, v = inputs.make_random(N, heads, kv_heads, d, dtype=dtype, seed=N + P + d)
+    out, lse = run_ring(q, k, v, P, causal)
+    ref_out, ref_lse = oracle.attention(q, k, v, causal=causal)
+    check_output(out, lse, ref_out, ref_lse, kind_of(dtype))
+
+
+def test_empty_sequence():
+    z = torch.zeros(0, 2, 64, dtype=torch.bfloat16, device=DEV)
+    out, lse = ra.ra_ring_forward(z, z, z, P=4, causal=True)
+    assert out.shape == (0, 2, 64) and lse.shape == (0, 2)
+
+
+def test_large_logits_stay_finite():
+    q, k, v = inputs.make_random(1024, 2, 2, 128, dtype=torch.bfloat16, seed=77)
+    q = (q.float() * 30).to(torch.bfloat16)  # scores of several hundred
+    out, lse = run_ring(q, k, v, 4, True)
+    assert torch.isfinite(out).all() and torch.isfinite(lse).all()
+    ref_out, ref_lse = oracle.attention(q, k, v, causal=True)
+    check_output(out, lse, ref_out, ref_lse, "bf16")
+
+
+def test_values_all_one_give_one():
+    q, k, _ = inputs.make_random(2048, 4, 2, 128, dtype=torch.bfloat16, seed=5)
+    v = torch.ones(2048, 2, 128, dtype=torch.bfloat16)
+    out, _ = run_ring(q, k, v, 8, True)
+    assert (out - 1).abs().max().item() <= TOL["bf16"]["o"]
+
+
+def test_block_count_does_not_change_the_result():
+    q, k, v = inputs.make_random(2048, 2, 1, 128, dtype=torch.bfloat16, seed=9)
+    ref_out, ref_lse = oracle.attention(q, k, v, causal=True)
+    outs = []
+    for P in (1, 2, 4, 8, 16):
+        out, lse = run_ring(q, k, v, P, True)
+        check_output(out, lse, ref_out, ref_lse, "bf16")
+        outs.append(out)
+    for x in outs[1:]:
+        assert (x - outs[0]).abs().max().item() <= TOL["bf16"]["o"]
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_ring_equals_its_steps_and_resumes_from_saved_state(dtype):
+    """ra_ring_forward equals init + ra_ring_step for s = 0..P-1 + finalize,
+    bit for bit.  Saving the (m, l, O~) state to the host after step k and
+    restoring it gives the same bits again (checkpoint and resume)."""
+    N, P, heads, kv_heads, d = 1024, 4, 2, 1, 64
+    q, k, v = (t.to(DEV) for t in inputs.make_random(N, heads, kv_heads, d, dtype=dtype, seed=13))
+    ref_out, ref_lse = ra.ra_ring_forward(q, k, v, P=P, causal=True)
+    m = torch.empty(N, heads, device=DEV)
+    l = torch.empty(N, heads, device=DEV)
+    o = torch.empty(N, heads, d, device=DEV)
+    ra.ra_state_init(m, l, o)
+    for s in range(P):
+        ra.ra_ring_step(q, k, v, m, l, o, P=P, s=s, causal=True)
+        if s == 1:
+            saved = [x.cpu() for x in (m, l, o)]
+            for x in (m, l, o):
+                x.fill_(float("nan"))
+            for x, y in zip((m, l, o), saved):
+                x.copy_(y)
+    out, lse = ra.ra_finalize(m, l, o)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref_out)
+    assert torch.equal(lse, ref_lse)
+
+
+def test_ring_equals_single_pair_calls():
+    """The all-ranks ring step computes, for every rank, the same bits as
+    per-pair ra_block_update calls made in ring order."""
+    N, P, heads, d = 768, 3, 2, 128
+    q, k, v = (t.to(DEV) for t in inputs.make_random(N, heads, heads, d, seed=15))
+    ref_out, ref_lse = ra.ra_ring_forward(q, k, v, P=P, causal=True)
+    c = N // P
+    for i in range(P):
+        m = torch.empty(c, heads, device=DEV)
+        l = torch.empty(c, heads, device=DEV)
+        o = torch.empty(c, heads, d, device=DEV)
+        ra.ra_state_init(m, l, o)
+        for s in range(P):
+            j = (i - s) % P
+            if j > i:
+                continue
+            sl = slice(i * c, (i + 1) * c)
+            kv = slice(j * c, (j + 1) * c)
+            ra.ra_block_update(q[sl], k[kv], v[kv], m, l, o, q_off=i * c, kv_off=j * c,
+                               causal=True)
+        out, lse = ra.ra_finalize(m, l, o)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref_out[i * c:(i + 1) * c])
+        assert torch.equal(lse, ref_lse[i * c:(i + 1) * c])
+
+
+def test_host_buffer_entry_point():
+    q, k, v = inputs.make_random(1024, 4, 2, 128, dtype=torch.bfloat16, seed=19)
+    qp, kp, vp = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    out_h, lse_h = ra.ra_ring_forward_host(qp, kp, vp, P=4, causal=True)
+    out_d, lse_d = run_ring(q, k, v, 4, True)
+    assert not out_h.is_cuda
+    assert torch.equal(out_h, out_d.cpu()) and torch.equal(lse_h, lse_d.cpu())
+
+
+def test_trace_counts_launches():
+    q, k, v = (t.to(DEV) for t in inputs.make_random(1024, 2, 2, 128, seed=21))
+    ra.ra_trace_reset()
+    ra.ra_trace_enable(True)
+    try:
+        ra.ra_ring_forward(q, k, v, P=4, causal=True)
+        n_upd, ms_upd = ra.ra_trace_query("block_update_bf16")
+        n_init, _ = ra.ra_trace_query("state_init")
+        n_fin, _ = ra.ra_trace_query("finalize")
+    finally:
+        ra.ra_trace_enable(False)
+        ra.ra_trace_reset()
+    assert (n_upd, n_init, n_fin) == (4, 1, 1)
+    assert ms_upd > 0
