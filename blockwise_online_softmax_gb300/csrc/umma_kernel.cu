@@ -27,14 +27,16 @@
 // tcgen05.mma of the CTA come from one thread and run in issue order.
 // That order is what lets QK^T(t+2) overwrite the TMEM that PV(t) reads.
 //
-// Lazy rescale: the row max in use (m_used) only moves when the true
-// running max exceeds it by more than 2^8 (log2 units).  Until then P <=
-// 2^8, and l and O stay exact relative to m_used.  At the end the state is
-// rescaled once to the exact running max, so the stored (m, l, O~) is the
-// unique canonical state.  This keeps the read-scale-write of O in TMEM off
-// most tiles.  The recurrence is unchanged: alpha = exp(m_old - m_new) is
-// applied whenever m_used moves, and the same factor is folded in at the
-// end.
+// Rescale rule: the row max in use (m_used) follows the true running max
+// exactly (RESCALE_THRESHOLD = 0).  The largest weight of a row is then
+// exactly 1 and is exact in bf16.  A lazy rule, moving m_used only when the
+// max grows by 2^k, would save read-scale-writes of O in TMEM.  But the
+// dominant weight would become 2^delta, and bf16 rounds that by up to
+// 2^-8 relative.  On rows where one key dominates (large logits, planted
+// keys) that error reaches |v| * 2^-8 in O.  The code keeps m_used and
+// m_true apart, so the threshold stays a single constant.  At the end
+// the state is rescaled to the exact running max, so the stored
+// (m, l, O~) is the unique canonical state.
 //
 // Every wait is bounded.  A time-out records a code in g_umma_status.  All
 // roles then leave their loops, in-flight TMA and MMA work is drained
@@ -60,7 +62,7 @@ constexpr uint32_t CHUNK_BYTES = 128 * 128;  // 128 rows x 128 B (one swizzle sp
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t S_COL0 = 0;
 constexpr uint32_t O_COL = 256;
-constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units: rescale when max grows > 2^8
+constexpr float RESCALE_THRESHOLD = 0.0f;  // log2 units; see the rescale rule above
 
 template <int D>
 struct Cfg {
@@ -373,24 +375,32 @@ umma_update_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
           for (int j = 0; j < 32; ++j) r[j] = pk[32 + j];
           tmem_st32(tl + S_COL0 + b * BN + 32, r);
         }
+        // PV(t-1) must have landed before O~ is touched and before PV(t)
+        // is released.  Waiting on every tile keeps this thread's count of
+        // the PV barrier's phases exact: at this point PV(t) is not issued
+        // yet, so at most PV(t-1) is outstanding and the parity test cannot
+        // alias.  PV(t-1) was issued when softmax(t) started, so the wait
+        // rarely blocks.
+        if (t > 0) {
+          ok = wait_bar(bar(C::B_OD), static_cast<uint32_t>(t - 1) & 1u, abort_flag,
+                        &g_umma_status, 0x32, lim);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          tc_fence_after();
+        }
         if (__any_sync(0xffffffffu, need)) {
-          // Rescale O~ in TMEM.  PV(t-1) must have landed first.
-          if (t > 0) {
-            ok = wait_bar(bar(C::B_OD), static_cast<uint32_t>(t - 1) & 1u, abort_flag,
-                          &g_umma_status, 0x32, lim);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            tc_fence_after();
-          }
+          // Rescale O~ in TMEM by alpha (1 for rows whose max did not move).
+          uint32_t r[D / 32][32];
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(tl + O_COL + cc * 32, r[cc]);
+          tmem_wait_ld();
 #pragma unroll
           for (int cc = 0; cc < D / 32; ++cc) {
-            uint32_t r[32];
-            tmem_ld32(tl + O_COL + cc * 32, r);
-            tmem_wait_ld();
-            reg_fence32(r);
+            reg_fence32(r[cc]);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
-            tmem_st32(tl + O_COL + cc * 32, r);
+            for (int j = 0; j < 32; ++j)
+              r[cc][j] = __float_as_uint(__uint_as_float(r[cc][j]) * alpha);
+            tmem_st32(tl + O_COL + cc * 32, r[cc]);
           }
         }
         tmem_wait_st();
@@ -399,6 +409,7 @@ umma_update_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       }
 
       if (ok) {
+        // PV(nt-1) is the only one that can still be outstanding.
         ok = wait_bar(bar(C::B_OD), static_cast<uint32_t>(nt - 1) & 1u, abort_flag,
                       &g_umma_status, 0x33, lim);
         ok = __all_sync(0xffffffffu, ok);
