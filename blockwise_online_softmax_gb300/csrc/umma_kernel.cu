@@ -1,50 +1,58 @@
 // bf16 block update on the 5th-generation tensor cores (tcgen05 / TMEM / TMA).
 //
-// One CTA folds one K/V block into the running state of a 128-row query
-// tile of one head.  This is the "FlashAttention_Update(Q_i, K_j, V_j, m_i,
-// l_i, O_i)" of "Ring Attention Paper Breakdown", section 2.  Inside the
-// block, the K/V tiles of 128 keys stream through shared memory.  This is
-// the inner level of the two-level blocking in "Ring Attention：
-// 把超长序列沿设备环流动", section "两层分块如何嵌套".
+// One CTA folds one K/V block into the running state of 256 query rows of
+// one head, held as two 128-row query tiles Q0 and Q1.  This is the
+// "FlashAttention_Update(Q_i, K_j, V_j, m_i, l_i, O_i)" of "Ring Attention
+// Paper Breakdown", section 2.  Inside the block, K/V tiles of 128 keys
+// stream through shared memory.  This is the inner level of the two-level
+// blocking in "Ring Attention：把超长序列沿设备环流动", section
+// "两层分块如何嵌套".  Both query tiles share each K/V tile, which halves
+// the L2-to-SM traffic per FLOP.
 //
-// Warp roles (192 threads):
-//   warp 0      TMA producer.  It loads the Q tile once, then the K and V
-//               tiles into an NST-deep ring of shared-memory stages.
-//   warp 1      Allocates TMEM.  Lane 0 issues every tcgen05.mma: S = Q K^T
-//               into one of two TMEM S buffers, then O += P V with P read
-//               from TMEM (P overwrites its S buffer).
-//   warps 2..5  Softmax / correction / epilogue, one thread per query row.
-//               A thread owns TMEM lane (row) 32*(warp%4)+lane.  It reads
-//               its S row, takes the row max, exponentiates, writes P back
-//               as bf16, rescales its O row when the max grows, and stores
-//               the state at the end.
+// Warp roles (384 threads, three warpgroups):
+//   warps 0..3  softmax group 0: one thread per row of Q0 (TMEM lane
+//               32*warp+lane).
+//   warps 4..7  softmax group 1: the same for Q1.
+//   warp 8      TMA producer.  It loads Q0 and Q1 once, then K and V tiles
+//               into an NST-deep ring of shared-memory stages.
+//   warp 9      Allocates TMEM.  Lane 0 issues every tcgen05.mma.
+//   warps 10-11 idle.
+// A softmax thread reads its S row from TMEM, takes the row max,
+// exponentiates, writes P back as bf16 over its S row, rescales its O~ row
+// in TMEM when the max grows, and loads and stores the state.
 //
-// TMEM columns: S0 [0,128), S1 [128,256), O [256, 256+D).  512 are
-// allocated.
+// Registers: the CTA launches with 168 per thread (three warps share each
+// SM sub-partition's 16K registers).  The producer/MMA warpgroup then gives
+// back down to 56, and the softmax warpgroups take up to 224 (setmaxnreg).
+// 2*128*224 + 128*56 = 384*168.
 //
-// Pipelining: QK^T of tile t+1 is issued before PV of tile t, so the
-// tensor pipe runs S(t+1) while the softmax warps work on S(t).  All
-// tcgen05.mma of the CTA come from one thread and run in issue order.
-// That order is what lets QK^T(t+2) overwrite the TMEM that PV(t) reads.
+// TMEM columns: S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [256+D,256+2D).
+// P_g overwrites the first 64 columns of S_g, two bf16 per 32-bit column,
+// and is the A operand of O_g += P_g V read from TMEM.
 //
-// Rescale rule: the row max in use (m_used) follows the true running max
-// exactly (RESCALE_THRESHOLD = 0).  The largest weight of a row is then
-// exactly 1 and is exact in bf16.  A lazy rule, moving m_used only when the
-// max grows by 2^k, would save read-scale-writes of O in TMEM.  But the
-// dominant weight would become 2^delta, and bf16 rounds that by up to
-// 2^-8 relative.  On rows where one key dominates (large logits, planted
-// keys) that error reaches |v| * 2^-8 in O.  The code keeps m_used and
-// m_true apart, so the threshold stays a single constant.  At the end
-// the state is rescaled to the exact running max, so the stored
-// (m, l, O~) is the unique canonical state.
+// MMA issue order per K/V tile t (prologue: QK0(0), QK1(0)):
+//   PV0(t), QK0(t+1), PV1(t), QK1(t+1).
+// While softmax group 0 works on S0(t+1), the tensor pipe runs PV1(t) and
+// QK1(t+1).  While group 1 works on S1(t+1), it runs PV0(t+1) and
+// QK0(t+2).  Every tcgen05.mma of the CTA comes from one thread, and they
+// run in issue order.  That order lets QK_g(t+1) overwrite the columns
+// from which PV_g(t) reads P_g(t).
+//
+// Rescale rule: each row's max in use follows the exact running max, so the
+// largest weight of a row is exactly 1 and is exact in bf16.  A lazy rule
+// (move the max only when it grows by 2^k) saves O~ read-scale-writes.  But
+// it makes the dominant weight 2^delta, which bf16 rounds by up to 2^-8
+// relative, and on rows where one key dominates that error reaches
+// |v| * 2^-8.  The code keeps the max in use and the true max apart, so
+// the threshold is a single constant.  The stored state is canonical: it
+// is relative to the exact running max.
 //
 // Every wait is bounded.  A time-out records a code in g_umma_status.  All
-// roles then leave their loops, in-flight TMA and MMA work is drained
-// (bounded), and TMEM is freed before exit.
+// roles of the CTA then leave their loops, in-flight TMA and MMA work is
+// drained (bounded), and TMEM is freed.  CTAs that start later in the
+// launch do no work.
 #include <cmath>
 #include <cstdint>
-
-#include <cuda_bf16.h>
 
 #include "ptx.cuh"
 #include "ra_internal.h"
@@ -55,113 +63,93 @@ __device__ int g_umma_status = 0;
 
 namespace {
 
-constexpr int BM = 128;  // query rows per CTA (= TMEM lanes)
+constexpr int BM = 128;  // rows per query tile (= TMEM lanes)
+constexpr int NQ = 2;    // query tiles per CTA
 constexpr int BN = 128;  // keys per K/V tile
-constexpr int NTHREADS = 192;
+constexpr int NTHREADS = (NQ + 1) * 128;
+constexpr uint32_t REGS_LAUNCH = 168;
+constexpr uint32_t REGS_SOFTMAX = 224;
+constexpr uint32_t REGS_CONTROL = 56;
+static_assert(NQ * 128 * REGS_SOFTMAX + 128 * REGS_CONTROL == NTHREADS * REGS_LAUNCH,
+              "setmaxnreg split must add up to the launch allocation");
 constexpr uint32_t CHUNK_BYTES = 128 * 128;  // 128 rows x 128 B (one swizzle span)
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t S_COL0 = 0;
-constexpr uint32_t O_COL = 256;
 constexpr float RESCALE_THRESHOLD = 0.0f;  // log2 units; see the rescale rule above
 
 template <int D>
 struct Cfg {
-  static constexpr int NCH = D / 64;                       // 128-byte chunks per row
-  static constexpr uint32_t TILE_BYTES = BM * D * 2;       // one Q/K/V tile
-  static constexpr int NST = (D == 64) ? 4 : 2;            // K/V stages
+  static constexpr int NCH = D / 64;                  // 128-byte chunks per row
+  static constexpr uint32_t TILE_BYTES = BM * D * 2;  // one Q, K or V tile
+  static constexpr int NST = (D == 64) ? 4 : 2;       // K/V stages
+  static constexpr uint32_t S_COL = 0;                // S_g at S_COL + g * BN
+  static constexpr uint32_t O_COL = 2 * BN;           // O_g at O_COL + g * D
   // barriers
   static constexpr int B_Q = 0;
   static constexpr int B_KF = 1;
   static constexpr int B_KE = B_KF + NST;
   static constexpr int B_VF = B_KE + NST;
   static constexpr int B_VE = B_VF + NST;
-  static constexpr int B_SF = B_VE + NST;  // 2
-  static constexpr int B_PF = B_SF + 2;    // 2
-  static constexpr int B_OD = B_PF + 2;
-  static constexpr int B_DRAIN = B_OD + 1;
+  static constexpr int B_SF = B_VE + NST;  // NQ: QK_g done
+  static constexpr int B_PF = B_SF + NQ;   // NQ: P_g written (128 arrivals)
+  static constexpr int B_OD = B_PF + NQ;   // NQ: PV_g done
+  static constexpr int B_DRAIN = B_OD + NQ;
   static constexpr int NBAR = B_DRAIN + 1;
   static constexpr uint32_t OFF_Q = 0;
-  static constexpr uint32_t OFF_K = OFF_Q + TILE_BYTES;
+  static constexpr uint32_t OFF_K = OFF_Q + NQ * TILE_BYTES;
   static constexpr uint32_t OFF_V = OFF_K + NST * TILE_BYTES;
   static constexpr uint32_t OFF_BAR = OFF_V + NST * TILE_BYTES;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
+  static_assert(O_COL + NQ * D <= TMEM_COLS, "TMEM budget");
 };
 
-template <int D>
-__global__ void __launch_bounds__(NTHREADS, 1)
-umma_update_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
-  using C = Cfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const uint32_t s_base = smem_u32(smem);
-  const uint32_t sQ = s_base + C::OFF_Q;
-  const uint32_t sK = s_base + C::OFF_K;
-  const uint32_t sV = s_base + C::OFF_V;
-  const uint32_t bar0 = s_base + C::OFF_BAR;
-  auto bar = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+// Number of K/V tiles holding a key that some row of the query tile
+// [row0, row0 + BM) may see.  Zero if the tile is past the block end or,
+// under causal masking, all its keys lie in the future.
+__device__ __forceinline__ int tiles_for(const FwdArgs& a, const Work& wk, long long row0) {
+  if (row0 >= a.c) return 0;
+  const long long kv_tiles = (a.c + BN - 1) / BN;
+  if (!a.causal) return static_cast<int>(kv_tiles);
+  const long long last_row = (row0 + BM - 1 < a.c - 1) ? row0 + BM - 1 : a.c - 1;
+  const long long last_key = wk.q_pos0 + last_row - wk.kv_pos0;  // local key index
+  if (last_key < 0) return 0;
+  const long long n = last_key / BN + 1;
+  return static_cast<int>(n < kv_tiles ? n : kv_tiles);
+}
 
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
+// Producer (warp 8) and MMA issuer (warp 9); warps 10 and 11 fall through.
+template <int D>
+__device__ __forceinline__ void control_roles(const FwdArgs& a, const Work& wk, long long row0,
+                                              const int (&ntq)[NQ], int nt, uint32_t tmem,
+                                              uint32_t sQ, uint32_t sK, uint32_t sV,
+                                              uint32_t bar0, volatile int* abort_flag,
+                                              const CUtensorMap* tmQ, const CUtensorMap* tmK,
+                                              const CUtensorMap* tmV) {
+  using C = Cfg<D>;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
   const int h = blockIdx.y;
   const int kh = h / (a.heads / a.kv_heads);
-  const Work wk = decode_work(a, blockIdx.z);
-  const long long q_tile0 = static_cast<long long>(blockIdx.x) * BM;
-
-  // Key tiles to visit: all of them, or, under causal masking, up to the
-  // one holding the last key some row of this tile may see.
-  const long long kv_tiles = (a.c + BN - 1) / BN;
-  long long nt_ll = kv_tiles;
-  if (a.causal) {
-    const long long last_row = (q_tile0 + BM - 1 < a.c - 1) ? q_tile0 + BM - 1 : a.c - 1;
-    const long long last_key = wk.q_pos0 + last_row - wk.kv_pos0;
-    nt_ll = (last_key < 0) ? 0 : (last_key / BN + 1 < kv_tiles ? last_key / BN + 1 : kv_tiles);
-  }
-  const int nt = static_cast<int>(nt_ll);
-
-  if (tid == 0) {
-    for (int i = 0; i < C::NBAR; ++i) {
-      uint32_t cnt = 1;
-      if (i == C::B_PF || i == C::B_PF + 1) cnt = 128;  // every softmax thread arrives
-      mbar_init(bar(i), cnt);
-    }
-    // A CTA that starts after another one of this launch gave up a wait
-    // does no work.
-    *abort_flag = *reinterpret_cast<volatile int*>(&g_umma_status) != 0 ? 1 : 0;
-    fence_mbar_init();
-    fence_proxy_async_smem();
-  }
-  __syncthreads();
-  if (*abort_flag) return;  // uniform across the CTA: read after the barrier
-  if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
   const long long lim = a.wait_limit;
-
-  if (warp == 0) {
+  auto bar = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
+  if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && nt > 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      const int q_row = static_cast<int>(wk.q_base + q_tile0);
-      mbar_arrive_expect_tx(bar(C::B_Q), C::TILE_BYTES);
+      tma_prefetch_desc(tmQ);
+      tma_prefetch_desc(tmK);
+      tma_prefetch_desc(tmV);
+      mbar_arrive_expect_tx(bar(C::B_Q), NQ * C::TILE_BYTES);
 #pragma unroll
-      for (int ch = 0; ch < C::NCH; ++ch)
-        tma_load_3d(sQ + ch * CHUNK_BYTES, &tmQ, bar(C::B_Q), ch * 64, h, q_row);
-      int issued = 0;
+      for (int g = 0; g < NQ; ++g) {
+        const int q_row = static_cast<int>(wk.q_base + row0 + g * BM);
+#pragma unroll
+        for (int ch = 0; ch < C::NCH; ++ch)
+          tma_load_3d(sQ + g * C::TILE_BYTES + ch * CHUNK_BYTES, tmQ, bar(C::B_Q), ch * 64, h,
+                      q_row);
+      }
+      int issued_k = 0, issued_v = 0;
       bool ok = true;
-      for (int t = 0; t < nt && ok; ++t) {
+      for (int t = 0; t < nt; ++t) {
         const int st = t % C::NST;
         const uint32_t ph = static_cast<uint32_t>(t / C::NST) & 1u;
         const int kv_row = static_cast<int>(wk.kv_base + static_cast<long long>(t) * BN);
@@ -171,86 +159,104 @@ umma_update_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         mbar_arrive_expect_tx(bar(C::B_KF + st), C::TILE_BYTES);
 #pragma unroll
         for (int ch = 0; ch < C::NCH; ++ch)
-          tma_load_3d(sK + st * C::TILE_BYTES + ch * CHUNK_BYTES, &tmK, bar(C::B_KF + st),
+          tma_load_3d(sK + st * C::TILE_BYTES + ch * CHUNK_BYTES, tmK, bar(C::B_KF + st),
                       ch * 64, kh, kv_row);
+        issued_k = t + 1;
         if (t >= C::NST)
           ok = wait_bar(bar(C::B_VE + st), ph ^ 1u, abort_flag, &g_umma_status, 0x12, lim);
-        if (!ok) {
-          issued = t + 1;  // K of tile t is in flight
-          break;
-        }
+        if (!ok) break;
         mbar_arrive_expect_tx(bar(C::B_VF + st), C::TILE_BYTES);
 #pragma unroll
         for (int ch = 0; ch < C::NCH; ++ch)
-          tma_load_3d(sV + st * C::TILE_BYTES + ch * CHUNK_BYTES, &tmV, bar(C::B_VF + st),
+          tma_load_3d(sV + st * C::TILE_BYTES + ch * CHUNK_BYTES, tmV, bar(C::B_VF + st),
                       ch * 64, kh, kv_row);
-        issued = t + 1;
+        issued_v = t + 1;
       }
       if (!ok) {
-        // Drain: wait (bounded) for the copies still in flight before the
-        // CTA's shared memory is given up.
+        // Drain: wait (bounded) for copies still in flight before the CTA's
+        // shared memory is released.
         volatile int no_abort = 0;
         wait_bar(bar(C::B_Q), 0, &no_abort, nullptr, 0, lim);
-        for (int t = (issued > C::NST ? issued - C::NST : 0); t < issued; ++t) {
-          const int st = t % C::NST;
-          const uint32_t ph = static_cast<uint32_t>(t / C::NST) & 1u;
-          wait_bar(bar(C::B_KF + st), ph, &no_abort, nullptr, 0, lim);
-          wait_bar(bar(C::B_VF + st), ph, &no_abort, nullptr, 0, lim);
-        }
+        for (int t = (issued_k > C::NST ? issued_k - C::NST : 0); t < issued_k; ++t)
+          wait_bar(bar(C::B_KF + t % C::NST), static_cast<uint32_t>(t / C::NST) & 1u, &no_abort,
+                   nullptr, 0, lim);
+        for (int t = (issued_v > C::NST ? issued_v - C::NST : 0); t < issued_v; ++t)
+          wait_bar(bar(C::B_VF + t % C::NST), static_cast<uint32_t>(t / C::NST) & 1u, &no_abort,
+                   nullptr, 0, lim);
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && nt > 0) {
       constexpr uint32_t idesc_qk = idesc_bf16(BM, BN, 0);
       constexpr uint32_t idesc_pv = idesc_bf16(BM, D, 1);
-      bool ok = wait_bar(bar(C::B_Q), 0, abort_flag, &g_umma_status, 0x21, lim);
-      tc_fence_after();
-      auto issue_qk = [&](int t) -> bool {
-        const int st = t % C::NST;
-        const uint32_t ph = static_cast<uint32_t>(t / C::NST) & 1u;
-        if (!wait_bar(bar(C::B_KF + st), ph, abort_flag, &g_umma_status, 0x22, lim)) return false;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem + S_COL0 + static_cast<uint32_t>(t & 1) * BN;
+      auto qk = [&](int g, int st) {
+        const uint32_t d_tmem = tmem + C::S_COL + static_cast<uint32_t>(g) * BN;
+        const uint32_t qbase = sQ + g * C::TILE_BYTES;
         const uint32_t kbase = sK + st * C::TILE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
+          // K-major, 128-byte swizzle: 16 elements = 32 bytes along a row;
+          // every 4 steps move to the next 64-wide column chunk.
           const uint32_t off = (kk >> 2) * CHUNK_BYTES + (kk & 3) * 32;
-          mma_ss(d_tmem, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
+          mma_ss(d_tmem, sdesc_sw128(qbase + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
                  idesc_qk, kk > 0 ? 1u : 0u);
         }
-        tc_commit(bar(C::B_SF + (t & 1)));
-        tc_commit(bar(C::B_KE + st));
-        return true;
+        tc_commit(bar(C::B_SF + g));
       };
-      if (ok) ok = issue_qk(0);
-      for (int t = 0; t < nt && ok; ++t) {
-        if (t + 1 < nt) {
-          ok = issue_qk(t + 1);
-          if (!ok) break;
-        }
-        const int b = t & 1;
-        ok = wait_bar(bar(C::B_PF + b), static_cast<uint32_t>(t >> 1) & 1u, abort_flag,
-                      &g_umma_status, 0x23, lim);
-        if (!ok) break;
-        const int st = t % C::NST;
-        ok = wait_bar(bar(C::B_VF + st), static_cast<uint32_t>(t / C::NST) & 1u, abort_flag,
-                      &g_umma_status, 0x24, lim);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t p_tmem = tmem + S_COL0 + static_cast<uint32_t>(b) * BN;
+      auto pv = [&](int g, int st) {
+        const uint32_t p_tmem = tmem + C::S_COL + static_cast<uint32_t>(g) * BN;
+        const uint32_t o_tmem = tmem + C::O_COL + static_cast<uint32_t>(g) * D;
         const uint32_t vbase = sV + st * C::TILE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
-          // P columns: two bf16 per 32-bit column, 8 columns per 16 keys.
-          // V (MN-major): 16 keys = two 8-row groups of 1024 B; the 64-wide
-          // column chunks of V sit CHUNK_BYTES apart.
-          mma_ts(tmem + O_COL, p_tmem + kk * 8,
-                 sdesc_sw128(vbase + kk * 2048, CHUNK_BYTES, 1024), idesc_pv, 1u);
+          // P: two bf16 per 32-bit TMEM column, 8 columns per 16 keys.
+          // V (MN-major, 128-byte swizzle): 16 keys = two 8-row groups of
+          // 1024 B (SBO); the 64-wide column chunks sit CHUNK_BYTES apart (LBO).
+          mma_ts(o_tmem, p_tmem + kk * 8, sdesc_sw128(vbase + kk * 2048, CHUNK_BYTES, 1024),
+                 idesc_pv, 1u);
         }
-        tc_commit(bar(C::B_OD));
+        tc_commit(bar(C::B_OD + g));
+      };
+      bool ok = wait_bar(bar(C::B_Q), 0, abort_flag, &g_umma_status, 0x21, lim);
+      if (ok) ok = wait_bar(bar(C::B_KF), 0, abort_flag, &g_umma_status, 0x22, lim);
+      if (ok) {
+        tc_fence_after();
+        if (ntq[0] > 0) qk(0, 0);
+        if (ntq[1] > 0) qk(1, 0);
+        tc_commit(bar(C::B_KE));
+      }
+      for (int t = 0; t < nt && ok; ++t) {
+        const int st = t % C::NST;
+        const int st1 = (t + 1) % C::NST;
+        ok = wait_bar(bar(C::B_VF + st), static_cast<uint32_t>(t / C::NST) & 1u, abort_flag,
+                      &g_umma_status, 0x24, lim);
+        if (!ok) break;
+        bool k_ready = false;
+#pragma unroll
+        for (int g = 0; g < NQ; ++g) {
+          if (t < ntq[g]) {
+            ok = wait_bar(bar(C::B_PF + g), static_cast<uint32_t>(t) & 1u, abort_flag,
+                          &g_umma_status, 0x23, lim);
+            if (!ok) break;
+            tc_fence_after();
+            pv(g, st);
+          }
+          if (t + 1 < ntq[g]) {
+            if (!k_ready) {
+              ok = wait_bar(bar(C::B_KF + st1), static_cast<uint32_t>((t + 1) / C::NST) & 1u,
+                            abort_flag, &g_umma_status, 0x22, lim);
+              if (!ok) break;
+              tc_fence_after();
+              k_ready = true;
+            }
+            qk(g, st1);
+          }
+        }
+        if (!ok) break;
         tc_commit(bar(C::B_VE + st));
+        if (t + 1 < nt) tc_commit(bar(C::B_KE + st1));
       }
       // Drain every MMA issued so far before TMEM can be freed.
       volatile int no_abort = 0;
@@ -258,18 +264,37 @@ umma_update_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       wait_bar(bar(C::B_DRAIN), 0, &no_abort, nullptr, 0, lim);
     }
     __syncwarp();
-  } else {
+  }
+}
+
+// Softmax groups: warps 0..3 own the rows of Q0, warps 4..7 those of Q1.
+template <int D>
+__device__ __forceinline__ void softmax_role(const FwdArgs& a, const Work& wk, long long row0,
+                                             const int (&ntq)[NQ], uint32_t tmem, uint32_t bar0,
+                                             volatile int* abort_flag) {
+  using C = Cfg<D>;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int h = blockIdx.y;
+  const long long lim = a.wait_limit;
+  auto bar = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
+  {
     // ------------------------------------------------------------ softmax
-    const int quarter = warp & 3;
+    const int g = warp >> 2;       // query tile of this group
+    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
     const int row = quarter * 32 + lane;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const long long grow = q_tile0 + row;
+    const uint32_t s_col = C::S_COL + static_cast<uint32_t>(g) * BN;
+    const uint32_t o_col = C::O_COL + static_cast<uint32_t>(g) * D;
+    const long long grow = row0 + g * BM + row;  // row within the block
     const bool valid = grow < a.c;
     const long long sidx = (wk.state_base + grow) * a.heads + h;
     const long long qpos = wk.q_pos0 + grow;
     const float sl2 = a.scale_log2;
+    const uint64_t sl2x2 = f2pack(sl2, sl2);
+    const int ntg = ntq[g];
 
-    if (nt > 0) {
+    if (ntg > 0) {
       float m_ld = -INFINITY, l_run = 0.f;
       if (valid) {
         m_ld = a.m[sidx];
@@ -293,7 +318,7 @@ umma_update_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 #pragma unroll
           for (int j = 0; j < 32; ++j) r[j] = 0u;
         }
-        tmem_st32(tl + O_COL + cc * 32, r);
+        tmem_st32(tl + o_col + cc * 32, r);
       }
       tmem_wait_st();
 
@@ -302,28 +327,23 @@ umma_update_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       bool m_moved = false;
       bool ok = true;
 
-      for (int t = 0; t < nt; ++t) {
-        const int b = t & 1;
-        ok = wait_bar(bar(C::B_SF + b), static_cast<uint32_t>(t >> 1) & 1u, abort_flag,
+      for (int t = 0; t < ntg; ++t) {
+        ok = wait_bar(bar(C::B_SF + g), static_cast<uint32_t>(t) & 1u, abort_flag,
                       &g_umma_status, 0x31, lim);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        float s[BN];
-        {
-          uint32_t r[32];
+        // S row: 128 fp32 scores, loaded once into registers.
+        uint32_t sr[BN / 32][32];
 #pragma unroll
-          for (int cc = 0; cc < BN / 32; ++cc) {
-            tmem_ld32(tl + S_COL0 + b * BN + cc * 32, r);
-            tmem_wait_ld();
-            reg_fence32(r);
+        for (int cc = 0; cc < BN / 32; ++cc) tmem_ld32(tl + s_col + cc * 32, sr[cc]);
+        tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) s[cc * 32 + j] = __uint_as_float(r[j]);
-          }
-        }
-        // Mask: key j of this tile is allowed iff j < lim_j.  The tail
-        // (kv local index < c) and the causal rule (key position <= query
-        // position) are both upper bounds on j.
+        for (int cc = 0; cc < BN / 32; ++cc) reg_fence32(sr[cc]);
+#define RA_S(j) __uint_as_float(sr[(j) >> 5][(j) & 31])
+        // Mask: key j of this tile is allowed iff j < lim_j.  The tail (key
+        // index < c) and the causal rule (key position <= query position)
+        // are both upper bounds on j.
         long long lim_j = a.c - static_cast<long long>(t) * BN;
         if (a.causal) {
           const long long cl = qpos - wk.kv_pos0 - static_cast<long long>(t) * BN + 1;
@@ -332,17 +352,21 @@ umma_update_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         if (lim_j < BN) {
 #pragma unroll
           for (int j = 0; j < BN; ++j)
-            if (j >= lim_j) s[j] = -INFINITY;
+            if (j >= lim_j) sr[j >> 5][j & 31] = 0xff800000u;  // -inf
         }
-        float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+        // Row max: four independent chains over columns 0..127, two new
+        // values per three-input max.
+        float mx0 = fmaxf(RA_S(0), RA_S(4)), mx1 = fmaxf(RA_S(1), RA_S(5));
+        float mx2 = fmaxf(RA_S(2), RA_S(6)), mx3 = fmaxf(RA_S(3), RA_S(7));
 #pragma unroll
-        for (int j = 4; j < BN; j += 4) {
-          mx0 = fmaxf(mx0, s[j + 0]);
-          mx1 = fmaxf(mx1, s[j + 1]);
-          mx2 = fmaxf(mx2, s[j + 2]);
-          mx3 = fmaxf(mx3, s[j + 3]);
+        for (int j = 8; j < BN; j += 8) {
+          mx0 = fmax3(mx0, RA_S(j + 0), RA_S(j + 4));
+          mx1 = fmax3(mx1, RA_S(j + 1), RA_S(j + 5));
+          mx2 = fmax3(mx2, RA_S(j + 2), RA_S(j + 6));
+          mx3 = fmax3(mx3, RA_S(j + 3), RA_S(j + 7));
         }
-        const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+        static_assert(BN % 8 == 0, "the max loop covers columns in groups of 8");
+        const float m_tile = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
         if (m_tile > m_true) {
           m_true = m_tile;
           m_moved = true;
@@ -354,63 +378,71 @@ umma_update_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
           m_used = m_true;
         }
         const float mref = (m_used == -INFINITY) ? 0.f : m_used;
-        float sum0 = 0.f, sum1 = 0.f;
-        uint32_t pk[BN / 2];
+        const uint64_t nmref2 = f2pack(-mref, -mref);
+        // P = 2^(s * log2(e)/sqrt(d) - m), two lanes per FFMA2; row sum in
+        // two FADD2 accumulators; P rounded to bf16 in pairs, written over
+        // the first half of the same registers.
+        uint64_t acc0 = f2pack(0.f, 0.f), acc1 = acc0;
 #pragma unroll
-        for (int j = 0; j < BN; j += 2) {
-          const float p0 = ex2(fmaf(s[j], sl2, -mref));
-          const float p1 = ex2(fmaf(s[j + 1], sl2, -mref));
-          sum0 += p0;
-          sum1 += p1;
-          __nv_bfloat162 v2 = __floats2bfloat162_rn(p0, p1);  // p0 in the low half
-          pk[j / 2] = *reinterpret_cast<uint32_t*>(&v2);
+        for (int j = 0; j < BN; j += 4) {
+          float x0, x1, x2, x3;
+          f2unpack(ffma2(f2pack(RA_S(j), RA_S(j + 1)), sl2x2, nmref2), x0, x1);
+          f2unpack(ffma2(f2pack(RA_S(j + 2), RA_S(j + 3)), sl2x2, nmref2), x2, x3);
+          const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
+          acc0 = fadd2(acc0, f2pack(p0, p1));
+          acc1 = fadd2(acc1, f2pack(p2, p3));
+          // pair k = j/2 goes to word k; k < j, so the scores it overwrites
+          // have already been read.
+          sr[(j / 2) >> 5][(j / 2) & 31] = bf16x2_rn(p0, p1);
+          sr[(j / 2 + 1) >> 5][(j / 2 + 1) & 31] = bf16x2_rn(p2, p3);
         }
-        l_run = l_run * alpha + (sum0 + sum1);
-        {
-          uint32_t r[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) r[j] = pk[j];
-          tmem_st32(tl + S_COL0 + b * BN, r);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) r[j] = pk[32 + j];
-          tmem_st32(tl + S_COL0 + b * BN + 32, r);
-        }
-        // PV(t-1) must have landed before O~ is touched and before PV(t)
+#undef RA_S
+        float sa, sb;
+        f2unpack(fadd2(acc0, acc1), sa, sb);
+        l_run = l_run * alpha + (sa + sb);
+        tmem_st32(tl + s_col, sr[0]);
+        tmem_st32(tl + s_col + 32, sr[1]);
+        // PV_g(t-1) must have landed before O~ is touched and before PV_g(t)
         // is released.  Waiting on every tile keeps this thread's count of
-        // the PV barrier's phases exact: at this point PV(t) is not issued
-        // yet, so at most PV(t-1) is outstanding and the parity test cannot
-        // alias.  PV(t-1) was issued when softmax(t) started, so the wait
-        // rarely blocks.
+        // the barrier's phases exact: PV_g(t) is not issued yet, so at most
+        // PV_g(t-1) is outstanding and the parity test cannot alias.
         if (t > 0) {
-          ok = wait_bar(bar(C::B_OD), static_cast<uint32_t>(t - 1) & 1u, abort_flag,
+          ok = wait_bar(bar(C::B_OD + g), static_cast<uint32_t>(t - 1) & 1u, abort_flag,
                         &g_umma_status, 0x32, lim);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
           tc_fence_after();
         }
         if (__any_sync(0xffffffffu, need)) {
-          // Rescale O~ in TMEM by alpha (1 for rows whose max did not move).
+          // Rescale O~ by alpha (1 for rows whose max did not move).
+          const uint64_t al2 = f2pack(alpha, alpha);
           uint32_t r[D / 32][32];
 #pragma unroll
-          for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(tl + O_COL + cc * 32, r[cc]);
+          for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(tl + o_col + cc * 32, r[cc]);
           tmem_wait_ld();
 #pragma unroll
           for (int cc = 0; cc < D / 32; ++cc) {
             reg_fence32(r[cc]);
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              r[cc][j] = __float_as_uint(__uint_as_float(r[cc][j]) * alpha);
-            tmem_st32(tl + O_COL + cc * 32, r[cc]);
+            for (int j = 0; j < 32; j += 2) {
+              float y0, y1;
+              f2unpack(fmul2(f2pack(__uint_as_float(r[cc][j]), __uint_as_float(r[cc][j + 1])),
+                             al2),
+                       y0, y1);
+              r[cc][j] = __float_as_uint(y0);
+              r[cc][j + 1] = __float_as_uint(y1);
+            }
+            tmem_st32(tl + o_col + cc * 32, r[cc]);
           }
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar(C::B_PF + b));
+        mbar_arrive(bar(C::B_PF + g));
       }
 
       if (ok) {
-        // PV(nt-1) is the only one that can still be outstanding.
-        ok = wait_bar(bar(C::B_OD), static_cast<uint32_t>(nt - 1) & 1u, abort_flag,
+        // PV_g(ntg-1) is the only one that can still be outstanding.
+        ok = wait_bar(bar(C::B_OD + g), static_cast<uint32_t>(ntg - 1) & 1u, abort_flag,
                       &g_umma_status, 0x33, lim);
         ok = __all_sync(0xffffffffu, ok);
       }
@@ -418,20 +450,21 @@ umma_update_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         tc_fence_after();
         // Canonical state: rescale once from m_used to the exact running max.
         const float fin = (m_used == m_true) ? 1.f : ex2(m_used - m_true);
+        uint32_t r[D / 32][32];
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(tl + o_col + cc * 32, r[cc]);
+        tmem_wait_ld();
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t r[32];
-          tmem_ld32(tl + O_COL + cc * 32, r);
-          tmem_wait_ld();
-          reg_fence32(r);
+          reg_fence32(r[cc]);
           if (valid) {
             float4* dst = reinterpret_cast<float4*>(a.o + sidx * D + cc * 32);
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-              dst[j] = make_float4(__uint_as_float(r[4 * j + 0]) * fin,
-                                   __uint_as_float(r[4 * j + 1]) * fin,
-                                   __uint_as_float(r[4 * j + 2]) * fin,
-                                   __uint_as_float(r[4 * j + 3]) * fin);
+              dst[j] = make_float4(__uint_as_float(r[cc][4 * j + 0]) * fin,
+                                   __uint_as_float(r[cc][4 * j + 1]) * fin,
+                                   __uint_as_float(r[cc][4 * j + 2]) * fin,
+                                   __uint_as_float(r[cc][4 * j + 3]) * fin);
           }
         }
         if (valid) {
@@ -442,11 +475,77 @@ umma_update_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     }
   }
 
+}
+
+template <int D>
+__global__ void __launch_bounds__(NTHREADS, 1)
+umma_update_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t s_base = smem_u32(smem);
+  const uint32_t sQ = s_base + C::OFF_Q;
+  const uint32_t sK = s_base + C::OFF_K;
+  const uint32_t sV = s_base + C::OFF_V;
+  const uint32_t bar0 = s_base + C::OFF_BAR;
+  auto bar = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const Work wk = decode_work(a, blockIdx.z);
+  // Under causal masking the later query rows carry more work, so they are
+  // launched first.
+  const int pair = a.causal ? static_cast<int>(gridDim.x - 1 - blockIdx.x)
+                            : static_cast<int>(blockIdx.x);
+  const long long row0 = static_cast<long long>(pair) * (NQ * BM);
+  int ntq[NQ];
+#pragma unroll
+  for (int g = 0; g < NQ; ++g) ntq[g] = tiles_for(a, wk, row0 + g * BM);
+  const int nt = ntq[0] > ntq[1] ? ntq[0] : ntq[1];
+
+  if (tid == 0) {
+    for (int i = 0; i < C::NBAR; ++i) {
+      const bool pf = i >= C::B_PF && i < C::B_PF + NQ;
+      mbar_init(bar(i), pf ? 128u : 1u);  // P_g: every thread of group g arrives
+    }
+    // A CTA that starts after another one of this launch gave up a wait
+    // does no work.
+    *abort_flag = *reinterpret_cast<volatile int*>(&g_umma_status) != 0 ? 1 : 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  __syncthreads();
+  if (*abort_flag) return;  // uniform across the CTA: read after the barrier
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // The role branches never merge again: each ends at named barrier 1 (all
+  // threads), after which the MMA warp frees TMEM.  Register budgets differ
+  // per branch.
+  if (warp >= 8) {
+    regs_dec<REGS_CONTROL>();
+    control_roles<D>(a, wk, row0, ntq, nt, tmem, sQ, sK, sV, bar0, abort_flag, &tmQ, &tmK, &tmV);
+    tc_fence_before();
+    named_bar_sync(1, NTHREADS);
+    if (warp == 9) {
+      tc_fence_after();
+      tmem_dealloc(tmem, TMEM_COLS);
+    }
+  } else {
+    regs_inc<REGS_SOFTMAX>();
+    softmax_role<D>(a, wk, row0, ntq, tmem, bar0, abort_flag);
+    tc_fence_before();
+    named_bar_sync(1, NTHREADS);
   }
 }
 
@@ -474,7 +573,7 @@ cudaError_t launch_d(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap&
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(C::SMEM_BYTES));
   if (e != cudaSuccess) return e;
-  dim3 grid(static_cast<unsigned>((a.c + BM - 1) / BM), a.heads, a.nwork);
+  dim3 grid(static_cast<unsigned>((a.c + NQ * BM - 1) / (NQ * BM)), a.heads, a.nwork);
   umma_update_kernel<D><<<grid, NTHREADS, C::SMEM_BYTES, st>>>(tq, tk, tv, a);
   return cudaGetLastError();
 }
