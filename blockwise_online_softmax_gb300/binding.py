@@ -51,6 +51,7 @@ _SIGNATURES = {
     "ra_ring_step": ("PPPPPPLiiiiiiiP", "i"),
     "ra_ring_forward": ("PPPPPLiiiiiiP", "i"),
     "ra_ring_forward_host": ("PPPPPLiiiiiiP", "i"),
+    "ra_ring_forward_noalloc": ("PPPPPLiiiiiiP", "i"),
     "ra_device_status": ("P", "i"),
     "ra_selftest_wait_timeout": ("LP", "i"),
     "ra_trace_enable": ("i", "i"),
@@ -199,6 +200,27 @@ def ra_ring_forward(q, k, v, *, P: int, causal: bool, out=None, lse=None, stream
         lse = torch.empty((N, heads), dtype=torch.float32, device=q.device)
     _state_shapes(lse, lse, out, N, heads, d)
     _check(lib().ra_ring_forward(
+        _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(out, "out", torch.float32),
+        _dev(lse, "lse", torch.float32), N, int(P), int(bool(causal)), d, heads, kv_heads,
+        _qkv_dtype(q), _stream(stream)))
+    return out, lse
+
+
+def ra_ring_forward_noalloc(q, k, v, *, P: int, causal: bool, out=None, lse=None,
+                            stream=None):
+    """ra_ring_forward with its l scratch in the library's fixed device array
+    (N * heads <= 4,194,304).  It calls no allocator inside the library.
+    The output tensors, when not passed in, are still created here by torch.
+    Calls that overlap on the GPU share that array and race."""
+    N, heads, kv_heads, d = _shapes(q, k, v)
+    if k.shape[0] != N:
+        raise ValueError("q, k and v must cover the same N tokens")
+    if out is None:
+        out = torch.empty((N, heads, d), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((N, heads), dtype=torch.float32, device=q.device)
+    _state_shapes(lse, lse, out, N, heads, d)
+    _check(lib().ra_ring_forward_noalloc(
         _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(out, "out", torch.float32),
         _dev(lse, "lse", torch.float32), N, int(P), int(bool(causal)), d, heads, kv_heads,
         _qkv_dtype(q), _stream(stream)))

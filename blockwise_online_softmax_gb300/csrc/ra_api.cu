@@ -230,6 +230,37 @@ int ring_forward_impl(const void* q, const void* k, const void* v, float* out, f
   return RA_OK;
 }
 
+// ----------------------------------------------------------------- fixed scratch
+// Scratch for ra_ring_forward_noalloc: the l state ([N, heads] fp32) of the
+// ring lives in this statically sized device array instead of memory taken
+// from an allocator.  The array is part of the library's device image, so
+// every GPU that loads libra.so holds its 16 MiB until the process exits.
+constexpr long long kNoAllocMaxRowsHeads = 1LL << 22;  // N * heads <= 4,194,304
+static __device__ __align__(256) float g_noalloc_l[kNoAllocMaxRowsHeads];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+float* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of g_noalloc_l on the current device.  Host code only sees
+// a host-side stand-in for the symbol, so the address must be looked up;
+// this happens once per device, with that device current.
+int noalloc_scratch(float** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(RA_ERR_UNSUPPORTED, "device ordinal %d >= %d", dev, kMaxDevices);
+  std::lock_guard<std::mutex> g(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_l);
+    if (e != cudaSuccess || !p) return cuda_fail(e, "cudaGetSymbolAddress of the fixed scratch");
+    g_noalloc_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return RA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -404,6 +435,26 @@ int ra_ring_forward_host(const void* q_host, const void* k_host, const void* v_h
   const int st_rc = ra_device_status(stream);
   if (rc != RA_OK) return rc;
   return st_rc;
+}
+
+int ra_ring_forward_noalloc(const void* q, const void* k, const void* v, float* out, float* lse,
+                            long long N, int P, int causal, int d, int heads, int kv_heads,
+                            int dtype, void* stream) {
+  int rc = ring_args_check(q, k, v, N, P, 0, d, heads, kv_heads, dtype);
+  if (rc != RA_OK) return rc;
+  if (N == 0) return RA_OK;
+  if ((rc = check_ptrs({q, k, v, out, lse})) != RA_OK) return rc;
+  if (N * heads > kNoAllocMaxRowsHeads)
+    return fail(RA_ERR_UNSUPPORTED,
+                "N * heads = %lld exceeds the fixed scratch of ra_ring_forward_noalloc (%lld "
+                "rows x heads); use ra_ring_forward",
+                N * heads, kNoAllocMaxRowsHeads);
+  float* l_scratch = nullptr;
+  if ((rc = noalloc_scratch(&l_scratch)) != RA_OK) return rc;
+  // The state-init kernel zeroes the l rows this call uses, so whatever a
+  // previous call left in the array does not matter.
+  return ring_forward_impl(q, k, v, out, lse, N, P, causal, d, heads, kv_heads, dtype,
+                           static_cast<cudaStream_t>(stream), l_scratch);
 }
 
 int ra_device_status(void* stream) {

@@ -185,6 +185,32 @@ int ra_ring_forward_host(const void* q_host, const void* k_host, const void* v_h
                          int heads, int kv_heads, int dtype, void* stream);
 
 /*
+ * ra_ring_forward_noalloc -- ra_ring_forward for callers that cannot let the
+ * library allocate device memory.  Examples: an application that reserves
+ * the whole GPU for its own memory pool, where a cudaMalloc from inside the
+ * library would fail or break the pool's accounting; or one that must fix
+ * its peak device footprint before it starts.  The pages have no
+ * counterpart to this call; it is a deployment convenience.
+ *   Arguments, layouts and results are those of ra_ring_forward.  The l
+ *   state lives in a fixed 16 MiB device array that is part of the library
+ *   (N * heads <= 4,194,304 fp32 entries), instead of memory from
+ *   cudaMallocAsync.  Every GPU that loads the library holds that array until
+ *   the process exits.  The call calls no cudaMalloc, cudaFree or other
+ *   allocating routine.
+ *   Larger problems return RA_ERR_UNSUPPORTED; use ra_ring_forward for them.
+ *   The first call on a device looks up the array's device address once,
+ *   with that device current.  Make that first call before any stream
+ *   capture starts.
+ *   All calls share the one array.  Each call clears the rows it uses
+ *   first, so what an earlier call left there does not matter.  But two
+ *   calls that overlap on the GPU (different streams, not ordered) race on
+ *   the array and both results are undefined.
+ */
+int ra_ring_forward_noalloc(const void* q, const void* k, const void* v, float* out, float* lse,
+                            long long N, int P, int causal, int d, int heads, int kv_heads,
+                            int dtype, void* stream);
+
+/*
  * ra_device_status -- synchronize `stream`, then read and clear the
  * library's device-side error words.  Every mbarrier wait in the kernels is
  * bounded.  A wait that runs out records a code and makes its CTA leave
