@@ -47,23 +47,31 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity)
 // the CTA's abort flag and returns false.  With status == null the wait
 // only ends on completion or on the cycle limit (used to drain copies).  It
 // never traps.
+//
+// One flat loop: the flags and the clock are read only every 64 probes,
+// and the clock baseline is taken at the first such check.  An
+// already-completed phase therefore costs about a probe plus a branch.
+// Nested loops or a separate probe in front cost about three times more
+// on this path, which the MMA issuer takes several times per K/V tile.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                          int* status, int code, long long limit) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  for (;;) {
-#pragma unroll 1
-    for (int i = 0; i < 16; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (status && *reinterpret_cast<volatile int*>(status) != 0) {
-      *abort_flag = 1;
-      return false;
-    }
-    if (clock64() - t0 > limit) {
-      if (status) atomicCAS(status, 0, code);
-      *abort_flag = 1;
-      return false;
+  long long t0 = 0;
+  for (uint32_t n = 0;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 63u) == 63u) {
+      if (*abort_flag) return false;
+      if (status && *reinterpret_cast<volatile int*>(status) != 0) {
+        *abort_flag = 1;
+        return false;
+      }
+      const long long now = clock64();
+      if (n == 63u) {
+        t0 = now;
+      } else if (now - t0 > limit) {
+        if (status) atomicCAS(status, 0, code);
+        *abort_flag = 1;
+        return false;
+      }
     }
   }
 }
@@ -135,6 +143,39 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Warp-uniform forms: every lane of the issuing warp executes them, and the
+// instruction is predicated on `leader` (nonzero on exactly one lane).  The
+// issuing warp then never diverges around its MMAs and commits.
+__device__ __forceinline__ void mma_ss_lead(uint32_t leader, uint32_t d_tmem, uint64_t adesc,
+                                            uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.ne.b32 q, %5, 0;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(leader)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_lead(uint32_t leader, uint32_t d_tmem, uint32_t a_tmem,
+                                            uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.ne.b32 q, %5, 0;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(leader)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit_lead(uint32_t leader, uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\t"
+      "setp.ne.b32 q, %1, 0;\n\t"
+      "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          bar),
+      "r"(leader)
+      : "memory");
+}
+
 // Same, with A read from tensor memory.
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
                                        uint32_t idesc, uint32_t accumulate) {

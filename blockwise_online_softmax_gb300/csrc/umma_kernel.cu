@@ -13,18 +13,20 @@
 //   warps 0..3  softmax group 0: one thread per row of Q0 (TMEM lane
 //               32*warp+lane).
 //   warps 4..7  softmax group 1: the same for Q1.
-//   warp 8      TMA producer.  It loads Q0 and Q1 once, then K and V tiles
-//               into an NST-deep ring of shared-memory stages.
+//   warp 8      TMA producer for Q0, Q1 (once) and the K tiles.
 //   warp 9      Allocates TMEM.  Lane 0 issues every tcgen05.mma.
-//   warps 10-11 idle.
+//   warp 10     TMA producer for the V tiles.
+//   warp 11     idle.
+// K and V stream through separate rings of shared-memory stages (2 and 3
+// deep at d = 128).
 // A softmax thread reads its S row from TMEM, takes the row max,
 // exponentiates, writes P back as bf16 over its S row, rescales its O~ row
 // in TMEM when the max grows, and loads and stores the state.
 //
 // Registers: the CTA launches with 168 per thread (three warps share each
 // SM sub-partition's 16K registers).  The producer/MMA warpgroup then gives
-// back down to 56, and the softmax warpgroups take up to 224 (setmaxnreg).
-// 2*128*224 + 128*56 = 384*168.
+// some back and the softmax warpgroups take them (setmaxnreg): 216/72 at
+// d = 128 and 224/56 at d = 64, with 2*128*softmax + 128*control = 384*168.
 //
 // TMEM columns: S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [256+D,256+2D).
 // P_g overwrites the first 64 columns of S_g, two bf16 per 32-bit column,
@@ -68,10 +70,6 @@ constexpr int NQ = 2;    // query tiles per CTA
 constexpr int BN = 128;  // keys per K/V tile
 constexpr int NTHREADS = (NQ + 1) * 128;
 constexpr uint32_t REGS_LAUNCH = 168;
-constexpr uint32_t REGS_SOFTMAX = 224;
-constexpr uint32_t REGS_CONTROL = 56;
-static_assert(NQ * 128 * REGS_SOFTMAX + 128 * REGS_CONTROL == NTHREADS * REGS_LAUNCH,
-              "setmaxnreg split must add up to the launch allocation");
 constexpr uint32_t CHUNK_BYTES = 128 * 128;  // 128 rows x 128 B (one swizzle span)
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_THRESHOLD = 0.0f;  // log2 units; see the rescale rule above
@@ -80,27 +78,38 @@ template <int D>
 struct Cfg {
   static constexpr int NCH = D / 64;                  // 128-byte chunks per row
   static constexpr uint32_t TILE_BYTES = BM * D * 2;  // one Q, K or V tile
-  static constexpr int NST = (D == 64) ? 4 : 2;       // K/V stages
+  // K and V stage counts (192 KB of shared memory in all at d = 128).  A
+  // third V stage fits in 227 KB but measured slower: the L1 share of the
+  // unified SRAM drops too far for the state loads and stores.
+  static constexpr int NSK = (D == 64) ? 4 : 2;
+  static constexpr int NSV = (D == 64) ? 4 : 2;
   static constexpr uint32_t S_COL = 0;                // S_g at S_COL + g * BN
   static constexpr uint32_t O_COL = 2 * BN;           // O_g at O_COL + g * D
   // barriers
   static constexpr int B_Q = 0;
   static constexpr int B_KF = 1;
-  static constexpr int B_KE = B_KF + NST;
-  static constexpr int B_VF = B_KE + NST;
-  static constexpr int B_VE = B_VF + NST;
-  static constexpr int B_SF = B_VE + NST;  // NQ: QK_g done
-  static constexpr int B_PF = B_SF + NQ;   // NQ: P_g written (128 arrivals)
-  static constexpr int B_OD = B_PF + NQ;   // NQ: PV_g done
+  static constexpr int B_KE = B_KF + NSK;
+  static constexpr int B_VF = B_KE + NSK;
+  static constexpr int B_VE = B_VF + NSV;
+  static constexpr int B_SF = B_VE + NSV;     // NQ: QK_g done
+  static constexpr int B_PF = B_SF + NQ;  // NQ: P_g written (128 arrivals)
+  static constexpr int B_OD = B_PF + NQ;  // NQ: last PV_g done
   static constexpr int B_DRAIN = B_OD + NQ;
   static constexpr int NBAR = B_DRAIN + 1;
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = OFF_Q + NQ * TILE_BYTES;
-  static constexpr uint32_t OFF_V = OFF_K + NST * TILE_BYTES;
-  static constexpr uint32_t OFF_BAR = OFF_V + NST * TILE_BYTES;
+  static constexpr uint32_t OFF_V = OFF_K + NSK * TILE_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_V + NSV * TILE_BYTES;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
   static_assert(O_COL + NQ * D <= TMEM_COLS, "TMEM budget");
+  // setmaxnreg split of the launch allocation (the best split, without
+  // spills, differs with d).
+  static constexpr uint32_t REGS_SOFTMAX = (D == 64) ? 224 : 216;
+  static constexpr uint32_t REGS_CONTROL = (D == 64) ? 56 : 72;
+  static_assert(NQ * 128 * REGS_SOFTMAX + 128 * REGS_CONTROL == NTHREADS * REGS_LAUNCH,
+                "setmaxnreg split must add up to the launch allocation");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget (227 KB per CTA)");
 };
 
 // Number of K/V tiles holding a key that some row of the query tile
@@ -117,7 +126,41 @@ __device__ __forceinline__ int tiles_for(const FwdArgs& a, const Work& wk, long 
   return static_cast<int>(n < kv_tiles ? n : kv_tiles);
 }
 
-// Producer (warp 8) and MMA issuer (warp 9); warps 10 and 11 fall through.
+// Streams the nt K (or V) tiles of the block into an NST-deep ring of
+// shared-memory stages; full/empty are the first stage's barriers.  Returns
+// false on an abort, after draining (bounded) the copies still in flight.
+template <int D, int NST>
+__device__ __forceinline__ bool produce_tiles(const Work& wk, int nt, int kh, uint32_t sbase,
+                                              uint32_t b_full, uint32_t b_empty,
+                                              const CUtensorMap* tm, volatile int* abort_flag,
+                                              int code, long long lim) {
+  using C = Cfg<D>;
+  tma_prefetch_desc(tm);
+  int issued = 0;
+  bool ok = true;
+  for (int t = 0; t < nt; ++t) {
+    const int st = t % NST;
+    const uint32_t ph = static_cast<uint32_t>(t / NST) & 1u;
+    const int kv_row = static_cast<int>(wk.kv_base + static_cast<long long>(t) * BN);
+    if (t >= NST) ok = wait_bar(b_empty + 8u * st, ph ^ 1u, abort_flag, &g_umma_status, code, lim);
+    if (!ok) break;
+    mbar_arrive_expect_tx(b_full + 8u * st, C::TILE_BYTES);
+#pragma unroll
+    for (int ch = 0; ch < C::NCH; ++ch)
+      tma_load_3d(sbase + st * C::TILE_BYTES + ch * CHUNK_BYTES, tm, b_full + 8u * st, ch * 64, kh,
+                  kv_row);
+    issued = t + 1;
+  }
+  if (!ok) {
+    volatile int no_abort = 0;
+    for (int t = (issued > NST ? issued - NST : 0); t < issued; ++t)
+      wait_bar(b_full + 8u * (t % NST), static_cast<uint32_t>(t / NST) & 1u, &no_abort, nullptr,
+               0, lim);
+  }
+  return ok;
+}
+
+// Producers (warps 8 and 10) and MMA issuer (warp 9); warp 11 falls through.
 template <int D>
 __device__ __forceinline__ void control_roles(const FwdArgs& a, const Work& wk, long long row0,
                                               const int (&ntq)[NQ], int nt, uint32_t tmem,
@@ -132,92 +175,77 @@ __device__ __forceinline__ void control_roles(const FwdArgs& a, const Work& wk, 
   const int kh = h / (a.heads / a.kv_heads);
   const long long lim = a.wait_limit;
   auto bar = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
-  if (warp == 8) {
-    // ------------------------------------------------------------ producer
+  if (warp == 8 || warp == 10) {
+    // ------------------------------------------------------------ producers
+    // Warp 8 loads Q0, Q1 and the K tiles; warp 10 loads the V tiles.  Each
+    // waits only on its own stages, so a V stage still held by the PV
+    // products never delays a K load.
     if (lane == 0 && nt > 0) {
-      tma_prefetch_desc(tmQ);
-      tma_prefetch_desc(tmK);
-      tma_prefetch_desc(tmV);
-      mbar_arrive_expect_tx(bar(C::B_Q), NQ * C::TILE_BYTES);
+      if (warp == 8) {
+        tma_prefetch_desc(tmQ);
+        mbar_arrive_expect_tx(bar(C::B_Q), NQ * C::TILE_BYTES);
 #pragma unroll
-      for (int g = 0; g < NQ; ++g) {
-        const int q_row = static_cast<int>(wk.q_base + row0 + g * BM);
+        for (int g = 0; g < NQ; ++g) {
+          const int q_row = static_cast<int>(wk.q_base + row0 + g * BM);
 #pragma unroll
-        for (int ch = 0; ch < C::NCH; ++ch)
-          tma_load_3d(sQ + g * C::TILE_BYTES + ch * CHUNK_BYTES, tmQ, bar(C::B_Q), ch * 64, h,
-                      q_row);
-      }
-      int issued_k = 0, issued_v = 0;
-      bool ok = true;
-      for (int t = 0; t < nt; ++t) {
-        const int st = t % C::NST;
-        const uint32_t ph = static_cast<uint32_t>(t / C::NST) & 1u;
-        const int kv_row = static_cast<int>(wk.kv_base + static_cast<long long>(t) * BN);
-        if (t >= C::NST)
-          ok = wait_bar(bar(C::B_KE + st), ph ^ 1u, abort_flag, &g_umma_status, 0x11, lim);
-        if (!ok) break;
-        mbar_arrive_expect_tx(bar(C::B_KF + st), C::TILE_BYTES);
-#pragma unroll
-        for (int ch = 0; ch < C::NCH; ++ch)
-          tma_load_3d(sK + st * C::TILE_BYTES + ch * CHUNK_BYTES, tmK, bar(C::B_KF + st),
-                      ch * 64, kh, kv_row);
-        issued_k = t + 1;
-        if (t >= C::NST)
-          ok = wait_bar(bar(C::B_VE + st), ph ^ 1u, abort_flag, &g_umma_status, 0x12, lim);
-        if (!ok) break;
-        mbar_arrive_expect_tx(bar(C::B_VF + st), C::TILE_BYTES);
-#pragma unroll
-        for (int ch = 0; ch < C::NCH; ++ch)
-          tma_load_3d(sV + st * C::TILE_BYTES + ch * CHUNK_BYTES, tmV, bar(C::B_VF + st),
-                      ch * 64, kh, kv_row);
-        issued_v = t + 1;
-      }
-      if (!ok) {
-        // Drain: wait (bounded) for copies still in flight before the CTA's
-        // shared memory is released.
-        volatile int no_abort = 0;
-        wait_bar(bar(C::B_Q), 0, &no_abort, nullptr, 0, lim);
-        for (int t = (issued_k > C::NST ? issued_k - C::NST : 0); t < issued_k; ++t)
-          wait_bar(bar(C::B_KF + t % C::NST), static_cast<uint32_t>(t / C::NST) & 1u, &no_abort,
-                   nullptr, 0, lim);
-        for (int t = (issued_v > C::NST ? issued_v - C::NST : 0); t < issued_v; ++t)
-          wait_bar(bar(C::B_VF + t % C::NST), static_cast<uint32_t>(t / C::NST) & 1u, &no_abort,
-                   nullptr, 0, lim);
+          for (int ch = 0; ch < C::NCH; ++ch)
+            tma_load_3d(sQ + g * C::TILE_BYTES + ch * CHUNK_BYTES, tmQ, bar(C::B_Q), ch * 64, h,
+                        q_row);
+        }
+        if (!produce_tiles<D, C::NSK>(wk, nt, kh, sK, bar(C::B_KF), bar(C::B_KE), tmK, abort_flag,
+                                      0x11, lim)) {
+          volatile int no_abort = 0;
+          wait_bar(bar(C::B_Q), 0, &no_abort, nullptr, 0, lim);
+        }
+      } else {
+        produce_tiles<D, C::NSV>(wk, nt, kh, sV, bar(C::B_VF), bar(C::B_VE), tmV, abort_flag, 0x12,
+                                 lim);
       }
     }
     __syncwarp();
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && nt > 0) {
+    // The whole warp runs this loop in step; the MMAs and commits are
+    // predicated on lane 0 inside their asm, so the warp never diverges.
+    // Every wait below reads the same barrier state on all lanes, so the
+    // outcome is warp-uniform.
+    const uint32_t lead = lane == 0 ? 1u : 0u;
+    if (nt > 0) {
       constexpr uint32_t idesc_qk = idesc_bf16(BM, BN, 0);
       constexpr uint32_t idesc_pv = idesc_bf16(BM, D, 1);
-      auto qk = [&](int g, int st) {
+      // All shared-memory descriptors are built once.  Moving a descriptor's
+      // start address by `off` bytes adds off >> 4 to it (the field cannot
+      // carry out, since shared addresses are below 256 KB).
+      const uint64_t qdesc = sdesc_sw128(sQ, 16, 1024);
+      const uint64_t kdesc = sdesc_sw128(sK, 16, 1024);
+      const uint64_t vdesc = sdesc_sw128(sV, CHUNK_BYTES, 1024);
+      constexpr uint64_t TILE16 = C::TILE_BYTES >> 4;  // one tile, in descriptor units
+      auto qk = [&](int g, int sk) {
         const uint32_t d_tmem = tmem + C::S_COL + static_cast<uint32_t>(g) * BN;
-        const uint32_t qbase = sQ + g * C::TILE_BYTES;
-        const uint32_t kbase = sK + st * C::TILE_BYTES;
+        const uint64_t a0 = qdesc + static_cast<uint64_t>(g) * TILE16;
+        const uint64_t b0 = kdesc + static_cast<uint64_t>(sk) * TILE16;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           // K-major, 128-byte swizzle: 16 elements = 32 bytes along a row;
           // every 4 steps move to the next 64-wide column chunk.
-          const uint32_t off = (kk >> 2) * CHUNK_BYTES + (kk & 3) * 32;
-          mma_ss(d_tmem, sdesc_sw128(qbase + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
-                 idesc_qk, kk > 0 ? 1u : 0u);
+          const uint64_t off = ((kk >> 2) * CHUNK_BYTES + (kk & 3) * 32) >> 4;
+          mma_ss_lead(lead, d_tmem, a0 + off, b0 + off, idesc_qk, kk > 0 ? 1u : 0u);
         }
-        tc_commit(bar(C::B_SF + g));
+        tc_commit_lead(lead, bar(C::B_SF + g));
       };
-      auto pv = [&](int g, int st) {
+      // O_g += P_g V over the 128 keys of the tile.
+      auto pv = [&](int g, int sv) {
         const uint32_t p_tmem = tmem + C::S_COL + static_cast<uint32_t>(g) * BN;
         const uint32_t o_tmem = tmem + C::O_COL + static_cast<uint32_t>(g) * D;
-        const uint32_t vbase = sV + st * C::TILE_BYTES;
+        const uint64_t b0 = vdesc + static_cast<uint64_t>(sv) * TILE16;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
           // P: two bf16 per 32-bit TMEM column, 8 columns per 16 keys.
           // V (MN-major, 128-byte swizzle): 16 keys = two 8-row groups of
           // 1024 B (SBO); the 64-wide column chunks sit CHUNK_BYTES apart (LBO).
-          mma_ts(o_tmem, p_tmem + kk * 8, sdesc_sw128(vbase + kk * 2048, CHUNK_BYTES, 1024),
-                 idesc_pv, 1u);
+          mma_ts_lead(lead, o_tmem, p_tmem + kk * 8,
+                      b0 + static_cast<uint64_t>((kk * 2048) >> 4), idesc_pv, 1u);
         }
-        tc_commit(bar(C::B_OD + g));
       };
       bool ok = wait_bar(bar(C::B_Q), 0, abort_flag, &g_umma_status, 0x21, lim);
       if (ok) ok = wait_bar(bar(C::B_KF), 0, abort_flag, &g_umma_status, 0x22, lim);
@@ -225,15 +253,19 @@ __device__ __forceinline__ void control_roles(const FwdArgs& a, const Work& wk, 
         tc_fence_after();
         if (ntq[0] > 0) qk(0, 0);
         if (ntq[1] > 0) qk(1, 0);
-        tc_commit(bar(C::B_KE));
+        tc_commit_lead(lead, bar(C::B_KE));
       }
       for (int t = 0; t < nt && ok; ++t) {
-        const int st = t % C::NST;
-        const int st1 = (t + 1) % C::NST;
-        ok = wait_bar(bar(C::B_VF + st), static_cast<uint32_t>(t / C::NST) & 1u, abort_flag,
+        const int sv = t % C::NSV;
+        const int sk1 = (t + 1) % C::NSK;
+        // Both operand tiles of this iteration first, so the PV and QK
+        // products of a group issue back to back.
+        ok = wait_bar(bar(C::B_VF + sv), static_cast<uint32_t>(t / C::NSV) & 1u, abort_flag,
                       &g_umma_status, 0x24, lim);
+        if (ok && t + 1 < nt)
+          ok = wait_bar(bar(C::B_KF + sk1), static_cast<uint32_t>((t + 1) / C::NSK) & 1u,
+                        abort_flag, &g_umma_status, 0x22, lim);
         if (!ok) break;
-        bool k_ready = false;
 #pragma unroll
         for (int g = 0; g < NQ; ++g) {
           if (t < ntq[g]) {
@@ -241,26 +273,21 @@ __device__ __forceinline__ void control_roles(const FwdArgs& a, const Work& wk, 
                           &g_umma_status, 0x23, lim);
             if (!ok) break;
             tc_fence_after();
-            pv(g, st);
+            pv(g, sv);
+            // Only the epilogue waits for PV_g: each tile's softmax already
+            // knows PV_g(t-1) is done from S_g(t).  So only the last product
+            // of the group is signalled.
+            if (t + 1 == ntq[g]) tc_commit_lead(lead, bar(C::B_OD + g));
           }
-          if (t + 1 < ntq[g]) {
-            if (!k_ready) {
-              ok = wait_bar(bar(C::B_KF + st1), static_cast<uint32_t>((t + 1) / C::NST) & 1u,
-                            abort_flag, &g_umma_status, 0x22, lim);
-              if (!ok) break;
-              tc_fence_after();
-              k_ready = true;
-            }
-            qk(g, st1);
-          }
+          if (t + 1 < ntq[g]) qk(g, sk1);
         }
         if (!ok) break;
-        tc_commit(bar(C::B_VE + st));
-        if (t + 1 < nt) tc_commit(bar(C::B_KE + st1));
+        tc_commit_lead(lead, bar(C::B_VE + sv));
+        if (t + 1 < nt) tc_commit_lead(lead, bar(C::B_KE + sk1));
       }
       // Drain every MMA issued so far before TMEM can be freed.
       volatile int no_abort = 0;
-      tc_commit(bar(C::B_DRAIN));
+      tc_commit_lead(lead, bar(C::B_DRAIN));
       wait_bar(bar(C::B_DRAIN), 0, &no_abort, nullptr, 0, lim);
     }
     __syncwarp();
@@ -377,6 +404,30 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, const Work& wk, l
           alpha = ex2(m_used - m_true);  // m_used = -inf gives 0
           m_used = m_true;
         }
+        // O~_g is stable here: S_g(t) comes from QK_g(t), which the MMA thread
+        // issued after PV_g(t-1), and the commit that signalled S_g(t)
+        // covers every earlier MMA.  Rescale it before any of P_g(t) is
+        // published, since PV_g(t) accumulates on top.
+        if (__any_sync(0xffffffffu, need)) {
+          // 32 columns at a time: the S row still occupies 128 registers.
+          const uint64_t al2 = f2pack(alpha, alpha);
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t r[32];
+            tmem_ld32(tl + o_col + cc * 32, r);
+            tmem_wait_ld();
+            reg_fence32(r);
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              float y0, y1;
+              f2unpack(fmul2(f2pack(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), al2), y0,
+                       y1);
+              r[j] = __float_as_uint(y0);
+              r[j + 1] = __float_as_uint(y1);
+            }
+            tmem_st32(tl + o_col + cc * 32, r);
+          }
+        }
         const float mref = (m_used == -INFINITY) ? 0.f : m_used;
         const uint64_t nmref2 = f2pack(-mref, -mref);
         // P = 2^(s * log2(e)/sqrt(d) - m), two lanes per FFMA2; row sum in
@@ -396,54 +447,20 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, const Work& wk, l
           sr[(j / 2) >> 5][(j / 2) & 31] = bf16x2_rn(p0, p1);
           sr[(j / 2 + 1) >> 5][(j / 2 + 1) & 31] = bf16x2_rn(p2, p3);
         }
+        tmem_st32(tl + s_col, sr[0]);
+        tmem_st32(tl + s_col + 32, sr[1]);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(C::B_PF + g));
 #undef RA_S
         float sa, sb;
         f2unpack(fadd2(acc0, acc1), sa, sb);
         l_run = l_run * alpha + (sa + sb);
-        tmem_st32(tl + s_col, sr[0]);
-        tmem_st32(tl + s_col + 32, sr[1]);
-        // PV_g(t-1) must have landed before O~ is touched and before PV_g(t)
-        // is released.  Waiting on every tile keeps this thread's count of
-        // the barrier's phases exact: PV_g(t) is not issued yet, so at most
-        // PV_g(t-1) is outstanding and the parity test cannot alias.
-        if (t > 0) {
-          ok = wait_bar(bar(C::B_OD + g), static_cast<uint32_t>(t - 1) & 1u, abort_flag,
-                        &g_umma_status, 0x32, lim);
-          ok = __all_sync(0xffffffffu, ok);
-          if (!ok) break;
-          tc_fence_after();
-        }
-        if (__any_sync(0xffffffffu, need)) {
-          // Rescale O~ by alpha (1 for rows whose max did not move).
-          const uint64_t al2 = f2pack(alpha, alpha);
-          uint32_t r[D / 32][32];
-#pragma unroll
-          for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(tl + o_col + cc * 32, r[cc]);
-          tmem_wait_ld();
-#pragma unroll
-          for (int cc = 0; cc < D / 32; ++cc) {
-            reg_fence32(r[cc]);
-#pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              float y0, y1;
-              f2unpack(fmul2(f2pack(__uint_as_float(r[cc][j]), __uint_as_float(r[cc][j + 1])),
-                             al2),
-                       y0, y1);
-              r[cc][j] = __float_as_uint(y0);
-              r[cc][j + 1] = __float_as_uint(y1);
-            }
-            tmem_st32(tl + o_col + cc * 32, r[cc]);
-          }
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar(C::B_PF + g));
       }
 
       if (ok) {
-        // PV_g(ntg-1) is the only one that can still be outstanding.
-        ok = wait_bar(bar(C::B_OD + g), static_cast<uint32_t>(ntg - 1) & 1u, abort_flag,
-                      &g_umma_status, 0x33, lim);
+        // The one commit on B_OD + g follows PV_g(ntg-1), the last product.
+        ok = wait_bar(bar(C::B_OD + g), 0u, abort_flag, &g_umma_status, 0x33, lim);
         ok = __all_sync(0xffffffffu, ok);
       }
       if (ok) {
@@ -533,7 +550,7 @@ umma_update_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   // threads), after which the MMA warp frees TMEM.  Register budgets differ
   // per branch.
   if (warp >= 8) {
-    regs_dec<REGS_CONTROL>();
+    regs_dec<C::REGS_CONTROL>();
     control_roles<D>(a, wk, row0, ntq, nt, tmem, sQ, sK, sV, bar0, abort_flag, &tmQ, &tmK, &tmV);
     tc_fence_before();
     named_bar_sync(1, NTHREADS);
@@ -542,7 +559,7 @@ umma_update_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       tmem_dealloc(tmem, TMEM_COLS);
     }
   } else {
-    regs_inc<REGS_SOFTMAX>();
+    regs_inc<C::REGS_SOFTMAX>();
     softmax_role<D>(a, wk, row0, ntq, tmem, bar0, abort_flag);
     tc_fence_before();
     named_bar_sync(1, NTHREADS);
