@@ -58,15 +58,15 @@ def _load():
         if _lib is None:
             build_library()
             lib = ctypes.CDLL(_LIB_PATH)
-            f = lib.oracle_partial_state
+            f = lib.oracle_partial_state_masked
             P = ctypes.c_void_p
             LL = ctypes.c_longlong
             f.argtypes = [P, P, P, ctypes.c_int, LL, LL, ctypes.c_int, ctypes.c_int,
-                          ctypes.c_int, ctypes.c_double, ctypes.c_int, P, P, P, LL, P, P, P,
-                          ctypes.c_int]
+                          ctypes.c_int, ctypes.c_double, ctypes.c_int, LL, P, P, P, P, P, LL,
+                          P, P, P, ctypes.c_int]
             f.restype = ctypes.c_int
             lib.oracle_abi_version.restype = ctypes.c_int
-            if lib.oracle_abi_version() != 1:
+            if lib.oracle_abi_version() != 2:
                 raise RuntimeError("liboracle.so is stale; rebuild it")
             _lib = lib
     return _lib
@@ -94,14 +94,19 @@ def _as_input(x):
 
 
 def partial_state(q, k, v, *, causal: bool, q_pos=None, k_pos=None, rows=None,
-                  scale: float | None = None, threads: int | None = None):
+                  scale: float | None = None, threads: int | None = None, window: int = 0,
+                  q_doc=None, k_doc=None):
     """Partial online-softmax state of query rows against a key set, in fp64.
 
     q: [nq, hq, d]; k, v: [nk, hkv, d] (token-major).  ``q_pos``/``k_pos``
     are global token positions (default: the index).  ``rows`` selects the
-    query rows (default: all).  Returns ``(m, l, o)`` of shapes
-    ``[nrows, hq]``, ``[nrows, hq]`` and ``[nrows, hq, d]``, as defined in
-    ``attention.c``.  The default scale is 1/sqrt(d).
+    query rows (default: all).  ``window`` > 0 allows only keys with
+    |q_pos - k_pos| < window.  ``q_doc``/``k_doc`` are per-row document ids
+    (both or neither); a key is allowed only within its query's document,
+    and id -1 marks a padding row that sees and is seen by nothing.
+    Returns ``(m, l, o)`` of shapes ``[nrows, hq]``, ``[nrows, hq]`` and
+    ``[nrows, hq, d]``, as defined in ``attention.c``.  The default scale is
+    1/sqrt(d).
     """
     qa, dt = _as_input(q)
     ka, dk = _as_input(k)
@@ -123,6 +128,12 @@ def partial_state(q, k, v, *, causal: bool, q_pos=None, k_pos=None, rows=None,
         raise ValueError("q_pos must have one entry per query row")
     if kp is not None and kp.shape != (nk,):
         raise ValueError("k_pos must have one entry per key")
+    if (q_doc is None) != (k_doc is None):
+        raise ValueError("give both q_doc and k_doc, or neither")
+    qd = None if q_doc is None else np.ascontiguousarray(np.asarray(q_doc, dtype=np.int64))
+    kd = None if k_doc is None else np.ascontiguousarray(np.asarray(k_doc, dtype=np.int64))
+    if qd is not None and (qd.shape != (nq,) or kd.shape != (nk,)):
+        raise ValueError("q_doc / k_doc must have one entry per row")
     if scale is None:
         scale = 1.0 / np.sqrt(d)
     if threads is None:
@@ -135,23 +146,26 @@ def partial_state(q, k, v, *, causal: bool, q_pos=None, k_pos=None, rows=None,
     def ptr(a):
         return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
-    rc = _load().oracle_partial_state(
+    rc = _load().oracle_partial_state_masked(
         ptr(qa), ptr(ka), ptr(va), dt, nq, nk, hq, hkv, d, float(scale), int(bool(causal)),
-        ptr(qp), ptr(kp), ptr(rows), nr, ptr(m), ptr(l), ptr(o), int(threads))
+        int(window), ptr(qp), ptr(kp), ptr(qd), ptr(kd), ptr(rows), nr, ptr(m), ptr(l), ptr(o),
+        int(threads))
     if rc != 0:
         raise ValueError(f"oracle_partial_state failed with code {rc}")
     return m, l, o
 
 
 def attention(q, k, v, *, causal: bool, q_pos=None, k_pos=None, rows=None,
-              scale: float | None = None, threads: int | None = None):
+              scale: float | None = None, threads: int | None = None, window: int = 0,
+              q_doc=None, k_doc=None):
     """Dense attention O = softmax(q k^T * scale) v and its row log-sum-exp.
 
     Returns ``(O [nrows, hq, d], LSE [nrows, hq])`` in fp64.  A row with no
     allowed key gets O = 0 and LSE = -inf.
     """
     m, l, o = partial_state(q, k, v, causal=causal, q_pos=q_pos, k_pos=k_pos, rows=rows,
-                            scale=scale, threads=threads)
+                            scale=scale, threads=threads, window=window, q_doc=q_doc,
+                            k_doc=k_doc)
     with np.errstate(divide="ignore", invalid="ignore"):
         out = np.where(l[..., None] > 0, o / np.where(l > 0, l, 1.0)[..., None], 0.0)
         lse = np.where(l > 0, m + np.log(np.where(l > 0, l, 1.0)), -np.inf)

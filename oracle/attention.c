@@ -20,11 +20,16 @@
  *   l = sum_t exp(s_rt - m)
  *   o = sum_t exp(s_rt - m) v_t    (a vector of length d)
  * where s_rt = (q_r . k_t) * scale.  Key t is allowed for row r unless
- * `causal` is set and k_pos[t] > q_pos[r].  Causal masking on global token
- * positions follows "Ring Attention：把超长序列沿设备环流动", section
- * "位置编码必须使用全局位置" (positions are global, device p local index i
- * maps to p * N_local + i).  A row with no allowed key returns m = -inf,
- * l = 0, o = 0.
+ *   - `causal` is set and k_pos[t] > q_pos[r], or
+ *   - `window` > 0 and |q_pos[r] - k_pos[t]| >= window, or
+ *   - document ids are given and q_doc[r] < 0 or k_doc[t] != q_doc[r].
+ * Causal masking on global token positions follows "Ring Attention：把超长
+ * 序列沿设备环流动", section "位置编码必须使用全局位置" (positions are
+ * global, device p local index i maps to p * N_local + i).  The window, the
+ * packed documents that must not see each other, and the padding rows of
+ * the last rank (document id -1: they see nothing and nobody sees them)
+ * are the cases the same page lists under "正确性测试应覆盖哪些边界".  A
+ * row with no allowed key returns m = -inf, l = 0, o = 0.
  *
  * Query head h reads KV head h / (hq / hkv).  The pages only name GQA, so
  * this maps consecutive groups of query heads to one KV head.
@@ -57,6 +62,9 @@ typedef struct {
   int hq, hkv, d;
   double scale;
   int causal;
+  long long window;
+  const long long* q_doc;
+  const long long* k_doc;
   const long long* q_pos;
   const long long* k_pos;
   const long long* rows;
@@ -85,6 +93,7 @@ static void one_row(job_t* J, long long item, double* score, char* allowed, doub
   const int kh = h / group;
   const long long r = J->rows[ri];
   const long long qp = J->q_pos ? J->q_pos[r] : r;
+  const long long qd = J->q_doc ? J->q_doc[r] : 0;
 
   for (int x = 0; x < d; ++x) qrow[x] = widen(J->q, J->dtype, ((size_t)r * J->hq + h) * d + x);
 
@@ -93,8 +102,11 @@ static void one_row(job_t* J, long long item, double* score, char* allowed, doub
   long long n_allowed = 0;
   for (long long t = 0; t < J->nk; ++t) {
     const long long kp = J->k_pos ? J->k_pos[t] : t;
-    allowed[t] = !(J->causal && kp > qp);
-    if (!allowed[t]) continue;
+    int ok = !(J->causal && kp > qp);
+    if (J->window > 0 && (qp - kp >= J->window || kp - qp >= J->window)) ok = 0;
+    if (J->q_doc && (qd < 0 || J->k_doc[t] != qd)) ok = 0;
+    allowed[t] = (char)ok;
+    if (!ok) continue;
     const size_t kb = ((size_t)t * J->hkv + kh) * d;
     double s = 0.0;
     for (int x = 0; x < d; ++x) s += qrow[x] * widen(J->k, J->dtype, kb + x);
@@ -147,14 +159,18 @@ static void* worker(void* arg) {
 
 /*
  * Returns 0 on success, -1 on a bad argument, -2 when memory or threads
- * could not be had.  q_pos / k_pos may be NULL (position = index).
+ * could not be had.  q_pos / k_pos may be NULL (position = index).  q_doc
+ * and k_doc are both NULL (one document) or both given.
  */
-int oracle_partial_state(const void* q, const void* k, const void* v, int dtype,
-                         long long nq, long long nk, int hq, int hkv, int d, double scale,
-                         int causal, const long long* q_pos, const long long* k_pos,
-                         const long long* rows, long long nrows, double* m_out,
-                         double* l_out, double* o_out, int nthreads) {
+int oracle_partial_state_masked(const void* q, const void* k, const void* v, int dtype,
+                                long long nq, long long nk, int hq, int hkv, int d,
+                                double scale, int causal, long long window,
+                                const long long* q_pos, const long long* k_pos,
+                                const long long* q_doc, const long long* k_doc,
+                                const long long* rows, long long nrows, double* m_out,
+                                double* l_out, double* o_out, int nthreads) {
   if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return -1;
+  if (window < 0 || (!q_doc) != (!k_doc)) return -1;
   if (hq <= 0 || hkv <= 0 || d <= 0 || hq % hkv != 0 || nq < 0 || nk < 0 || nrows < 0) return -1;
   if (nrows > 0 && (!q || !rows || !m_out || !l_out || !o_out)) return -1;
   if (nk > 0 && (!k || !v)) return -1;
@@ -166,7 +182,8 @@ int oracle_partial_state(const void* q, const void* k, const void* v, int dtype,
   memset(&J, 0, sizeof J);
   J.q = q; J.k = k; J.v = v; J.dtype = dtype;
   J.nq = nq; J.nk = nk; J.hq = hq; J.hkv = hkv; J.d = d;
-  J.scale = scale; J.causal = causal;
+  J.scale = scale; J.causal = causal; J.window = window;
+  J.q_doc = q_doc; J.k_doc = k_doc;
   J.q_pos = q_pos; J.k_pos = k_pos; J.rows = rows; J.nrows = nrows;
   J.m_out = m_out; J.l_out = l_out; J.o_out = o_out;
 
@@ -183,5 +200,16 @@ int oracle_partial_state(const void* q, const void* k, const void* v, int dtype,
   return J.failed ? -2 : 0;
 }
 
+/* The causal-only form: no window, one document. */
+int oracle_partial_state(const void* q, const void* k, const void* v, int dtype,
+                         long long nq, long long nk, int hq, int hkv, int d, double scale,
+                         int causal, const long long* q_pos, const long long* k_pos,
+                         const long long* rows, long long nrows, double* m_out,
+                         double* l_out, double* o_out, int nthreads) {
+  return oracle_partial_state_masked(q, k, v, dtype, nq, nk, hq, hkv, d, scale, causal, 0, q_pos,
+                                     k_pos, NULL, NULL, rows, nrows, m_out, l_out, o_out,
+                                     nthreads);
+}
+
 /* Version tag so the Python side can tell a stale build. */
-int oracle_abi_version(void) { return 1; }
+int oracle_abi_version(void) { return 2; }

@@ -366,3 +366,82 @@ def test_normalize_then_average_is_wrong():
               for j in range(4)]
     wrong = sum(blocks) / 4
     assert np.abs(wrong - ref).max() > 1e-2
+
+
+# --- masks beyond causal: window, packed documents, padding ("Ring Attention：
+# 把超长序列沿设备环流动", "正确性测试应覆盖哪些边界")
+
+def _rand(n, h, d, seed):
+    g = np.random.default_rng(seed)
+    return g.standard_normal((n, h, d)).astype(np.float32)
+
+
+def test_causal_window_one_is_the_own_value():
+    # With causal and window 1 a row sees only itself: O = v_r, LSE = s_rr.
+    q, k, v = _rand(40, 2, 8, 1), _rand(40, 2, 8, 2), _rand(40, 2, 8, 3)
+    out, lse = oracle.attention(q, k, v, causal=True, window=1)
+    assert np.array_equal(out, v.astype(np.float64))
+    s_rr = (q.astype(np.float64) * k.astype(np.float64)).sum(-1) / math.sqrt(8)
+    assert np.abs(lse - s_rr).max() < 1e-13
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_window_equals_the_explicit_key_slice(causal):
+    # Row r with window W sees exactly the keys r-W+1 .. r+W-1 (.. r if
+    # causal).  Hand the oracle that slice, positions kept, with no window.
+    n, W = 57, 6
+    q, k, v = _rand(n, 3, 4, 4), _rand(n, 3, 4, 5), _rand(n, 3, 4, 6)
+    out, lse = oracle.attention(q, k, v, causal=causal, window=W)
+    for r in range(n):
+        lo, hi = max(0, r - W + 1), (r + 1 if causal else min(n, r + W))
+        o2, l2 = oracle.attention(q[r:r + 1], k[lo:hi], v[lo:hi], causal=False)
+        assert np.abs(out[r] - o2[0]).max() < 1e-13
+        assert np.abs(lse[r] - l2[0]).max() < 1e-13
+
+
+def test_window_wider_than_the_sequence_changes_nothing():
+    q, k, v = _rand(33, 2, 8, 7), _rand(33, 2, 8, 8), _rand(33, 2, 8, 9)
+    for causal in (False, True):
+        a = oracle.attention(q, k, v, causal=causal)
+        b = oracle.attention(q, k, v, causal=causal, window=33)
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_packed_documents_equal_separate_sequences(causal):
+    lens = [5, 1, 17, 9]
+    n = sum(lens)
+    q, k, v = _rand(n, 2, 8, 10), _rand(n, 2, 8, 11), _rand(n, 2, 8, 12)
+    doc = np.repeat(np.arange(len(lens)), lens)
+    out, lse = oracle.attention(q, k, v, causal=causal, q_doc=doc, k_doc=doc)
+    at = 0
+    for ln in lens:
+        o2, l2 = oracle.attention(q[at:at + ln], k[at:at + ln], v[at:at + ln], causal=causal)
+        assert np.abs(out[at:at + ln] - o2).max() < 1e-13
+        assert np.abs(lse[at:at + ln] - l2).max() < 1e-13
+        at += ln
+
+
+def test_padding_rows_see_nothing_and_are_not_seen():
+    n, pad = 30, 7
+    q, k, v = _rand(n, 2, 8, 13), _rand(n, 2, 8, 14), _rand(n, 2, 8, 15)
+    doc = np.where(np.arange(n) < n - pad, 0, -1)
+    out, lse = oracle.attention(q, k, v, causal=True, q_doc=doc, k_doc=doc)
+    assert (out[n - pad:] == 0).all() and np.isneginf(lse[n - pad:]).all()
+    o2, l2 = oracle.attention(q[:n - pad], k[:n - pad], v[:n - pad], causal=True)
+    assert np.abs(out[:n - pad] - o2).max() < 1e-13
+    assert np.abs(lse[:n - pad] - l2).max() < 1e-13
+
+
+def test_positions_not_indices_decide_the_mask():
+    # Permuting rows together with their positions changes nothing but the
+    # row order: the mask reads positions, not indices.
+    n, W = 48, 9
+    q, k, v = _rand(n, 2, 8, 16), _rand(n, 2, 8, 17), _rand(n, 2, 8, 18)
+    doc = np.repeat([0, 1, 2], [20, 12, 16])
+    perm = np.random.default_rng(19).permutation(n)
+    a = oracle.attention(q, k, v, causal=True, window=W, q_doc=doc, k_doc=doc)
+    b = oracle.attention(q[perm], k[perm], v[perm], causal=True, window=W, q_pos=perm,
+                         k_pos=perm, q_doc=doc[perm], k_doc=doc[perm])
+    assert np.abs(b[0] - a[0][perm]).max() < 1e-13
+    assert np.abs(b[1] - a[1][perm]).max() < 1e-13
