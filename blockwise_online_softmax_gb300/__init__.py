@@ -7,14 +7,20 @@ loads it, and raises if it has not been built.
 """
 
 from .binding import (  # noqa: E402,F401
+    LAYOUTS,
     RaError,
+    layout_positions,
     ra_block_update,
+    ra_block_update_masked,
     ra_device_status,
     ra_finalize,
     ra_merge,
     ra_ring_forward,
     ra_ring_forward_host,
+    ra_ring_forward_masked,
+    ra_ring_forward_noalloc,
     ra_ring_step,
+    ra_ring_step_masked,
     ra_selftest_wait_timeout,
     ra_state_init,
     ra_trace_enable,

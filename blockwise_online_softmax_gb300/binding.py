@@ -24,6 +24,8 @@ RA_ERR_TIMEOUT = -4
 RA_ERR_ALLOC = -5
 RA_F32 = 0
 RA_BF16 = 1
+LAYOUTS = {"contiguous": 0, "zigzag": 1, "striped": 2}
+ABI_VERSION = 2
 KERNEL_KINDS = {
     "state_init": 0,
     "block_update_bf16": 1,
@@ -52,6 +54,9 @@ _SIGNATURES = {
     "ra_ring_forward": ("PPPPPLiiiiiiP", "i"),
     "ra_ring_forward_host": ("PPPPPLiiiiiiP", "i"),
     "ra_ring_forward_noalloc": ("PPPPPLiiiiiiP", "i"),
+    "ra_block_update_masked": ("PPPPPPLLiiiiiiiLLiLLPiiP", "i"),
+    "ra_ring_step_masked": ("PPPPPPLiiiiLLPiiiiiP", "i"),
+    "ra_ring_forward_masked": ("PPPPPLiiiLLPiiiiiP", "i"),
     "ra_device_status": ("P", "i"),
     "ra_selftest_wait_timeout": ("LP", "i"),
     "ra_trace_enable": ("i", "i"),
@@ -78,7 +83,7 @@ def lib():
                 f = getattr(L, name)
                 f.argtypes = [_CT[c] for c in args]
                 f.restype = _CT[res]
-            if L.ra_abi_version() != 1:
+            if L.ra_abi_version() != ABI_VERSION:
                 raise RaError(RA_ERR_UNSUPPORTED, "libra.so ABI version mismatch; rebuild it")
             _lib = L
     return _lib
@@ -203,6 +208,103 @@ def ra_ring_forward(q, k, v, *, P: int, causal: bool, out=None, lse=None, stream
         _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(out, "out", torch.float32),
         _dev(lse, "lse", torch.float32), N, int(P), int(bool(causal)), d, heads, kv_heads,
         _qkv_dtype(q), _stream(stream)))
+    return out, lse
+
+
+def _layout(layout) -> int:
+    if isinstance(layout, str):
+        if layout not in LAYOUTS:
+            raise ValueError(f"layout must be one of {sorted(LAYOUTS)}, got {layout!r}")
+        return LAYOUTS[layout]
+    return int(layout)
+
+
+def _docs(cu_seqlens):
+    """Device pointer and document count of an int32 cu_seqlens tensor (or None)."""
+    if cu_seqlens is None:
+        return 0, 0
+    if cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2:
+        raise ValueError("cu_seqlens must be 1-D with ndocs + 1 >= 2 entries")
+    return _dev(cu_seqlens, "cu_seqlens", torch.int32), cu_seqlens.numel() - 1
+
+
+def layout_positions(N: int, P: int, layout="contiguous") -> torch.Tensor:
+    """Global sequence position held by each row of a ring tensor of N rows
+    under `layout` (int64, CPU).  Host index arithmetic for callers that lay
+    their tensors out; x_layout = x[argsort(positions)] is not needed, since
+    x_layout[r] = x[positions[r]]."""
+    lay = _layout(layout)
+    if N % P:
+        raise ValueError("N must be a multiple of P")
+    c = N // P
+    r = torch.arange(c, dtype=torch.int64)
+    out = []
+    for b in range(P):
+        if lay == 0:
+            out.append(b * c + r)
+        elif lay == 1:
+            if c % 2:
+                raise ValueError("zigzag needs an even block length N / P")
+            h = c // 2
+            out.append(torch.where(r < h, b * h + r, (2 * P - 1 - b) * h + (r - h)))
+        else:
+            out.append(r * P + b)
+    return torch.cat(out)
+
+
+def ra_block_update_masked(q, k, v, m, l, o, *, layout="contiguous", P: int = 1,
+                           q_block: int = 0, kv_block: int = 0, q_off: int = 0, kv_off: int = 0,
+                           causal: bool = False, window: int = 0, n_valid: int = -1,
+                           cu_seqlens=None, stream=None):
+    if q.dim() != 3 or k.dim() != 3 or v.dim() != 3 or k.shape != v.shape:
+        raise ValueError("q: [c_q, heads, d]; k, v: [c_kv, kv_heads, d]")
+    if k.dtype != q.dtype or v.dtype != q.dtype or q.shape[2] != k.shape[2]:
+        raise ValueError("q, k, v must share dtype and head dim")
+    c_q, heads, d = q.shape
+    c_kv, kv_heads = k.shape[0], k.shape[1]
+    _state_shapes(m, l, o, c_q, heads, d)
+    cu_ptr, ndocs = _docs(cu_seqlens)
+    _check(lib().ra_block_update_masked(
+        _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(m, "m", torch.float32),
+        _dev(l, "l", torch.float32), _dev(o, "o", torch.float32), c_q, c_kv, d, heads, kv_heads,
+        _layout(layout), int(P), int(q_block), int(kv_block), int(q_off), int(kv_off),
+        int(bool(causal)), int(window), int(n_valid), cu_ptr, ndocs, _qkv_dtype(q),
+        _stream(stream)))
+
+
+def ra_ring_step_masked(q, k, v, m, l, o, *, P: int, s: int, layout="contiguous",
+                        causal: bool = False, window: int = 0, n_valid: int = -1,
+                        cu_seqlens=None, stream=None):
+    N, heads, kv_heads, d = _shapes(q, k, v)
+    if k.shape[0] != N:
+        raise ValueError("q, k and v must cover the same N tokens")
+    _state_shapes(m, l, o, N, heads, d)
+    cu_ptr, ndocs = _docs(cu_seqlens)
+    _check(lib().ra_ring_step_masked(
+        _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(m, "m", torch.float32),
+        _dev(l, "l", torch.float32), _dev(o, "o", torch.float32), N, int(P), int(s),
+        _layout(layout), int(bool(causal)), int(window), int(n_valid), cu_ptr, ndocs, d, heads,
+        kv_heads, _qkv_dtype(q), _stream(stream)))
+
+
+def ra_ring_forward_masked(q, k, v, *, P: int, layout="contiguous", causal: bool = False,
+                           window: int = 0, n_valid: int = -1, cu_seqlens=None, out=None,
+                           lse=None, stream=None):
+    """Returns (out [N, heads, d] fp32, lse [N, heads] fp32), rows in q's order."""
+    N, heads, kv_heads, d = _shapes(q, k, v)
+    if k.shape[0] != N:
+        raise ValueError("q, k and v must cover the same N tokens")
+    if out is None:
+        out = torch.empty((N, heads, d), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((N, heads), dtype=torch.float32, device=q.device)
+    _state_shapes(lse, lse, out, N, heads, d)
+    cu_ptr, ndocs = _docs(cu_seqlens)
+    _check(lib().ra_ring_forward_masked(
+        _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(out, "out", torch.float32),
+        _dev(lse, "lse", torch.float32), N, int(P), _layout(layout), int(bool(causal)),
+        int(window), int(n_valid), cu_ptr, ndocs, d, heads, kv_heads, _qkv_dtype(q),
+        _stream(stream)))
     return out, lse
 
 

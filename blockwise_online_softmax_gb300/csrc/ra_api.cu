@@ -157,7 +157,7 @@ int run_update(ra::FwdArgs& a, int d, int dtype, cudaStream_t st) {
   a.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
   a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
   a.wait_limit = kWaitLimit;
-  if (a.nwork == 0 || a.c == 0) return RA_OK;
+  if (a.nwork == 0 || a.cq == 0 || a.ck == 0) return RA_OK;
   cudaError_t e;
   if (dtype == RA_BF16) {
     int rc = get_encoder();
@@ -178,48 +178,170 @@ int run_update(ra::FwdArgs& a, int d, int dtype, cudaStream_t st) {
   return RA_OK;
 }
 
-int ring_args_check(const void* q, const void* k, const void* v, long long N, int P, int s,
-                    int d, int heads, int kv_heads, int dtype) {
+// ----------------------------------------------------------------- masks
+// "All positions valid": larger than any sequence, small enough that
+// position arithmetic on it cannot overflow.
+constexpr long long kAllValid = 1LL << 60;
+
+// Host copy of the mask arguments, checked.
+struct MaskSpec {
+  int layout = RA_LAYOUT_CONTIGUOUS;
+  int causal = 0;
+  long long window = 0;
+  long long n_valid = kAllValid;
+  const int* cu_seqlens = nullptr;
+  int ndocs = 0;
+};
+
+int check_mask(int layout, int causal, long long window, long long n_valid,
+               const int* cu_seqlens, int ndocs, MaskSpec* out) {
+  if (layout != RA_LAYOUT_CONTIGUOUS && layout != RA_LAYOUT_ZIGZAG && layout != RA_LAYOUT_STRIPED)
+    return fail(RA_ERR_INVALID, "layout=%d is not a ra_layout value", layout);
+  if (causal != 0 && causal != 1) return fail(RA_ERR_INVALID, "causal=%d is not 0 or 1", causal);
+  if (window < 0) return fail(RA_ERR_INVALID, "window=%lld is negative", window);
+  if (ndocs < 0) return fail(RA_ERR_INVALID, "ndocs=%d is negative", ndocs);
+  if (ndocs > 0 && !cu_seqlens) return fail(RA_ERR_INVALID, "ndocs=%d with a NULL cu_seqlens", ndocs);
+  if (ndocs > 0 && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u))
+    return fail(RA_ERR_INVALID, "cu_seqlens is not 4-byte aligned");
+  out->layout = layout;
+  out->causal = causal;
+  out->window = window > kAllValid ? kAllValid : window;  // wider than any sequence
+  out->n_valid = (n_valid < 0 || n_valid > kAllValid) ? kAllValid : n_valid;
+  out->cu_seqlens = ndocs > 0 ? cu_seqlens : nullptr;
+  out->ndocs = ndocs;
+  return RA_OK;
+}
+
+void put_mask(ra::FwdArgs& a, const MaskSpec& mk) {
+  a.layout = mk.layout;
+  a.mask.causal = mk.causal;
+  a.mask.window = mk.window;
+  a.mask.n_valid = mk.n_valid;
+  a.mask.cu_seqlens = mk.cu_seqlens;
+  a.mask.ndocs = mk.ndocs;
+}
+
+// Positions of a block's rows below n_valid, as arithmetic progressions
+// (start, count, step): one for contiguous and striped blocks, two for a
+// zigzag block.
+struct Prog {
+  long long start, count, step;
+};
+
+int block_progs(const MaskSpec& mk, int P, long long c, long long blk, Prog out[2]) {
+  int n = 0;
+  if (mk.layout == RA_LAYOUT_ZIGZAG) {
+    const long long h = c / 2;
+    out[n++] = {blk * h, h, 1};
+    out[n++] = {(2LL * P - 1 - blk) * h, h, 1};
+  } else if (mk.layout == RA_LAYOUT_STRIPED) {
+    out[n++] = {blk, c, P};
+  } else {
+    out[n++] = {blk * c, c, 1};
+  }
+  for (int i = 0; i < n; ++i) {
+    Prog& g = out[i];
+    if (g.start >= mk.n_valid) {
+      g.count = 0;
+    } else {
+      const long long fit = (mk.n_valid - g.start + g.step - 1) / g.step;
+      g.count = fit < g.count ? fit : g.count;
+    }
+  }
+  return n;
+}
+
+long long floor_div(long long a, long long b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
+long long ceil_div(long long a, long long b) { return -floor_div(-a, b); }
+
+// Whether ring pair (i, j) may hold an allowed (query, key) pair under the
+// causal and window rules and the valid length.  Documents are ignored, so
+// the answer is exact or a safe "yes".
+bool pair_may_see(const MaskSpec& mk, int P, long long c, int i, int j) {
+  const long long big = 1LL << 61;
+  // Allowed values of q - k.
+  const long long A = mk.causal ? 0 : (mk.window > 0 ? -(mk.window - 1) : -big);
+  const long long B = mk.window > 0 ? mk.window - 1 : big;
+  Prog qp[2], kp[2];
+  const int nq = block_progs(mk, P, c, i, qp), nk = block_progs(mk, P, c, j, kp);
+  for (int x = 0; x < nq; ++x)
+    for (int y = 0; y < nk; ++y) {
+      const Prog& u = qp[x];
+      const Prog& w = kp[y];
+      if (u.count == 0 || w.count == 0) continue;
+      // q - k = delta + step * m with m = a - b in [-(w.count-1), u.count-1].
+      const long long delta = u.start - w.start;
+      long long mlo = ceil_div(A - delta, u.step), mhi = floor_div(B - delta, u.step);
+      if (mlo < -(w.count - 1)) mlo = -(w.count - 1);
+      if (mhi > u.count - 1) mhi = u.count - 1;
+      if (mlo <= mhi) return true;
+    }
+  return false;
+}
+
+// Ranks i that take part in ring step s.  The launch covers one range of
+// ranks: the span of those whose pair may see a key; the CTAs of a rank in
+// that span with nothing to do exit at once.
+constexpr int kMaxScannedRanks = 4096;
+
+void set_step_ranks(ra::FwdArgs& a, const MaskSpec& mk, int P, long long c, int s) {
+  a.i0 = 0;
+  a.nwork = P;
+  if (P > kMaxScannedRanks) return;
+  int first = -1, last = -1;
+  for (int i = 0; i < P; ++i) {
+    if (!pair_may_see(mk, P, c, i, ((i - s) % P + P) % P)) continue;
+    if (first < 0) first = i;
+    last = i;
+  }
+  a.i0 = first < 0 ? 0 : first;
+  a.nwork = first < 0 ? 0 : last - first + 1;
+}
+
+int ring_args_check(long long N, int P, int s, int d, int heads, int kv_heads, int dtype,
+                    int layout) {
   int rc;
   if ((rc = check_common(d, heads, dtype)) != RA_OK) return rc;
   if ((rc = check_heads(heads, kv_heads)) != RA_OK) return rc;
   if (N < 0) return fail(RA_ERR_INVALID, "N=%lld is negative", N);
   if (P < 1 || P > 65535) return fail(RA_ERR_INVALID, "P=%d out of range [1, 65535]", P);
   if (N % P != 0) return fail(RA_ERR_INVALID, "N=%lld is not a multiple of P=%d", N, P);
+  if (layout == RA_LAYOUT_ZIGZAG && (N / P) % 2 != 0)
+    return fail(RA_ERR_INVALID, "zigzag layout: the block length N/P=%lld is odd", N / P);
   if (s < 0 || s >= P) return fail(RA_ERR_INVALID, "ring step s=%d out of range [0, P)", s);
   if (N > (1LL << 31) - 256) return fail(RA_ERR_UNSUPPORTED, "N=%lld exceeds the 32-bit TMA row coordinate", N);
-  (void)q; (void)k; (void)v;
   return RA_OK;
 }
 
 int ring_step_impl(const void* q, const void* k, const void* v, float* m, float* l, float* o,
-                   long long N, int P, int s, int causal, int d, int heads, int kv_heads,
+                   long long N, int P, int s, const MaskSpec& mk, int d, int heads, int kv_heads,
                    int dtype, cudaStream_t st) {
   ra::FwdArgs a{};
   a.q = q; a.k = k; a.v = v; a.m = m; a.l = l; a.o = o;
-  a.c = N / P;
+  a.cq = N / P;
+  a.ck = N / P;
   a.q_rows = N;
   a.kv_rows = N;
   a.heads = heads;
   a.kv_heads = kv_heads;
-  a.causal = causal ? 1 : 0;
   a.mode = 1;
   a.P = P;
   a.s = s;
-  a.nwork = causal ? P - s : P;  // causal: ranks i < s would fold a future block
+  put_mask(a, mk);
+  set_step_ranks(a, mk, P, N / P, s);
   return run_update(a, d, dtype, st);
 }
 
 int ring_forward_impl(const void* q, const void* k, const void* v, float* out, float* lse,
-                      long long N, int P, int causal, int d, int heads, int kv_heads, int dtype,
-                      cudaStream_t st, float* l_scratch) {
+                      long long N, int P, const MaskSpec& mk, int d, int heads, int kv_heads,
+                      int dtype, cudaStream_t st, float* l_scratch) {
   const long long rows = N;
   TraceScope t0(RA_KERNEL_STATE_INIT, st);
   cudaError_t e = ra::launch_state_init(lse, l_scratch, out, rows, heads, d, st);
   t0.done(e == cudaSuccess);
   if (e != cudaSuccess) return cuda_fail(e, "state-init launch");
   for (int s = 0; s < P; ++s) {
-    int rc = ring_step_impl(q, k, v, lse, l_scratch, out, N, P, s, causal, d, heads, kv_heads,
+    int rc = ring_step_impl(q, k, v, lse, l_scratch, out, N, P, s, mk, d, heads, kv_heads,
                             dtype, st);
     if (rc != RA_OK) return rc;
   }
@@ -228,6 +350,34 @@ int ring_forward_impl(const void* q, const void* k, const void* v, float* out, f
   t1.done(e == cudaSuccess);
   if (e != cudaSuccess) return cuda_fail(e, "finalize launch");
   return RA_OK;
+}
+
+MaskSpec plain_mask(int causal) {
+  MaskSpec mk;
+  mk.causal = causal ? 1 : 0;
+  return mk;
+}
+
+// ra_ring_forward and ra_ring_forward_masked: l scratch from the stream's
+// pool allocator.
+int ring_forward_alloc(const void* q, const void* k, const void* v, float* out, float* lse,
+                       long long N, int P, const MaskSpec& mk, int d, int heads, int kv_heads,
+                       int dtype, void* stream) {
+  int rc;
+  if ((rc = check_ptrs({q, k, v, out, lse})) != RA_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  float* l_scratch = nullptr;
+  const size_t l_bytes = static_cast<size_t>(N) * heads * sizeof(float);
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&l_scratch), l_bytes, st);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(RA_ERR_ALLOC, "cudaMallocAsync of %zu bytes for the l state failed: %s", l_bytes,
+                cudaGetErrorString(e));
+  }
+  rc = ring_forward_impl(q, k, v, out, lse, N, P, mk, d, heads, kv_heads, dtype, st, l_scratch);
+  e = cudaFreeAsync(l_scratch, st);
+  if (rc == RA_OK && e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync");
+  return rc;
 }
 
 // ----------------------------------------------------------------- fixed scratch
@@ -265,7 +415,7 @@ int noalloc_scratch(float** out) {
 
 extern "C" {
 
-int ra_abi_version(void) { return 1; }
+int ra_abi_version(void) { return 2; }
 
 const char* ra_status_string(int status) {
   switch (status) {
@@ -295,31 +445,55 @@ int ra_state_init(float* m, float* l, float* o, long long c, int d, int heads, v
   return RA_OK;
 }
 
-int ra_block_update(const void* q, const void* k, const void* v, float* m, float* l, float* o,
-                    long long c, int d, int heads, int kv_heads, long long q_off,
-                    long long kv_off, int causal, int dtype, void* stream) {
+int ra_block_update_masked(const void* q, const void* k, const void* v, float* m, float* l,
+                           float* o, long long c_q, long long c_kv, int d, int heads,
+                           int kv_heads, int layout, int P, int q_block, int kv_block,
+                           long long q_off, long long kv_off, int causal, long long window,
+                           long long n_valid, const int* cu_seqlens, int ndocs, int dtype,
+                           void* stream) {
   int rc;
   if ((rc = check_common(d, heads, dtype)) != RA_OK) return rc;
   if ((rc = check_heads(heads, kv_heads)) != RA_OK) return rc;
-  if (c < 0) return fail(RA_ERR_INVALID, "c=%lld is negative", c);
-  if (c > (1LL << 31) - 256) return fail(RA_ERR_UNSUPPORTED, "c=%lld exceeds the 32-bit TMA row coordinate", c);
-  if (c == 0) return RA_OK;
+  MaskSpec mk;
+  if ((rc = check_mask(layout, causal, window, n_valid, cu_seqlens, ndocs, &mk)) != RA_OK) return rc;
+  if (c_q < 0 || c_kv < 0) return fail(RA_ERR_INVALID, "c_q=%lld or c_kv=%lld is negative", c_q, c_kv);
+  if (c_q > (1LL << 31) - 256 || c_kv > (1LL << 31) - 256)
+    return fail(RA_ERR_UNSUPPORTED, "a block length exceeds the 32-bit TMA row coordinate");
+  if (layout != RA_LAYOUT_CONTIGUOUS) {
+    if (P < 1 || P > 65535) return fail(RA_ERR_INVALID, "P=%d out of range [1, 65535]", P);
+    if (q_block < 0 || q_block >= P || kv_block < 0 || kv_block >= P)
+      return fail(RA_ERR_INVALID, "q_block=%d / kv_block=%d out of range [0, P)", q_block, kv_block);
+  }
+  if (layout == RA_LAYOUT_ZIGZAG && (c_q != c_kv || c_q % 2 != 0))
+    return fail(RA_ERR_INVALID, "zigzag layout needs c_q == c_kv and an even block length");
+  if (c_q == 0 || c_kv == 0) return RA_OK;
   if ((rc = check_ptrs({q, k, v, m, l, o})) != RA_OK) return rc;
   ra::FwdArgs a{};
   a.q = q; a.k = k; a.v = v; a.m = m; a.l = l; a.o = o;
-  a.c = c;
-  a.q_rows = c;
-  a.kv_rows = c;
+  a.cq = c_q;
+  a.ck = c_kv;
+  a.q_rows = c_q;
+  a.kv_rows = c_kv;
   a.q_off = q_off;
   a.kv_off = kv_off;
+  a.q_blk = layout == RA_LAYOUT_CONTIGUOUS ? 0 : q_block;
+  a.kv_blk = layout == RA_LAYOUT_CONTIGUOUS ? 0 : kv_block;
   a.heads = heads;
   a.kv_heads = kv_heads;
-  a.causal = causal ? 1 : 0;
   a.mode = 0;
-  a.P = 1;
+  a.P = layout == RA_LAYOUT_CONTIGUOUS ? 1 : P;
   a.s = 0;
   a.nwork = 1;
+  put_mask(a, mk);
   return run_update(a, d, dtype, static_cast<cudaStream_t>(stream));
+}
+
+int ra_block_update(const void* q, const void* k, const void* v, float* m, float* l, float* o,
+                    long long c, int d, int heads, int kv_heads, long long q_off,
+                    long long kv_off, int causal, int dtype, void* stream) {
+  return ra_block_update_masked(q, k, v, m, l, o, c, c, d, heads, kv_heads, RA_LAYOUT_CONTIGUOUS,
+                                1, 0, 0, q_off, kv_off, causal ? 1 : 0, 0, -1, nullptr, 0, dtype,
+                                stream);
 }
 
 int ra_merge(float* m_a, float* l_a, float* o_a, const float* m_b, const float* l_b,
@@ -352,43 +526,53 @@ int ra_finalize(const float* m, const float* l, const float* o, float* out, floa
   return RA_OK;
 }
 
+int ra_ring_step_masked(const void* q, const void* k, const void* v, float* m, float* l,
+                        float* o, long long N, int P, int s, int layout, int causal,
+                        long long window, long long n_valid, const int* cu_seqlens, int ndocs,
+                        int d, int heads, int kv_heads, int dtype, void* stream) {
+  int rc = ring_args_check(N, P, s, d, heads, kv_heads, dtype, layout);
+  if (rc != RA_OK) return rc;
+  MaskSpec mk;
+  if ((rc = check_mask(layout, causal, window, n_valid, cu_seqlens, ndocs, &mk)) != RA_OK) return rc;
+  if (N == 0) return RA_OK;
+  if ((rc = check_ptrs({q, k, v, m, l, o})) != RA_OK) return rc;
+  return ring_step_impl(q, k, v, m, l, o, N, P, s, mk, d, heads, kv_heads, dtype,
+                        static_cast<cudaStream_t>(stream));
+}
+
 int ra_ring_step(const void* q, const void* k, const void* v, float* m, float* l, float* o,
                  long long N, int P, int s, int causal, int d, int heads, int kv_heads,
                  int dtype, void* stream) {
-  int rc = ring_args_check(q, k, v, N, P, s, d, heads, kv_heads, dtype);
+  return ra_ring_step_masked(q, k, v, m, l, o, N, P, s, RA_LAYOUT_CONTIGUOUS, causal ? 1 : 0, 0,
+                             -1, nullptr, 0, d, heads, kv_heads, dtype, stream);
+}
+
+int ra_ring_forward_masked(const void* q, const void* k, const void* v, float* out, float* lse,
+                           long long N, int P, int layout, int causal, long long window,
+                           long long n_valid, const int* cu_seqlens, int ndocs, int d,
+                           int heads, int kv_heads, int dtype, void* stream) {
+  int rc = ring_args_check(N, P, 0, d, heads, kv_heads, dtype, layout);
   if (rc != RA_OK) return rc;
+  MaskSpec mk;
+  if ((rc = check_mask(layout, causal, window, n_valid, cu_seqlens, ndocs, &mk)) != RA_OK) return rc;
   if (N == 0) return RA_OK;
-  if ((rc = check_ptrs({q, k, v, m, l, o})) != RA_OK) return rc;
-  return ring_step_impl(q, k, v, m, l, o, N, P, s, causal, d, heads, kv_heads, dtype,
-                        static_cast<cudaStream_t>(stream));
+  return ring_forward_alloc(q, k, v, out, lse, N, P, mk, d, heads, kv_heads, dtype, stream);
 }
 
 int ra_ring_forward(const void* q, const void* k, const void* v, float* out, float* lse,
                     long long N, int P, int causal, int d, int heads, int kv_heads, int dtype,
                     void* stream) {
-  int rc = ring_args_check(q, k, v, N, P, 0, d, heads, kv_heads, dtype);
+  int rc = ring_args_check(N, P, 0, d, heads, kv_heads, dtype, RA_LAYOUT_CONTIGUOUS);
   if (rc != RA_OK) return rc;
   if (N == 0) return RA_OK;
-  if ((rc = check_ptrs({q, k, v, out, lse})) != RA_OK) return rc;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  float* l_scratch = nullptr;
-  const size_t l_bytes = static_cast<size_t>(N) * heads * sizeof(float);
-  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&l_scratch), l_bytes, st);
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return fail(RA_ERR_ALLOC, "cudaMallocAsync of %zu bytes for the l state failed: %s", l_bytes,
-                cudaGetErrorString(e));
-  }
-  rc = ring_forward_impl(q, k, v, out, lse, N, P, causal, d, heads, kv_heads, dtype, st, l_scratch);
-  e = cudaFreeAsync(l_scratch, st);
-  if (rc == RA_OK && e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync");
-  return rc;
+  return ring_forward_alloc(q, k, v, out, lse, N, P, plain_mask(causal), d, heads, kv_heads,
+                            dtype, stream);
 }
 
 int ra_ring_forward_host(const void* q_host, const void* k_host, const void* v_host,
                          float* out_host, float* lse_host, long long N, int P, int causal, int d,
                          int heads, int kv_heads, int dtype, void* stream) {
-  int rc = ring_args_check(q_host, k_host, v_host, N, P, 0, d, heads, kv_heads, dtype);
+  int rc = ring_args_check(N, P, 0, d, heads, kv_heads, dtype, RA_LAYOUT_CONTIGUOUS);
   if (rc != RA_OK) return rc;
   if (N == 0) return RA_OK;
   if (!q_host || !k_host || !v_host || !out_host || !lse_host)
@@ -421,7 +605,8 @@ int ra_ring_forward_host(const void* q_host, const void* k_host, const void* v_h
     if (e != cudaSuccess) {
       rc = cuda_fail(e, "host-to-device copy");
     } else {
-      rc = ring_forward_impl(dq, dk, dv, dout, dlse, N, P, causal, d, heads, kv_heads, dtype, st, dl);
+      rc = ring_forward_impl(dq, dk, dv, dout, dlse, N, P, plain_mask(causal), d, heads, kv_heads,
+                             dtype, st, dl);
       if (rc == RA_OK) {
         e = cudaMemcpyAsync(out_host, dout, out_bytes, cudaMemcpyDeviceToHost, st);
         if (e == cudaSuccess) e = cudaMemcpyAsync(lse_host, dlse, rh_bytes, cudaMemcpyDeviceToHost, st);
@@ -440,7 +625,7 @@ int ra_ring_forward_host(const void* q_host, const void* k_host, const void* v_h
 int ra_ring_forward_noalloc(const void* q, const void* k, const void* v, float* out, float* lse,
                             long long N, int P, int causal, int d, int heads, int kv_heads,
                             int dtype, void* stream) {
-  int rc = ring_args_check(q, k, v, N, P, 0, d, heads, kv_heads, dtype);
+  int rc = ring_args_check(N, P, 0, d, heads, kv_heads, dtype, RA_LAYOUT_CONTIGUOUS);
   if (rc != RA_OK) return rc;
   if (N == 0) return RA_OK;
   if ((rc = check_ptrs({q, k, v, out, lse})) != RA_OK) return rc;
@@ -453,7 +638,7 @@ int ra_ring_forward_noalloc(const void* q, const void* k, const void* v, float* 
   if ((rc = noalloc_scratch(&l_scratch)) != RA_OK) return rc;
   // The state-init kernel zeroes the l rows this call uses, so whatever a
   // previous call left in the array does not matter.
-  return ring_forward_impl(q, k, v, out, lse, N, P, causal, d, heads, kv_heads, dtype,
+  return ring_forward_impl(q, k, v, out, lse, N, P, plain_mask(causal), d, heads, kv_heads, dtype,
                            static_cast<cudaStream_t>(stream), l_scratch);
 }
 

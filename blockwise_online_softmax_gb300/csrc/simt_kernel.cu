@@ -5,10 +5,10 @@
 // A CTA owns 64 query rows of one head.  It stages 64-key K/V tiles in
 // shared memory and loops over the tiles of the K/V block:
 //   S = Q K^T * scale   (4x4 register tile per thread),
-//   mask,               (causal on global positions, ragged tail)
+//   mask,               (each row's interval of allowed keys)
 //   row max / sum       (one warp per 8 rows, warp shuffles),
 //   O = alpha O + P V   (O in registers, 4 rows x d/16 columns per thread).
-// Key tiles wholly in the future are not visited.
+// Only key tiles that some row of the CTA may see are visited.
 #include <cmath>
 #include <cstdint>
 
@@ -33,6 +33,8 @@ struct SimtSmem {
   float m[BQ];
   float l[BQ];
   float alpha[BQ];
+  int lo[BQ];  // allowed keys of row r: lo[r] <= key index < hi[r]
+  int hi[BQ];
 };
 
 template <int D>
@@ -46,28 +48,30 @@ __global__ void __launch_bounds__(NT) simt_update_kernel(const FwdArgs a) {
   const int kh = h / (a.heads / a.kv_heads);
   const Work wk = decode_work(a, blockIdx.z);
   const long long q_tile0 = static_cast<long long>(blockIdx.x) * BQ;
-  if (q_tile0 >= a.c) return;
+  if (q_tile0 >= a.cq) return;
 
   const float* __restrict__ Q = static_cast<const float*>(a.q);
   const float* __restrict__ K = static_cast<const float*>(a.k);
   const float* __restrict__ V = static_cast<const float*>(a.v);
 
-  // Number of key tiles with at least one allowed key for this query tile.
-  const long long kv_tiles = (a.c + BK - 1) / BK;
-  long long nt = kv_tiles;
-  if (a.causal) {
-    const long long last_row = (q_tile0 + BQ - 1 < a.c - 1) ? q_tile0 + BQ - 1 : a.c - 1;
-    const long long last_key = wk.q_pos0 + last_row - wk.kv_pos0;  // local index
-    nt = (last_key < 0) ? 0 : (last_key / BK + 1 < kv_tiles ? last_key / BK + 1 : kv_tiles);
+  // Key tiles [t_first, t_end) hold every key some row of this tile may see.
+  const long long vb = valid_bound(a.mask);
+  int t_first, t_end;
+  tile_range(a, wk, q_tile0, q_tile0 + BQ, vb, BK, &t_first, &t_end);
+  if (t_end <= t_first) return;  // state unchanged
+  if (tid < BQ) {
+    long long lo = 0, hi = 0;
+    if (q_tile0 + tid < a.cq) row_keys(a, wk, q_tile0 + tid, vb, &lo, &hi);
+    sm.lo[tid] = static_cast<int>(lo);
+    sm.hi[tid] = static_cast<int>(hi);
   }
-  if (nt == 0) return;  // state unchanged
 
   // Q tile and state in.
   for (int i = tid; i < BQ * D / 4; i += NT) {
     const int r = i / (D / 4), c4 = i % (D / 4);
     const long long gr = q_tile0 + r;
     float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (gr < a.c)
+    if (gr < a.cq)
       x = reinterpret_cast<const float4*>(Q + ((wk.q_base + gr) * a.heads + h) * D)[c4];
     sm.q[r][4 * c4 + 0] = x.x;
     sm.q[r][4 * c4 + 1] = x.y;
@@ -77,7 +81,7 @@ __global__ void __launch_bounds__(NT) simt_update_kernel(const FwdArgs a) {
   if (tid < BQ) {
     const long long gr = q_tile0 + tid;
     float mm = -INFINITY, ll = 0.f;
-    if (gr < a.c) {
+    if (gr < a.cq) {
       const long long si = (wk.state_base + gr) * a.heads + h;
       mm = a.m[si];
       ll = a.l[si];
@@ -92,16 +96,16 @@ __global__ void __launch_bounds__(NT) simt_update_kernel(const FwdArgs a) {
     const long long gr = q_tile0 + ty + 16 * i;
     const float* src = a.o + ((wk.state_base + gr) * a.heads + h) * D;
 #pragma unroll
-    for (int j = 0; j < OC; ++j) acc[i][j] = (gr < a.c) ? src[tx + 16 * j] : 0.f;
+    for (int j = 0; j < OC; ++j) acc[i][j] = (gr < a.cq) ? src[tx + 16 * j] : 0.f;
   }
   __syncthreads();
 
-  for (long long t = 0; t < nt; ++t) {
+  for (long long t = t_first; t < t_end; ++t) {
     const long long k0 = t * BK;
     for (int i = tid; i < BK * D / 4; i += NT) {
       const int r = i / (D / 4), c4 = i % (D / 4);
       float4 x = make_float4(0.f, 0.f, 0.f, 0.f), y = x;
-      if (k0 + r < a.c) {
+      if (k0 + r < a.ck) {
         const long long off = ((wk.kv_base + k0 + r) * a.kv_heads + kh) * D;
         x = reinterpret_cast<const float4*>(K + off)[c4];
         y = reinterpret_cast<const float4*>(V + off)[c4];
@@ -134,12 +138,12 @@ __global__ void __launch_bounds__(NT) simt_update_kernel(const FwdArgs a) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int r = ty + 16 * i;
-      const long long qpos = wk.q_pos0 + q_tile0 + r;
+      const long long lo = sm.lo[r], hi = sm.hi[r];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int cidx = tx + 16 * j;
         const long long kl = k0 + cidx;
-        const bool ok = (kl < a.c) && (!a.causal || wk.kv_pos0 + kl <= qpos);
+        const bool ok = kl >= lo && kl < hi;
         sm.s[r][cidx] = ok ? sacc[i][j] * a.scale : -INFINITY;
       }
     }
@@ -199,7 +203,7 @@ __global__ void __launch_bounds__(NT) simt_update_kernel(const FwdArgs a) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const long long gr = q_tile0 + ty + 16 * i;
-    if (gr < a.c) {
+    if (gr < a.cq) {
       float* dst = a.o + ((wk.state_base + gr) * a.heads + h) * D;
 #pragma unroll
       for (int j = 0; j < OC; ++j) dst[tx + 16 * j] = acc[i][j];
@@ -207,7 +211,7 @@ __global__ void __launch_bounds__(NT) simt_update_kernel(const FwdArgs a) {
   }
   if (tid < BQ) {
     const long long gr = q_tile0 + tid;
-    if (gr < a.c) {
+    if (gr < a.cq) {
       const long long si = (wk.state_base + gr) * a.heads + h;
       a.m[si] = sm.m[tid];
       a.l[si] = sm.l[tid];
@@ -222,7 +226,7 @@ cudaError_t launch_d(const FwdArgs& a, cudaStream_t st) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  dim3 grid(static_cast<unsigned>((a.c + BQ - 1) / BQ), a.heads, a.nwork);
+  dim3 grid(static_cast<unsigned>((a.cq + BQ - 1) / BQ), a.heads, a.nwork);
   simt_update_kernel<D><<<grid, NT, smem, st>>>(a);
   return cudaGetLastError();
 }

@@ -112,25 +112,47 @@ struct Cfg {
   static_assert(SMEM_BYTES <= 232448, "shared memory budget (227 KB per CTA)");
 };
 
-// Number of K/V tiles holding a key that some row of the query tile
-// [row0, row0 + BM) may see.  Zero if the tile is past the block end or,
-// under causal masking, all its keys lie in the future.
-__device__ __forceinline__ int tiles_for(const FwdArgs& a, const Work& wk, long long row0) {
-  if (row0 >= a.c) return 0;
-  const long long kv_tiles = (a.c + BN - 1) / BN;
-  if (!a.causal) return static_cast<int>(kv_tiles);
-  const long long last_row = (row0 + BM - 1 < a.c - 1) ? row0 + BM - 1 : a.c - 1;
-  const long long last_key = wk.q_pos0 + last_row - wk.kv_pos0;  // local key index
-  if (last_key < 0) return 0;
-  const long long n = last_key / BN + 1;
-  return static_cast<int>(n < kv_tiles ? n : kv_tiles);
+// The K/V tiles a CTA visits: the union of its two query tiles' ranges
+// [ta[g], tb[g]), in increasing order.  Ranges that overlap or touch merge;
+// otherwise the visit is two runs with the gap skipped.
+struct TileSeq {
+  int a0;  // first tile of the first run
+  int na;  // length of the first run
+  int b0;  // first tile of the second run
+  int n;   // total tiles
+  __device__ __forceinline__ int at(int k) const { return k < na ? a0 + k : b0 + (k - na); }
+};
+
+__device__ __forceinline__ TileSeq make_seq(const int (&ta)[NQ], const int (&tb)[NQ]) {
+  // Written with selects only: a runtime index into ta/tb would put them
+  // in local memory.
+  const int a0 = ta[0], b0 = tb[0], a1 = ta[1], b1 = tb[1];
+  const int n0 = b0 - a0, n1 = b1 - a1;
+  TileSeq q{0, 0, 0, 0};
+  if (n0 <= 0 && n1 <= 0) return q;
+  if (n0 <= 0 || n1 <= 0) {
+    q.a0 = n0 > 0 ? a0 : a1;
+    q.na = n0 > 0 ? n0 : n1;
+  } else if (a1 <= b0 && a0 <= b1) {
+    q.a0 = a0 < a1 ? a0 : a1;
+    q.na = (b0 > b1 ? b0 : b1) - q.a0;
+  } else {
+    const bool f0 = a0 < a1;
+    q.a0 = f0 ? a0 : a1;
+    q.na = f0 ? n0 : n1;
+    q.b0 = f0 ? a1 : a0;
+    q.n = f0 ? n1 : n0;
+  }
+  q.n += q.na;
+  return q;
 }
 
-// Streams the nt K (or V) tiles of the block into an NST-deep ring of
+// Streams the K (or V) tiles of the visit into an NST-deep ring of
 // shared-memory stages; full/empty are the first stage's barriers.  Returns
 // false on an abort, after draining (bounded) the copies still in flight.
 template <int D, int NST>
-__device__ __forceinline__ bool produce_tiles(const Work& wk, int nt, int kh, uint32_t sbase,
+__device__ __forceinline__ bool produce_tiles(const Work& wk, const TileSeq& seq, int kh,
+                                              uint32_t sbase,
                                               uint32_t b_full, uint32_t b_empty,
                                               const CUtensorMap* tm, volatile int* abort_flag,
                                               int code, long long lim) {
@@ -138,10 +160,10 @@ __device__ __forceinline__ bool produce_tiles(const Work& wk, int nt, int kh, ui
   tma_prefetch_desc(tm);
   int issued = 0;
   bool ok = true;
-  for (int t = 0; t < nt; ++t) {
+  for (int t = 0; t < seq.n; ++t) {
     const int st = t % NST;
     const uint32_t ph = static_cast<uint32_t>(t / NST) & 1u;
-    const int kv_row = static_cast<int>(wk.kv_base + static_cast<long long>(t) * BN);
+    const int kv_row = static_cast<int>(wk.kv_base + static_cast<long long>(seq.at(t)) * BN);
     if (t >= NST) ok = wait_bar(b_empty + 8u * st, ph ^ 1u, abort_flag, &g_umma_status, code, lim);
     if (!ok) break;
     mbar_arrive_expect_tx(b_full + 8u * st, C::TILE_BYTES);
@@ -163,7 +185,8 @@ __device__ __forceinline__ bool produce_tiles(const Work& wk, int nt, int kh, ui
 // Producers (warps 8 and 10) and MMA issuer (warp 9); warp 11 falls through.
 template <int D>
 __device__ __forceinline__ void control_roles(const FwdArgs& a, const Work& wk, long long row0,
-                                              const int (&ntq)[NQ], int nt, uint32_t tmem,
+                                              const int (&ta)[NQ], const int (&tb)[NQ],
+                                              const TileSeq& seq, uint32_t tmem,
                                               uint32_t sQ, uint32_t sK, uint32_t sV,
                                               uint32_t bar0, volatile int* abort_flag,
                                               const CUtensorMap* tmQ, const CUtensorMap* tmK,
@@ -180,7 +203,7 @@ __device__ __forceinline__ void control_roles(const FwdArgs& a, const Work& wk, 
     // Warp 8 loads Q0, Q1 and the K tiles; warp 10 loads the V tiles.  Each
     // waits only on its own stages, so a V stage still held by the PV
     // products never delays a K load.
-    if (lane == 0 && nt > 0) {
+    if (lane == 0 && seq.n > 0) {
       if (warp == 8) {
         tma_prefetch_desc(tmQ);
         mbar_arrive_expect_tx(bar(C::B_Q), NQ * C::TILE_BYTES);
@@ -192,13 +215,13 @@ __device__ __forceinline__ void control_roles(const FwdArgs& a, const Work& wk, 
             tma_load_3d(sQ + g * C::TILE_BYTES + ch * CHUNK_BYTES, tmQ, bar(C::B_Q), ch * 64, h,
                         q_row);
         }
-        if (!produce_tiles<D, C::NSK>(wk, nt, kh, sK, bar(C::B_KF), bar(C::B_KE), tmK, abort_flag,
+        if (!produce_tiles<D, C::NSK>(wk, seq, kh, sK, bar(C::B_KF), bar(C::B_KE), tmK, abort_flag,
                                       0x11, lim)) {
           volatile int no_abort = 0;
           wait_bar(bar(C::B_Q), 0, &no_abort, nullptr, 0, lim);
         }
       } else {
-        produce_tiles<D, C::NSV>(wk, nt, kh, sV, bar(C::B_VF), bar(C::B_VE), tmV, abort_flag, 0x12,
+        produce_tiles<D, C::NSV>(wk, seq, kh, sV, bar(C::B_VF), bar(C::B_VE), tmV, abort_flag, 0x12,
                                  lim);
       }
     }
@@ -210,7 +233,7 @@ __device__ __forceinline__ void control_roles(const FwdArgs& a, const Work& wk, 
     // Every wait below reads the same barrier state on all lanes, so the
     // outcome is warp-uniform.
     const uint32_t lead = lane == 0 ? 1u : 0u;
-    if (nt > 0) {
+    if (seq.n > 0) {
       constexpr uint32_t idesc_qk = idesc_bf16(BM, BN, 0);
       constexpr uint32_t idesc_pv = idesc_bf16(BM, D, 1);
       // All shared-memory descriptors are built once.  Moving a descriptor's
@@ -249,27 +272,32 @@ __device__ __forceinline__ void control_roles(const FwdArgs& a, const Work& wk, 
       };
       bool ok = wait_bar(bar(C::B_Q), 0, abort_flag, &g_umma_status, 0x21, lim);
       if (ok) ok = wait_bar(bar(C::B_KF), 0, abort_flag, &g_umma_status, 0x22, lim);
+      // Group g takes part in tile t when ta[g] <= t < tb[g].
+      auto in = [&](int g, int t) -> bool { return t >= ta[g] && t < tb[g]; };
       if (ok) {
         tc_fence_after();
-        if (ntq[0] > 0) qk(0, 0);
-        if (ntq[1] > 0) qk(1, 0);
+        const int t0 = seq.at(0);
+        if (in(0, t0)) qk(0, 0);
+        if (in(1, t0)) qk(1, 0);
         tc_commit_lead(lead, bar(C::B_KE));
       }
-      for (int t = 0; t < nt && ok; ++t) {
-        const int sv = t % C::NSV;
-        const int sk1 = (t + 1) % C::NSK;
+      for (int k = 0; k < seq.n && ok; ++k) {
+        const int t = seq.at(k);
+        const int tn = k + 1 < seq.n ? seq.at(k + 1) : -1;
+        const int sv = k % C::NSV;
+        const int sk1 = (k + 1) % C::NSK;
         // Both operand tiles of this iteration first, so the PV and QK
         // products of a group issue back to back.
-        ok = wait_bar(bar(C::B_VF + sv), static_cast<uint32_t>(t / C::NSV) & 1u, abort_flag,
+        ok = wait_bar(bar(C::B_VF + sv), static_cast<uint32_t>(k / C::NSV) & 1u, abort_flag,
                       &g_umma_status, 0x24, lim);
-        if (ok && t + 1 < nt)
-          ok = wait_bar(bar(C::B_KF + sk1), static_cast<uint32_t>((t + 1) / C::NSK) & 1u,
+        if (ok && tn >= 0)
+          ok = wait_bar(bar(C::B_KF + sk1), static_cast<uint32_t>((k + 1) / C::NSK) & 1u,
                         abort_flag, &g_umma_status, 0x22, lim);
         if (!ok) break;
 #pragma unroll
         for (int g = 0; g < NQ; ++g) {
-          if (t < ntq[g]) {
-            ok = wait_bar(bar(C::B_PF + g), static_cast<uint32_t>(t) & 1u, abort_flag,
+          if (in(g, t)) {
+            ok = wait_bar(bar(C::B_PF + g), static_cast<uint32_t>(t - ta[g]) & 1u, abort_flag,
                           &g_umma_status, 0x23, lim);
             if (!ok) break;
             tc_fence_after();
@@ -277,13 +305,13 @@ __device__ __forceinline__ void control_roles(const FwdArgs& a, const Work& wk, 
             // Only the epilogue waits for PV_g: each tile's softmax already
             // knows PV_g(t-1) is done from S_g(t).  So only the last product
             // of the group is signalled.
-            if (t + 1 == ntq[g]) tc_commit_lead(lead, bar(C::B_OD + g));
+            if (t + 1 == tb[g]) tc_commit_lead(lead, bar(C::B_OD + g));
           }
-          if (t + 1 < ntq[g]) qk(g, sk1);
+          if (tn >= 0 && in(g, tn)) qk(g, sk1);
         }
         if (!ok) break;
         tc_commit_lead(lead, bar(C::B_VE + sv));
-        if (t + 1 < nt) tc_commit_lead(lead, bar(C::B_KE + sk1));
+        if (tn >= 0) tc_commit_lead(lead, bar(C::B_KE + sk1));
       }
       // Drain every MMA issued so far before TMEM can be freed.
       volatile int no_abort = 0;
@@ -297,7 +325,8 @@ __device__ __forceinline__ void control_roles(const FwdArgs& a, const Work& wk, 
 // Softmax groups: warps 0..3 own the rows of Q0, warps 4..7 those of Q1.
 template <int D>
 __device__ __forceinline__ void softmax_role(const FwdArgs& a, const Work& wk, long long row0,
-                                             const int (&ntq)[NQ], uint32_t tmem, uint32_t bar0,
+                                             const int (&ta)[NQ], const int (&tb)[NQ],
+                                             long long vb, uint32_t tmem, uint32_t bar0,
                                              volatile int* abort_flag) {
   using C = Cfg<D>;
   const int warp = threadIdx.x >> 5;
@@ -314,14 +343,22 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, const Work& wk, l
     const uint32_t s_col = C::S_COL + static_cast<uint32_t>(g) * BN;
     const uint32_t o_col = C::O_COL + static_cast<uint32_t>(g) * D;
     const long long grow = row0 + g * BM + row;  // row within the block
-    const bool valid = grow < a.c;
+    const bool valid = grow < a.cq;
     const long long sidx = (wk.state_base + grow) * a.heads + h;
-    const long long qpos = wk.q_pos0 + grow;
     const float sl2 = a.scale_log2;
     const uint64_t sl2x2 = f2pack(sl2, sl2);
-    const int ntg = ntq[g];
+    // Select, not index: g is not a compile-time constant here.
+    const int t_first = g ? ta[1] : ta[0], t_end = g ? tb[1] : tb[0];
 
-    if (ntg > 0) {
+    if (t_end > t_first) {
+      // Keys row_lo .. row_hi-1 of the K/V block are allowed for this row.
+      int row_lo = 0, row_hi = 0;
+      if (valid) {
+        long long lo, hi;
+        row_keys(a, wk, grow, vb, &lo, &hi);
+        row_lo = static_cast<int>(lo);
+        row_hi = static_cast<int>(hi);
+      }
       float m_ld = -INFINITY, l_run = 0.f;
       if (valid) {
         m_ld = a.m[sidx];
@@ -354,8 +391,8 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, const Work& wk, l
       bool m_moved = false;
       bool ok = true;
 
-      for (int t = 0; t < ntg; ++t) {
-        ok = wait_bar(bar(C::B_SF + g), static_cast<uint32_t>(t) & 1u, abort_flag,
+      for (int t = t_first; t < t_end; ++t) {
+        ok = wait_bar(bar(C::B_SF + g), static_cast<uint32_t>(t - t_first) & 1u, abort_flag,
                       &g_umma_status, 0x31, lim);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
@@ -368,18 +405,12 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, const Work& wk, l
 #pragma unroll
         for (int cc = 0; cc < BN / 32; ++cc) reg_fence32(sr[cc]);
 #define RA_S(j) __uint_as_float(sr[(j) >> 5][(j) & 31])
-        // Mask: key j of this tile is allowed iff j < lim_j.  The tail (key
-        // index < c) and the causal rule (key position <= query position)
-        // are both upper bounds on j.
-        long long lim_j = a.c - static_cast<long long>(t) * BN;
-        if (a.causal) {
-          const long long cl = qpos - wk.kv_pos0 - static_cast<long long>(t) * BN + 1;
-          lim_j = cl < lim_j ? cl : lim_j;
-        }
-        if (lim_j < BN) {
+        // Mask: key j of this tile is allowed iff lo_j <= j < hi_j.
+        const int lo_j = row_lo - t * BN, hi_j = row_hi - t * BN;
+        if (lo_j > 0 || hi_j < BN) {
 #pragma unroll
           for (int j = 0; j < BN; ++j)
-            if (j >= lim_j) sr[j >> 5][j & 31] = 0xff800000u;  // -inf
+            if (j < lo_j || j >= hi_j) sr[j >> 5][j & 31] = 0xff800000u;  // -inf
         }
         // Row max: four independent chains over columns 0..127, two new
         // values per three-input max.
@@ -459,7 +490,7 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, const Work& wk, l
       }
 
       if (ok) {
-        // The one commit on B_OD + g follows PV_g(ntg-1), the last product.
+        // The one commit on B_OD + g follows PV_g(t_end-1), the last product.
         ok = wait_bar(bar(C::B_OD + g), 0u, abort_flag, &g_umma_status, 0x33, lim);
         ok = __all_sync(0xffffffffu, ok);
       }
@@ -516,13 +547,17 @@ umma_update_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   const Work wk = decode_work(a, blockIdx.z);
   // Under causal masking the later query rows carry more work, so they are
   // launched first.
-  const int pair = a.causal ? static_cast<int>(gridDim.x - 1 - blockIdx.x)
-                            : static_cast<int>(blockIdx.x);
+  const int pair = a.mask.causal ? static_cast<int>(gridDim.x - 1 - blockIdx.x)
+                                 : static_cast<int>(blockIdx.x);
   const long long row0 = static_cast<long long>(pair) * (NQ * BM);
-  int ntq[NQ];
+  const long long vb = valid_bound(a.mask);
+  int ta[NQ], tb[NQ];
 #pragma unroll
-  for (int g = 0; g < NQ; ++g) ntq[g] = tiles_for(a, wk, row0 + g * BM);
-  const int nt = ntq[0] > ntq[1] ? ntq[0] : ntq[1];
+  for (int g = 0; g < NQ; ++g)
+    tile_range(a, wk, row0 + g * BM, row0 + (g + 1) * BM, vb, BN, &ta[g], &tb[g]);
+  const TileSeq seq = make_seq(ta, tb);
+  // A CTA whose rows see no key of this block leaves their state as it is.
+  if (seq.n == 0) return;
 
   if (tid == 0) {
     for (int i = 0; i < C::NBAR; ++i) {
@@ -551,7 +586,7 @@ umma_update_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   // per branch.
   if (warp >= 8) {
     regs_dec<C::REGS_CONTROL>();
-    control_roles<D>(a, wk, row0, ntq, nt, tmem, sQ, sK, sV, bar0, abort_flag, &tmQ, &tmK, &tmV);
+    control_roles<D>(a, wk, row0, ta, tb, seq, tmem, sQ, sK, sV, bar0, abort_flag, &tmQ, &tmK, &tmV);
     tc_fence_before();
     named_bar_sync(1, NTHREADS);
     if (warp == 9) {
@@ -560,7 +595,7 @@ umma_update_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     }
   } else {
     regs_inc<C::REGS_SOFTMAX>();
-    softmax_role<D>(a, wk, row0, ntq, tmem, bar0, abort_flag);
+    softmax_role<D>(a, wk, row0, ta, tb, vb, tmem, bar0, abort_flag);
     tc_fence_before();
     named_bar_sync(1, NTHREADS);
   }
@@ -590,7 +625,7 @@ cudaError_t launch_d(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap&
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(C::SMEM_BYTES));
   if (e != cudaSuccess) return e;
-  dim3 grid(static_cast<unsigned>((a.c + NQ * BM - 1) / (NQ * BM)), a.heads, a.nwork);
+  dim3 grid(static_cast<unsigned>((a.cq + NQ * BM - 1) / (NQ * BM)), a.heads, a.nwork);
   umma_update_kernel<D><<<grid, NTHREADS, C::SMEM_BYTES, st>>>(tq, tk, tv, a);
   return cudaGetLastError();
 }

@@ -23,7 +23,10 @@
  *          "局部 Softmax 为什么不能直接相加", "Causal Attention
  *          让环不再完全对称", "位置编码必须使用全局位置".
  *  [GUIDE] "RingAttention: Scaling LLM Context to 10M Tokens": "1.
- *          Incremental Online Softmax Accumulation".
+ *          Incremental Online Softmax Accumulation", "Causal Masking:
+ *          Striped and Zig-Zag RingAttention".
+ *  [TEST]  "Ring Attention：把超长序列沿设备环流动": "正确性测试应覆盖哪些边界"
+ *          (its lists "分片边界" and "Mask 与位置").
  *
  * Conventions shared by every call
  * --------------------------------
@@ -78,6 +81,27 @@ typedef enum {
 } ra_status;
 
 typedef enum { RA_F32 = 0, RA_BF16 = 1 } ra_dtype;
+
+/*
+ * Token layouts: which global sequence positions the c rows of block b
+ * (rows [b*c, (b+1)*c) of a ring tensor) hold.  [PB] section 5 and [GUIDE]
+ * "Causal Masking: Striped and Zig-Zag RingAttention" give the two
+ * balanced assignments; [MATH] "Causal masking, load balance, and other
+ * wrinkles" names them.
+ *   RA_LAYOUT_CONTIGUOUS: row r holds position b*c + r.
+ *   RA_LAYOUT_ZIGZAG:     the sequence is cut into 2P chunks of c/2; block
+ *                         b holds chunk b, then chunk 2P-1-b.
+ *   RA_LAYOUT_STRIPED:    row r holds position r*P + b (token t lives on
+ *                         rank t mod P).
+ * The caller lays the tensors out that way; the library only maps rows to
+ * positions for the mask.  Under every layout positions grow with the row
+ * index inside a block.
+ */
+typedef enum {
+  RA_LAYOUT_CONTIGUOUS = 0,
+  RA_LAYOUT_ZIGZAG = 1,
+  RA_LAYOUT_STRIPED = 2
+} ra_layout;
 
 /* Kernel kinds for the tracing calls. */
 typedef enum {
@@ -209,6 +233,69 @@ int ra_ring_forward_host(const void* q_host, const void* k_host, const void* v_h
 int ra_ring_forward_noalloc(const void* q, const void* k, const void* v, float* out, float* lse,
                             long long N, int P, int causal, int d, int heads, int kv_heads,
                             int dtype, void* stream);
+
+/*
+ * Masked variants.  The mask arguments below are the same in the three
+ * calls; [TEST] lists these cases (padding of the last rank with a valid
+ * length, packed documents that must not see each other, sliding-window
+ * and segment masks, non-causal and causal).  Key position kp is allowed
+ * for query position qp when all of these hold:
+ *   - qp < n_valid and kp < n_valid (n_valid < 0: no padding).  A query
+ *     row at or past n_valid sees nothing; after a whole ring its output
+ *     is 0 and its lse -inf.
+ *   - documents (ndocs > 0): cu_seqlens is a DEVICE array of ndocs + 1
+ *     nondecreasing int32 positions with cu_seqlens[0] = 0; document d is
+ *     [cu_seqlens[d], cu_seqlens[d+1]).  qp and kp lie in the same
+ *     document; positions at or past cu_seqlens[ndocs] belong to none and
+ *     are treated as padding.  The array is read by the kernels, not
+ *     checked; a malformed one gives undefined results (reads stay inside
+ *     its ndocs + 1 entries).
+ *   - causal: kp <= qp.
+ *   - window > 0: |qp - kp| < window.  With causal that is the `window`
+ *     most recent positions, qp itself included.
+ * A query with no allowed key keeps its state.  Key tiles that no row of a
+ * query tile may see are not visited, and only tiles that cut a row's
+ * interval are masked elementwise.
+ *
+ * ra_block_update_masked -- ra_block_update with the full mask, a layout,
+ * and query and key blocks of different lengths.
+ *   q: [c_q, heads, d]; k, v: [c_kv, kv_heads, d]; m, l, o: [c_q, heads(, d)].
+ *   layout RA_LAYOUT_CONTIGUOUS: positions are q_off + r and kv_off + t;
+ *     P, q_block and kv_block are ignored.
+ *   layout RA_LAYOUT_ZIGZAG / RA_LAYOUT_STRIPED: the blocks are blocks
+ *     q_block and kv_block (0 <= both < P) of that layout with block length
+ *     c_q (zigzag: c_q == c_kv, even); q_off and kv_off are ignored.
+ */
+int ra_block_update_masked(const void* q, const void* k, const void* v, float* m, float* l,
+                           float* o, long long c_q, long long c_kv, int d, int heads,
+                           int kv_heads, int layout, int P, int q_block, int kv_block,
+                           long long q_off, long long kv_off, int causal, long long window,
+                           long long n_valid, const int* cu_seqlens, int ndocs, int dtype,
+                           void* stream);
+
+/*
+ * ra_ring_step_masked -- ra_ring_step with a layout and the full mask.
+ * Block i of every tensor holds the positions `layout` gives it (N = P*c;
+ * zigzag needs c even).  Ranks whose pair (i, j) holds no allowed
+ * (query, key) pair under the causal, window and valid-length rules are
+ * not launched; with a zigzag or striped layout under causal every rank
+ * has work at every step [PB] section 5.
+ */
+int ra_ring_step_masked(const void* q, const void* k, const void* v, float* m, float* l,
+                        float* o, long long N, int P, int s, int layout, int causal,
+                        long long window, long long n_valid, const int* cu_seqlens, int ndocs,
+                        int d, int heads, int kv_heads, int dtype, void* stream);
+
+/*
+ * ra_ring_forward_masked -- ra_ring_forward with a layout and the full
+ * mask: state init, ra_ring_step_masked for s = 0 .. P-1, finalize.  The
+ * outputs are in the tensors' row order (the layout's order), like q.
+ * Scratch as in ra_ring_forward.
+ */
+int ra_ring_forward_masked(const void* q, const void* k, const void* v, float* out, float* lse,
+                           long long N, int P, int layout, int causal, long long window,
+                           long long n_valid, const int* cu_seqlens, int ndocs, int d,
+                           int heads, int kv_heads, int dtype, void* stream);
 
 /*
  * ra_device_status -- synchronize `stream`, then read and clear the
