@@ -103,10 +103,12 @@ struct Cfg {
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
   static_assert(O_COL + NQ * D <= TMEM_COLS, "TMEM budget");
-  // setmaxnreg split of the launch allocation (the best split, without
-  // spills, differs with d).
-  static constexpr uint32_t REGS_SOFTMAX = (D == 64) ? 224 : 216;
-  static constexpr uint32_t REGS_CONTROL = (D == 64) ? 56 : 72;
+  // setmaxnreg split of the launch allocation.  The MMA issuer must not
+  // spill: a local-memory access in its loop stalls the tensor pipe.  At
+  // d = 128 it needs more than 72 registers, so the softmax warps give up
+  // 8 (their few spills sit outside the tile loop).
+  static constexpr uint32_t REGS_SOFTMAX = (D == 64) ? 224 : 208;
+  static constexpr uint32_t REGS_CONTROL = (D == 64) ? 56 : 88;
   static_assert(NQ * 128 * REGS_SOFTMAX + 128 * REGS_CONTROL == NTHREADS * REGS_LAUNCH,
                 "setmaxnreg split must add up to the launch allocation");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget (227 KB per CTA)");
@@ -272,32 +274,40 @@ __device__ __forceinline__ void control_roles(const FwdArgs& a, const Work& wk, 
       };
       bool ok = wait_bar(bar(C::B_Q), 0, abort_flag, &g_umma_status, 0x21, lim);
       if (ok) ok = wait_bar(bar(C::B_KF), 0, abort_flag, &g_umma_status, 0x22, lim);
-      // Group g takes part in tile t when ta[g] <= t < tb[g].
-      auto in = [&](int g, int t) -> bool { return t >= ta[g] && t < tb[g]; };
+      // The loop runs over the visit index k (tile seq.at(k)); it needs no
+      // tile index, only where each group's run of tiles starts in the
+      // visit (ks) and how long it is (ne).  A group's tiles are contiguous
+      // in the visit.  Every instruction here delays the tensor pipe, so
+      // the per-group test is one subtract and one unsigned compare.
+      int ks[NQ], ne[NQ];
+#pragma unroll
+      for (int g = 0; g < NQ; ++g) {
+        ne[g] = tb[g] > ta[g] ? tb[g] - ta[g] : 0;
+        ks[g] = ta[g] < seq.a0 + seq.na ? ta[g] - seq.a0 : seq.na + (ta[g] - seq.b0);
+      }
       if (ok) {
         tc_fence_after();
-        const int t0 = seq.at(0);
-        if (in(0, t0)) qk(0, 0);
-        if (in(1, t0)) qk(1, 0);
+        if (ks[0] == 0 && ne[0] > 0) qk(0, 0);
+        if (ks[1] == 0 && ne[1] > 0) qk(1, 0);
         tc_commit_lead(lead, bar(C::B_KE));
       }
       for (int k = 0; k < seq.n && ok; ++k) {
-        const int t = seq.at(k);
-        const int tn = k + 1 < seq.n ? seq.at(k + 1) : -1;
+        const bool more = k + 1 < seq.n;
         const int sv = k % C::NSV;
         const int sk1 = (k + 1) % C::NSK;
         // Both operand tiles of this iteration first, so the PV and QK
         // products of a group issue back to back.
         ok = wait_bar(bar(C::B_VF + sv), static_cast<uint32_t>(k / C::NSV) & 1u, abort_flag,
                       &g_umma_status, 0x24, lim);
-        if (ok && tn >= 0)
+        if (ok && more)
           ok = wait_bar(bar(C::B_KF + sk1), static_cast<uint32_t>((k + 1) / C::NSK) & 1u,
                         abort_flag, &g_umma_status, 0x22, lim);
         if (!ok) break;
 #pragma unroll
         for (int g = 0; g < NQ; ++g) {
-          if (in(g, t)) {
-            ok = wait_bar(bar(C::B_PF + g), static_cast<uint32_t>(t - ta[g]) & 1u, abort_flag,
+          const int kg = k - ks[g];  // tile kg of group g's run
+          if (static_cast<unsigned>(kg) < static_cast<unsigned>(ne[g])) {
+            ok = wait_bar(bar(C::B_PF + g), static_cast<uint32_t>(kg) & 1u, abort_flag,
                           &g_umma_status, 0x23, lim);
             if (!ok) break;
             tc_fence_after();
@@ -305,13 +315,13 @@ __device__ __forceinline__ void control_roles(const FwdArgs& a, const Work& wk, 
             // Only the epilogue waits for PV_g: each tile's softmax already
             // knows PV_g(t-1) is done from S_g(t).  So only the last product
             // of the group is signalled.
-            if (t + 1 == tb[g]) tc_commit_lead(lead, bar(C::B_OD + g));
+            if (kg + 1 == ne[g]) tc_commit_lead(lead, bar(C::B_OD + g));
           }
-          if (tn >= 0 && in(g, tn)) qk(g, sk1);
+          if (static_cast<unsigned>(kg + 1) < static_cast<unsigned>(ne[g])) qk(g, sk1);
         }
         if (!ok) break;
         tc_commit_lead(lead, bar(C::B_VE + sv));
-        if (tn >= 0) tc_commit_lead(lead, bar(C::B_KE + sk1));
+        if (more) tc_commit_lead(lead, bar(C::B_KE + sk1));
       }
       // Drain every MMA issued so far before TMEM can be freed.
       volatile int no_abort = 0;
@@ -352,6 +362,8 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, const Work& wk, l
 
     if (t_end > t_first) {
       // Keys row_lo .. row_hi-1 of the K/V block are allowed for this row.
+      // Tiles full_0 .. full_0 + n_full - 1 lie wholly inside that range and
+      // need no mask.
       int row_lo = 0, row_hi = 0;
       if (valid) {
         long long lo, hi;
@@ -359,6 +371,8 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, const Work& wk, l
         row_lo = static_cast<int>(lo);
         row_hi = static_cast<int>(hi);
       }
+      const int full_0 = (row_lo + BN - 1) / BN;
+      const int n_full = row_hi / BN - full_0 > 0 ? row_hi / BN - full_0 : 0;
       float m_ld = -INFINITY, l_run = 0.f;
       if (valid) {
         m_ld = a.m[sidx];
@@ -406,8 +420,8 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, const Work& wk, l
         for (int cc = 0; cc < BN / 32; ++cc) reg_fence32(sr[cc]);
 #define RA_S(j) __uint_as_float(sr[(j) >> 5][(j) & 31])
         // Mask: key j of this tile is allowed iff lo_j <= j < hi_j.
-        const int lo_j = row_lo - t * BN, hi_j = row_hi - t * BN;
-        if (lo_j > 0 || hi_j < BN) {
+        if (static_cast<unsigned>(t - full_0) >= static_cast<unsigned>(n_full)) {
+          const int lo_j = row_lo - t * BN, hi_j = row_hi - t * BN;
 #pragma unroll
           for (int j = 0; j < BN; ++j)
             if (j < lo_j || j >= hi_j) sr[j >> 5][j & 31] = 0xff800000u;  // -inf
