@@ -12,6 +12,8 @@ from .binding import (  # noqa: E402,F401
     layout_positions,
     ra_block_update,
     ra_block_update_masked,
+    ra_decode_forward,
+    ra_decode_partial,
     ra_device_status,
     ra_finalize,
     ra_merge,

@@ -32,6 +32,8 @@ KERNEL_KINDS = {
     "block_update_f32": 2,
     "merge": 3,
     "finalize": 4,
+    "decode_split": 5,
+    "decode_combine": 6,
 }
 
 _lock = threading.Lock()
@@ -57,6 +59,8 @@ _SIGNATURES = {
     "ra_block_update_masked": ("PPPPPPLLiiiiiiiLLiLLPiiP", "i"),
     "ra_ring_step_masked": ("PPPPPPLiiiiLLPiiiiiP", "i"),
     "ra_ring_forward_masked": ("PPPPPLiiiLLPiiiiiP", "i"),
+    "ra_decode_partial": ("PPPPPPLLiiiLLiLiP", "i"),
+    "ra_decode_forward": ("PPPPPLLiLiLiiiiP", "i"),
     "ra_device_status": ("P", "i"),
     "ra_selftest_wait_timeout": ("LP", "i"),
     "ra_trace_enable": ("i", "i"),
@@ -305,6 +309,47 @@ def ra_ring_forward_masked(q, k, v, *, P: int, layout="contiguous", causal: bool
         _dev(lse, "lse", torch.float32), N, int(P), _layout(layout), int(bool(causal)),
         int(window), int(n_valid), cu_ptr, ndocs, d, heads, kv_heads, _qkv_dtype(q),
         _stream(stream)))
+    return out, lse
+
+
+def _decode_shapes(q, k, v):
+    if q.dim() != 3 or k.dim() != 3 or v.dim() != 3 or k.shape != v.shape:
+        raise ValueError("q: [n_q, heads, d]; k, v: [n_kv, kv_heads, d]")
+    if k.dtype != q.dtype or v.dtype != q.dtype or q.shape[2] != k.shape[2]:
+        raise ValueError("q, k, v must share dtype and head dim")
+    return q.shape[0], q.shape[1], k.shape[0], k.shape[1], q.shape[2]
+
+
+def ra_decode_partial(q, k, v, m, l, o, *, q_off: int, kv_off: int = 0, causal: bool = True,
+                      window: int = 0, stream=None):
+    """Fold one K/V shard into the state (m, l, o) of n_q query rows, in place."""
+    n_q, heads, n_kv, kv_heads, d = _decode_shapes(q, k, v)
+    _state_shapes(m, l, o, n_q, heads, d)
+    _check(lib().ra_decode_partial(
+        _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(m, "m", torch.float32),
+        _dev(l, "l", torch.float32), _dev(o, "o", torch.float32), n_q, n_kv, d, heads, kv_heads,
+        int(q_off), int(kv_off), int(bool(causal)), int(window), _qkv_dtype(q), _stream(stream)))
+
+
+def ra_decode_forward(q, k, v, *, P: int, q_off: int | None = None, causal: bool = True,
+                      window: int = 0, out=None, lse=None, stream=None):
+    """Decode attention of q [n_q, heads, d] against k, v [n_kv, kv_heads, d]
+    held as P shards.  q_off defaults to n_kv - n_q (the new tokens are the
+    last ones of the history).  Returns (out [n_q, heads, d], lse [n_q, heads])."""
+    n_q, heads, n_kv, kv_heads, d = _decode_shapes(q, k, v)
+    if q_off is None:
+        q_off = n_kv - n_q
+    if out is None:
+        out = torch.empty((n_q, heads, d), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((n_q, heads), dtype=torch.float32, device=q.device)
+    _state_shapes(lse, lse, out, n_q, heads, d)
+    kp = _dev(k, "k") if n_kv else 0
+    vp = _dev(v, "v") if n_kv else 0
+    _check(lib().ra_decode_forward(
+        _dev(q, "q"), kp, vp, _dev(out, "out", torch.float32), _dev(lse, "lse", torch.float32),
+        n_q, n_kv, int(P), int(q_off), int(bool(causal)), int(window), d, heads, kv_heads,
+        _qkv_dtype(q), _stream(stream)))
     return out, lse
 
 

@@ -111,14 +111,15 @@ int get_encoder() {
 }
 
 // 3-D map over a token-major bf16 tensor [rows, heads, d]: dims (d, heads,
-// rows).  The box is 64 elements (128 B, one swizzle span) x 1 head x 128
-// rows, with 128-byte swizzle.  Rows past the end read as zero.
-int encode_map(CUtensorMap* map, const void* base, long long rows, int heads, int d) {
+// rows).  The box is 64 elements (128 B, one swizzle span) x 1 head x
+// box_rows rows, with 128-byte swizzle.  Rows past the end read as zero.
+int encode_map(CUtensorMap* map, const void* base, long long rows, int heads, int d,
+               int box_rows = 128) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
                               static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
                                  static_cast<cuuint64_t>(heads) * d * 2};
-  const cuuint32_t box[3] = {64, 1, 128};
+  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -411,6 +412,95 @@ int noalloc_scratch(float** out) {
   return RA_OK;
 }
 
+// ----------------------------------------------------------------- decode
+int decode_args_check(const void* q, const void* k, const void* v, long long n_q, long long n_kv,
+                      int d, int heads, int kv_heads, long long window, int dtype) {
+  int rc;
+  if ((rc = check_common(d, heads, dtype)) != RA_OK) return rc;
+  if ((rc = check_heads(heads, kv_heads)) != RA_OK) return rc;
+  if (dtype != RA_BF16) return fail(RA_ERR_UNSUPPORTED, "the decode path takes bf16 q, k, v");
+  if (n_q < 0 || n_kv < 0) return fail(RA_ERR_INVALID, "n_q=%lld or n_kv=%lld is negative", n_q, n_kv);
+  if (n_kv > (1LL << 31) - 256) return fail(RA_ERR_UNSUPPORTED, "n_kv=%lld exceeds the 32-bit TMA row coordinate", n_kv);
+  if (window < 0) return fail(RA_ERR_INVALID, "window=%lld is negative", window);
+  if (static_cast<long long>(heads / kv_heads) * n_q > 16)
+    return fail(RA_ERR_UNSUPPORTED,
+                "(heads / kv_heads) * n_q = %lld query rows per KV head exceeds 16; use "
+                "ra_block_update_masked for longer query blocks",
+                static_cast<long long>(heads / kv_heads) * n_q);
+  (void)q; (void)k; (void)v;
+  return RA_OK;
+}
+
+// Split-K launch over nshard shards of shard_len keys, then the combine of
+// each shard's partials into its state (m, l, o: [nshard][n_q][heads]).
+int decode_run(const void* q, const void* k, const void* v, float* m, float* l, float* o,
+               long long n_q, long long n_kv, long long shard_len, int nshard, long long q_off,
+               long long kv_off, int causal, long long window, int d, int heads, int kv_heads,
+               cudaStream_t st) {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // About four CTAs per SM over the whole launch, each at least 4 tiles
+  // (one per warp) of 32 keys.
+  long long want = (4LL * sms + static_cast<long long>(kv_heads) * nshard - 1) /
+                   (static_cast<long long>(kv_heads) * nshard);
+  if (want < 1) want = 1;
+  long long chunk = (shard_len + want - 1) / want;
+  chunk = ((chunk + 31) / 32) * 32;
+  if (chunk < 128) chunk = 128;
+  const long long nsplit = (shard_len + chunk - 1) / chunk;
+  const long long rows = n_q * heads;  // state rows of one shard
+  const size_t n_part = static_cast<size_t>(nshard) * nsplit * rows;
+  float* part = nullptr;
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&part),
+                                  n_part * (2 + static_cast<size_t>(d)) * sizeof(float), st);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(RA_ERR_ALLOC, "cudaMallocAsync of the decode partial states failed: %s",
+                cudaGetErrorString(e));
+  }
+  int rc = get_encoder();
+  CUtensorMap tk, tv;
+  if (rc == RA_OK) rc = encode_map(&tk, k, n_kv, kv_heads, d, 32);
+  if (rc == RA_OK) rc = encode_map(&tv, v, n_kv, kv_heads, d, 32);
+  if (rc == RA_OK) {
+    ra::DecArgs a{};
+    a.q = q;
+    a.po = part;
+    a.pm = part + n_part * d;
+    a.pl = a.pm + n_part;
+    a.n_q = n_q;
+    a.n_kv = n_kv;
+    a.shard_len = shard_len;
+    a.chunk = chunk;
+    a.q_off = q_off;
+    a.kv_off = kv_off;
+    a.heads = heads;
+    a.kv_heads = kv_heads;
+    a.nsplit = static_cast<int>(nsplit);
+    a.nshard = nshard;
+    a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+    a.wait_limit = kWaitLimit;
+    a.mask.causal = causal ? 1 : 0;
+    a.mask.window = window > kAllValid ? kAllValid : window;
+    a.mask.n_valid = kAllValid;
+    TraceScope t0(RA_KERNEL_DECODE_SPLIT, st);
+    e = ra::launch_decode_split(a, d, tk, tv, st);
+    t0.done(e == cudaSuccess);
+    if (e != cudaSuccess) {
+      rc = cuda_fail(e, "decode split launch");
+    } else {
+      TraceScope t1(RA_KERNEL_DECODE_COMBINE, st);
+      e = ra::launch_decode_combine(m, l, o, a.pm, a.pl, a.po, rows, a.nsplit, nshard, d, st);
+      t1.done(e == cudaSuccess);
+      if (e != cudaSuccess) rc = cuda_fail(e, "decode combine launch");
+    }
+  }
+  e = cudaFreeAsync(part, st);
+  if (rc == RA_OK && e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync");
+  return rc;
+}
+
 }  // namespace
 
 extern "C" {
@@ -642,14 +732,96 @@ int ra_ring_forward_noalloc(const void* q, const void* k, const void* v, float* 
                            static_cast<cudaStream_t>(stream), l_scratch);
 }
 
+int ra_decode_partial(const void* q, const void* k, const void* v, float* m, float* l, float* o,
+                      long long n_q, long long n_kv, int d, int heads, int kv_heads,
+                      long long q_off, long long kv_off, int causal, long long window,
+                      int dtype, void* stream) {
+  int rc = decode_args_check(q, k, v, n_q, n_kv, d, heads, kv_heads, window, dtype);
+  if (rc != RA_OK) return rc;
+  if (n_q == 0 || n_kv == 0) return RA_OK;
+  if ((rc = check_ptrs({q, k, v, m, l, o})) != RA_OK) return rc;
+  return decode_run(q, k, v, m, l, o, n_q, n_kv, n_kv, 1, q_off, kv_off, causal, window, d, heads,
+                    kv_heads, static_cast<cudaStream_t>(stream));
+}
+
+int ra_decode_forward(const void* q, const void* k, const void* v, float* out, float* lse,
+                      long long n_q, long long n_kv, int P, long long q_off, int causal,
+                      long long window, int d, int heads, int kv_heads, int dtype,
+                      void* stream) {
+  int rc = decode_args_check(q, k, v, n_q, n_kv, d, heads, kv_heads, window, dtype);
+  if (rc != RA_OK) return rc;
+  if (P < 1 || P > 65535) return fail(RA_ERR_INVALID, "P=%d out of range [1, 65535]", P);
+  if (n_q == 0) return RA_OK;
+  if ((rc = check_ptrs({q, out, lse})) != RA_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const long long rows = n_q * heads;
+  if (n_kv == 0) {  // no key: every row is empty (out = 0, lse = -inf)
+    float* l0 = nullptr;
+    cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&l0), rows * sizeof(float), st);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(RA_ERR_ALLOC, "cudaMallocAsync of %lld floats failed", rows);
+    }
+    e = ra::launch_state_init(lse, l0, out, n_q, heads, d, st);
+    if (e == cudaSuccess) e = ra::launch_finalize(lse, l0, out, out, lse, n_q, heads, d, st);
+    const cudaError_t ef = cudaFreeAsync(l0, st);
+    if (e != cudaSuccess) return cuda_fail(e, "decode empty-key launch");
+    return ef == cudaSuccess ? RA_OK : cuda_fail(ef, "cudaFreeAsync");
+  }
+  if ((rc = check_ptrs({k, v})) != RA_OK) return rc;
+  const long long shard_len = (n_kv + P - 1) / P;
+  const int nshard = static_cast<int>((n_kv + shard_len - 1) / shard_len);
+  // Shard states: m, l [nshard][rows], o [nshard][rows][d].
+  float* sstate = nullptr;
+  const size_t n_rows = static_cast<size_t>(nshard) * rows;
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&sstate),
+                                  n_rows * (2 + static_cast<size_t>(d)) * sizeof(float), st);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(RA_ERR_ALLOC, "cudaMallocAsync of the shard states failed: %s", cudaGetErrorString(e));
+  }
+  float* so = sstate;
+  float* sm = so + n_rows * d;
+  float* sl = sm + n_rows;
+  {
+    TraceScope t0(RA_KERNEL_STATE_INIT, st);
+    e = ra::launch_state_init(sm, sl, so, static_cast<long long>(nshard) * n_q, heads, d, st);
+    t0.done(e == cudaSuccess);
+  }
+  rc = e == cudaSuccess ? RA_OK : cuda_fail(e, "state-init launch");
+  if (rc == RA_OK)
+    rc = decode_run(q, k, v, sm, sl, so, n_q, n_kv, shard_len, nshard, q_off, 0, causal, window,
+                    d, heads, kv_heads, st);
+  // Global reduction: a tree of merges, shard b into shard a.
+  for (int cnt = nshard; rc == RA_OK && cnt > 1;) {
+    const int half = cnt / 2, keep = cnt - half;
+    TraceScope tm(RA_KERNEL_MERGE, st);
+    e = ra::launch_merge(sm, sl, so, sm + keep * rows, sl + keep * rows, so + keep * rows * d,
+                         static_cast<long long>(half) * n_q, heads, d, st);
+    tm.done(e == cudaSuccess);
+    if (e != cudaSuccess) rc = cuda_fail(e, "merge launch");
+    cnt = keep;
+  }
+  if (rc == RA_OK) {
+    TraceScope tf(RA_KERNEL_FINALIZE, st);
+    e = ra::launch_finalize(sm, sl, so, out, lse, n_q, heads, d, st);
+    tf.done(e == cudaSuccess);
+    if (e != cudaSuccess) rc = cuda_fail(e, "finalize launch");
+  }
+  e = cudaFreeAsync(sstate, st);
+  if (rc == RA_OK && e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync");
+  return rc;
+}
+
 int ra_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-  int a = 0, b = 0;
+  int a = 0, b = 0, c = 0;
   if ((e = ra::take_umma_status(&a)) != cudaSuccess) return cuda_fail(e, "reading the tcgen05 kernel status");
   if ((e = ra::take_simt_status(&b)) != cudaSuccess) return cuda_fail(e, "reading the fp32 kernel status");
-  if (a != 0 || b != 0)
-    return fail(RA_ERR_TIMEOUT, "a kernel gave up a bounded wait (codes 0x%x, 0x%x)", a, b);
+  if ((e = ra::take_decode_status(&c)) != cudaSuccess) return cuda_fail(e, "reading the decode kernel status");
+  if (a != 0 || b != 0 || c != 0)
+    return fail(RA_ERR_TIMEOUT, "a kernel gave up a bounded wait (codes 0x%x, 0x%x, 0x%x)", a, b, c);
   return RA_OK;
 }
 

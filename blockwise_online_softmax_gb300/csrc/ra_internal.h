@@ -201,6 +201,31 @@ __device__ __forceinline__ void tile_range(const FwdArgs& a, const Work& wk, lon
   *t1 = static_cast<int>((hi1 + bn - 1) / bn);
 }
 
+// One launch of the decode split-K kernel: n_q query tokens against n_kv
+// keys cut into nshard shards of shard_len keys, each shard into nsplit
+// chunks of `chunk` keys (a multiple of 32).  CTA (split, kv head, shard)
+// writes the partial state of its KV head's g * n_q rows to
+// pm/pl [nshard][nsplit][n_q][heads] and po [..][d].
+struct DecArgs {
+  const void* q;  // [n_q, heads, d] bf16
+  float* pm;
+  float* pl;
+  float* po;
+  long long n_q;
+  long long n_kv;
+  long long shard_len;
+  long long chunk;
+  long long q_off;   // position of query row 0
+  long long kv_off;  // position of key 0
+  int heads;
+  int kv_heads;
+  int nsplit;
+  int nshard;
+  float scale_log2;  // log2(e)/sqrt(d)
+  long long wait_limit;
+  MaskArgs mask;
+};
+
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -215,9 +240,15 @@ cudaError_t launch_simt_update(const FwdArgs& a, int d, cudaStream_t st);
 cudaError_t launch_umma_update(const FwdArgs& a, int d, const CUtensorMap& tq,
                                const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st);
 cudaError_t launch_wait_selftest(long long limit_cycles, cudaStream_t st);
+cudaError_t launch_decode_split(const DecArgs& a, int d, const CUtensorMap& tk,
+                                const CUtensorMap& tv, cudaStream_t st);
+cudaError_t launch_decode_combine(float* m, float* l, float* o, const float* pm, const float* pl,
+                                  const float* po, long long rows_per_shard, int nsplit,
+                                  int nshard, int d, cudaStream_t st);
 
 // Device status words (one per kernel translation unit): read and clear.
 cudaError_t take_umma_status(int* code);
 cudaError_t take_simt_status(int* code);
+cudaError_t take_decode_status(int* code);
 
 }  // namespace ra

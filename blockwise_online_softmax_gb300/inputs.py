@@ -216,3 +216,52 @@ def sample_rows(w: Workload | str, *, random_per_block: int = 16, seed: int = 12
             r0 = int(idx.min())
             rows.extend(r for r in range(r0, min(r0 + after_planted, w.N)))
     return np.unique(np.asarray(rows, dtype=np.int64))
+
+
+# ------------------------------------------------------------------ decode
+@dataclass(frozen=True)
+class DecodeWorkload:
+    """A decode step: n_q new query tokens against a K/V history of n_kv
+    tokens (the new ones included, so the queries sit at positions
+    n_kv - n_q .. n_kv - 1) held as P shards.  Causal.  Same recipe as
+    above: Q, K, V are tensor ids 0, 1, 2 of ``seed``, times ``scale``,
+    cast to bf16."""
+    name: str
+    seed: int
+    n_q: int
+    heads: int
+    kv_heads: int
+    d: int
+    n_kv: int
+    P: int
+    scale: float = 1.0
+    notes: str = ""
+
+    def kv_bytes(self) -> int:
+        """K and V, read once: the algorithmic HBM traffic of the step."""
+        return 2 * self.n_kv * self.kv_heads * self.d * 2
+
+    def flops(self) -> float:
+        """4*d per allowed (query, key) pair per query head."""
+        keys = sum(self.n_kv - self.n_q + i + 1 for i in range(self.n_q))
+        return 4.0 * self.d * self.heads * keys
+
+
+DECODE_WORKLOADS = {
+    "decode-1m": DecodeWorkload(
+        "decode-1m", seed=5, n_q=1, heads=32, kv_heads=8, d=128, n_kv=1 << 20, P=64,
+        notes="one new token after a 1M-token history in 64 shards, GQA 32/8"),
+    "decode-1m-q4": DecodeWorkload(
+        "decode-1m-q4", seed=6, n_q=4, heads=32, kv_heads=8, d=128, n_kv=1 << 20, P=64,
+        notes="four new tokens (a short query block) after a 1M-token history"),
+}
+
+
+def make_decode(w: DecodeWorkload | str):
+    """(q [n_q, heads, d], k, v [n_kv, kv_heads, d]) bf16 CPU tensors."""
+    if isinstance(w, str):
+        w = DECODE_WORKLOADS[w]
+    q = (randn_chunked((w.n_q, w.heads, w.d), w.seed, 0) * w.scale).to(torch.bfloat16)
+    k = (randn_chunked((w.n_kv, w.kv_heads, w.d), w.seed, 1) * w.scale).to(torch.bfloat16)
+    v = (randn_chunked((w.n_kv, w.kv_heads, w.d), w.seed, 2) * w.scale).to(torch.bfloat16)
+    return q, k, v

@@ -110,7 +110,9 @@ typedef enum {
   RA_KERNEL_BLOCK_UPDATE_F32 = 2,  /* fp32 FFMA kernel */
   RA_KERNEL_MERGE = 3,
   RA_KERNEL_FINALIZE = 4,
-  RA_KERNEL_KINDS = 5
+  RA_KERNEL_DECODE_SPLIT = 5,   /* decode split-K kernel (CUDA cores, TMA) */
+  RA_KERNEL_DECODE_COMBINE = 6, /* folds a shard's split partial states */
+  RA_KERNEL_KINDS = 7
 } ra_kernel_kind;
 
 /*
@@ -296,6 +298,52 @@ int ra_ring_forward_masked(const void* q, const void* k, const void* v, float* o
                            long long N, int P, int layout, int causal, long long window,
                            long long n_valid, const int* cu_seqlens, int ndocs, int d,
                            int heads, int kv_heads, int dtype, void* stream);
+
+/*
+ * Decode and short query blocks ("Ring Attention：把超长序列沿设备环流动",
+ * section "训练与推理的适用方式不同").  A decode step has a few new query
+ * tokens per sequence and a long K/V history.  Rotating K/V blocks around a
+ * ring does not pay there; the query goes to every K/V shard, each shard
+ * computes a partial (m, l, O~) state of the query rows, and the shards'
+ * states are combined by the online-softmax merge.
+ *
+ * ra_decode_partial -- fold one K/V shard into the running state of n_q
+ * query rows (in place, like ra_block_update), for deployments where each
+ * device holds one shard and merges states with ra_merge afterwards.
+ *   q: [n_q, heads, d] bf16, token positions q_off .. q_off + n_q - 1.
+ *   k, v: [n_kv, kv_heads, d] bf16, positions kv_off .. kv_off + n_kv - 1.
+ *   m, l: [n_q, heads] fp32; o: [n_q, heads, d] fp32 (updated in place).
+ *   causal and window: as in the masked calls (kp <= qp; |qp - kp| < window).
+ *   (heads / kv_heads) * n_q must be <= 16: every KV head's query rows are
+ *   held together, so each K/V byte is read once.  Longer query blocks
+ *   belong to ra_block_update_masked.  dtype must be RA_BF16.
+ * The work is HBM-bound: one CUDA-core kernel streams the keys of each KV
+ * head in chunks spread over the SMs (split-K) and writes one partial state
+ * per chunk; a second kernel folds them into m, l, o.  The partial states
+ * (chunks x n_q x heads x (d + 2) fp32) are allocated with cudaMallocAsync
+ * on `stream`.
+ */
+int ra_decode_partial(const void* q, const void* k, const void* v, float* m, float* l, float* o,
+                      long long n_q, long long n_kv, int d, int heads, int kv_heads,
+                      long long q_off, long long kv_off, int causal, long long window,
+                      int dtype, void* stream);
+
+/*
+ * ra_decode_forward -- the whole decode attention of n_q query tokens
+ * against a K/V history of n_kv tokens (positions 0 .. n_kv - 1) split into
+ * P shards of ceil(n_kv / P) keys: the partial state of every shard (one
+ * launch over all shards), then the global reduction as a tree of merges
+ * (ceil(log2 P) launches of the ra_merge kernel), then the finalize.
+ *   out: [n_q, heads, d] fp32; lse: [n_q, heads] fp32 (written).
+ * Query positions are q_off .. q_off + n_q - 1 (for decode after a history
+ * of n_kv tokens that includes the new ones: q_off = n_kv - n_q).  With
+ * n_kv = 0 every row gets out = 0 and lse = -inf.  Scratch as above, plus
+ * the P shard states.
+ */
+int ra_decode_forward(const void* q, const void* k, const void* v, float* out, float* lse,
+                      long long n_q, long long n_kv, int P, long long q_off, int causal,
+                      long long window, int d, int heads, int kv_heads, int dtype,
+                      void* stream);
 
 /*
  * ra_device_status -- synchronize `stream`, then read and clear the

@@ -124,3 +124,26 @@ def test_masked_zero_size_is_a_no_op(lib):
                                       64, 2, 2, 1, None) == 0
     assert lib.ra_ring_step_masked(None, None, None, None, None, None, 0, 4, 0, 2, 0, 0, -1, None,
                                    0, 64, 2, 2, 1, None) == 0
+
+
+def test_decode_rejects_bad_arguments(lib):
+    def fwd(n_q=1, heads=32, kv_heads=8, d=128, dtype=1, P=4, window=0):
+        return lib.ra_decode_forward(FAKE, FAKE, FAKE, FAKE, FAKE, n_q, 1000, P, 999, 1, window,
+                                     d, heads, kv_heads, dtype, None)
+    assert fwd(n_q=5) == -2 and b"exceeds 16" in lib.ra_last_error()
+    assert fwd(dtype=0) == -2 and b"bf16" in lib.ra_last_error()
+    assert fwd(P=0) == -1 and b"P=0" in lib.ra_last_error()
+    assert fwd(window=-3) == -1 and b"window" in lib.ra_last_error()
+    assert fwd(d=96) == -2
+    assert lib.ra_decode_forward(None, None, None, None, None, 0, 1000, 4, 0, 1, 0, 128, 32, 8,
+                                 1, None) == 0  # n_q = 0: nothing to do
+    assert lib.ra_decode_partial(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 0, 128, 32, 8, 0, 0, 1,
+                                 0, 1, None) == 0  # n_kv = 0: the state stays
+
+
+def test_decode_workload_sizes():
+    from blockwise_online_softmax_gb300 import inputs
+
+    w = inputs.DECODE_WORKLOADS["decode-1m"]
+    assert w.kv_bytes() == 2 * (1 << 20) * 8 * 128 * 2
+    assert w.flops() == 4.0 * 128 * 32 * (1 << 20)
