@@ -26,6 +26,17 @@ The JSON line also carries:
 --impl reference times the CPU oracle alone: a bounded sample per step, on
 the same workload, metric and unit.
 
+Decode runs (--decode decode-1m | decode-1m-q4) time ra_decode_forward: a
+few query tokens against a 1M-token K/V history in P shards.  That path is
+HBM-bound, so its metric is the K/V bytes read per second, and its
+roofline is against the measured HBM copy bandwidth.
+
+Masked runs (--layout zigzag|striped, --window W, --docs K, --n-valid V)
+time ra_ring_forward_masked on the same workload laid out and masked that
+way.  Their metric counts 4*d FLOPs per allowed (query, key) pair per query
+head, the exact count under the mask; they carry no e2e figure (the host
+entry point has no masked form).
+
 Multi-GPU (torchrun): each rank runs an independent replica of the
 workload on its own GPU.  The per-GPU work is fixed, the time is the max
 over ranks, and the value is the sum over ranks.
@@ -47,6 +58,47 @@ sys.path.insert(0, ROOT)
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 METRIC = "causal-adjusted attention TFLOP/s on 1 GB300 and % of dense BF16 tensor peak"
+METRIC_MASKED = "attention TFLOP/s over the allowed (query, key) pairs on 1 GB300"
+
+
+class MaskRun:
+    """Layout and mask of a masked run, with the per-position quantities the
+    FLOP count and the oracle sample need (host index arithmetic only)."""
+
+    def __init__(self, w, layout="contiguous", window=0, docs=0, n_valid=-1, seed=0):
+        import numpy as np
+
+        self.layout, self.window = layout, int(window)
+        self.n_valid = w.N if n_valid is None or n_valid < 0 else min(int(n_valid), w.N)
+        self.docs = int(docs)
+        N = w.N
+        if self.docs > 0:
+            rng = np.random.default_rng(1000 + seed)
+            cuts = np.sort(rng.choice(np.arange(1, self.n_valid), size=self.docs - 1,
+                                      replace=False))
+            self.cu = np.concatenate([[0], cuts, [self.n_valid]]).astype(np.int64)
+        else:
+            self.cu = np.array([0, self.n_valid], dtype=np.int64)
+        p = np.arange(N, dtype=np.int64)
+        d = np.clip(np.searchsorted(self.cu, p, side="right") - 1, 0, len(self.cu) - 2)
+        self.doc = np.where(p < self.n_valid, d, -1)
+        lo, hi = self.cu[d], np.minimum(self.cu[d + 1], self.n_valid)
+        if w.causal:
+            hi = np.minimum(hi, p + 1)
+        if self.window > 0:
+            lo = np.maximum(lo, p - self.window + 1)
+            if not w.causal:
+                hi = np.minimum(hi, p + self.window)
+        self.keys = np.where(p < self.n_valid, np.maximum(hi - lo, 0), 0)  # per position
+        self.pairs = int(self.keys.sum())
+
+    def active(self):
+        return (self.layout != "contiguous" or self.window > 0 or self.docs > 0
+                or self.n_valid < len(self.keys))
+
+    def describe(self):
+        return {"layout": self.layout, "window": self.window, "docs": self.docs,
+                "n_valid": self.n_valid, "allowed_pairs": self.pairs}
 
 
 def load_peaks():
@@ -165,38 +217,152 @@ def recorded_traffic(workload: str):
 
 
 # ------------------------------------------------------------------ CPU oracle sample
-def oracle_sample(w, q, k, v, target_s: float, seed: int = 7):
+def oracle_sample(w, q, k, v, target_s: float, seed: int = 7, mask: MaskRun | None = None):
     """Time the fp64 oracle on sampled query rows (all heads, full key
     range), sized to take about ``target_s`` seconds.  Returns (TFLOP/s,
-    cores, description)."""
+    cores, description).  With ``mask``, q/k/v are in sequence order and the
+    oracle applies the mask's window and documents."""
     import numpy as np
 
     import oracle
 
     cores = os.cpu_count() or 1
     rng = np.random.default_rng(seed)
+    kw = {}
+    if mask is not None:
+        kw = dict(window=mask.window, q_doc=mask.doc, k_doc=mask.doc)
 
     def flops(rows):
-        keys = (rows + 1) if w.causal else np.full_like(rows, w.N)
+        if mask is not None:
+            keys = mask.keys[rows]
+        else:
+            keys = (rows + 1) if w.causal else np.full_like(rows, w.N)
         return float(4.0 * w.d * w.heads * keys.sum())
 
     # calibrate on a few rows
     probe = np.sort(rng.integers(w.N // 2, w.N, size=max(2, cores // w.heads + 1)))
     t0 = time.perf_counter()
-    oracle.partial_state(q, k, v, causal=w.causal, rows=probe, threads=cores)
+    oracle.partial_state(q, k, v, causal=w.causal, rows=probe, threads=cores, **kw)
     dt = time.perf_counter() - t0
-    rate = flops(probe) / max(dt, 1e-6)
+    rate = max(flops(probe), 1.0) / max(dt, 1e-6)
     # rows drawn uniformly over the sequence; expected FLOPs per row
-    per_row = 4.0 * w.d * w.heads * (w.N / 2 if w.causal else w.N)
+    if mask is not None:
+        per_row = 4.0 * w.d * w.heads * max(mask.pairs / w.N, 1.0)
+    else:
+        per_row = 4.0 * w.d * w.heads * (w.N / 2 if w.causal else w.N)
     n_rows = int(max(1, min(w.N, target_s * rate / per_row)))
     rows = np.sort(rng.choice(w.N, size=n_rows, replace=False))
     t0 = time.perf_counter()
-    oracle.partial_state(q, k, v, causal=w.causal, rows=rows, threads=cores)
+    oracle.partial_state(q, k, v, causal=w.causal, rows=rows, threads=cores, **kw)
     dt = time.perf_counter() - t0
     f = flops(rows)
     desc = (f"{n_rows} query rows drawn uniformly from {w.N}, all {w.heads} heads, each over its "
-            f"full causal key range ({f:.3e} FLOPs, {dt:.1f} s)")
+            f"full {'masked' if mask is not None else 'causal'} key range ({f:.3e} FLOPs, "
+            f"{dt:.1f} s)")
     return f / dt / 1e12, cores, desc, dt
+
+
+# ------------------------------------------------------------------ decode
+METRIC_DECODE = "decode attention: K/V bytes read per second on 1 GB300 (HBM-bound)"
+
+
+def run_decode(args, ws, rank, local):
+    import numpy as np
+    import torch
+
+    import blockwise_online_softmax_gb300 as ra
+    import oracle
+    from blockwise_online_softmax_gb300 import binding, inputs
+
+    w = inputs.DECODE_WORKLOADS[args.decode]
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    binding.lib()
+    peaks, peak_src = load_peaks()
+    q, k, v = inputs.make_decode(w)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    out = torch.empty((w.n_q, w.heads, w.d), dtype=torch.float32, device=dev)
+    lse = torch.empty((w.n_q, w.heads), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ra.ra_decode_forward(qd, kd, vd, P=w.P, out=out, lse=lse, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    ra.ra_device_status(stream)
+    gpu_index = local
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    if vis and "," not in vis and vis.strip().isdigit():
+        gpu_index = int(vis)
+    clocks = ClockSampler(gpu_index)
+    clocks.start()
+    ra.ra_trace_reset()
+    ra.ra_trace_enable(True)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    ra.ra_trace_enable(False)
+    clk = clocks.stop()
+    ra.ra_device_status(stream)
+    ms_step = reduce_max(ev0.elapsed_time(ev1), ws) / args.steps
+    kinds = ("decode_split", "decode_combine", "merge", "finalize", "state_init")
+    trace = {kd_: ra.ra_trace_query(kd_) for kd_ in kinds}
+    ra.ra_trace_reset()
+    value = ws * w.kv_bytes() / (ms_step * 1e-3) / 1e9
+    n_split, ms_split = trace["decode_split"]
+    achieved = w.kv_bytes() * n_split / (ms_split * 1e-3) / 1e9 if ms_split > 0 else None
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        # The oracle over every query row, on as many query heads as fit the
+        # time budget; its rate is scaled to the same unit (K/V bytes of the
+        # whole step per second).
+        cores = os.cpu_count() or 1
+        qpos = w.n_kv - w.n_q + np.arange(w.n_q)
+        g = w.heads // w.kv_heads
+        t0 = time.perf_counter()
+        oracle.partial_state(q[:, :g], k[:, :1], v[:, :1], causal=True, q_pos=qpos,
+                             threads=cores)
+        per_kv_head = time.perf_counter() - t0
+        nh = int(max(1, min(w.kv_heads, args.cpu_seconds / max(per_kv_head, 1e-6))))
+        t0 = time.perf_counter()
+        oracle.partial_state(q[:, :g * nh], k[:, :nh], v[:, :nh], causal=True, q_pos=qpos,
+                             threads=cores)
+        dt = time.perf_counter() - t0
+        frac = nh / w.kv_heads
+        cpu = {"value": w.kv_bytes() * frac / dt / 1e9, "unit": "GB/s", "cores": cores,
+               "kind": "oracle",
+               "sample": f"all {w.n_q} query rows of the {g * nh} query heads of {nh} of "
+                         f"{w.kv_heads} KV heads, full history ({dt:.1f} s)"}
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC_DECODE, "value": value, "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "n_q": w.n_q, "n_kv": w.n_kv, "P": w.P,
+                   "heads": w.heads, "kv_heads": w.kv_heads, "d": w.d, "causal": True,
+                   "seed": w.seed, "parallelism": f"replicas{ws}",
+                   "kv_bytes_per_step": w.kv_bytes(), "flops_per_step": w.flops(),
+                   "l2": "K and V (4.3 GB) exceed L2; no flush"},
+        "clocks": clk, "e2e": None,
+        "gpu_launches": sum(n for n, _ in trace.values()),
+        "kernel_ms": {kd_: t / args.steps for kd_, (n, t) in trace.items()},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": (achieved / peaks["hbm_gbs"]) if achieved else None,
+                     "traffic": None, "kernel": "decode split-K (CUDA cores, TMA)",
+                     "peak_kind": f"hbm_gbs ({peak_src})"},
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
 
 
 # ------------------------------------------------------------------ arms
@@ -244,13 +410,25 @@ def run_ours(args, w, ws, rank, local):
     peaks, peak_src = load_peaks()
 
     q, k, v = inputs.make_workload(w)
-    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    mask = args.mask
+    if mask is not None:
+        pos = binding.layout_positions(w.N, w.P, mask.layout)
+        qd, kd, vd = q[pos].to(dev), k[pos].to(dev), v[pos].to(dev)
+        cu = torch.tensor(mask.cu, dtype=torch.int32, device=dev) if mask.docs > 0 else None
+    else:
+        qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
     out = torch.empty((w.N, w.heads, w.d), dtype=torch.float32, device=dev)
     lse = torch.empty((w.N, w.heads), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        ra.ra_ring_forward(qd, kd, vd, P=w.P, causal=w.causal, out=out, lse=lse, stream=stream)
+        if mask is None:
+            ra.ra_ring_forward(qd, kd, vd, P=w.P, causal=w.causal, out=out, lse=lse,
+                               stream=stream)
+        else:
+            ra.ra_ring_forward_masked(qd, kd, vd, P=w.P, layout=mask.layout, causal=w.causal,
+                                      window=mask.window, n_valid=mask.n_valid, cu_seqlens=cu,
+                                      out=out, lse=lse, stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -288,15 +466,50 @@ def run_ours(args, w, ws, rank, local):
 
     ms_max = reduce_max(ms_total, ws)
     ms_step = ms_max / args.steps
-    f_adj = w.flops_causal_adjusted()
+    if mask is None:
+        f_adj = w.flops_causal_adjusted()
+        f_exact = w.flops_exact()
+    else:
+        f_adj = f_exact = 4.0 * w.d * w.heads * mask.pairs
     value = ws * f_adj / (ms_step * 1e-3) / 1e12
 
     # roofline of the dominant kernel (block update): algorithmic FLOPs of
     # all its launches (exact allowed-pair count) over their summed time.
-    f_exact = w.flops_exact()
     achieved = (f_exact * args.steps) / (ms_upd * 1e-3) / 1e12 if ms_upd > 0 else None
     peak = peaks["bf16_tflops_sustained"]
     traffic = recorded_traffic(w.name)
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        val, cores, desc, _ = oracle_sample(w, q, k, v, args.cpu_seconds, mask=mask)
+        cpu = {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": desc}
+    if mask is not None:
+        if rank == 0:
+            line = {
+                "metric": METRIC_MASKED, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": w.dtype, "data": "synthetic",
+                "frac_of_dense_bf16_peak": value / ws / peaks["bf16_tflops"],
+                "peak_source": peak_src,
+                "config": {"workload": w.name, "N": w.N, "P": w.P, "c": w.c, "heads": w.heads,
+                           "kv_heads": w.kv_heads, "d": w.d, "causal": w.causal,
+                           "recipe": w.recipe, "seed": w.seed, "mask": mask.describe(),
+                           "parallelism": f"replicas{ws}", "flops_per_step": f_adj,
+                           "l2": "inputs larger than L2 (Q alone exceeds 129 MB); no flush"},
+                "clocks": clk, "e2e": None, "gpu_launches": n_upd + n_init + n_fin,
+                "kernel_ms": {"block_update": ms_upd / args.steps,
+                              "state_init": ms_init / args.steps,
+                              "finalize": ms_fin / args.steps},
+                "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                             "unit": "TFLOP/s", "frac": (achieved / peak) if achieved else None,
+                             "traffic": None, "kernel": "block update (tcgen05)",
+                             "peak_kind": f"bf16_tflops_sustained ({peak_src})"},
+                "cpu_baseline": cpu,
+            }
+            print(json.dumps(line), flush=True)
+        return
 
     # end to end through the host-buffer entry point
     qp, kp, vp = q.pin_memory(), k.pin_memory(), v.pin_memory()
@@ -314,12 +527,6 @@ def run_ours(args, w, ws, rank, local):
     h2d = sum(t.numel() * t.element_size() for t in (q, k, v))
     d2h = out_h.numel() * 4 + lse_h.numel() * 4
     e2e_value = ws * f_adj / e2e_s / 1e12
-
-    cpu = None
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        val, cores, desc, _ = oracle_sample(w, q, k, v, args.cpu_seconds)
-        cpu = {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-               "sample": desc}
 
     if rank != 0:
         return
@@ -375,11 +582,22 @@ def main():
     ap.add_argument("--ref-step-seconds", type=float, default=6.0)
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layout", default="contiguous", choices=["contiguous", "zigzag", "striped"])
+    ap.add_argument("--window", type=int, default=0, help="sliding window (0 = none)")
+    ap.add_argument("--docs", type=int, default=0, help="packed documents (0 = one sequence)")
+    ap.add_argument("--n-valid", type=int, default=-1, help="valid length (-1 = N)")
+    ap.add_argument("--decode", default=None, choices=["decode-1m", "decode-1m-q4"],
+                    help="time the decode path on this workload instead")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
     ws, rank, local = dist_info()
     w = WORKLOADS[args.workload]
+    args.mask = MaskRun(w, args.layout, args.window, args.docs, args.n_valid, seed=w.seed)
+    if not args.mask.active():
+        args.mask = None
+    elif args.impl == "reference":
+        ap.error("masked runs have no reference arm; time the oracle through cpu_baseline")
     if ws > 1:
         import torch
         import torch.distributed as dist
@@ -389,7 +607,11 @@ def main():
             torch.cuda.set_device(local)
         dist.init_process_group(backend)
     try:
-        if args.impl == "reference":
+        if args.decode is not None:
+            if args.impl == "reference":
+                ap.error("decode runs have no reference arm; time the oracle through cpu_baseline")
+            run_decode(args, ws, rank, local)
+        elif args.impl == "reference":
             run_reference(args, w, ws, rank)
         else:
             run_ours(args, w, ws, rank, local)

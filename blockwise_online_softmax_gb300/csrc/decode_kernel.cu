@@ -184,13 +184,17 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
   }
   __syncwarp();
 
-  float m_r[RM], l_r[RM], o_r[RM][C::COLS];
+  // Warp state per row: m (log2 units), this lane's share of l, and this
+  // lane's output columns as fp32 pairs (one FFMA2 updates two).
+  constexpr int CP = C::COLS / 2;
+  float m_r[RM], l_r[RM];
+  uint64_t o2[RM][CP];
 #pragma unroll
   for (int r = 0; r < RM; ++r) {
     m_r[r] = -INFINITY;
     l_r[r] = 0.f;
 #pragma unroll
-    for (int c = 0; c < C::COLS; ++c) o_r[r][c] = 0.f;
+    for (int c = 0; c < CP; ++c) o2[r][c] = f2pack(0.f, 0.f);
   }
   const uint32_t p_w = sb + S::OFF_P + warp * RM * KT * 4;
   const uint32_t q_sa = sb + S::OFF_Q;
@@ -206,33 +210,39 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     const uint32_t sV = sK + C::TILE;
     const int key = (t_begin + warp + it * DW) * KT + lane;
 
-    // S = q . k for this lane's key, every row (log2 units).
-    float s[RM];
+    // S = q . k for this lane's key, every row (log2 units): even and odd
+    // columns summed in the two halves of an FFMA2 accumulator.
+    uint64_t s2[RM];
 #pragma unroll
-    for (int r = 0; r < RM; ++r) s[r] = 0.f;
+    for (int r = 0; r < RM; ++r) s2[r] = f2pack(0.f, 0.f);
 #pragma unroll
     for (int ch = 0; ch < C::NCH; ++ch) {
 #pragma unroll
       for (int p = 0; p < 8; ++p) {
         const uint4 kw = lds128(sK + ch * CHUNK + lane * 128 + ((p ^ (lane & 7)) << 4));
-        const float k0 = bf_lo(kw.x), k1 = bf_hi(kw.x), k2 = bf_lo(kw.y), k3 = bf_hi(kw.y);
-        const float k4 = bf_lo(kw.z), k5 = bf_hi(kw.z), k6 = bf_lo(kw.w), k7 = bf_hi(kw.w);
+        const uint64_t k01 = f2pack(bf_lo(kw.x), bf_hi(kw.x));
+        const uint64_t k23 = f2pack(bf_lo(kw.y), bf_hi(kw.y));
+        const uint64_t k45 = f2pack(bf_lo(kw.z), bf_hi(kw.z));
+        const uint64_t k67 = f2pack(bf_lo(kw.w), bf_hi(kw.w));
 #pragma unroll
         for (int r = 0; r < RM; ++r) {
           const uint32_t qa = q_sa + (r * D + ch * 64 + p * 8) * 4;
           const uint4 x = lds128(qa), y = lds128(qa + 16);
-          float acc = s[r];
-          acc = fmaf(__uint_as_float(x.x), k0, acc);
-          acc = fmaf(__uint_as_float(x.y), k1, acc);
-          acc = fmaf(__uint_as_float(x.z), k2, acc);
-          acc = fmaf(__uint_as_float(x.w), k3, acc);
-          acc = fmaf(__uint_as_float(y.x), k4, acc);
-          acc = fmaf(__uint_as_float(y.y), k5, acc);
-          acc = fmaf(__uint_as_float(y.z), k6, acc);
-          acc = fmaf(__uint_as_float(y.w), k7, acc);
-          s[r] = acc;
+          uint64_t acc = s2[r];
+          acc = ffma2(f2pack(__uint_as_float(x.x), __uint_as_float(x.y)), k01, acc);
+          acc = ffma2(f2pack(__uint_as_float(x.z), __uint_as_float(x.w)), k23, acc);
+          acc = ffma2(f2pack(__uint_as_float(y.x), __uint_as_float(y.y)), k45, acc);
+          acc = ffma2(f2pack(__uint_as_float(y.z), __uint_as_float(y.w)), k67, acc);
+          s2[r] = acc;
         }
       }
+    }
+    float s[RM];
+#pragma unroll
+    for (int r = 0; r < RM; ++r) {
+      float a0, a1;
+      f2unpack(s2[r], a0, a1);
+      s[r] = a0 + a1;
     }
     // Mask, then the online-softmax update of each row's warp state.
 #pragma unroll
@@ -248,8 +258,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       const float pv = ex2(sv - mref);         // masked keys give 0
       m_r[r] = m_new;
       l_r[r] = l_r[r] * alpha + pv;
+      const uint64_t al2 = f2pack(alpha, alpha);
 #pragma unroll
-      for (int c = 0; c < C::COLS; ++c) o_r[r][c] *= alpha;
+      for (int c = 0; c < CP; ++c) o2[r][c] = fmul2(o2[r][c], al2);
       asm volatile("st.shared.f32 [%0], %1;" ::"r"(p_w + (r * KT + lane) * 4), "f"(pv) : "memory");
     }
     __syncwarp();
@@ -272,22 +283,21 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       for (int u = 0; u < 4; ++u) {
         const int t = t4 + u;
         const uint32_t va = vcol + t * 128 + ((piece ^ (t & 7)) << 4);
-        float v[C::COLS];
-        if constexpr (C::COLS == 4) {
+        uint64_t v2[CP];
+        if constexpr (CP == 2) {
           const uint2 w2 = lds64(va);
-          v[0] = bf_lo(w2.x);
-          v[1] = bf_hi(w2.x);
-          v[2] = bf_lo(w2.y);
-          v[3] = bf_hi(w2.y);
+          v2[0] = f2pack(bf_lo(w2.x), bf_hi(w2.x));
+          v2[1] = f2pack(bf_lo(w2.y), bf_hi(w2.y));
         } else {
           const uint32_t w1 = lds32(va);
-          v[0] = bf_lo(w1);
-          v[1] = bf_hi(w1);
+          v2[0] = f2pack(bf_lo(w1), bf_hi(w1));
         }
 #pragma unroll
-        for (int r = 0; r < RM; ++r)
+        for (int r = 0; r < RM; ++r) {
+          const uint64_t pp = f2pack(pr[r][u], pr[r][u]);
 #pragma unroll
-          for (int c = 0; c < C::COLS; ++c) o_r[r][c] = fmaf(pr[r][u], v[c], o_r[r][c]);
+          for (int c = 0; c < CP; ++c) o2[r][c] = ffma2(pp, v2[c], o2[r][c]);
+        }
       }
     }
     __syncwarp();
@@ -321,7 +331,12 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       mw[r * (D + 2) + 1] = ls;
     }
 #pragma unroll
-    for (int c = 0; c < C::COLS; ++c) mw[r * (D + 2) + 2 + C::COLS * lane + c] = o_r[r][c];
+    for (int c = 0; c < CP; ++c) {
+      float y0, y1;
+      f2unpack(o2[r][c], y0, y1);
+      mw[r * (D + 2) + 2 + C::COLS * lane + 2 * c] = y0;
+      mw[r * (D + 2) + 2 + C::COLS * lane + 2 * c + 1] = y1;
+    }
   }
   __syncthreads();
   if (*abort_flag) return;
