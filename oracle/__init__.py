@@ -65,8 +65,18 @@ def _load():
                           ctypes.c_int, ctypes.c_double, ctypes.c_int, LL, P, P, P, P, P, LL,
                           P, P, P, ctypes.c_int]
             f.restype = ctypes.c_int
+            gq = lib.oracle_grad_q
+            gq.argtypes = [P, P, P, P, ctypes.c_int, LL, LL, ctypes.c_int, ctypes.c_int,
+                           ctypes.c_int, ctypes.c_double, ctypes.c_int, LL, P, P, P, P, P, LL,
+                           P, P, P, ctypes.c_int]
+            gq.restype = ctypes.c_int
+            gkv = lib.oracle_grad_kv
+            gkv.argtypes = [P, P, P, P, ctypes.c_int, LL, LL, ctypes.c_int, ctypes.c_int,
+                            ctypes.c_int, ctypes.c_double, ctypes.c_int, LL, P, P, P, P, P, P,
+                            P, LL, P, P, ctypes.c_int]
+            gkv.restype = ctypes.c_int
             lib.oracle_abi_version.restype = ctypes.c_int
-            if lib.oracle_abi_version() != 2:
+            if lib.oracle_abi_version() != 3:
                 raise RuntimeError("liboracle.so is stale; rebuild it")
             _lib = lib
     return _lib
@@ -170,3 +180,91 @@ def attention(q, k, v, *, causal: bool, q_pos=None, k_pos=None, rows=None,
         out = np.where(l[..., None] > 0, o / np.where(l > 0, l, 1.0)[..., None], 0.0)
         lse = np.where(l > 0, m + np.log(np.where(l > 0, l, 1.0)), -np.inf)
     return out, lse
+
+
+# ------------------------------------------------------------------ gradients
+def _grad_inputs(q, k, v, dout, q_pos, k_pos, q_doc, k_doc, scale):
+    qa, dt = _as_input(q)
+    ka, dk_ = _as_input(k)
+    va, dv_ = _as_input(v)
+    ga, dg = _as_input(dout)
+    if not (dt == dk_ == dv_ == dg):
+        raise TypeError("q, k, v and dout must share one dtype")
+    nq, hq, d = qa.shape
+    nk, hkv, _ = ka.shape
+    if ga.shape != qa.shape or va.shape != ka.shape or ka.shape[2] != d:
+        raise ValueError("shape mismatch between q, k, v and dout")
+
+    def arr(x, n):
+        if x is None:
+            return None
+        a = np.ascontiguousarray(np.asarray(x, dtype=np.int64))
+        if a.shape != (n,):
+            raise ValueError("positions and document ids need one entry per row")
+        return a
+
+    qp, kp = arr(q_pos, nq), arr(k_pos, nk)
+    if (q_doc is None) != (k_doc is None):
+        raise ValueError("give both q_doc and k_doc, or neither")
+    qd, kd = arr(q_doc, nq), arr(k_doc, nk)
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    return qa, ka, va, ga, dt, nq, nk, hq, hkv, d, qp, kp, qd, kd, float(scale)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def grad_q(q, k, v, dout, *, causal: bool, rows=None, q_pos=None, k_pos=None, window: int = 0,
+           q_doc=None, k_doc=None, scale: float | None = None, threads: int | None = None):
+    """dQ, LSE and D = sum_t P dP of the listed query rows (default: all),
+    for the loss sum(dout * O).  Shapes [nrows, hq, d], [nrows, hq],
+    [nrows, hq]; fp64.  The definition is in ``attention.c``."""
+    qa, ka, va, ga, dt, nq, nk, hq, hkv, d, qp, kp, qd, kd, sc = _grad_inputs(
+        q, k, v, dout, q_pos, k_pos, q_doc, k_doc, scale)
+    rows = np.arange(nq, dtype=np.int64) if rows is None else np.ascontiguousarray(
+        np.asarray(rows, dtype=np.int64))
+    nr = rows.shape[0]
+    dq = np.empty((nr, hq, d))
+    lse = np.empty((nr, hq))
+    dvec = np.empty((nr, hq))
+    rc = _load().oracle_grad_q(_ptr(qa), _ptr(ka), _ptr(va), _ptr(ga), dt, nq, nk, hq, hkv, d,
+                               sc, int(bool(causal)), int(window), _ptr(qp), _ptr(kp), _ptr(qd),
+                               _ptr(kd), _ptr(rows), nr, _ptr(dq), _ptr(lse), _ptr(dvec),
+                               int(threads or os.cpu_count() or 1))
+    if rc != 0:
+        raise ValueError(f"oracle_grad_q failed with code {rc}")
+    return dq, lse, dvec
+
+
+def grad_kv(q, k, v, dout, lse_all, d_all, *, causal: bool, keys=None, q_pos=None, k_pos=None,
+            window: int = 0, q_doc=None, k_doc=None, scale: float | None = None,
+            threads: int | None = None):
+    """dK and dV of the listed keys (default: all), [nkeys, hkv, d] fp64,
+    given LSE and D of every query row (from ``grad_q`` over all rows)."""
+    qa, ka, va, ga, dt, nq, nk, hq, hkv, d, qp, kp, qd, kd, sc = _grad_inputs(
+        q, k, v, dout, q_pos, k_pos, q_doc, k_doc, scale)
+    lse_all = np.ascontiguousarray(np.asarray(lse_all, dtype=np.float64))
+    d_all = np.ascontiguousarray(np.asarray(d_all, dtype=np.float64))
+    if lse_all.shape != (nq, hq) or d_all.shape != (nq, hq):
+        raise ValueError("lse_all and d_all must be [nq, hq]")
+    keys = np.arange(nk, dtype=np.int64) if keys is None else np.ascontiguousarray(
+        np.asarray(keys, dtype=np.int64))
+    nkk = keys.shape[0]
+    dk = np.empty((nkk, hkv, d))
+    dv = np.empty((nkk, hkv, d))
+    rc = _load().oracle_grad_kv(_ptr(qa), _ptr(ka), _ptr(va), _ptr(ga), dt, nq, nk, hq, hkv, d,
+                                sc, int(bool(causal)), int(window), _ptr(qp), _ptr(kp), _ptr(qd),
+                                _ptr(kd), _ptr(lse_all), _ptr(d_all), _ptr(keys), nkk, _ptr(dk),
+                                _ptr(dv), int(threads or os.cpu_count() or 1))
+    if rc != 0:
+        raise ValueError(f"oracle_grad_kv failed with code {rc}")
+    return dk, dv
+
+
+def backward(q, k, v, dout, *, causal: bool, **kw):
+    """All gradients of sum(dout * attention(q, k, v)): (dq, dk, dv, lse)."""
+    dq, lse, dvec = grad_q(q, k, v, dout, causal=causal, **kw)
+    dk, dv = grad_kv(q, k, v, dout, lse, dvec, causal=causal, **kw)
+    return dq, dk, dv, lse

@@ -200,6 +200,232 @@ int oracle_partial_state_masked(const void* q, const void* k, const void* v, int
   return J.failed ? -2 : 0;
 }
 
+/*
+ * Gradients of dense attention -- the backward pass the ring runs again
+ * ("Ring Attention：把超长序列沿设备环流动", section "Backward 需要让梯度也
+ * 沿环传播": every (Q block, K/V block) pair adds to dQ, dK and dV, and the
+ * softmax statistics are recomputed from the saved log-sum-exp).  What is
+ * computed here is the plain calculus of O = softmax(S) V with S = scale *
+ * Q K^T over the allowed keys, for the loss L = sum(dO * O):
+ *   P_rt  = exp(s_rt - LSE_r)               (the row softmax)
+ *   dP_rt = dO_r . v_t
+ *   D_r   = sum_t P_rt dP_rt
+ *   dS_rt = P_rt (dP_rt - D_r)
+ *   dQ_r  = scale * sum_t dS_rt k_t
+ *   dK_t  = scale * sum over (r, query heads of t's KV head) dS_rt q_r
+ *   dV_t  = sum over (r, query heads of t's KV head) P_rt dO_r
+ * Everything in fp64.  Rows with no allowed key have P = 0 and contribute
+ * nothing.
+ *
+ * oracle_grad_q: for the listed query rows and every head, LSE, D and dQ.
+ * oracle_grad_kv: for the listed keys and every KV head, dK and dV; it
+ * needs LSE and D of every query row (from oracle_grad_q over all rows).
+ */
+typedef struct {
+  job_t base;  /* inputs, mask, positions, rows, threads */
+  const void* dout;
+  double* dq;   /* [nrows, hq, d] */
+  double* lse;  /* [nrows, hq] (grad_q: out; grad_kv: in, all nq rows) */
+  double* dvec; /* [nrows, hq] (same) */
+  double* dk;   /* [nkeys, hkv, d] */
+  double* dv;
+  const long long* keys;
+  long long nkeys;
+} gjob_t;
+
+static int pair_allowed(const job_t* J, long long r, long long t) {
+  const long long qp = J->q_pos ? J->q_pos[r] : r;
+  const long long kp = J->k_pos ? J->k_pos[t] : t;
+  if (J->causal && kp > qp) return 0;
+  if (J->window > 0 && (qp - kp >= J->window || kp - qp >= J->window)) return 0;
+  if (J->q_doc && (J->q_doc[r] < 0 || J->k_doc[t] != J->q_doc[r])) return 0;
+  return 1;
+}
+
+static double dot_rows(const job_t* J, const void* a, size_t ia, const void* b, size_t ib) {
+  double s = 0.0;
+  for (int x = 0; x < J->d; ++x) s += widen(a, J->dtype, ia + x) * widen(b, J->dtype, ib + x);
+  return s;
+}
+
+static void grad_q_item(gjob_t* G, long long item, double* sc) {
+  job_t* J = &G->base;
+  const long long ri = item / J->hq;
+  const int h = (int)(item % J->hq);
+  const int d = J->d, kh = h / (J->hq / J->hkv);
+  const long long r = J->rows[ri];
+  const size_t qb = ((size_t)r * J->hq + h) * d;
+  /* scores and their max */
+  double m = -INFINITY;
+  for (long long t = 0; t < J->nk; ++t) {
+    if (!pair_allowed(J, r, t)) { sc[t] = NAN; continue; }
+    sc[t] = dot_rows(J, J->q, qb, J->k, ((size_t)t * J->hkv + kh) * d) * J->scale;
+    if (sc[t] > m) m = sc[t];
+  }
+  double l = 0.0;
+  if (m > -INFINITY)
+    for (long long t = 0; t < J->nk; ++t)
+      if (!isnan(sc[t])) l += exp(sc[t] - m);
+  const double lse = l > 0.0 ? m + log(l) : -INFINITY;
+  /* D = sum P dP, then dQ */
+  double D = 0.0;
+  double* dq = G->dq + ((size_t)ri * J->hq + h) * d;
+  for (int x = 0; x < d; ++x) dq[x] = 0.0;
+  if (l > 0.0) {
+    for (long long t = 0; t < J->nk; ++t) {
+      if (isnan(sc[t])) continue;
+      const double p = exp(sc[t] - lse);
+      const double dp = dot_rows(J, G->dout, qb, J->v, ((size_t)t * J->hkv + kh) * d);
+      D += p * dp;
+    }
+    for (long long t = 0; t < J->nk; ++t) {
+      if (isnan(sc[t])) continue;
+      const double p = exp(sc[t] - lse);
+      const double dp = dot_rows(J, G->dout, qb, J->v, ((size_t)t * J->hkv + kh) * d);
+      const double ds = p * (dp - D);
+      const size_t kb = ((size_t)t * J->hkv + kh) * d;
+      for (int x = 0; x < d; ++x) dq[x] += J->scale * ds * widen(J->k, J->dtype, kb + x);
+    }
+  }
+  G->lse[ri * J->hq + h] = lse;
+  G->dvec[ri * J->hq + h] = D;
+}
+
+static void grad_kv_item(gjob_t* G, long long item) {
+  job_t* J = &G->base;
+  const long long ti = item / J->hkv;
+  const int kh = (int)(item % J->hkv);
+  const int d = J->d, g = J->hq / J->hkv;
+  const long long t = G->keys[ti];
+  const size_t kb = ((size_t)t * J->hkv + kh) * d;
+  double* dk = G->dk + ((size_t)ti * J->hkv + kh) * d;
+  double* dv = G->dv + ((size_t)ti * J->hkv + kh) * d;
+  for (int x = 0; x < d; ++x) dk[x] = dv[x] = 0.0;
+  for (int hl = 0; hl < g; ++hl) {
+    const int h = kh * g + hl;
+    for (long long r = 0; r < J->nq; ++r) {
+      const double lse = G->lse[r * J->hq + h];
+      if (lse == -INFINITY || !pair_allowed(J, r, t)) continue;
+      const size_t qb = ((size_t)r * J->hq + h) * d;
+      const double s = dot_rows(J, J->q, qb, J->k, kb) * J->scale;
+      const double p = exp(s - lse);
+      const double dp = dot_rows(J, G->dout, qb, J->v, kb);
+      const double ds = p * (dp - G->dvec[r * J->hq + h]);
+      for (int x = 0; x < d; ++x) {
+        dk[x] += J->scale * ds * widen(J->q, J->dtype, qb + x);
+        dv[x] += p * widen(G->dout, J->dtype, qb + x);
+      }
+    }
+  }
+}
+
+static void* gq_worker(void* arg) {
+  gjob_t* G = (gjob_t*)arg;
+  job_t* J = &G->base;
+  double* sc = (double*)malloc(sizeof(double) * (size_t)(J->nk > 0 ? J->nk : 1));
+  if (!sc) {
+    __atomic_store_n(&J->failed, 1, __ATOMIC_SEQ_CST);
+    return NULL;
+  }
+  const long long total = J->nrows * (long long)J->hq;
+  for (;;) {
+    const long long item = __atomic_fetch_add(&J->next, 1, __ATOMIC_RELAXED);
+    if (item >= total) break;
+    grad_q_item(G, item, sc);
+  }
+  free(sc);
+  return NULL;
+}
+
+static void* gkv_worker(void* arg) {
+  gjob_t* G = (gjob_t*)arg;
+  job_t* J = &G->base;
+  const long long total = G->nkeys * (long long)J->hkv;
+  for (;;) {
+    const long long item = __atomic_fetch_add(&J->next, 1, __ATOMIC_RELAXED);
+    if (item >= total) break;
+    grad_kv_item(G, item);
+  }
+  return NULL;
+}
+
+static int run_threads(void* (*fn)(void*), void* arg, int nthreads) {
+  pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)nthreads);
+  if (!th) return -2;
+  int started = 0;
+  for (int i = 0; i < nthreads; ++i) {
+    if (pthread_create(&th[i], NULL, fn, arg) != 0) break;
+    ++started;
+  }
+  if (started == 0) fn(arg);
+  for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
+  free(th);
+  return 0;
+}
+
+static int grad_setup(gjob_t* G, const void* q, const void* k, const void* v, const void* dout,
+                      int dtype, long long nq, long long nk, int hq, int hkv, int d,
+                      double scale, int causal, long long window, const long long* q_pos,
+                      const long long* k_pos, const long long* q_doc, const long long* k_doc) {
+  if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return -1;
+  if (hq <= 0 || hkv <= 0 || d <= 0 || hq % hkv != 0 || nq < 0 || nk < 0) return -1;
+  if (window < 0 || (!q_doc) != (!k_doc)) return -1;
+  if ((nq > 0 && (!q || !dout)) || (nk > 0 && (!k || !v))) return -1;
+  memset(G, 0, sizeof *G);
+  job_t* J = &G->base;
+  J->q = q; J->k = k; J->v = v; J->dtype = dtype;
+  J->nq = nq; J->nk = nk; J->hq = hq; J->hkv = hkv; J->d = d;
+  J->scale = scale; J->causal = causal; J->window = window;
+  J->q_pos = q_pos; J->k_pos = k_pos; J->q_doc = q_doc; J->k_doc = k_doc;
+  G->dout = dout;
+  return 0;
+}
+
+int oracle_grad_q(const void* q, const void* k, const void* v, const void* dout, int dtype,
+                  long long nq, long long nk, int hq, int hkv, int d, double scale, int causal,
+                  long long window, const long long* q_pos, const long long* k_pos,
+                  const long long* q_doc, const long long* k_doc, const long long* rows,
+                  long long nrows, double* dq_out, double* lse_out, double* d_out,
+                  int nthreads) {
+  gjob_t G;
+  int rc = grad_setup(&G, q, k, v, dout, dtype, nq, nk, hq, hkv, d, scale, causal, window, q_pos,
+                      k_pos, q_doc, k_doc);
+  if (rc != 0) return rc;
+  if (nrows < 0 || (nrows > 0 && (!rows || !dq_out || !lse_out || !d_out))) return -1;
+  for (long long i = 0; i < nrows; ++i)
+    if (rows[i] < 0 || rows[i] >= nq) return -1;
+  G.base.rows = rows;
+  G.base.nrows = nrows;
+  G.dq = dq_out;
+  G.lse = lse_out;
+  G.dvec = d_out;
+  if (run_threads(gq_worker, &G, nthreads < 1 ? 1 : nthreads) != 0) return -2;
+  return G.base.failed ? -2 : 0;
+}
+
+int oracle_grad_kv(const void* q, const void* k, const void* v, const void* dout, int dtype,
+                   long long nq, long long nk, int hq, int hkv, int d, double scale, int causal,
+                   long long window, const long long* q_pos, const long long* k_pos,
+                   const long long* q_doc, const long long* k_doc, const double* lse_all,
+                   const double* d_all, const long long* keys, long long nkeys, double* dk_out,
+                   double* dv_out, int nthreads) {
+  gjob_t G;
+  int rc = grad_setup(&G, q, k, v, dout, dtype, nq, nk, hq, hkv, d, scale, causal, window, q_pos,
+                      k_pos, q_doc, k_doc);
+  if (rc != 0) return rc;
+  if (nkeys < 0 || (nkeys > 0 && (!keys || !dk_out || !dv_out || !lse_all || !d_all))) return -1;
+  for (long long i = 0; i < nkeys; ++i)
+    if (keys[i] < 0 || keys[i] >= nk) return -1;
+  G.lse = (double*)lse_all;
+  G.dvec = (double*)d_all;
+  G.keys = keys;
+  G.nkeys = nkeys;
+  G.dk = dk_out;
+  G.dv = dv_out;
+  if (run_threads(gkv_worker, &G, nthreads < 1 ? 1 : nthreads) != 0) return -2;
+  return G.base.failed ? -2 : 0;
+}
+
 /* The causal-only form: no window, one document. */
 int oracle_partial_state(const void* q, const void* k, const void* v, int dtype,
                          long long nq, long long nk, int hq, int hkv, int d, double scale,
@@ -212,4 +438,4 @@ int oracle_partial_state(const void* q, const void* k, const void* v, int dtype,
 }
 
 /* Version tag so the Python side can tell a stale build. */
-int oracle_abi_version(void) { return 2; }
+int oracle_abi_version(void) { return 3; }

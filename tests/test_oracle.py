@@ -445,3 +445,111 @@ def test_positions_not_indices_decide_the_mask():
                          k_pos=perm, q_doc=doc[perm], k_doc=doc[perm])
     assert np.abs(b[0] - a[0][perm]).max() < 1e-13
     assert np.abs(b[1] - a[1][perm]).max() < 1e-13
+
+
+# --- gradients (the backward ring: "Ring Attention：把超长序列沿设备环流动",
+# "Backward 需要让梯度也沿环传播")
+
+def _loss(q, k, v, dout, **kw):
+    out, _ = oracle.attention(q, k, v, **kw)
+    return float((out * dout.astype(np.float64)).sum())
+
+
+@pytest.mark.parametrize("kw", [dict(causal=False), dict(causal=True),
+                                dict(causal=True, window=3),
+                                dict(causal=False, q_doc=np.array([0, 0, 1, 1, 1, 2]),
+                                     k_doc=np.array([0, 0, 1, 1, 1, 2]))])
+def test_gradients_match_finite_differences(kw):
+    """Central differences of the forward oracle's loss sum(dout * O) pin
+    every element of dQ, dK and dV (GQA 2:1)."""
+    rng = np.random.default_rng(41)
+    q = rng.standard_normal((6, 2, 3)).astype(np.float32)
+    k = rng.standard_normal((6, 1, 3)).astype(np.float32)
+    v = rng.standard_normal((6, 1, 3)).astype(np.float32)
+    g = rng.standard_normal((6, 2, 3)).astype(np.float32)
+    dq, dk, dv, _ = oracle.backward(q, k, v, g, **kw)
+    h = np.float32(2.0 ** -9)
+    for name, x, grad in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] = x[idx] + h
+            xm[idx] = x[idx] - h
+            step = float(xp[idx]) - float(xm[idx])  # exact after fp32 rounding
+            args = {"q": q, "k": k, "v": v}
+            lp = _loss(**{**args, name: xp}, dout=g, **kw)
+            lm = _loss(**{**args, name: xm}, dout=g, **kw)
+            fd = (lp - lm) / step
+            assert abs(fd - grad[idx]) < 2e-5 * max(1.0, abs(fd)), (name, idx, fd, grad[idx])
+
+
+def test_gradients_single_key_per_row():
+    # Causal window 1: each row's softmax is the constant 1, so dQ = dK = 0
+    # and dV_t gathers dout of row t over the heads of its group.
+    rng = np.random.default_rng(43)
+    q = rng.standard_normal((9, 4, 8)).astype(np.float32)
+    k = rng.standard_normal((9, 2, 8)).astype(np.float32)
+    v = rng.standard_normal((9, 2, 8)).astype(np.float32)
+    g = rng.standard_normal((9, 4, 8)).astype(np.float32)
+    dq, dk, dv, _ = oracle.backward(q, k, v, g, causal=True, window=1)
+    assert np.abs(dq).max() < 1e-15 and np.abs(dk).max() < 1e-15
+    want = g.astype(np.float64).reshape(9, 2, 2, 8).sum(2)
+    assert np.abs(dv - want).max() < 1e-13
+
+
+def test_gradients_equal_values_give_zero_dq_dk():
+    # Equal value rows: O does not depend on the softmax weights.
+    rng = np.random.default_rng(45)
+    q = rng.standard_normal((12, 2, 8)).astype(np.float32)
+    k = rng.standard_normal((12, 2, 8)).astype(np.float32)
+    v = np.repeat(rng.standard_normal((1, 2, 8)).astype(np.float32), 12, axis=0)
+    g = rng.standard_normal((12, 2, 8)).astype(np.float32)
+    dq, dk, _, _ = oracle.backward(q, k, v, g, causal=True)
+    assert np.abs(dq).max() < 1e-12 and np.abs(dk).max() < 1e-12
+
+
+def test_gradient_sums_and_d_identity():
+    # sum_t dV_t = sum of dout over the group's rows; sum_t dK_t = 0 (each
+    # row's dS sums to zero); D_r = dout_r . O_r.
+    rng = np.random.default_rng(47)
+    n = 40
+    q = rng.standard_normal((n, 6, 16)).astype(np.float32)
+    k = rng.standard_normal((n, 2, 16)).astype(np.float32)
+    v = rng.standard_normal((n, 2, 16)).astype(np.float32)
+    g = rng.standard_normal((n, 6, 16)).astype(np.float32)
+    dq, lse, dvec = oracle.grad_q(q, k, v, g, causal=True)
+    dk, dv = oracle.grad_kv(q, k, v, g, lse, dvec, causal=True)
+    gsum = g.astype(np.float64).reshape(n, 2, 3, 16).sum((0, 2))
+    assert np.abs(dv.sum(0) - gsum).max() < 1e-12
+    assert np.abs(dk.sum(0)).max() < 1e-12
+    out, lse2 = oracle.attention(q, k, v, causal=True)
+    assert np.abs(dvec - (out * g.astype(np.float64)).sum(-1)).max() < 1e-12
+    assert np.abs(lse - lse2).max() < 1e-13
+
+
+def test_gradients_gqa_equal_summed_repeated_heads():
+    rng = np.random.default_rng(49)
+    q = rng.standard_normal((20, 4, 8)).astype(np.float32)
+    k = rng.standard_normal((20, 2, 8)).astype(np.float32)
+    v = rng.standard_normal((20, 2, 8)).astype(np.float32)
+    g = rng.standard_normal((20, 4, 8)).astype(np.float32)
+    dq, dk, dv, _ = oracle.backward(q, k, v, g, causal=True)
+    kr, vr = np.repeat(k, 2, axis=1), np.repeat(v, 2, axis=1)
+    dq2, dk2, dv2, _ = oracle.backward(q, kr, vr, g, causal=True)
+    assert np.abs(dq - dq2).max() < 1e-13
+    assert np.abs(dk - dk2.reshape(20, 2, 2, 8).sum(2)).max() < 1e-13
+    assert np.abs(dv - dv2.reshape(20, 2, 2, 8).sum(2)).max() < 1e-13
+
+
+def test_gradient_rows_and_keys_subsets():
+    rng = np.random.default_rng(51)
+    q = rng.standard_normal((30, 2, 8)).astype(np.float32)
+    k = rng.standard_normal((30, 1, 8)).astype(np.float32)
+    v = rng.standard_normal((30, 1, 8)).astype(np.float32)
+    g = rng.standard_normal((30, 2, 8)).astype(np.float32)
+    dq, dk, dv, lse = oracle.backward(q, k, v, g, causal=True)
+    rows = np.array([29, 0, 7])
+    dq_r, lse_r, _ = oracle.grad_q(q, k, v, g, causal=True, rows=rows, threads=2)
+    assert np.array_equal(dq_r, dq[rows]) and np.array_equal(lse_r, lse[rows])
+    _, lse_a, d_a = oracle.grad_q(q, k, v, g, causal=True)
+    dk_k, dv_k = oracle.grad_kv(q, k, v, g, lse_a, d_a, causal=True, keys=[3, 29], threads=3)
+    assert np.array_equal(dk_k, dk[[3, 29]]) and np.array_equal(dv_k, dv[[3, 29]])
