@@ -31,6 +31,12 @@ few query tokens against a 1M-token K/V history in P shards.  That path is
 HBM-bound, so its metric is the K/V bytes read per second, and its
 roofline is against the measured HBM copy bandwidth.
 
+Backward runs (--backward) time ra_ring_backward on the workload, given
+the forward's outputs: the pre-pass, then per ring step the dQ and the
+dK/dV kernels.  The FLOP convention is the FlashAttention one for the
+backward: five products per pair (S recomputed, dP, dV, dK, dQ), 10*d
+FLOPs per allowed pair per query head, causal-adjusted.
+
 Masked runs (--layout zigzag|striped, --window W, --docs K, --n-valid V)
 time ra_ring_forward_masked on the same workload laid out and masked that
 way.  Their metric counts 4*d FLOPs per allowed (query, key) pair per query
@@ -365,6 +371,112 @@ def run_decode(args, ws, rank, local):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ backward
+METRIC_BWD = ("backward attention TFLOP/s (10*d FLOPs per allowed pair per query head, "
+              "causal-adjusted) on 1 GB300")
+
+
+def run_backward(args, w, ws, rank, local):
+    import numpy as np
+    import torch
+
+    import blockwise_online_softmax_gb300 as ra
+    import oracle
+    from blockwise_online_softmax_gb300 import binding, inputs
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    binding.lib()
+    peaks, peak_src = load_peaks()
+    q, k, v = inputs.make_workload(w)
+    g = inputs.randn_chunked((w.N, w.heads, w.d), w.seed, 3).to(torch.bfloat16)
+    qd, kd, vd, gd = q.to(dev), k.to(dev), v.to(dev), g.to(dev)
+    stream = torch.cuda.current_stream(dev)
+    out, lse = ra.ra_ring_forward(qd, kd, vd, P=w.P, causal=w.causal, stream=stream)
+    dq = torch.empty((w.N, w.heads, w.d), dtype=torch.float32, device=dev)
+    dk = torch.empty((w.N, w.kv_heads, w.d), dtype=torch.float32, device=dev)
+    dv = torch.empty_like(dk)
+
+    def step():
+        ra.ra_ring_backward(qd, kd, vd, out, lse, gd, P=w.P, causal=w.causal, dq=dq, dk=dk,
+                            dv=dv, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    ra.ra_device_status(stream)
+    gpu_index = local
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    if vis and "," not in vis and vis.strip().isdigit():
+        gpu_index = int(vis)
+    clocks = ClockSampler(gpu_index)
+    clocks.start()
+    ra.ra_trace_reset()
+    ra.ra_trace_enable(True)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    ra.ra_trace_enable(False)
+    clk = clocks.stop()
+    ra.ra_device_status(stream)
+    ms_step = reduce_max(ev0.elapsed_time(ev1), ws) / args.steps
+    trace = {kd_: ra.ra_trace_query(kd_) for kd_ in ("bwd_pre", "bwd_dq", "bwd_dkdv")}
+    ra.ra_trace_reset()
+    f_adj = 2.5 * w.flops_causal_adjusted()
+    f_exact = 2.5 * w.flops_exact()
+    value = ws * f_adj / (ms_step * 1e-3) / 1e12
+    ms_dq, ms_dkdv = trace["bwd_dq"][1], trace["bwd_dkdv"][1]
+    # dQ kernel: S, dP, dQ products (3 of the 5); dK/dV kernel: S, dP, dV, dK (4).
+    ach_dq = (0.6 * f_exact * args.steps) / (ms_dq * 1e-3) / 1e12 if ms_dq > 0 else None
+    ach_dkdv = (0.8 * f_exact * args.steps) / (ms_dkdv * 1e-3) / 1e12 if ms_dkdv > 0 else None
+    peak = peaks["bf16_tflops_sustained"]
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cores = os.cpu_count() or 1
+        rng = np.random.default_rng(7)
+        rows = np.sort(rng.choice(w.N, size=max(1, cores), replace=False))
+        t0 = time.perf_counter()
+        oracle.grad_q(q, k, v, g, causal=w.causal, rows=rows, threads=cores)
+        dt = time.perf_counter() - t0
+        keys = (rows + 1) if w.causal else np.full_like(rows, w.N)
+        # grad_q makes three passes over a row's keys (scores, D, dQ): count
+        # the S, dP and dQ products, 6*d FLOPs per pair per head.
+        f = 6.0 * w.d * w.heads * float(keys.sum())
+        cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": f"dQ of {len(rows)} query rows drawn uniformly, all {w.heads} heads, "
+                         f"full causal key range ({f:.3e} FLOPs of S, dP, dQ, {dt:.1f} s)"}
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC_BWD, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic",
+        "frac_of_dense_bf16_peak": value / ws / peaks["bf16_tflops"], "peak_source": peak_src,
+        "config": {"workload": w.name, "N": w.N, "P": w.P, "c": w.c, "heads": w.heads,
+                   "kv_heads": w.kv_heads, "d": w.d, "causal": w.causal, "recipe": w.recipe,
+                   "seed": w.seed, "parallelism": f"replicas{ws}",
+                   "flops_per_step_causal_adjusted": f_adj, "flops_per_step_exact": f_exact,
+                   "l2": "inputs larger than L2; no flush"},
+        "clocks": clk, "e2e": None,
+        "gpu_launches": sum(n for n, _ in trace.values()),
+        "kernel_ms": {kd_: t / args.steps for kd_, (n, t) in trace.items()},
+        "roofline": {"bound": "tensor", "achieved": ach_dkdv, "peak": peak, "unit": "TFLOP/s",
+                     "frac": (ach_dkdv / peak) if ach_dkdv else None, "traffic": None,
+                     "kernel": "backward dK/dV (tcgen05)",
+                     "peak_kind": f"bf16_tflops_sustained ({peak_src})",
+                     "dq_kernel_achieved": ach_dq},
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
 # ------------------------------------------------------------------ arms
 def run_reference(args, w, ws, rank):
     if rank != 0:
@@ -588,6 +700,8 @@ def main():
     ap.add_argument("--n-valid", type=int, default=-1, help="valid length (-1 = N)")
     ap.add_argument("--decode", default=None, choices=["decode-1m", "decode-1m-q4"],
                     help="time the decode path on this workload instead")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the backward ring (ra_ring_backward) instead")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
@@ -607,7 +721,11 @@ def main():
             torch.cuda.set_device(local)
         dist.init_process_group(backend)
     try:
-        if args.decode is not None:
+        if args.backward:
+            if args.impl == "reference":
+                ap.error("backward runs have no reference arm; the oracle is the cpu_baseline")
+            run_backward(args, w, ws, rank, local)
+        elif args.decode is not None:
             if args.impl == "reference":
                 ap.error("decode runs have no reference arm; time the oracle through cpu_baseline")
             run_decode(args, ws, rank, local)

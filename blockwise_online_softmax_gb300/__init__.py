@@ -20,6 +20,8 @@ from .binding import (  # noqa: E402,F401
     ra_ring_forward,
     ra_ring_forward_host,
     ra_ring_forward_masked,
+    ra_ring_backward,
+    ra_ring_backward_masked,
     ra_ring_forward_noalloc,
     ra_ring_step,
     ra_ring_step_masked,

@@ -34,6 +34,9 @@ KERNEL_KINDS = {
     "finalize": 4,
     "decode_split": 5,
     "decode_combine": 6,
+    "bwd_pre": 7,
+    "bwd_dq": 8,
+    "bwd_dkdv": 9,
 }
 
 _lock = threading.Lock()
@@ -60,6 +63,8 @@ _SIGNATURES = {
     "ra_ring_step_masked": ("PPPPPPLiiiiLLPiiiiiP", "i"),
     "ra_ring_forward_masked": ("PPPPPLiiiLLPiiiiiP", "i"),
     "ra_decode_partial": ("PPPPPPLLiiiLLiLiP", "i"),
+    "ra_ring_backward": ("PPPPPPPPPLiiiiiiP", "i"),
+    "ra_ring_backward_masked": ("PPPPPPPPPLiiiLLPiiiiiP", "i"),
     "ra_decode_forward": ("PPPPPLLiLiLiiiiP", "i"),
     "ra_device_status": ("P", "i"),
     "ra_selftest_wait_timeout": ("LP", "i"),
@@ -310,6 +315,55 @@ def ra_ring_forward_masked(q, k, v, *, P: int, layout="contiguous", causal: bool
         int(window), int(n_valid), cu_ptr, ndocs, d, heads, kv_heads, _qkv_dtype(q),
         _stream(stream)))
     return out, lse
+
+
+def ra_ring_backward_masked(q, k, v, out, lse, dout, *, P: int, layout="contiguous",
+                            causal: bool = False, window: int = 0, n_valid: int = -1,
+                            cu_seqlens=None, dq=None, dk=None, dv=None, stream=None):
+    """Gradients (dq [N, heads, d], dk, dv [N, kv_heads, d], fp32) of the
+    ring forward whose outputs are out, lse, for the upstream gradient dout
+    (bf16, like q).  Same layout and mask arguments as the forward."""
+    N, heads, kv_heads, d = _shapes(q, k, v)
+    if k.shape[0] != N:
+        raise ValueError("q, k and v must cover the same N tokens")
+    _state_shapes(lse, lse, out, N, heads, d)
+    if tuple(dout.shape) != (N, heads, d) or dout.dtype != q.dtype:
+        raise ValueError("dout must match q in shape and dtype")
+    if dq is None:
+        dq = torch.empty((N, heads, d), dtype=torch.float32, device=q.device)
+    if dk is None:
+        dk = torch.empty((N, kv_heads, d), dtype=torch.float32, device=q.device)
+    if dv is None:
+        dv = torch.empty((N, kv_heads, d), dtype=torch.float32, device=q.device)
+    cu_ptr, ndocs = _docs(cu_seqlens)
+    _check(lib().ra_ring_backward_masked(
+        _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(out, "out", torch.float32),
+        _dev(lse, "lse", torch.float32), _dev(dout, "dout"), _dev(dq, "dq", torch.float32),
+        _dev(dk, "dk", torch.float32), _dev(dv, "dv", torch.float32), N, int(P),
+        _layout(layout), int(bool(causal)), int(window), int(n_valid), cu_ptr, ndocs, d, heads,
+        kv_heads, _qkv_dtype(q), _stream(stream)))
+    return dq, dk, dv
+
+
+def ra_ring_backward(q, k, v, out, lse, dout, *, P: int, causal: bool, dq=None, dk=None,
+                     dv=None, stream=None):
+    """ra_ring_backward_masked with the contiguous layout and no extra mask."""
+    N, heads, kv_heads, d = _shapes(q, k, v)
+    _state_shapes(lse, lse, out, N, heads, d)
+    if tuple(dout.shape) != (N, heads, d) or dout.dtype != q.dtype:
+        raise ValueError("dout must match q in shape and dtype")
+    if dq is None:
+        dq = torch.empty((N, heads, d), dtype=torch.float32, device=q.device)
+    if dk is None:
+        dk = torch.empty((N, kv_heads, d), dtype=torch.float32, device=q.device)
+    if dv is None:
+        dv = torch.empty((N, kv_heads, d), dtype=torch.float32, device=q.device)
+    _check(lib().ra_ring_backward(
+        _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(out, "out", torch.float32),
+        _dev(lse, "lse", torch.float32), _dev(dout, "dout"), _dev(dq, "dq", torch.float32),
+        _dev(dk, "dk", torch.float32), _dev(dv, "dv", torch.float32), N, int(P),
+        int(bool(causal)), d, heads, kv_heads, _qkv_dtype(q), _stream(stream)))
+    return dq, dk, dv
 
 
 def _decode_shapes(q, k, v):

@@ -19,7 +19,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libra.so")
-SOURCES = ["ra_api.cu", "state_kernels.cu", "simt_kernel.cu", "umma_kernel.cu", "decode_kernel.cu"]
+SOURCES = ["ra_api.cu", "state_kernels.cu", "simt_kernel.cu", "umma_kernel.cu", "decode_kernel.cu",
+           "bwd_kernel.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

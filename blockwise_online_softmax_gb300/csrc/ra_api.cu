@@ -412,6 +412,75 @@ int noalloc_scratch(float** out) {
   return RA_OK;
 }
 
+// ----------------------------------------------------------------- backward
+int ring_backward_impl(const void* q, const void* k, const void* v, const float* out,
+                       const float* lse, const void* dout, float* dq, float* dk, float* dv,
+                       long long N, int P, const MaskSpec& mk, int d, int heads, int kv_heads,
+                       cudaStream_t st) {
+  float* dvec = nullptr;
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&dvec),
+                                  static_cast<size_t>(N) * heads * sizeof(float), st);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(RA_ERR_ALLOC, "cudaMallocAsync of the D vector failed: %s", cudaGetErrorString(e));
+  }
+  int rc = RA_OK;
+  {
+    TraceScope t0(RA_KERNEL_BWD_PRE, st);
+    e = ra::launch_bwd_pre(out, dout, dvec, N, heads, d, st);
+    t0.done(e == cudaSuccess);
+  }
+  if (e == cudaSuccess) e = cudaMemsetAsync(dq, 0, static_cast<size_t>(N) * heads * d * 4, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(dk, 0, static_cast<size_t>(N) * kv_heads * d * 4, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(dv, 0, static_cast<size_t>(N) * kv_heads * d * 4, st);
+  if (e != cudaSuccess) rc = cuda_fail(e, "backward set-up");
+  CUtensorMap tq, tk, tv, to;
+  if (rc == RA_OK) rc = get_encoder();
+  if (rc == RA_OK) rc = encode_map(&tq, q, N, heads, d);
+  if (rc == RA_OK) rc = encode_map(&tk, k, N, kv_heads, d);
+  if (rc == RA_OK) rc = encode_map(&tv, v, N, kv_heads, d);
+  if (rc == RA_OK) rc = encode_map(&to, dout, N, heads, d);
+  for (int s = 0; rc == RA_OK && s < P; ++s) {
+    ra::BwdArgs b{};
+    ra::FwdArgs& a = b.f;
+    a.q = q; a.k = k; a.v = v;
+    a.cq = N / P;
+    a.ck = N / P;
+    a.q_rows = N;
+    a.kv_rows = N;
+    a.heads = heads;
+    a.kv_heads = kv_heads;
+    a.mode = 1;
+    a.P = P;
+    a.s = s;
+    a.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
+    a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+    a.wait_limit = kWaitLimit;
+    put_mask(a, mk);
+    set_step_ranks(a, mk, P, N / P, s);
+    if (a.nwork == 0 || a.cq == 0) continue;
+    b.lse = lse;
+    b.dvec = dvec;
+    b.dq = dq;
+    b.dk = dk;
+    b.dv = dv;
+    {
+      TraceScope t1(RA_KERNEL_BWD_DQ, st);
+      e = ra::launch_bwd_dq(b, d, tq, tk, tv, to, st);
+      t1.done(e == cudaSuccess);
+    }
+    if (e == cudaSuccess) {
+      TraceScope t2(RA_KERNEL_BWD_DKDV, st);
+      e = ra::launch_bwd_dkdv(b, d, tq, tk, tv, to, st);
+      t2.done(e == cudaSuccess);
+    }
+    if (e != cudaSuccess) rc = cuda_fail(e, "backward launch");
+  }
+  e = cudaFreeAsync(dvec, st);
+  if (rc == RA_OK && e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync");
+  return rc;
+}
+
 // ----------------------------------------------------------------- decode
 int decode_args_check(const void* q, const void* k, const void* v, long long n_q, long long n_kv,
                       int d, int heads, int kv_heads, long long window, int dtype) {
@@ -732,6 +801,31 @@ int ra_ring_forward_noalloc(const void* q, const void* k, const void* v, float* 
                            static_cast<cudaStream_t>(stream), l_scratch);
 }
 
+int ra_ring_backward_masked(const void* q, const void* k, const void* v, const float* out,
+                            const float* lse, const void* dout, float* dq, float* dk, float* dv,
+                            long long N, int P, int layout, int causal, long long window,
+                            long long n_valid, const int* cu_seqlens, int ndocs, int d, int heads,
+                            int kv_heads, int dtype, void* stream) {
+  int rc = ring_args_check(N, P, 0, d, heads, kv_heads, dtype, layout);
+  if (rc != RA_OK) return rc;
+  if (dtype != RA_BF16) return fail(RA_ERR_UNSUPPORTED, "the backward ring takes bf16 q, k, v, dout");
+  MaskSpec mk;
+  if ((rc = check_mask(layout, causal, window, n_valid, cu_seqlens, ndocs, &mk)) != RA_OK) return rc;
+  if (N == 0) return RA_OK;
+  if ((rc = check_ptrs({q, k, v, out, lse, dout, dq, dk, dv})) != RA_OK) return rc;
+  return ring_backward_impl(q, k, v, out, lse, dout, dq, dk, dv, N, P, mk, d, heads, kv_heads,
+                            static_cast<cudaStream_t>(stream));
+}
+
+int ra_ring_backward(const void* q, const void* k, const void* v, const float* out,
+                     const float* lse, const void* dout, float* dq, float* dk, float* dv,
+                     long long N, int P, int causal, int d, int heads, int kv_heads, int dtype,
+                     void* stream) {
+  return ra_ring_backward_masked(q, k, v, out, lse, dout, dq, dk, dv, N, P, RA_LAYOUT_CONTIGUOUS,
+                                 causal ? 1 : 0, 0, -1, nullptr, 0, d, heads, kv_heads, dtype,
+                                 stream);
+}
+
 int ra_decode_partial(const void* q, const void* k, const void* v, float* m, float* l, float* o,
                       long long n_q, long long n_kv, int d, int heads, int kv_heads,
                       long long q_off, long long kv_off, int causal, long long window,
@@ -816,12 +910,14 @@ int ra_decode_forward(const void* q, const void* k, const void* v, float* out, f
 int ra_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-  int a = 0, b = 0, c = 0;
+  int a = 0, b = 0, c = 0, w = 0;
   if ((e = ra::take_umma_status(&a)) != cudaSuccess) return cuda_fail(e, "reading the tcgen05 kernel status");
   if ((e = ra::take_simt_status(&b)) != cudaSuccess) return cuda_fail(e, "reading the fp32 kernel status");
   if ((e = ra::take_decode_status(&c)) != cudaSuccess) return cuda_fail(e, "reading the decode kernel status");
-  if (a != 0 || b != 0 || c != 0)
-    return fail(RA_ERR_TIMEOUT, "a kernel gave up a bounded wait (codes 0x%x, 0x%x, 0x%x)", a, b, c);
+  if ((e = ra::take_bwd_status(&w)) != cudaSuccess) return cuda_fail(e, "reading the backward kernel status");
+  if (a != 0 || b != 0 || c != 0 || w != 0)
+    return fail(RA_ERR_TIMEOUT, "a kernel gave up a bounded wait (codes 0x%x, 0x%x, 0x%x, 0x%x)",
+                a, b, c, w);
   return RA_OK;
 }
 

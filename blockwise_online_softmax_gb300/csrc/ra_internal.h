@@ -226,6 +226,17 @@ struct DecArgs {
   MaskArgs mask;
 };
 
+// One launch of a backward kernel: the forward's launch description (q, k,
+// v, blocks, ranks, mask; m, l, o unused) plus the gradient tensors.
+struct BwdArgs {
+  FwdArgs f;
+  const float* lse;   // [q_rows, heads], natural log
+  const float* dvec;  // [q_rows, heads]: rowsum(dO * O)
+  float* dq;          // [q_rows, heads, d], accumulated
+  float* dk;          // [kv_rows, kv_heads, d], accumulated
+  float* dv;
+};
+
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -250,5 +261,12 @@ cudaError_t launch_decode_combine(float* m, float* l, float* o, const float* pm,
 cudaError_t take_umma_status(int* code);
 cudaError_t take_simt_status(int* code);
 cudaError_t take_decode_status(int* code);
+cudaError_t launch_bwd_pre(const float* out, const void* dout, float* dvec, long long rows,
+                           int heads, int d, cudaStream_t st);
+cudaError_t launch_bwd_dq(const BwdArgs& b, int d, const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, const CUtensorMap& to, cudaStream_t st);
+cudaError_t launch_bwd_dkdv(const BwdArgs& b, int d, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const CUtensorMap& to, cudaStream_t st);
+cudaError_t take_bwd_status(int* code);
 
 }  // namespace ra

@@ -112,7 +112,10 @@ typedef enum {
   RA_KERNEL_FINALIZE = 4,
   RA_KERNEL_DECODE_SPLIT = 5,   /* decode split-K kernel (CUDA cores, TMA) */
   RA_KERNEL_DECODE_COMBINE = 6, /* folds a shard's split partial states */
-  RA_KERNEL_KINDS = 7
+  RA_KERNEL_BWD_PRE = 7,        /* backward: D = rowsum(dO * O) */
+  RA_KERNEL_BWD_DQ = 8,         /* backward: dQ (tcgen05, Q-stationary) */
+  RA_KERNEL_BWD_DKDV = 9,       /* backward: dK, dV (tcgen05, K/V-stationary) */
+  RA_KERNEL_KINDS = 10
 } ra_kernel_kind;
 
 /*
@@ -298,6 +301,39 @@ int ra_ring_forward_masked(const void* q, const void* k, const void* v, float* o
                            long long N, int P, int layout, int causal, long long window,
                            long long n_valid, const int* cu_seqlens, int ndocs, int d,
                            int heads, int kv_heads, int dtype, void* stream);
+
+/*
+ * ra_ring_backward -- gradients of the ring forward for all P virtual ranks
+ * ("Ring Attention：把超长序列沿设备环流动", section "Backward 需要让梯度也
+ * 沿环传播"; [XF] "End-to-end flow": the backward ring carries the K/V
+ * blocks and their gradient accumulators, which arrive home fully summed
+ * after P steps).  For the loss L with dL/dO = dout:
+ *   P = exp(S - LSE) is recomputed from the saved lse, D = rowsum(dout * out),
+ *   dP = dout V^T, dS = P (dP - D) / sqrt(d),
+ *   dq = dS K, dk = dS^T Q (summed over each KV head's query heads),
+ *   dv = P^T dout (likewise).
+ *   q, k, v: the forward's inputs (bf16).  out [N, heads, d] and lse
+ *   [N, heads]: the forward's outputs (fp32).  dout: [N, heads, d] bf16.
+ *   dq: [N, heads, d]; dk, dv: [N, kv_heads, d]: fp32, written (zeroed
+ *   first, then accumulated over the ring steps).
+ * Step s runs, for every rank i with block j = (i - s) mod P, a
+ * Q-stationary tcgen05 kernel adding to dq of block i and a
+ * K/V-stationary one adding to dk, dv of block j; within a launch every
+ * block has one writer, so nothing is atomic.  P and dS are rounded to bf16
+ * for their products, as in the forward.  Scratch: D ([N, heads] fp32),
+ * from cudaMallocAsync on `stream`.  dtype must be RA_BF16.
+ */
+int ra_ring_backward(const void* q, const void* k, const void* v, const float* out,
+                     const float* lse, const void* dout, float* dq, float* dk, float* dv,
+                     long long N, int P, int causal, int d, int heads, int kv_heads, int dtype,
+                     void* stream);
+
+/* ra_ring_backward with a layout and the full mask (as ra_ring_forward_masked). */
+int ra_ring_backward_masked(const void* q, const void* k, const void* v, const float* out,
+                            const float* lse, const void* dout, float* dq, float* dk, float* dv,
+                            long long N, int P, int layout, int causal, long long window,
+                            long long n_valid, const int* cu_seqlens, int ndocs, int d, int heads,
+                            int kv_heads, int dtype, void* stream);
 
 /*
  * Decode and short query blocks ("Ring Attention：把超长序列沿设备环流动",

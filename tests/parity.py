@@ -13,11 +13,18 @@ exact running max:
 * |l - l_ref| <= tol_l * l_ref
 * |O~ - O~_ref| <= tol_o * l_ref, elementwise.  O~ is a weighted sum with
   total weight l, so its error scales with l.
+
+Gradients (bf16 inputs only) are compared per tensor against the largest
+reference magnitude: max |dX - dX_ref| <= 2e-2 * max |dX_ref|.  Each
+product in the backward rounds one operand to bf16 (P for dV, dS for dQ
+and dK), a relative error of at most 2^-9 per term; summed over the keys
+(or queries) with mixed signs, the error of an output element stays a few
+times 2^-9 of the largest |term| sums, which the bar covers with margin.
 """
 import numpy as np
 
 TOL = {
-    "bf16": {"o": 1e-2, "lse": 1e-3, "l": 2e-3},
+    "bf16": {"o": 1e-2, "lse": 1e-3, "l": 2e-3, "grad": 2e-2},
     "f32": {"o": 1e-5, "lse": 1e-5, "l": 1e-5},
 }
 
@@ -61,3 +68,16 @@ def check_state(m, l, o, ref, kind):
         assert eo <= t["o"], f"O~ err / l = {eo:.3e}"
     # rows with no allowed key keep the identity state
     assert (l[~fin] == 0).all() and (o[~fin] == 0).all()
+
+
+def check_grad(x, ref, name="grad"):
+    """max |x - ref| <= TOL["bf16"]["grad"] * max |ref| (the gradient bar)."""
+    x = _np(x)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert x.shape == ref.shape, (x.shape, ref.shape)
+    assert np.isfinite(x).all(), f"non-finite {name}"
+    scale = np.abs(ref).max() if ref.size else 0.0
+    err = np.abs(x - ref).max() if ref.size else 0.0
+    assert err <= TOL["bf16"]["grad"] * max(scale, 1e-30), \
+        f"{name}: max err {err:.3e} > {TOL['bf16']['grad']} x {scale:.3e}"
+    return err / max(scale, 1e-30)
