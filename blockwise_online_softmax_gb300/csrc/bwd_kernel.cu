@@ -540,7 +540,9 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       tc_fence_after();
       const uint32_t nlb = smem_u32(nl + (it & 1) * BT);
       const int2* lb = lmt + (it & 1) * BT;
-#pragma unroll
+      // Rolled: the chunk loop body is large, and one copy keeps the
+      // softmax warps' code in the instruction cache.
+#pragma unroll 1
       for (int c = 0; c < BT / 32; ++c) {
         uint32_t s[32], dp[32], wp[16], wd[16];
         tmem_ld32(tl + C::C_S + c * 32, s);
