@@ -419,6 +419,333 @@ __global__ void decode_combine_kernel(float* __restrict__ m, float* __restrict__
   }
 }
 
+// ------------------------------------------------------------------ tensor-core form
+// For more query rows per KV head (g * n_q up to 128) the same split-K
+// partial states come from tcgen05 products: the KV head's g * n_q rows are
+// gathered into one 128-row query tile (a 3-D TMA box of g heads x n_q
+// tokens; the rest of the tile is zero), and the CTA walks its key chunk in
+// 128-key tiles with S = Q K^T and O += P V in TMEM and the online softmax
+// of the forward kernel on one thread per row.  Roles (256 threads): warps
+// 0-3 softmax, warp 4 TMA, warp 5 MMA issuer and TMEM owner.  Every wait is
+// bounded.
+namespace tc {
+
+constexpr int BT = 128;
+constexpr uint32_t CHB = 128 * 128;  // one 64-column swizzled chunk of a 128-row tile
+
+template <int D>
+struct TCfg {
+  static constexpr int NCH = D / 64;
+  static constexpr uint32_t TILE = BT * D * 2;
+  static constexpr int NST = 2;                      // K/V stages (K and V of one tile each)
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_ST = OFF_Q + TILE;   // stage s: K at OFF_ST + 2*s*TILE, V after
+  static constexpr uint32_t OFF_BAR = OFF_ST + NST * 2 * TILE;
+  static constexpr int B_Q = 0, B_F = 1, B_E = B_F + NST, B_S = B_E + NST, B_P = B_S + 1,
+                       B_O = B_P + 1, B_DRAIN = B_O + 1, NBAR = B_DRAIN + 1;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr uint32_t SMEM = OFF_MISC + 16 + 1024;
+  static_assert(SMEM <= 232448, "shared memory budget");
+  static constexpr uint32_t C_S = 0, C_O = BT;  // TMEM: S (then P), O
+  static constexpr uint32_t TMEM_COLS = 256;
+  static_assert(C_O + D <= TMEM_COLS, "TMEM budget");
+};
+
+template <int D>
+__global__ void __launch_bounds__(256, 1)
+decode_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                 const __grid_constant__ CUtensorMap tmV, const DecArgs a) {
+  using C = TCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sb + C::OFF_BAR + 8u * static_cast<uint32_t>(i); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int split = blockIdx.x, kh = blockIdx.y, shard = blockIdx.z;
+  const int g = a.heads / a.kv_heads;
+  const int R = g * static_cast<int>(a.n_q);
+  const long long sh0 = static_cast<long long>(shard) * a.shard_len;
+  const long long sh1 = sh0 + a.shard_len < a.n_kv ? sh0 + a.shard_len : a.n_kv;
+  const long long c0 = sh0 + static_cast<long long>(split) * a.chunk;
+  const long long c1 = c0 + a.chunk < sh1 ? c0 + a.chunk : sh1;
+  const long long vb = valid_bound(a.mask);
+  const PosMap km{kContiguous, 1, a.n_kv, 0, a.kv_off};
+  // Allowed keys of query token qi, clipped to this CTA's chunk.
+  auto keys_of = [&](long long qi, long long* lo, long long* hi) {
+    *lo = c0;
+    *hi = c0;
+    const long long qp = a.q_off + qi;
+    long long plo, phi;
+    if (qp < vb && allowed_positions(a.mask, qp, &plo, &phi)) {
+      const long long l = count_below(km, plo), h = count_below(km, phi);
+      *lo = l > c0 ? l : c0;
+      *hi = h < c1 ? h : c1;
+      if (*hi < *lo) *hi = *lo;
+    }
+  };
+  // Rows grow in position with r (r = qi * g + hl), so the first and last
+  // query tokens bound the key range of the tile.
+  long long lo0, hi0, lo1, hi1;
+  keys_of(0, &lo0, &hi0);
+  keys_of(a.n_q - 1, &lo1, &hi1);
+  const long long klo = lo0 < lo1 ? lo0 : lo1, khi = hi0 > hi1 ? hi0 : hi1;
+  const long long kb = (klo / BT) * BT;
+  const int n = khi > klo ? static_cast<int>((khi - kb + BT - 1) / BT) : 0;
+  const long long lim = a.wait_limit;
+  const long long pbase = (static_cast<long long>(shard) * a.nsplit + split) * a.n_q;
+  if (n == 0) {
+    // No key of this chunk is allowed: an empty partial state.
+    for (int i = tid; i < R * D; i += 256) {
+      const long long qi = (i / D) / g;
+      const int h = kh * g + (i / D) % g;
+      const long long pidx = (pbase + qi) * a.heads + h;
+      a.po[pidx * D + i % D] = 0.f;
+      if (i % D == 0) {
+        a.pm[pidx] = -INFINITY;
+        a.pl[pidx] = 0.f;
+      }
+    }
+    return;
+  }
+  // Zero the query tile: rows R..127 stay zero, rows 0..R-1 come by TMA.
+  for (int i = tid; i < static_cast<int>(C::TILE / 16); i += 256)
+    reinterpret_cast<uint4*>(smem + C::OFF_Q)[i] = make_uint4(0u, 0u, 0u, 0u);
+  if (tid == 0) {
+    for (int i = 0; i < C::NBAR; ++i) mbar_init(bar(i), i == C::B_P ? 128u : 1u);
+    *abort_flag = *reinterpret_cast<volatile int*>(&g_decode_status) != 0 ? 1 : 0;
+    fence_mbar_init();
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+  if (*abort_flag) return;
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 4) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar(C::B_Q), static_cast<uint32_t>(R) * 128u * C::NCH);
+      for (int ch = 0; ch < C::NCH; ++ch)
+        tma_load_3d(sb + C::OFF_Q + ch * CHB, &tmQ, bar(C::B_Q), ch * 64, kh * g, 0);
+      int issued = 0;
+      bool ok = true;
+      for (int k = 0; k < n; ++k) {
+        const int st = k % C::NST;
+        if (k >= C::NST)
+          ok = wait_bar(bar(C::B_E + st), (static_cast<uint32_t>(k / C::NST) & 1u) ^ 1u,
+                        abort_flag, &g_decode_status, 0x71, lim);
+        if (!ok) break;
+        const uint32_t dst = sb + C::OFF_ST + st * 2 * C::TILE;
+        const int krow = static_cast<int>(kb + static_cast<long long>(k) * BT);
+        mbar_arrive_expect_tx(bar(C::B_F + st), 2 * C::TILE);
+        for (int ch = 0; ch < C::NCH; ++ch) {
+          tma_load_3d(dst + ch * CHB, &tmK, bar(C::B_F + st), ch * 64, kh, krow);
+          tma_load_3d(dst + C::TILE + ch * CHB, &tmV, bar(C::B_F + st), ch * 64, kh, krow);
+        }
+        issued = k + 1;
+      }
+      if (!ok) {
+        volatile int no_abort = 0;
+        for (int k = issued > C::NST ? issued - C::NST : 0; k < issued; ++k)
+          wait_bar(bar(C::B_F + k % C::NST), static_cast<uint32_t>(k / C::NST) & 1u, &no_abort,
+                   nullptr, 0, lim);
+        wait_bar(bar(C::B_Q), 0, &no_abort, nullptr, 0, lim);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ---------------------------------------------------------------- MMA issuer
+    const uint32_t lead = lane == 0 ? 1u : 0u;
+    constexpr uint32_t idesc_qk = idesc_bf16(BT, BT, 0);
+    constexpr uint32_t idesc_pv = idesc_bf16(BT, D, 1);
+    const uint64_t qdesc = sdesc_sw128(sb + C::OFF_Q, 16, 1024);
+    auto qk = [&](int st) {
+      const uint64_t kd = sdesc_sw128(sb + C::OFF_ST + st * 2 * C::TILE, 16, 1024);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t off = ((kk >> 2) * CHB + (kk & 3) * 32) >> 4;
+        mma_ss_lead(lead, tmem + C::C_S, qdesc + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
+      }
+      tc_commit_lead(lead, bar(C::B_S));
+    };
+    bool ok = wait_bar(bar(C::B_Q), 0, abort_flag, &g_decode_status, 0x72, lim);
+    if (ok) ok = wait_bar(bar(C::B_F), 0, abort_flag, &g_decode_status, 0x73, lim);
+    if (ok) {
+      tc_fence_after();
+      qk(0);
+    }
+    for (int k = 0; k < n && ok; ++k) {
+      const int st = k % C::NST;
+      ok = wait_bar(bar(C::B_P), static_cast<uint32_t>(k) & 1u, abort_flag, &g_decode_status,
+                    0x74, lim);
+      if (!ok) break;
+      tc_fence_after();
+      const uint64_t vd = sdesc_sw128(sb + C::OFF_ST + st * 2 * C::TILE + C::TILE, CHB, 1024);
+#pragma unroll
+      for (int kk = 0; kk < BT / 16; ++kk)
+        mma_ts_lead(lead, tmem + C::C_O, tmem + C::C_S + kk * 8,
+                    vd + static_cast<uint64_t>((kk * 2048) >> 4), idesc_pv, 1u);
+      tc_commit_lead(lead, bar(C::B_E + st));
+      if (k + 1 == n) {
+        tc_commit_lead(lead, bar(C::B_O));
+      } else {
+        ok = wait_bar(bar(C::B_F + (k + 1) % C::NST), static_cast<uint32_t>((k + 1) / C::NST) & 1u,
+                      abort_flag, &g_decode_status, 0x73, lim);
+        if (!ok) break;
+        tc_fence_after();
+        qk((k + 1) % C::NST);  // in issue order after P V, which reads P from S's columns
+      }
+    }
+    volatile int no_abort = 0;
+    tc_commit_lead(lead, bar(C::B_DRAIN));
+    wait_bar(bar(C::B_DRAIN), 0, &no_abort, nullptr, 0, lim);
+    __syncwarp();
+  } else if (warp < 4) {
+    // ---------------------------------------------------------------- softmax
+    const int r = warp * 32 + lane;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const bool valid = r < R;
+    long long rlo = 0, rhi = 0;
+    if (valid) keys_of(r / g, &rlo, &rhi);
+    const int row_lo = static_cast<int>(rlo - kb), row_hi = static_cast<int>(rhi - kb);
+    {
+      uint32_t z[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) z[j] = 0u;
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) tmem_st32(tl + C::C_O + cc * 32, z);
+      tmem_wait_st();
+    }
+    // Each thread's first arrival on B_P comes after its zeroed O row is in
+    // TMEM, so the first P V accumulates onto zeros.
+    const float sl2 = a.scale_log2;
+    const uint64_t sl2x2 = f2pack(sl2, sl2);
+    float m_used = -INFINITY, m_true = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int k = 0; k < n; ++k) {
+      ok = wait_bar(bar(C::B_S), static_cast<uint32_t>(k) & 1u, abort_flag, &g_decode_status,
+                    0x75, lim);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) tmem_ld32(tl + C::C_S + cc * 32, sr[cc]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) reg_fence32(sr[cc]);
+      const int lo_j = row_lo - k * BT, hi_j = row_hi - k * BT;
+      if (lo_j > 0 || hi_j < BT) {
+#pragma unroll
+        for (int j = 0; j < BT; ++j)
+          if (j < lo_j || j >= hi_j) sr[j >> 5][j & 31] = 0xff800000u;  // -inf
+      }
+#define RA_S(j) __uint_as_float(sr[(j) >> 5][(j) & 31])
+      float mx0 = fmaxf(RA_S(0), RA_S(4)), mx1 = fmaxf(RA_S(1), RA_S(5));
+      float mx2 = fmaxf(RA_S(2), RA_S(6)), mx3 = fmaxf(RA_S(3), RA_S(7));
+#pragma unroll
+      for (int j = 8; j < BT; j += 8) {
+        mx0 = fmax3(mx0, RA_S(j + 0), RA_S(j + 4));
+        mx1 = fmax3(mx1, RA_S(j + 1), RA_S(j + 5));
+        mx2 = fmax3(mx2, RA_S(j + 2), RA_S(j + 6));
+        mx3 = fmax3(mx3, RA_S(j + 3), RA_S(j + 7));
+      }
+      const float m_tile = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
+      float alpha = 1.f;
+      if (m_tile > m_true) {
+        m_true = m_tile;
+        alpha = ex2(m_used - m_true);  // m_used = -inf gives 0
+        m_used = m_true;
+      }
+      if (__any_sync(0xffffffffu, alpha != 1.f)) {
+        // O is stable: S(k) comes after P V(k-1) in issue order.
+        const uint64_t al2 = f2pack(alpha, alpha);
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(tl + C::C_O + cc * 32, o);
+          tmem_wait_ld();
+          reg_fence32(o);
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            float y0, y1;
+            f2unpack(fmul2(f2pack(__uint_as_float(o[j]), __uint_as_float(o[j + 1])), al2), y0, y1);
+            o[j] = __float_as_uint(y0);
+            o[j + 1] = __float_as_uint(y1);
+          }
+          tmem_st32(tl + C::C_O + cc * 32, o);
+        }
+      }
+      const float mref = m_used == -INFINITY ? 0.f : m_used;
+      const uint64_t nm2 = f2pack(-mref, -mref);
+      uint64_t acc0 = f2pack(0.f, 0.f), acc1 = acc0;
+#pragma unroll
+      for (int j = 0; j < BT; j += 4) {
+        float x0, x1, x2, x3;
+        f2unpack(ffma2(f2pack(RA_S(j), RA_S(j + 1)), sl2x2, nm2), x0, x1);
+        f2unpack(ffma2(f2pack(RA_S(j + 2), RA_S(j + 3)), sl2x2, nm2), x2, x3);
+        const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
+        acc0 = fadd2(acc0, f2pack(p0, p1));
+        acc1 = fadd2(acc1, f2pack(p2, p3));
+        sr[(j / 2) >> 5][(j / 2) & 31] = bf16x2_rn(p0, p1);
+        sr[(j / 2 + 1) >> 5][(j / 2 + 1) & 31] = bf16x2_rn(p2, p3);
+      }
+#undef RA_S
+      tmem_st32(tl + C::C_S, sr[0]);
+      tmem_st32(tl + C::C_S + 32, sr[1]);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(C::B_P));
+      float sa, sbb;
+      f2unpack(fadd2(acc0, acc1), sa, sbb);
+      l_run = l_run * alpha + (sa + sbb);
+    }
+    if (ok) {
+      ok = wait_bar(bar(C::B_O), 0u, abort_flag, &g_decode_status, 0x76, lim);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      tc_fence_after();
+      uint32_t o[D / 32][32];
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(tl + C::C_O + cc * 32, o[cc]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) reg_fence32(o[cc]);
+      if (valid) {
+        const long long pidx = (pbase + r / g) * a.heads + kh * g + r % g;
+        float4* dst = reinterpret_cast<float4*>(a.po + pidx * D);
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc)
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            dst[cc * 8 + j] = make_float4(__uint_as_float(o[cc][4 * j]), __uint_as_float(o[cc][4 * j + 1]),
+                                          __uint_as_float(o[cc][4 * j + 2]),
+                                          __uint_as_float(o[cc][4 * j + 3]));
+        a.pm[pidx] = m_true == -INFINITY ? -INFINITY : m_true * kLn2;
+        a.pl[pidx] = l_run;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+}  // namespace tc
+
 template <int D, int RM>
 cudaError_t launch_split(const DecArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                          cudaStream_t st) {
@@ -440,7 +767,26 @@ cudaError_t launch_split_d(const DecArgs& a, int rows, const CUtensorMap& tk,
   return launch_split<D, 16>(a, tk, tv, st);
 }
 
+template <int D>
+cudaError_t launch_tc_d(const DecArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                        const CUtensorMap& tv, cudaStream_t st) {
+  using C = tc::TCfg<D>;
+  cudaError_t e = cudaFuncSetAttribute(tc::decode_tc_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(C::SMEM));
+  if (e != cudaSuccess) return e;
+  dim3 grid(static_cast<unsigned>(a.nsplit), static_cast<unsigned>(a.kv_heads),
+            static_cast<unsigned>(a.nshard));
+  tc::decode_tc_kernel<D><<<grid, 256, C::SMEM, st>>>(tq, tk, tv, a);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_decode_tc(const DecArgs& a, int d, const CUtensorMap& tq, const CUtensorMap& tk,
+                             const CUtensorMap& tv, cudaStream_t st) {
+  return d == 128 ? launch_tc_d<128>(a, tq, tk, tv, st) : launch_tc_d<64>(a, tq, tk, tv, st);
+}
 
 cudaError_t launch_decode_split(const DecArgs& a, int d, const CUtensorMap& tk,
                                 const CUtensorMap& tv, cudaStream_t st) {

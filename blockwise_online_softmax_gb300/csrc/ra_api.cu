@@ -129,6 +129,25 @@ int encode_map(CUtensorMap* map, const void* base, long long rows, int heads, in
   return RA_OK;
 }
 
+// 3-D map over the decode queries [n_q, heads, d] whose box is all n_q
+// tokens of g consecutive heads (one KV head's query rows), 64 columns
+// wide: the box lands in shared memory as g * n_q rows of 128 bytes, row
+// qi * g + hl, with 128-byte swizzle.
+int encode_q_group_map(CUtensorMap* map, const void* base, long long n_q, int heads, int g, int d) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
+                              static_cast<cuuint64_t>(n_q)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(heads) * d * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(g), static_cast<cuuint32_t>(n_q)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled (query group) failed (CUresult %d)", (int)r);
+  return RA_OK;
+}
+
 // ----------------------------------------------------------------- checks
 int check_common(int d, int heads, int dtype) {
   if (dtype != RA_F32 && dtype != RA_BF16) return fail(RA_ERR_INVALID, "dtype %d is not RA_F32 or RA_BF16", dtype);
@@ -482,6 +501,11 @@ int ring_backward_impl(const void* q, const void* k, const void* v, const float*
 }
 
 // ----------------------------------------------------------------- decode
+// Query rows per KV head (g * n_q) the decode path takes; up to
+// kDecodeFmaRows it runs on the CUDA cores, above on the tensor cores.
+constexpr int kDecodeMaxRows = 128;
+constexpr int kDecodeFmaRows = 4;
+
 int decode_args_check(const void* q, const void* k, const void* v, long long n_q, long long n_kv,
                       int d, int heads, int kv_heads, long long window, int dtype) {
   int rc;
@@ -491,11 +515,11 @@ int decode_args_check(const void* q, const void* k, const void* v, long long n_q
   if (n_q < 0 || n_kv < 0) return fail(RA_ERR_INVALID, "n_q=%lld or n_kv=%lld is negative", n_q, n_kv);
   if (n_kv > (1LL << 31) - 256) return fail(RA_ERR_UNSUPPORTED, "n_kv=%lld exceeds the 32-bit TMA row coordinate", n_kv);
   if (window < 0) return fail(RA_ERR_INVALID, "window=%lld is negative", window);
-  if (static_cast<long long>(heads / kv_heads) * n_q > 16)
+  if (static_cast<long long>(heads / kv_heads) * n_q > kDecodeMaxRows)
     return fail(RA_ERR_UNSUPPORTED,
-                "(heads / kv_heads) * n_q = %lld query rows per KV head exceeds 16; use "
+                "(heads / kv_heads) * n_q = %lld query rows per KV head exceeds %d; use "
                 "ra_block_update_masked for longer query blocks",
-                static_cast<long long>(heads / kv_heads) * n_q);
+                static_cast<long long>(heads / kv_heads) * n_q, kDecodeMaxRows);
   (void)q; (void)k; (void)v;
   return RA_OK;
 }
@@ -509,13 +533,17 @@ int decode_run(const void* q, const void* k, const void* v, float* m, float* l, 
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  // About four CTAs per SM over the whole launch, each at least 4 tiles
-  // (one per warp) of 32 keys.
-  long long want = (4LL * sms + static_cast<long long>(kv_heads) * nshard - 1) /
+  const bool use_tc = static_cast<long long>(heads / kv_heads) * n_q > kDecodeFmaRows;
+  // CUDA-core kernel: about four CTAs per SM over the whole launch, each at
+  // least 4 tiles (one per warp) of 32 keys.  Tensor-core kernel: one CTA
+  // per SM at a time, about three waves, chunks of whole 128-key tiles.
+  const long long waves = use_tc ? 3 : 4;
+  const long long gran = use_tc ? 128 : 32;
+  long long want = (waves * sms + static_cast<long long>(kv_heads) * nshard - 1) /
                    (static_cast<long long>(kv_heads) * nshard);
   if (want < 1) want = 1;
   long long chunk = (shard_len + want - 1) / want;
-  chunk = ((chunk + 31) / 32) * 32;
+  chunk = ((chunk + gran - 1) / gran) * gran;
   if (chunk < 128) chunk = 128;
   const long long nsplit = (shard_len + chunk - 1) / chunk;
   const long long rows = n_q * heads;  // state rows of one shard
@@ -529,9 +557,10 @@ int decode_run(const void* q, const void* k, const void* v, float* m, float* l, 
                 cudaGetErrorString(e));
   }
   int rc = get_encoder();
-  CUtensorMap tk, tv;
-  if (rc == RA_OK) rc = encode_map(&tk, k, n_kv, kv_heads, d, 32);
-  if (rc == RA_OK) rc = encode_map(&tv, v, n_kv, kv_heads, d, 32);
+  CUtensorMap tk, tv, tq;
+  if (rc == RA_OK) rc = encode_map(&tk, k, n_kv, kv_heads, d, use_tc ? 128 : 32);
+  if (rc == RA_OK) rc = encode_map(&tv, v, n_kv, kv_heads, d, use_tc ? 128 : 32);
+  if (rc == RA_OK && use_tc) rc = encode_q_group_map(&tq, q, n_q, heads, heads / kv_heads, d);
   if (rc == RA_OK) {
     ra::DecArgs a{};
     a.q = q;
@@ -554,7 +583,7 @@ int decode_run(const void* q, const void* k, const void* v, float* m, float* l, 
     a.mask.window = window > kAllValid ? kAllValid : window;
     a.mask.n_valid = kAllValid;
     TraceScope t0(RA_KERNEL_DECODE_SPLIT, st);
-    e = ra::launch_decode_split(a, d, tk, tv, st);
+    e = use_tc ? ra::launch_decode_tc(a, d, tq, tk, tv, st) : ra::launch_decode_split(a, d, tk, tv, st);
     t0.done(e == cudaSuccess);
     if (e != cudaSuccess) {
       rc = cuda_fail(e, "decode split launch");

@@ -253,6 +253,8 @@ cudaError_t launch_umma_update(const FwdArgs& a, int d, const CUtensorMap& tq,
 cudaError_t launch_wait_selftest(long long limit_cycles, cudaStream_t st);
 cudaError_t launch_decode_split(const DecArgs& a, int d, const CUtensorMap& tk,
                                 const CUtensorMap& tv, cudaStream_t st);
+cudaError_t launch_decode_tc(const DecArgs& a, int d, const CUtensorMap& tq, const CUtensorMap& tk,
+                             const CUtensorMap& tv, cudaStream_t st);
 cudaError_t launch_decode_combine(float* m, float* l, float* o, const float* pm, const float* pl,
                                   const float* po, long long rows_per_shard, int nsplit,
                                   int nshard, int d, cudaStream_t st);

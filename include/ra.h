@@ -350,12 +350,14 @@ int ra_ring_backward_masked(const void* q, const void* k, const void* v, const f
  *   k, v: [n_kv, kv_heads, d] bf16, positions kv_off .. kv_off + n_kv - 1.
  *   m, l: [n_q, heads] fp32; o: [n_q, heads, d] fp32 (updated in place).
  *   causal and window: as in the masked calls (kp <= qp; |qp - kp| < window).
- *   (heads / kv_heads) * n_q must be <= 16: every KV head's query rows are
+ *   (heads / kv_heads) * n_q must be <= 128: every KV head's query rows are
  *   held together, so each K/V byte is read once.  Longer query blocks
  *   belong to ra_block_update_masked.  dtype must be RA_BF16.
- * The work is HBM-bound: one CUDA-core kernel streams the keys of each KV
- * head in chunks spread over the SMs (split-K) and writes one partial state
- * per chunk; a second kernel folds them into m, l, o.  The partial states
+ * The work is HBM-bound: the keys of each KV head are streamed in chunks
+ * spread over the SMs (split-K), each chunk giving one partial state, and a
+ * second kernel folds them into m, l, o.  Up to 4 query rows per KV head
+ * the chunks run on the CUDA cores; above that, on the tensor cores (the
+ * KV head's query rows gathered into one 128-row tile).  The partial states
  * (chunks x n_q x heads x (d + 2) fp32) are allocated with cudaMallocAsync
  * on `stream`.
  */

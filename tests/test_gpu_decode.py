@@ -43,6 +43,12 @@ CASES = [
     (3, 12, 4, 64, 10000, 5, True, 1000),    # sliding window
     (16, 16, 16, 128, 4096, 2, True, 0),     # 16 new tokens, causal among them
     (1, 8, 2, 128, 31, 7, True, 0),          # fewer keys than a tile; empty shards
+    # more than 4 rows per KV head: the tensor-core chunks
+    (32, 32, 8, 128, 9000, 4, True, 0),      # 128 rows per KV head
+    (100, 4, 4, 64, 3000, 3, True, 0),       # 100 rows, MHA, d = 64
+    (8, 64, 8, 128, 20000, 16, True, 2048),  # 64 rows, windowed
+    (5, 8, 8, 128, 777, 2, False, 0),        # 5 rows, non-causal, ragged
+    (3, 32, 8, 64, 130, 8, True, 0),         # 12 rows, shards shorter than a tile
 ]
 
 
