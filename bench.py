@@ -223,7 +223,59 @@ def recorded_traffic(workload: str):
 
 
 # ------------------------------------------------------------------ CPU oracle sample
-def oracle_sample(w, q, k, v, target_s: float, seed: int = 7, mask: MaskRun | None = None):
+ARM_PARTS = {"0xd4f": "Arm Neoverse V2", "0xd40": "Arm Neoverse V1", "0xd0c": "Arm Neoverse N1",
+             "0xd49": "Arm Neoverse N2"}
+
+
+def cpu_model() -> str:
+    """The host CPU's model name, or its Arm part number (named when known)."""
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if ":" in line:
+                    key, val = line.split(":", 1)
+                    fields.setdefault(key.strip().lower(), val.strip())
+    except OSError:
+        pass
+    if "model name" in fields:
+        return fields["model name"]
+    if "cpu part" in fields:
+        part = fields["cpu part"]
+        return f"{ARM_PARTS.get(part, 'Arm')} (cpu part {part})"
+    import platform
+
+    return platform.processor() or platform.machine()
+
+
+def parity_check(w, q, k, v, out, lse, per_block: int = 2):
+    """Sampled-row parity of the timed run's own output against the fp64
+    oracle (rows {0, 1, 127, 128, c/2, c-1} and `per_block` random rows of
+    every block, all heads, each over its full key range)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from blockwise_online_softmax_gb300 import inputs
+
+    rows = inputs.sample_rows(w, random_per_block=per_block)
+    idx = torch.from_numpy(rows).to(out.device)
+    got_o = out.index_select(0, idx).cpu().double().numpy()
+    got_l = lse.index_select(0, idx).cpu().double().numpy()
+    t0 = time.perf_counter()
+    ref_o, ref_l = oracle.attention(q, k, v, causal=w.causal, rows=rows)
+    dt = time.perf_counter() - t0
+    fin = np.isfinite(ref_l)
+    e_o = float(np.abs(got_o - ref_o).max())
+    e_l = float((np.abs(got_l[fin] - ref_l[fin]) / np.maximum(1.0, np.abs(ref_l[fin]))).max())
+    tol_o, tol_l = (1e-2, 1e-3) if w.dtype == "bf16" else (1e-5, 1e-5)
+    return {"rows": int(len(rows)), "heads": w.heads, "max_abs_o": e_o, "max_rel_lse": e_l,
+            "tol_o": tol_o, "tol_lse": tol_l, "pass": bool(e_o <= tol_o and e_l <= tol_l),
+            "oracle_s": dt}
+
+
+def oracle_sample(w, q, k, v, target_s: float, seed: int = 7, mask: MaskRun | None = None,
+                  threads: int | None = None):
     """Time the fp64 oracle on sampled query rows (all heads, full key
     range), sized to take about ``target_s`` seconds.  Returns (TFLOP/s,
     cores, description).  With ``mask``, q/k/v are in sequence order and the
@@ -232,7 +284,7 @@ def oracle_sample(w, q, k, v, target_s: float, seed: int = 7, mask: MaskRun | No
 
     import oracle
 
-    cores = os.cpu_count() or 1
+    cores = threads or os.cpu_count() or 1
     rng = np.random.default_rng(seed)
     kw = {}
     if mask is not None:
@@ -556,20 +608,20 @@ def run_ours(args, w, ws, rank, local):
     clocks.start()
     ra.ra_trace_reset()
     ra.ra_trace_enable(True)
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     torch.cuda.synchronize(dev)
     barrier(ws)
-    ev0.record(stream)
-    for _ in range(args.steps):
+    evs[0].record(stream)
+    for i in range(args.steps):
         step()
-    ev1.record(stream)
+        evs[i + 1].record(stream)
     torch.cuda.synchronize(dev)
     barrier(ws)
     ra.ra_trace_enable(False)
     clk = clocks.stop()
     ra.ra_device_status(stream)
-    ms_total = ev0.elapsed_time(ev1)
+    ms_total = evs[0].elapsed_time(evs[-1])
+    per_step = [evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps)]
     n_upd, ms_upd = ra.ra_trace_query("block_update_bf16" if w.dtype == "bf16"
                                       else "block_update_f32")
     n_init, ms_init = ra.ra_trace_query("state_init")
@@ -594,8 +646,14 @@ def run_ours(args, w, ws, rank, local):
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         val, cores, desc, _ = oracle_sample(w, q, k, v, args.cpu_seconds, mask=mask)
+        val1, _, desc1, _ = oracle_sample(w, q, k, v, min(3.0, args.cpu_seconds / 5), seed=11,
+                                          mask=mask, threads=1)
         cpu = {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-               "sample": desc}
+               "sample": desc, "cpu_model": cpu_model(), "value_1core": val1,
+               "sample_1core": desc1}
+    parity = None
+    if rank == 0 and mask is None and not args.no_check:
+        parity = parity_check(w, q, k, v, out, lse)
     if mask is not None:
         if rank == 0:
             line = {
@@ -677,6 +735,9 @@ def run_ours(args, w, ws, rank, local):
                      f"bf16_tflops_sustained ({peak_src})",
                      "frac_of_burst": (achieved / peaks["bf16_tflops"]) if achieved else None},
         "cpu_baseline": cpu,
+        "ms_per_step_median": statistics.median(per_step),
+        "ms_per_step_best": min(per_step),
+        "parity": parity,
     }
     print(json.dumps(line), flush=True)
 
@@ -694,6 +755,8 @@ def main():
     ap.add_argument("--ref-step-seconds", type=float, default=6.0)
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-check", action="store_true",
+                    help="skip the sampled-row parity check of the timed run's output")
     ap.add_argument("--layout", default="contiguous", choices=["contiguous", "zigzag", "striped"])
     ap.add_argument("--window", type=int, default=0, help="sliding window (0 = none)")
     ap.add_argument("--docs", type=int, default=0, help="packed documents (0 = one sequence)")
