@@ -153,10 +153,18 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, log_dir: str | None = None):
+        """The raw samples go to log_dir/clocks_gpu<i>.csv when log_dir is
+        given (--clock-log), else to a temporary file."""
+        import tempfile
+
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+        self.keep = bool(log_dir)
+        if log_dir:
+            self.path = os.path.join(log_dir, f"clocks_gpu{gpu_index}.csv")
+        else:
+            self.path = os.path.join(tempfile.gettempdir(), f"ra_clocks_{os.getpid()}_{gpu_index}.csv")
 
     def start(self):
         try:
@@ -192,6 +200,11 @@ class ClockSampler:
                 for nm, val in zip(names, parts[5:9]):
                     if val.lower().startswith("active"):
                         reasons.add(nm)
+        if not self.keep:
+            try:
+                os.remove(self.path)
+            except OSError:
+                pass
         if not sms:
             return None
         return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes),
@@ -353,7 +366,7 @@ def run_decode(args, ws, rank, local):
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
     if vis and "," not in vis and vis.strip().isdigit():
         gpu_index = int(vis)
-    clocks = ClockSampler(gpu_index)
+    clocks = ClockSampler(gpu_index, args.clock_log)
     clocks.start()
     ra.ra_trace_reset()
     ra.ra_trace_enable(True)
@@ -460,7 +473,7 @@ def run_backward(args, w, ws, rank, local):
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
     if vis and "," not in vis and vis.strip().isdigit():
         gpu_index = int(vis)
-    clocks = ClockSampler(gpu_index)
+    clocks = ClockSampler(gpu_index, args.clock_log)
     clocks.start()
     ra.ra_trace_reset()
     ra.ra_trace_enable(True)
@@ -604,7 +617,7 @@ def run_ours(args, w, ws, rank, local):
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
     if vis and "," not in vis and vis.strip().isdigit():
         gpu_index = int(vis)
-    clocks = ClockSampler(gpu_index)
+    clocks = ClockSampler(gpu_index, args.clock_log)
     clocks.start()
     ra.ra_trace_reset()
     ra.ra_trace_enable(True)
@@ -755,6 +768,8 @@ def main():
     ap.add_argument("--ref-step-seconds", type=float, default=6.0)
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clock-log", default=None,
+                    help="directory for the raw nvidia-smi clock samples of the timed region")
     ap.add_argument("--no-check", action="store_true",
                     help="skip the sampled-row parity check of the timed run's output")
     ap.add_argument("--layout", default="contiguous", choices=["contiguous", "zigzag", "striped"])
