@@ -694,6 +694,24 @@ def run_ours(args, w, ws, rank, local):
             print(json.dumps(line), flush=True)
         return
 
+    if w.dtype == "bf16":
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": (achieved / peak) if achieved else None, "traffic": traffic,
+                "kernel": "block update (tcgen05)",
+                "peak_kind": f"bf16_tflops_sustained ({peak_src})",
+                "frac_of_burst": (achieved / peaks["bf16_tflops"]) if achieved else None}
+    else:
+        # fp32 FFMA path: the FP32 pipe peak from unit counts and clock,
+        # SMs x 128 FMA lanes x 2 FLOPs x max SM clock.
+        import torch as _t
+
+        sms = _t.cuda.get_device_properties(dev).multi_processor_count
+        alu_peak = sms * 128 * 2 * 2.07e9 / 1e12
+        roof = {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
+                "frac": (achieved / alu_peak) if achieved else None, "traffic": None,
+                "kernel": "block update (fp32 FFMA)",
+                "peak_kind": f"{sms} SMs x 128 FP32 lanes x 2 FLOPs x 2070 MHz"}
+
     # end to end through the host-buffer entry point
     qp, kp, vp = q.pin_memory(), k.pin_memory(), v.pin_memory()
     out_h = torch.empty((w.N, w.heads, w.d), dtype=torch.float32, pin_memory=True)
@@ -742,11 +760,7 @@ def run_ours(args, w, ws, rank, local):
         "gpu_launches": n_upd + n_init + n_fin,
         "kernel_ms": {"block_update": ms_upd / args.steps, "state_init": ms_init / args.steps,
                       "finalize": ms_fin / args.steps},
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": (achieved / peak) if achieved else None, "traffic": traffic,
-                     "kernel": "block update (tcgen05)", "peak_kind":
-                     f"bf16_tflops_sustained ({peak_src})",
-                     "frac_of_burst": (achieved / peaks["bf16_tflops"]) if achieved else None},
+        "roofline": roof,
         "cpu_baseline": cpu,
         "ms_per_step_median": statistics.median(per_step),
         "ms_per_step_best": min(per_step),
