@@ -5,23 +5,20 @@
 // blocks, the query goes to every K/V shard, each shard computes a local
 // attention state, and a global online-softmax reduction combines them.
 //
-// The work is HBM-bound: each K/V byte is read once and meets only
-// g * n_q query rows (g = heads / kv_heads), a few FLOPs per byte.  So this
-// path runs on the CUDA cores, not the tensor pipe, and is built to keep
-// HBM busy:
-//   * a CTA takes one KV head and one chunk of one shard's keys (split-K);
-//     the grid covers splits x KV heads x shards, a few waves of the SMs;
-//   * its four warps each stream their own 32-key K/V tiles through a
-//     private ring of shared-memory stages, filled by TMA with 128-byte
-//     swizzle, so no warp waits on another inside the loop;
-//   * lane t owns key t of a tile for Q K^T (the query rows, pre-scaled by
-//     log2(e)/sqrt(d), are broadcast from shared memory) and a slice of the
-//     d output columns for P V;
-//   * each warp keeps its own online-softmax state; the four are merged in
-//     shared memory, and the CTA writes one partial state (m, l, O~).
-// decode_combine_kernel then folds a shard's partial states into that
-// shard's running state, one warp per (query row, head).  Across shards the
-// host reduces with the merge kernel of ra_merge, in a tree.
+// The work is HBM-bound: each K/V byte is read once and meets only the
+// g * n_q query rows of its KV head (g = heads / kv_heads).  The layout is
+// built around that read:
+//   * decode_tc_kernel: a CTA takes one KV head and one chunk of one
+//     shard's keys (split-K; the grid covers chunks x KV heads x shards, a
+//     few waves of the SMs).  The KV head's query rows sit in one 128-row
+//     tile, so tcgen05 products give S = Q K^T and O += P V for a whole
+//     128-key tile at a time; the unused rows of the tile cost tensor time,
+//     which the pipe has to spare, not bytes.  It writes one partial state
+//     (m, l, O~) per chunk.
+//   * decode_combine_kernel folds a shard's chunk states into that shard's
+//     running state, one warp per (shard, query row, head).
+// Across shards the host reduces with the merge kernel of ra_merge, in a
+// tree.
 #include <cmath>
 #include <cstdint>
 
@@ -36,398 +33,16 @@ __device__ int g_decode_status = 0;
 
 namespace {
 
-constexpr int DW = 4;         // warps per CTA, each an independent stream
-constexpr int KT = 32;        // keys per warp tile: one per lane
-constexpr int CHUNK = KT * 128;  // one 64-column swizzled chunk of a 32-row tile
-
-template <int D>
-struct DecCfg {
-  static constexpr int NCH = D / 64;                 // 64-column chunks per row
-  static constexpr int TILE = NCH * CHUNK;           // bytes of one K (or V) tile
-  static constexpr int NST = D == 128 ? 3 : 4;       // stages per warp
-  static constexpr int STAGE = 2 * TILE;             // K tile, then V tile
-  static constexpr int WARP_BYTES = NST * STAGE;
-  static constexpr int COLS = D / 32;                // output columns per lane
-};
-
-template <int D, int RM>
-struct DecSmem {
-  static constexpr int OFF_STAGES = 0;
-  static constexpr int OFF_Q = OFF_STAGES + DW * DecCfg<D>::WARP_BYTES;  // fp32 [RM][D]
-  static constexpr int OFF_P = OFF_Q + RM * D * 4;                       // fp32 [DW][RM][KT]
-  static constexpr int OFF_LIM = OFF_P + DW * RM * KT * 4;               // int [RM][2]
-  static constexpr int OFF_BAR = OFF_LIM + RM * 8;                       // [DW][NST] mbarriers
-  static constexpr int OFF_FLAG = OFF_BAR + DW * DecCfg<D>::NST * 8;
-  static constexpr int BYTES = OFF_FLAG + 16 + 1024;                     // + alignment slack
-  static_assert(BYTES <= 232448, "shared memory budget");
-  // The warps' merge area reuses their stage buffers after the loop.
-  static_assert(RM * (D + 2) * 4 <= DecCfg<D>::WARP_BYTES, "merge area fits a warp's stages");
-};
-
-__device__ __forceinline__ uint4 lds128(uint32_t a) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(a));
-  return v;
-}
-__device__ __forceinline__ uint2 lds64(uint32_t a) {
-  uint2 v;
-  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
-  return v;
-}
-__device__ __forceinline__ uint32_t lds32(uint32_t a) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
-  return v;
-}
-// bf16 pair -> two fp32 (exact: a bf16 is the high half of an fp32).
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
-template <int D, int RM>
-__global__ void __launch_bounds__(DW * 32, 1)
-decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                    const DecArgs a) {
-  using C = DecCfg<D>;
-  using S = DecSmem<D, RM>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const uint32_t sb = smem_u32(smem);
-  float* q_s = reinterpret_cast<float*>(smem + S::OFF_Q);
-  int* lim = reinterpret_cast<int*>(smem + S::OFF_LIM);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::OFF_FLAG);
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int split = blockIdx.x, kh = blockIdx.y, shard = blockIdx.z;
-  const int g = a.heads / a.kv_heads;
-  const int R = g * static_cast<int>(a.n_q);  // rows r = qi * g + hl, head kh * g + hl
-
-  // Keys of this CTA: [c0, c1) of shard `shard`.
-  const long long sh0 = static_cast<long long>(shard) * a.shard_len;
-  const long long sh1 = sh0 + a.shard_len < a.n_kv ? sh0 + a.shard_len : a.n_kv;
-  const long long c0 = sh0 + static_cast<long long>(split) * a.chunk;
-  const long long c1 = c0 + a.chunk < sh1 ? c0 + a.chunk : sh1;
-
-  // Allowed keys of each row, clipped to [c0, c1).
-  const long long vb = valid_bound(a.mask);
-  if (tid < RM) {
-    long long lo = 0, hi = 0;
-    if (tid < R) {
-      const long long qp = a.q_off + tid / g;
-      long long plo, phi;
-      if (qp < vb && allowed_positions(a.mask, qp, &plo, &phi)) {
-        const PosMap km{kContiguous, 1, a.n_kv, 0, a.kv_off};
-        lo = count_below(km, plo);
-        hi = count_below(km, phi);
-      }
-    }
-    lo = lo > c0 ? lo : c0;
-    hi = hi < c1 ? hi : c1;
-    if (hi < lo) hi = lo;
-    lim[2 * tid] = static_cast<int>(lo);
-    lim[2 * tid + 1] = static_cast<int>(hi);
-  }
-  // Query rows -> fp32, scaled into log2 units.
-  const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
-  for (int i = tid; i < RM * D; i += DW * 32) {
-    const int r = i / D, x = i % D;
-    float val = 0.f;
-    if (r < R) {
-      const long long qi = r / g;
-      const int h = kh * g + r % g;
-      val = __bfloat162float(q[(qi * a.heads + h) * D + x]) * a.scale_log2;
-    }
-    q_s[i] = val;
-  }
-  if (tid == 0) {
-    for (int i = 0; i < DW * C::NST; ++i) mbar_init(sb + S::OFF_BAR + 8 * i, 1);
-    *abort_flag = *reinterpret_cast<volatile int*>(&g_decode_status) != 0 ? 1 : 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
-
-  // Key range some row may see; tiles of 32 keys aligned on the global key
-  // index, dealt round-robin to the warps.
-  int klo = static_cast<int>(c1), khi = static_cast<int>(c0);
-  for (int r = 0; r < R && r < RM; ++r) {
-    if (lim[2 * r + 1] > lim[2 * r]) {
-      klo = lim[2 * r] < klo ? lim[2 * r] : klo;
-      khi = lim[2 * r + 1] > khi ? lim[2 * r + 1] : khi;
-    }
-  }
-  const int t_begin = klo / KT;
-  const int t_end = khi > klo ? (khi + KT - 1) / KT : t_begin;
-  const int n_tiles = t_end - t_begin;
-  const int nw = n_tiles > warp ? (n_tiles - warp + DW - 1) / DW : 0;  // this warp's tiles
-
-  const uint32_t wbase = sb + S::OFF_STAGES + warp * C::WARP_BYTES;
-  const uint32_t wbar = sb + S::OFF_BAR + 8 * warp * C::NST;
-  const long long lim_cycles = a.wait_limit;
-  auto issue = [&](int it) {  // lane 0: tile `it` of this warp into its stage
-    const int st = it % C::NST;
-    const int key0 = (t_begin + warp + it * DW) * KT;
-    const uint32_t dst = wbase + st * C::STAGE;
-    mbar_arrive_expect_tx(wbar + 8 * st, C::STAGE);
-#pragma unroll
-    for (int ch = 0; ch < C::NCH; ++ch) {
-      tma_load_3d(dst + ch * CHUNK, &tmK, wbar + 8 * st, ch * 64, kh, key0);
-      tma_load_3d(dst + C::TILE + ch * CHUNK, &tmV, wbar + 8 * st, ch * 64, kh, key0);
-    }
-  };
-  int issued = 0;  // lane 0: tiles whose copies were started
-  if (lane == 0 && !*abort_flag) {
-    tma_prefetch_desc(&tmK);
-    tma_prefetch_desc(&tmV);
-    for (; issued < nw && issued < C::NST; ++issued) issue(issued);
-  }
-  __syncwarp();
-
-  // Warp state per row: m (log2 units), this lane's share of l, and this
-  // lane's output columns as fp32 pairs (one FFMA2 updates two).
-  constexpr int CP = C::COLS / 2;
-  float m_r[RM], l_r[RM];
-  uint64_t o2[RM][CP];
-#pragma unroll
-  for (int r = 0; r < RM; ++r) {
-    m_r[r] = -INFINITY;
-    l_r[r] = 0.f;
-#pragma unroll
-    for (int c = 0; c < CP; ++c) o2[r][c] = f2pack(0.f, 0.f);
-  }
-  const uint32_t p_w = sb + S::OFF_P + warp * RM * KT * 4;
-  const uint32_t q_sa = sb + S::OFF_Q;
-  bool ok = !*abort_flag;
-  int done = 0;  // tiles consumed
-  for (int it = 0; it < nw && ok; ++it) {
-    const int st = it % C::NST;
-    ok = wait_bar(wbar + 8 * st, static_cast<uint32_t>(it / C::NST) & 1u, abort_flag,
-                  &g_decode_status, 0x41, lim_cycles);
-    ok = __all_sync(0xffffffffu, ok);
-    if (!ok) break;
-    const uint32_t sK = wbase + st * C::STAGE;
-    const uint32_t sV = sK + C::TILE;
-    const int key = (t_begin + warp + it * DW) * KT + lane;
-
-    // S = q . k for this lane's key, every row (log2 units): even and odd
-    // columns summed in the two halves of an FFMA2 accumulator.
-    uint64_t s2[RM];
-#pragma unroll
-    for (int r = 0; r < RM; ++r) s2[r] = f2pack(0.f, 0.f);
-#pragma unroll
-    for (int ch = 0; ch < C::NCH; ++ch) {
-#pragma unroll
-      for (int p = 0; p < 8; ++p) {
-        const uint4 kw = lds128(sK + ch * CHUNK + lane * 128 + ((p ^ (lane & 7)) << 4));
-        const uint64_t k01 = f2pack(bf_lo(kw.x), bf_hi(kw.x));
-        const uint64_t k23 = f2pack(bf_lo(kw.y), bf_hi(kw.y));
-        const uint64_t k45 = f2pack(bf_lo(kw.z), bf_hi(kw.z));
-        const uint64_t k67 = f2pack(bf_lo(kw.w), bf_hi(kw.w));
-#pragma unroll
-        for (int r = 0; r < RM; ++r) {
-          const uint32_t qa = q_sa + (r * D + ch * 64 + p * 8) * 4;
-          const uint4 x = lds128(qa), y = lds128(qa + 16);
-          uint64_t acc = s2[r];
-          acc = ffma2(f2pack(__uint_as_float(x.x), __uint_as_float(x.y)), k01, acc);
-          acc = ffma2(f2pack(__uint_as_float(x.z), __uint_as_float(x.w)), k23, acc);
-          acc = ffma2(f2pack(__uint_as_float(y.x), __uint_as_float(y.y)), k45, acc);
-          acc = ffma2(f2pack(__uint_as_float(y.z), __uint_as_float(y.w)), k67, acc);
-          s2[r] = acc;
-        }
-      }
-    }
-    float s[RM];
-#pragma unroll
-    for (int r = 0; r < RM; ++r) {
-      float a0, a1;
-      f2unpack(s2[r], a0, a1);
-      s[r] = a0 + a1;
-    }
-    // Mask, then the online-softmax update of each row's warp state.
-#pragma unroll
-    for (int r = 0; r < RM; ++r) {
-      const bool allowed = key >= lim[2 * r] && key < lim[2 * r + 1];
-      const float sv = allowed ? s[r] : -INFINITY;
-      float mt = sv;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
-      const float m_new = fmaxf(m_r[r], mt);
-      const float mref = m_new == -INFINITY ? 0.f : m_new;
-      const float alpha = ex2(m_r[r] - mref);  // m_r = -inf gives 0 (the sums are 0 then)
-      const float pv = ex2(sv - mref);         // masked keys give 0
-      m_r[r] = m_new;
-      l_r[r] = l_r[r] * alpha + pv;
-      const uint64_t al2 = f2pack(alpha, alpha);
-#pragma unroll
-      for (int c = 0; c < CP; ++c) o2[r][c] = fmul2(o2[r][c], al2);
-      asm volatile("st.shared.f32 [%0], %1;" ::"r"(p_w + (r * KT + lane) * 4), "f"(pv) : "memory");
-    }
-    __syncwarp();
-    // O += P V: lane owns columns [COLS*lane, COLS*lane + COLS).
-    const int x0 = C::COLS * lane;
-    const int ch = x0 / 64, piece = (x0 % 64) / 8;
-    const uint32_t vcol = sV + ch * CHUNK + (x0 % 8) * 2;
-#pragma unroll 4
-    for (int t4 = 0; t4 < KT; t4 += 4) {
-      float pr[RM][4];
-#pragma unroll
-      for (int r = 0; r < RM; ++r) {
-        const uint4 w4 = lds128(p_w + (r * KT + t4) * 4);
-        pr[r][0] = __uint_as_float(w4.x);
-        pr[r][1] = __uint_as_float(w4.y);
-        pr[r][2] = __uint_as_float(w4.z);
-        pr[r][3] = __uint_as_float(w4.w);
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int t = t4 + u;
-        const uint32_t va = vcol + t * 128 + ((piece ^ (t & 7)) << 4);
-        uint64_t v2[CP];
-        if constexpr (CP == 2) {
-          const uint2 w2 = lds64(va);
-          v2[0] = f2pack(bf_lo(w2.x), bf_hi(w2.x));
-          v2[1] = f2pack(bf_lo(w2.y), bf_hi(w2.y));
-        } else {
-          const uint32_t w1 = lds32(va);
-          v2[0] = f2pack(bf_lo(w1), bf_hi(w1));
-        }
-#pragma unroll
-        for (int r = 0; r < RM; ++r) {
-          const uint64_t pp = f2pack(pr[r][u], pr[r][u]);
-#pragma unroll
-          for (int c = 0; c < CP; ++c) o2[r][c] = ffma2(pp, v2[c], o2[r][c]);
-        }
-      }
-    }
-    __syncwarp();
-    done = it + 1;
-    // Stage st is free again: refill it with tile it + NST.
-    if (lane == 0 && it + C::NST < nw) {
-      fence_proxy_async_smem();
-      issue(it + C::NST);
-      issued = it + C::NST + 1;
-    }
-    __syncwarp();
-  }
-  if (!ok && lane == 0) {
-    // Drain (bounded) the copies still in flight before the CTA exits.
-    volatile int no_abort = 0;
-    for (int it = done; it < issued; ++it)
-      wait_bar(wbar + 8 * (it % C::NST), static_cast<uint32_t>(it / C::NST) & 1u, &no_abort,
-               nullptr, 0, lim_cycles);
-  }
-  __syncwarp();
-
-  // Warp state -> shared memory (over this warp's own stages, all consumed).
-  float* mw = reinterpret_cast<float*>(smem + S::OFF_STAGES + warp * C::WARP_BYTES);
-#pragma unroll
-  for (int r = 0; r < RM; ++r) {
-    float ls = l_r[r];
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, off);
-    if (lane == 0) {
-      mw[r * (D + 2)] = m_r[r];
-      mw[r * (D + 2) + 1] = ls;
-    }
-#pragma unroll
-    for (int c = 0; c < CP; ++c) {
-      float y0, y1;
-      f2unpack(o2[r][c], y0, y1);
-      mw[r * (D + 2) + 2 + C::COLS * lane + 2 * c] = y0;
-      mw[r * (D + 2) + 2 + C::COLS * lane + 2 * c + 1] = y1;
-    }
-  }
-  __syncthreads();
-  if (*abort_flag) return;
-
-  // Merge the DW warp states; write this CTA's partial state in natural-log
-  // units: partial index ((shard * nsplit + split) * n_q + qi) * heads + h.
-  for (int i = tid; i < R * D; i += DW * 32) {
-    const int r = i / D, x = i % D;
-    float mx = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < DW; ++w) {
-      const float* mr = reinterpret_cast<float*>(smem + S::OFF_STAGES + w * C::WARP_BYTES);
-      mx = fmaxf(mx, mr[r * (D + 2)]);
-    }
-    const float mref = mx == -INFINITY ? 0.f : mx;
-    float ov = 0.f, lv = 0.f;
-#pragma unroll
-    for (int w = 0; w < DW; ++w) {
-      const float* mr = reinterpret_cast<float*>(smem + S::OFF_STAGES + w * C::WARP_BYTES);
-      const float e = ex2(mr[r * (D + 2)] - mref);
-      ov = fmaf(e, mr[r * (D + 2) + 2 + x], ov);
-      lv = fmaf(e, mr[r * (D + 2) + 1], lv);
-    }
-    const long long qi = r / g;
-    const int h = kh * g + r % g;
-    const long long pidx =
-        ((static_cast<long long>(shard) * a.nsplit + split) * a.n_q + qi) * a.heads + h;
-    a.po[pidx * D + x] = ov;
-    if (x == 0) {
-      a.pm[pidx] = mx == -INFINITY ? -INFINITY : mx * kLn2;
-      a.pl[pidx] = lv;
-    }
-  }
-}
-
-// Folds the nsplit partial states of each shard into that shard's running
-// state (in place), one warp per (shard, query row, head).  The running
-// state takes part as one more term, so a call adds to what was there.
-template <int D>
-__global__ void decode_combine_kernel(float* __restrict__ m, float* __restrict__ l,
-                                      float* __restrict__ o, const float* __restrict__ pm,
-                                      const float* __restrict__ pl, const float* __restrict__ po,
-                                      long long rows_per_shard, int nsplit, long long n_rh) {
-  const int lane = threadIdx.x & 31;
-  const long long rh = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  if (rh >= n_rh) return;  // warp-uniform
-  const long long shard = rh / rows_per_shard, row = rh % rows_per_shard;
-  auto pidx = [&](int s) -> long long {
-    return (shard * nsplit + s) * rows_per_shard + row;
-  };
-  // Max over the running state and every split, lanes striding the splits.
-  const float m0 = m[rh];
-  float mx = m0;
-  for (int s = lane; s < nsplit; s += 32) mx = fmaxf(mx, pm[pidx(s)]);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-  if (mx == -INFINITY) return;  // nothing allowed anywhere: the state stays as it is
-  float lsum = 0.f;
-  for (int s = lane; s < nsplit; s += 32) lsum += expf(pm[pidx(s)] - mx) * pl[pidx(s)];
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
-  const float e0 = expf(m0 - mx);  // m0 = -inf gives 0
-  constexpr int CPL = D / 32;      // columns per lane
-  float acc[CPL];
-#pragma unroll
-  for (int c = 0; c < CPL; ++c) acc[c] = e0 * o[rh * D + CPL * lane + c];
-  for (int s = 0; s < nsplit; ++s) {
-    const float ms = pm[pidx(s)];
-    if (ms == -INFINITY) continue;  // warp-uniform
-    const float e = expf(ms - mx);
-    const float* src = po + pidx(s) * D + CPL * lane;
-#pragma unroll
-    for (int c = 0; c < CPL; ++c) acc[c] = fmaf(e, src[c], acc[c]);
-  }
-#pragma unroll
-  for (int c = 0; c < CPL; ++c) o[rh * D + CPL * lane + c] = acc[c];
-  if (lane == 0) {
-    l[rh] = e0 * l[rh] + lsum;
-    m[rh] = mx;
-  }
-}
-
-// ------------------------------------------------------------------ tensor-core form
-// For more query rows per KV head (g * n_q up to 128) the same split-K
-// partial states come from tcgen05 products: the KV head's g * n_q rows are
-// gathered into one 128-row query tile (a 3-D TMA box of g heads x n_q
-// tokens; the rest of the tile is zero), and the CTA walks its key chunk in
-// 128-key tiles with S = Q K^T and O += P V in TMEM and the online softmax
-// of the forward kernel on one thread per row.  Roles (256 threads): warps
-// 0-3 softmax, warp 4 TMA, warp 5 MMA issuer and TMEM owner.  Every wait is
-// bounded.
+// ------------------------------------------------------------------ chunk kernel
+// The KV head's g * n_q query rows (up to 128) are gathered into one 128-row
+// query tile (a 3-D TMA box of g heads x n_q tokens; the rest of the tile
+// is zero), and the CTA walks its key chunk in 128-key tiles with
+// S = Q K^T and O += P V in TMEM and the online softmax of the forward
+// kernel on one thread per row.  S is double-buffered in
+// TMEM: the product S(k+2) runs while the softmax works on S(k), and the
+// softmax waits for P V(k-1) before it touches O.  Roles (256 threads):
+// warps 0-3 softmax, warp 4 TMA, warp 5 MMA issuer and TMEM owner.  Every
+// wait is bounded.
 namespace tc {
 
 constexpr int BT = 128;
@@ -437,17 +52,19 @@ template <int D>
 struct TCfg {
   static constexpr int NCH = D / 64;
   static constexpr uint32_t TILE = BT * D * 2;
-  static constexpr int NST = 2;                      // K/V stages (K and V of one tile each)
+  // K/V stages (K and V of one tile each): QK runs two tiles ahead of P V.
+  static constexpr int NST = D == 128 ? 3 : 4;
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_ST = OFF_Q + TILE;   // stage s: K at OFF_ST + 2*s*TILE, V after
   static constexpr uint32_t OFF_BAR = OFF_ST + NST * 2 * TILE;
-  static constexpr int B_Q = 0, B_F = 1, B_E = B_F + NST, B_S = B_E + NST, B_P = B_S + 1,
-                       B_O = B_P + 1, B_DRAIN = B_O + 1, NBAR = B_DRAIN + 1;
+  static constexpr int B_Q = 0, B_F = 1, B_E = B_F + NST, B_S = B_E + NST,  // B_S: 2 buffers
+                       B_P = B_S + 2, B_PV = B_P + 1, B_O = B_PV + 1, B_DRAIN = B_O + 1,
+                       NBAR = B_DRAIN + 1;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t SMEM = OFF_MISC + 16 + 1024;
   static_assert(SMEM <= 232448, "shared memory budget");
-  static constexpr uint32_t C_S = 0, C_O = BT;  // TMEM: S (then P), O
-  static constexpr uint32_t TMEM_COLS = 256;
+  static constexpr uint32_t C_S = 0, C_O = 2 * BT;  // TMEM: S buffers 0, 1 (then P), O
+  static constexpr uint32_t TMEM_COLS = 512;
   static_assert(C_O + D <= TMEM_COLS, "TMEM budget");
 };
 
@@ -568,20 +185,34 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     constexpr uint32_t idesc_qk = idesc_bf16(BT, BT, 0);
     constexpr uint32_t idesc_pv = idesc_bf16(BT, D, 1);
     const uint64_t qdesc = sdesc_sw128(sb + C::OFF_Q, 16, 1024);
-    auto qk = [&](int st) {
+    // S(k) = Q K(k)^T into S buffer k % 2.
+    auto qk = [&](int k) {
+      const int st = k % C::NST;
+      const uint32_t sbuf = tmem + C::C_S + static_cast<uint32_t>(k & 1) * BT;
       const uint64_t kd = sdesc_sw128(sb + C::OFF_ST + st * 2 * C::TILE, 16, 1024);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint64_t off = ((kk >> 2) * CHB + (kk & 3) * 32) >> 4;
-        mma_ss_lead(lead, tmem + C::C_S, qdesc + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
+        mma_ss_lead(lead, sbuf, qdesc + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
       }
-      tc_commit_lead(lead, bar(C::B_S));
+      tc_commit_lead(lead, bar(C::B_S + (k & 1)));
+    };
+    auto wait_full = [&](int k) -> bool {
+      return wait_bar(bar(C::B_F + k % C::NST), static_cast<uint32_t>(k / C::NST) & 1u,
+                      abort_flag, &g_decode_status, 0x73, lim);
     };
     bool ok = wait_bar(bar(C::B_Q), 0, abort_flag, &g_decode_status, 0x72, lim);
-    if (ok) ok = wait_bar(bar(C::B_F), 0, abort_flag, &g_decode_status, 0x73, lim);
+    if (ok) ok = wait_full(0);
     if (ok) {
       tc_fence_after();
       qk(0);
+      if (n > 1) {
+        ok = wait_full(1);
+        if (ok) {
+          tc_fence_after();
+          qk(1);
+        }
+      }
     }
     for (int k = 0; k < n && ok; ++k) {
       const int st = k % C::NST;
@@ -590,19 +221,19 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       if (!ok) break;
       tc_fence_after();
       const uint64_t vd = sdesc_sw128(sb + C::OFF_ST + st * 2 * C::TILE + C::TILE, CHB, 1024);
+      const uint32_t pbuf = tmem + C::C_S + static_cast<uint32_t>(k & 1) * BT;
 #pragma unroll
       for (int kk = 0; kk < BT / 16; ++kk)
-        mma_ts_lead(lead, tmem + C::C_O, tmem + C::C_S + kk * 8,
+        mma_ts_lead(lead, tmem + C::C_O, pbuf + kk * 8,
                     vd + static_cast<uint64_t>((kk * 2048) >> 4), idesc_pv, 1u);
       tc_commit_lead(lead, bar(C::B_E + st));
-      if (k + 1 == n) {
-        tc_commit_lead(lead, bar(C::B_O));
-      } else {
-        ok = wait_bar(bar(C::B_F + (k + 1) % C::NST), static_cast<uint32_t>((k + 1) / C::NST) & 1u,
-                      abort_flag, &g_decode_status, 0x73, lim);
+      tc_commit_lead(lead, bar(C::B_PV));
+      if (k + 1 == n) tc_commit_lead(lead, bar(C::B_O));
+      if (k + 2 < n) {
+        ok = wait_full(k + 2);
         if (!ok) break;
         tc_fence_after();
-        qk((k + 1) % C::NST);  // in issue order after P V, which reads P from S's columns
+        qk(k + 2);  // into buffer k % 2, in issue order after P V(k), which reads P(k) there
       }
     }
     volatile int no_abort = 0;
@@ -632,14 +263,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     float m_used = -INFINITY, m_true = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int k = 0; k < n; ++k) {
-      ok = wait_bar(bar(C::B_S), static_cast<uint32_t>(k) & 1u, abort_flag, &g_decode_status,
-                    0x75, lim);
+      const uint32_t s_col = C::C_S + static_cast<uint32_t>(k & 1) * BT;
+      ok = wait_bar(bar(C::B_S + (k & 1)), static_cast<uint32_t>(k >> 1) & 1u, abort_flag,
+                    &g_decode_status, 0x75, lim);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
       uint32_t sr[4][32];
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) tmem_ld32(tl + C::C_S + cc * 32, sr[cc]);
+      for (int cc = 0; cc < 4; ++cc) tmem_ld32(tl + s_col + cc * 32, sr[cc]);
       tmem_wait_ld();
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) reg_fence32(sr[cc]);
@@ -666,8 +298,17 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         alpha = ex2(m_used - m_true);  // m_used = -inf gives 0
         m_used = m_true;
       }
+      // O is stable once P V(k-1) is done.  Wait for it on every tile (not
+      // only when rescaling), so each phase of the barrier is waited in
+      // order and a parity can never match a stale phase.
+      if (k > 0) {
+        ok = wait_bar(bar(C::B_PV), static_cast<uint32_t>(k - 1) & 1u, abort_flag,
+                      &g_decode_status, 0x77, lim);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+      }
       if (__any_sync(0xffffffffu, alpha != 1.f)) {
-        // O is stable: S(k) comes after P V(k-1) in issue order.
         const uint64_t al2 = f2pack(alpha, alpha);
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
@@ -700,8 +341,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         sr[(j / 2 + 1) >> 5][(j / 2 + 1) & 31] = bf16x2_rn(p2, p3);
       }
 #undef RA_S
-      tmem_st32(tl + C::C_S, sr[0]);
-      tmem_st32(tl + C::C_S + 32, sr[1]);
+      tmem_st32(tl + s_col, sr[0]);
+      tmem_st32(tl + s_col + 32, sr[1]);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(C::B_P));
@@ -746,25 +387,51 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 
 }  // namespace tc
 
-template <int D, int RM>
-cudaError_t launch_split(const DecArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
-                         cudaStream_t st) {
-  using S = DecSmem<D, RM>;
-  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, RM>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, S::BYTES);
-  if (e != cudaSuccess) return e;
-  dim3 grid(static_cast<unsigned>(a.nsplit), static_cast<unsigned>(a.kv_heads),
-            static_cast<unsigned>(a.nshard));
-  decode_split_kernel<D, RM><<<grid, DW * 32, S::BYTES, st>>>(tk, tv, a);
-  return cudaGetLastError();
-}
-
+// Folds the nsplit partial states of each shard into that shard's running
+// state (in place), one warp per (shard, query row, head).  The running
+// state takes part as one more term, so a call adds to what was there.
 template <int D>
-cudaError_t launch_split_d(const DecArgs& a, int rows, const CUtensorMap& tk,
-                           const CUtensorMap& tv, cudaStream_t st) {
-  if (rows <= 4) return launch_split<D, 4>(a, tk, tv, st);
-  if (rows <= 8) return launch_split<D, 8>(a, tk, tv, st);
-  return launch_split<D, 16>(a, tk, tv, st);
+__global__ void decode_combine_kernel(float* __restrict__ m, float* __restrict__ l,
+                                      float* __restrict__ o, const float* __restrict__ pm,
+                                      const float* __restrict__ pl, const float* __restrict__ po,
+                                      long long rows_per_shard, int nsplit, long long n_rh) {
+  const int lane = threadIdx.x & 31;
+  const long long rh = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (rh >= n_rh) return;  // warp-uniform
+  const long long shard = rh / rows_per_shard, row = rh % rows_per_shard;
+  auto pidx = [&](int s) -> long long {
+    return (shard * nsplit + s) * rows_per_shard + row;
+  };
+  // Max over the running state and every split, lanes striding the splits.
+  const float m0 = m[rh];
+  float mx = m0;
+  for (int s = lane; s < nsplit; s += 32) mx = fmaxf(mx, pm[pidx(s)]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  if (mx == -INFINITY) return;  // nothing allowed anywhere: the state stays as it is
+  float lsum = 0.f;
+  for (int s = lane; s < nsplit; s += 32) lsum += expf(pm[pidx(s)] - mx) * pl[pidx(s)];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+  const float e0 = expf(m0 - mx);  // m0 = -inf gives 0
+  constexpr int CPL = D / 32;      // columns per lane
+  float acc[CPL];
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) acc[c] = e0 * o[rh * D + CPL * lane + c];
+  for (int s = 0; s < nsplit; ++s) {
+    const float ms = pm[pidx(s)];
+    if (ms == -INFINITY) continue;  // warp-uniform
+    const float e = expf(ms - mx);
+    const float* src = po + pidx(s) * D + CPL * lane;
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) acc[c] = fmaf(e, src[c], acc[c]);
+  }
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) o[rh * D + CPL * lane + c] = acc[c];
+  if (lane == 0) {
+    l[rh] = e0 * l[rh] + lsum;
+    m[rh] = mx;
+  }
 }
 
 template <int D>
@@ -786,12 +453,6 @@ cudaError_t launch_tc_d(const DecArgs& a, const CUtensorMap& tq, const CUtensorM
 cudaError_t launch_decode_tc(const DecArgs& a, int d, const CUtensorMap& tq, const CUtensorMap& tk,
                              const CUtensorMap& tv, cudaStream_t st) {
   return d == 128 ? launch_tc_d<128>(a, tq, tk, tv, st) : launch_tc_d<64>(a, tq, tk, tv, st);
-}
-
-cudaError_t launch_decode_split(const DecArgs& a, int d, const CUtensorMap& tk,
-                                const CUtensorMap& tv, cudaStream_t st) {
-  const int rows = (a.heads / a.kv_heads) * static_cast<int>(a.n_q);
-  return d == 128 ? launch_split_d<128>(a, rows, tk, tv, st) : launch_split_d<64>(a, rows, tk, tv, st);
 }
 
 cudaError_t launch_decode_combine(float* m, float* l, float* o, const float* pm, const float* pl,

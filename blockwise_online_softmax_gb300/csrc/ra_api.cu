@@ -501,10 +501,8 @@ int ring_backward_impl(const void* q, const void* k, const void* v, const float*
 }
 
 // ----------------------------------------------------------------- decode
-// Query rows per KV head (g * n_q) the decode path takes; up to
-// kDecodeFmaRows it runs on the CUDA cores, above on the tensor cores.
+// Query rows per KV head (g * n_q) the decode path takes: one 128-row tile.
 constexpr int kDecodeMaxRows = 128;
-constexpr int kDecodeFmaRows = 4;
 
 int decode_args_check(const void* q, const void* k, const void* v, long long n_q, long long n_kv,
                       int d, int heads, int kv_heads, long long window, int dtype) {
@@ -533,12 +531,9 @@ int decode_run(const void* q, const void* k, const void* v, float* m, float* l, 
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const bool use_tc = static_cast<long long>(heads / kv_heads) * n_q > kDecodeFmaRows;
-  // CUDA-core kernel: about four CTAs per SM over the whole launch, each at
-  // least 4 tiles (one per warp) of 32 keys.  Tensor-core kernel: one CTA
-  // per SM at a time, about three waves, chunks of whole 128-key tiles.
-  const long long waves = use_tc ? 3 : 4;
-  const long long gran = use_tc ? 128 : 32;
+  // One CTA per SM at a time; about three waves; chunks of whole 128-key
+  // tiles, at least one.
+  const long long waves = 3, gran = 128;
   long long want = (waves * sms + static_cast<long long>(kv_heads) * nshard - 1) /
                    (static_cast<long long>(kv_heads) * nshard);
   if (want < 1) want = 1;
@@ -558,9 +553,9 @@ int decode_run(const void* q, const void* k, const void* v, float* m, float* l, 
   }
   int rc = get_encoder();
   CUtensorMap tk, tv, tq;
-  if (rc == RA_OK) rc = encode_map(&tk, k, n_kv, kv_heads, d, use_tc ? 128 : 32);
-  if (rc == RA_OK) rc = encode_map(&tv, v, n_kv, kv_heads, d, use_tc ? 128 : 32);
-  if (rc == RA_OK && use_tc) rc = encode_q_group_map(&tq, q, n_q, heads, heads / kv_heads, d);
+  if (rc == RA_OK) rc = encode_map(&tk, k, n_kv, kv_heads, d);
+  if (rc == RA_OK) rc = encode_map(&tv, v, n_kv, kv_heads, d);
+  if (rc == RA_OK) rc = encode_q_group_map(&tq, q, n_q, heads, heads / kv_heads, d);
   if (rc == RA_OK) {
     ra::DecArgs a{};
     a.q = q;
@@ -583,7 +578,7 @@ int decode_run(const void* q, const void* k, const void* v, float* m, float* l, 
     a.mask.window = window > kAllValid ? kAllValid : window;
     a.mask.n_valid = kAllValid;
     TraceScope t0(RA_KERNEL_DECODE_SPLIT, st);
-    e = use_tc ? ra::launch_decode_tc(a, d, tq, tk, tv, st) : ra::launch_decode_split(a, d, tk, tv, st);
+    e = ra::launch_decode_tc(a, d, tq, tk, tv, st);
     t0.done(e == cudaSuccess);
     if (e != cudaSuccess) {
       rc = cuda_fail(e, "decode split launch");

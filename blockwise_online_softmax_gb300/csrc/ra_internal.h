@@ -201,9 +201,9 @@ __device__ __forceinline__ void tile_range(const FwdArgs& a, const Work& wk, lon
   *t1 = static_cast<int>((hi1 + bn - 1) / bn);
 }
 
-// One launch of the decode split-K kernel: n_q query tokens against n_kv
+// One launch of the decode chunk kernel: n_q query tokens against n_kv
 // keys cut into nshard shards of shard_len keys, each shard into nsplit
-// chunks of `chunk` keys (a multiple of 32).  CTA (split, kv head, shard)
+// chunks of `chunk` keys (a multiple of 128).  CTA (split, kv head, shard)
 // writes the partial state of its KV head's g * n_q rows to
 // pm/pl [nshard][nsplit][n_q][heads] and po [..][d].
 struct DecArgs {
@@ -251,8 +251,6 @@ cudaError_t launch_simt_update(const FwdArgs& a, int d, cudaStream_t st);
 cudaError_t launch_umma_update(const FwdArgs& a, int d, const CUtensorMap& tq,
                                const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st);
 cudaError_t launch_wait_selftest(long long limit_cycles, cudaStream_t st);
-cudaError_t launch_decode_split(const DecArgs& a, int d, const CUtensorMap& tk,
-                                const CUtensorMap& tv, cudaStream_t st);
 cudaError_t launch_decode_tc(const DecArgs& a, int d, const CUtensorMap& tq, const CUtensorMap& tk,
                              const CUtensorMap& tv, cudaStream_t st);
 cudaError_t launch_decode_combine(float* m, float* l, float* o, const float* pm, const float* pl,

@@ -110,7 +110,7 @@ typedef enum {
   RA_KERNEL_BLOCK_UPDATE_F32 = 2,  /* fp32 FFMA kernel */
   RA_KERNEL_MERGE = 3,
   RA_KERNEL_FINALIZE = 4,
-  RA_KERNEL_DECODE_SPLIT = 5,   /* decode split-K kernel (CUDA cores, TMA) */
+  RA_KERNEL_DECODE_SPLIT = 5,   /* decode split-K chunk kernel (tcgen05, TMA) */
   RA_KERNEL_DECODE_COMBINE = 6, /* folds a shard's split partial states */
   RA_KERNEL_BWD_PRE = 7,        /* backward: D = rowsum(dO * O) */
   RA_KERNEL_BWD_DQ = 8,         /* backward: dQ (tcgen05, Q-stationary) */
@@ -355,9 +355,8 @@ int ra_ring_backward_masked(const void* q, const void* k, const void* v, const f
  *   belong to ra_block_update_masked.  dtype must be RA_BF16.
  * The work is HBM-bound: the keys of each KV head are streamed in chunks
  * spread over the SMs (split-K), each chunk giving one partial state, and a
- * second kernel folds them into m, l, o.  Up to 4 query rows per KV head
- * the chunks run on the CUDA cores; above that, on the tensor cores (the
- * KV head's query rows gathered into one 128-row tile).  The partial states
+ * second kernel folds them into m, l, o.  A chunk runs on the tensor cores
+ * with the KV head's query rows gathered into one 128-row tile.  The partial states
  * (chunks x n_q x heads x (d + 2) fp32) are allocated with cudaMallocAsync
  * on `stream`.
  */
