@@ -158,3 +158,10 @@ def test_backward_gqa_128k_sampled():
     # 2^-9 relative) add up like a random walk over the N keys.
     dk_sum = dk.double().sum(0).cpu()
     assert dk_sum.abs().max().item() <= 2.0 ** -8 * np.sqrt(w.N) * dk.abs().max().item()
+
+
+@pytest.mark.slow
+def test_backward_mha_8k_window_and_documents():
+    w = inputs.WORKLOADS["mha-8k"]
+    run(w.N, w.P, w.heads, w.kv_heads, w.d, True, layout="zigzag", window=2000,
+        docs=[3000, 17, 4000, 1175], seed=w.seed + 1)

@@ -213,3 +213,31 @@ def test_zigzag_gqa_large_sampled_rows():
     ref_out, ref_lse = oracle.attention(ql, kl, vl, causal=True, q_pos=pos.numpy(),
                                         k_pos=pos.numpy(), rows=rows)
     check_output(got_out, got_lse, ref_out, ref_lse, "bf16")
+
+
+@pytest.mark.slow
+def test_masked_gqa_128k_sampled_rows():
+    """The gqa-128k shape with the zigzag layout, a 16384-token causal window
+    and 32 packed documents: sampled rows over their full allowed key range."""
+    w = inputs.WORKLOADS["gqa-128k"]
+    q, k, v = inputs.make_workload(w)
+    pos = binding.layout_positions(w.N, w.P, "zigzag")
+    rng = np.random.default_rng(77)
+    cuts = np.sort(rng.choice(np.arange(1, w.N), size=31, replace=False))
+    bounds = np.concatenate([[0], cuts, [w.N]])
+    cu = torch.tensor(bounds, dtype=torch.int32, device=DEV)
+    ql, kl, vl = q[pos], k[pos], v[pos]
+    del q, k, v
+    out, lse = ra.ra_ring_forward_masked(ql.to(DEV), kl.to(DEV), vl.to(DEV), P=w.P,
+                                         layout="zigzag", causal=True, window=16384,
+                                         cu_seqlens=cu)
+    ra.ra_device_status()
+    rows = inputs.sample_rows(w, random_per_block=4)
+    idx = torch.from_numpy(rows).to(DEV)
+    got_out, got_lse = out.index_select(0, idx).cpu(), lse.index_select(0, idx).cpu()
+    del out, lse
+    torch.cuda.empty_cache()
+    ids = (np.searchsorted(bounds, np.arange(w.N), side="right") - 1)[pos.numpy()]
+    ref_out, ref_lse = oracle.attention(ql, kl, vl, causal=True, window=16384, q_pos=pos.numpy(),
+                                        k_pos=pos.numpy(), q_doc=ids, k_doc=ids, rows=rows)
+    check_output(got_out, got_lse, ref_out, ref_lse, "bf16")
