@@ -17,15 +17,18 @@
 //   warp 9      Allocates TMEM.  Lane 0 issues every tcgen05.mma.
 //   warp 10     TMA producer for the V tiles.
 //   warp 11     idle.
-// K and V stream through separate rings of shared-memory stages (2 and 3
-// deep at d = 128).
+// K and V stream through two rings of shared-memory stages (2 deep at
+// d = 128, 4 at d = 64).  Slot c of the rings holds K(c) and V(c-1) of the
+// visit: the MMA thread needs exactly that pair in iteration c-1 (PV with
+// V(c-1), QK with K(c)), so one full barrier (both producers' bytes) and one
+// empty barrier (one commit) per slot cover both rings.
 // A softmax thread reads its S row from TMEM, takes the row max,
 // exponentiates, writes P back as bf16 over its S row, rescales its O~ row
 // in TMEM when the max grows, and loads and stores the state.
 //
 // Registers: the CTA launches with 168 per thread (three warps share each
 // SM sub-partition's 16K registers).  The producer/MMA warpgroup then gives
-// some back and the softmax warpgroups take them (setmaxnreg): 216/72 at
+// some back and the softmax warpgroups take them (setmaxnreg): 208/88 at
 // d = 128 and 224/56 at d = 64, with 2*128*softmax + 128*control = 384*168.
 //
 // TMEM columns: S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [256+D,256+2D).
@@ -78,20 +81,22 @@ template <int D>
 struct Cfg {
   static constexpr int NCH = D / 64;                  // 128-byte chunks per row
   static constexpr uint32_t TILE_BYTES = BM * D * 2;  // one Q, K or V tile
-  // K and V stage counts (192 KB of shared memory in all at d = 128).  A
-  // third V stage fits in 227 KB but measured slower: the L1 share of the
-  // unified SRAM drops too far for the state loads and stores.
+  // K and V stage counts, equal since a slot takes one stage of each ring
+  // (192 KB of shared memory in all at d = 128).  A third V stage fits in
+  // 227 KB but measured slower: the L1 share of the unified SRAM drops too
+  // far for the state loads and stores.
   static constexpr int NSK = (D == 64) ? 4 : 2;
-  static constexpr int NSV = (D == 64) ? 4 : 2;
+  static constexpr int NSV = NSK;
   static constexpr uint32_t S_COL = 0;                // S_g at S_COL + g * BN
   static constexpr uint32_t O_COL = 2 * BN;           // O_g at O_COL + g * D
   // barriers
   static constexpr int B_Q = 0;
+  // Slot c of the K/V rings carries K(c) and V(c-1) (visit order), both
+  // in stage c % NSK: one full barrier (2 arrivals + bytes) and one empty
+  // barrier per stage.
   static constexpr int B_KF = 1;
   static constexpr int B_KE = B_KF + NSK;
-  static constexpr int B_VF = B_KE + NSK;
-  static constexpr int B_VE = B_VF + NSV;
-  static constexpr int B_SF = B_VE + NSV;     // NQ: QK_g done
+  static constexpr int B_SF = B_KE + NSK;     // NQ: QK_g done
   static constexpr int B_PF = B_SF + NQ;  // NQ: P_g written (128 arrivals)
   static constexpr int B_OD = B_PF + NQ;  // NQ: last PV_g done
   static constexpr int B_DRAIN = B_OD + NQ;
@@ -149,37 +154,44 @@ __device__ __forceinline__ TileSeq make_seq(const int (&ta)[NQ], const int (&tb)
   return q;
 }
 
-// Streams the K (or V) tiles of the visit into an NST-deep ring of
-// shared-memory stages; full/empty are the first stage's barriers.  Returns
-// false on an abort, after draining (bounded) the copies still in flight.
-template <int D, int NST>
-__device__ __forceinline__ bool produce_tiles(const Work& wk, const TileSeq& seq, int kh,
-                                              uint32_t sbase,
-                                              uint32_t b_full, uint32_t b_empty,
-                                              const CUtensorMap* tm, volatile int* abort_flag,
-                                              int code, long long lim) {
+// Slot-ring producer: slot c = 0..n takes tile c of the visit (K, v_lag = 0)
+// or tile c - 1 (V, v_lag = 1) into stage c % NS; a slot without a tile is
+// a plain arrival.  The two producers share the slot barriers: a full
+// barrier completes on both arrivals and all bytes, an empty barrier on the
+// MMA thread's one commit per slot.  Returns false on an abort, after draining (bounded) the
+// copies still in flight.
+template <int D, int NS>
+__device__ __forceinline__ bool produce_slots(const Work& wk, const TileSeq& seq, int kh,
+                                              uint32_t sbase, uint32_t b_full, uint32_t b_empty,
+                                              const CUtensorMap* tm, int v_lag,
+                                              volatile int* abort_flag, int code, long long lim) {
   using C = Cfg<D>;
   tma_prefetch_desc(tm);
   int issued = 0;
   bool ok = true;
-  for (int t = 0; t < seq.n; ++t) {
-    const int st = t % NST;
-    const uint32_t ph = static_cast<uint32_t>(t / NST) & 1u;
-    const int kv_row = static_cast<int>(wk.kv_base + static_cast<long long>(seq.at(t)) * BN);
-    if (t >= NST) ok = wait_bar(b_empty + 8u * st, ph ^ 1u, abort_flag, &g_umma_status, code, lim);
+  for (int c = 0; c <= seq.n; ++c) {
+    const int st = c % NS;
+    const uint32_t ph = static_cast<uint32_t>(c / NS) & 1u;
+    if (c >= NS) ok = wait_bar(b_empty + 8u * st, ph ^ 1u, abort_flag, &g_umma_status, code, lim);
     if (!ok) break;
-    mbar_arrive_expect_tx(b_full + 8u * st, C::TILE_BYTES);
+    const int t = c - v_lag;
+    if (t >= 0 && t < seq.n) {
+      const int kv_row = static_cast<int>(wk.kv_base + static_cast<long long>(seq.at(t)) * BN);
+      mbar_arrive_expect_tx(b_full + 8u * st, C::TILE_BYTES);
 #pragma unroll
-    for (int ch = 0; ch < C::NCH; ++ch)
-      tma_load_3d(sbase + st * C::TILE_BYTES + ch * CHUNK_BYTES, tm, b_full + 8u * st, ch * 64, kh,
-                  kv_row);
-    issued = t + 1;
+      for (int ch = 0; ch < C::NCH; ++ch)
+        tma_load_3d(sbase + st * C::TILE_BYTES + ch * CHUNK_BYTES, tm, b_full + 8u * st, ch * 64,
+                    kh, kv_row);
+    } else {
+      mbar_arrive(b_full + 8u * st);
+    }
+    issued = c + 1;
   }
   if (!ok) {
     volatile int no_abort = 0;
-    for (int t = (issued > NST ? issued - NST : 0); t < issued; ++t)
-      wait_bar(b_full + 8u * (t % NST), static_cast<uint32_t>(t / NST) & 1u, &no_abort, nullptr,
-               0, lim);
+    for (int c = (issued > NS ? issued - NS : 0); c < issued; ++c)
+      wait_bar(b_full + 8u * (c % NS), static_cast<uint32_t>(c / NS) & 1u, &no_abort, nullptr, 0,
+               lim);
   }
   return ok;
 }
@@ -217,14 +229,14 @@ __device__ __forceinline__ void control_roles(const FwdArgs& a, const Work& wk, 
             tma_load_3d(sQ + g * C::TILE_BYTES + ch * CHUNK_BYTES, tmQ, bar(C::B_Q), ch * 64, h,
                         q_row);
         }
-        if (!produce_tiles<D, C::NSK>(wk, seq, kh, sK, bar(C::B_KF), bar(C::B_KE), tmK, abort_flag,
-                                      0x11, lim)) {
+        if (!produce_slots<D, C::NSK>(wk, seq, kh, sK, bar(C::B_KF), bar(C::B_KE), tmK, 0,
+                                      abort_flag, 0x11, lim)) {
           volatile int no_abort = 0;
           wait_bar(bar(C::B_Q), 0, &no_abort, nullptr, 0, lim);
         }
       } else {
-        produce_tiles<D, C::NSV>(wk, seq, kh, sV, bar(C::B_VF), bar(C::B_VE), tmV, abort_flag, 0x12,
-                                 lim);
+        produce_slots<D, C::NSK>(wk, seq, kh, sV, bar(C::B_KF), bar(C::B_KE), tmV, 1, abort_flag,
+                                 0x12, lim);
       }
     }
     __syncwarp();
@@ -292,16 +304,13 @@ __device__ __forceinline__ void control_roles(const FwdArgs& a, const Work& wk, 
         tc_commit_lead(lead, bar(C::B_KE));
       }
       for (int k = 0; k < seq.n && ok; ++k) {
-        const bool more = k + 1 < seq.n;
-        const int sv = k % C::NSV;
-        const int sk1 = (k + 1) % C::NSK;
-        // Both operand tiles of this iteration first, so the PV and QK
-        // products of a group issue back to back.
-        ok = wait_bar(bar(C::B_VF + sv), static_cast<uint32_t>(k / C::NSV) & 1u, abort_flag,
+        // Slot k + 1: V(k) and K(k + 1), both in stage (k + 1) % NSK.
+        const int sv = (k + 1) % C::NSK;
+        const int sk1 = sv;
+        // Both operand tiles of this iteration first (one wait), so the PV
+        // and QK products of a group issue back to back.
+        ok = wait_bar(bar(C::B_KF + sv), static_cast<uint32_t>((k + 1) / C::NSK) & 1u, abort_flag,
                       &g_umma_status, 0x24, lim);
-        if (ok && more)
-          ok = wait_bar(bar(C::B_KF + sk1), static_cast<uint32_t>((k + 1) / C::NSK) & 1u,
-                        abort_flag, &g_umma_status, 0x22, lim);
         if (!ok) break;
 #pragma unroll
         for (int g = 0; g < NQ; ++g) {
@@ -320,8 +329,7 @@ __device__ __forceinline__ void control_roles(const FwdArgs& a, const Work& wk, 
           if (static_cast<unsigned>(kg + 1) < static_cast<unsigned>(ne[g])) qk(g, sk1);
         }
         if (!ok) break;
-        tc_commit_lead(lead, bar(C::B_VE + sv));
-        if (more) tc_commit_lead(lead, bar(C::B_KE + sk1));
+        tc_commit_lead(lead, bar(C::B_KE + sv));
       }
       // Drain every MMA issued so far before TMEM can be freed.
       volatile int no_abort = 0;
@@ -576,7 +584,8 @@ umma_update_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   if (tid == 0) {
     for (int i = 0; i < C::NBAR; ++i) {
       const bool pf = i >= C::B_PF && i < C::B_PF + NQ;
-      mbar_init(bar(i), pf ? 128u : 1u);  // P_g: every thread of group g arrives
+      const bool kvf = i >= C::B_KF && i < C::B_KF + C::NSK;
+      mbar_init(bar(i), pf ? 128u : (kvf ? 2u : 1u));
     }
     // A CTA that starts after another one of this launch gave up a wait
     // does no work.
