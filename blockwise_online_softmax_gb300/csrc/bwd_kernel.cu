@@ -190,12 +190,78 @@ __global__ void bwd_pre_kernel(const float* __restrict__ out, const __nv_bfloat1
 }
 
 // ------------------------------------------------------------------ dQ kernel
+// Shared memory and TMEM of the dQ kernel.  S is double-buffered in TMEM so
+// that the softmax warps work on tile k while the tensor pipe runs
+// dQ += dS(k-1) K(k-1) and S(k+1) = Q K(k+1)^T.  K and V stream through
+// separate rings: K(k) is read by S(k) and by dQ(k), V(k) only by dP(k).
+template <int D>
+struct QCfg {
+  static constexpr int NCH = D / 64;
+  static constexpr uint32_t TILE = BT * D * 2;
+  static constexpr int NSK = (D == 64) ? 4 : 3;
+  static constexpr int NSV = 2;
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_O = OFF_Q + TILE;
+  static constexpr uint32_t OFF_K = OFF_O + TILE;
+  static constexpr uint32_t OFF_V = OFF_K + NSK * TILE;
+  static constexpr uint32_t OFF_BAR = OFF_V + NSV * TILE;
+  static constexpr int B_R = 0;            // Q and dO loaded
+  static constexpr int B_KF = 1;           // NSK: K stage full
+  static constexpr int B_KE = B_KF + NSK;  // NSK: K stage free
+  static constexpr int B_VF = B_KE + NSK;  // NSV: V stage full
+  static constexpr int B_VE = B_VF + NSV;  // NSV: V stage free
+  static constexpr int B_S = B_VE + NSV;   // S(k) and dP(k) done
+  static constexpr int B_P = B_S + 1;      // dS(k) in TMEM (128 arrivals)
+  static constexpr int B_O = B_P + 1;      // last dQ product done
+  static constexpr int B_DRAIN = B_O + 1;
+  static constexpr int NBAR = B_DRAIN + 1;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr uint32_t SMEM = OFF_MISC + 16 + 1024;
+  static_assert(SMEM <= 232448, "shared memory budget");
+  // TMEM columns: S buffers (dS written over them as bf16 pairs), dP, dQ.
+  static constexpr uint32_t C_S0 = 0;
+  static constexpr uint32_t C_DP = BT;
+  static constexpr uint32_t C_A = 2 * BT;
+  static constexpr uint32_t C_S1 = 2 * BT + D;
+  static_assert(C_S1 + BT <= TMEM_COLS, "TMEM budget");
+};
+
+// Streams tiles 0..n-1 of a K or V ring (rows kv_base + (t0 + k) * BT) into
+// NS shared-memory stages.  Returns false on an abort, after draining
+// (bounded) the copies still in flight.
+template <int NS>
+__device__ __forceinline__ bool produce_ring(const CUtensorMap* tm, uint32_t base, uint32_t tile,
+                                             int nch, uint32_t b_full, uint32_t b_empty,
+                                             int head, long long row0, int n,
+                                             volatile int* abort_flag, int code, long long lim) {
+  int issued = 0;
+  bool ok = true;
+  for (int k = 0; k < n; ++k) {
+    const int st = k % NS;
+    if (k >= NS)
+      ok = wait_bar(b_empty + 8u * st, (static_cast<uint32_t>(k / NS) & 1u) ^ 1u, abort_flag,
+                    &g_bwd_status, code, lim);
+    if (!ok) break;
+    mbar_arrive_expect_tx(b_full + 8u * st, tile);
+    load_tile(base + st * tile, tm, b_full + 8u * st, nch, head,
+              static_cast<int>(row0 + static_cast<long long>(k) * BT));
+    issued = k + 1;
+  }
+  if (!ok) {
+    volatile int no_abort = 0;
+    for (int k = issued > NS ? issued - NS : 0; k < issued; ++k)
+      wait_bar(b_full + 8u * (k % NS), static_cast<uint32_t>(k / NS) & 1u, &no_abort, nullptr, 0,
+               lim);
+  }
+  return ok;
+}
+
 template <int D>
 __global__ void __launch_bounds__(NTH, 1)
 bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
               const BwdArgs b) {
-  using C = BCfg<D>;
+  using C = QCfg<D>;
   const FwdArgs& a = b.f;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -231,64 +297,83 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t sQ = sb + C::OFF_R0, sO = sb + C::OFF_R1;
+  const uint32_t sQ = sb + C::OFF_Q, sO = sb + C::OFF_O;
+  const long long krow0 = wk.kv_base + static_cast<long long>(t0) * BT;
 
   if (warp == 4) {
-    // ---------------------------------------------------------------- producer
+    // ---------------------------------------------------------------- K producer (and Q, dO)
     if (lane == 0) {
       const int qrow = static_cast<int>(wk.q_base + row0);
       mbar_arrive_expect_tx(bar(C::B_R), 2 * C::TILE);
       load_tile(sQ, &tmQ, bar(C::B_R), C::NCH, h, qrow);
       load_tile(sO, &tmO, bar(C::B_R), C::NCH, h, qrow);
-      int issued = 0;
-      bool ok = true;
-      for (int k = 0; k < n; ++k) {
-        const int st = k % C::NST;
-        if (k >= C::NST)
-          ok = wait_bar(bar(C::B_E + st), (static_cast<uint32_t>(k / C::NST) & 1u) ^ 1u,
-                        abort_flag, &g_bwd_status, 0x51, lim);
-        if (!ok) break;
-        const uint32_t dst = sb + C::OFF_ST + st * 2 * C::TILE;
-        const int krow = static_cast<int>(wk.kv_base + static_cast<long long>(t0 + k) * BT);
-        mbar_arrive_expect_tx(bar(C::B_F + st), 2 * C::TILE);
-        load_tile(dst, &tmK, bar(C::B_F + st), C::NCH, kh, krow);
-        load_tile(dst + C::TILE, &tmV, bar(C::B_F + st), C::NCH, kh, krow);
-        issued = k + 1;
-      }
-      if (!ok) {  // drain (bounded) the copies in flight
+      if (!produce_ring<C::NSK>(&tmK, sb + C::OFF_K, C::TILE, C::NCH, bar(C::B_KF), bar(C::B_KE),
+                                kh, krow0, n, abort_flag, 0x51, lim)) {
         volatile int no_abort = 0;
-        for (int k = issued > C::NST ? issued - C::NST : 0; k < issued; ++k)
-          wait_bar(bar(C::B_F + k % C::NST), static_cast<uint32_t>(k / C::NST) & 1u, &no_abort,
-                   nullptr, 0, lim);
         wait_bar(bar(C::B_R), 0, &no_abort, nullptr, 0, lim);
       }
     }
     __syncwarp();
+  } else if (warp == 6) {
+    // ---------------------------------------------------------------- V producer
+    if (lane == 0)
+      produce_ring<C::NSV>(&tmV, sb + C::OFF_V, C::TILE, C::NCH, bar(C::B_VF), bar(C::B_VE), kh,
+                           krow0, n, abort_flag, 0x57, lim);
+    __syncwarp();
   } else if (warp == 5) {
     // ---------------------------------------------------------------- MMA issuer
+    // Order: S(0), dP(0); S(1); then per tile k, once dS(k) is in TMEM:
+    // dP(k+1), dQ += dS(k) K(k), S(k+2).  The softmax of tile k+1 needs only
+    // dP(k+1) after dS(k): it overlaps dQ(k) and S(k+2).  S(k+2) overwrites
+    // the buffer dQ(k) reads; the tensor pipe runs them in issue order.
     const uint32_t lead = lane == 0 ? 1u : 0u;
     const uint64_t qdesc = sdesc_sw128(sQ, 16, 1024);
     const uint64_t odesc = sdesc_sw128(sO, 16, 1024);
+    auto k_st = [&](int k) { return sb + C::OFF_K + static_cast<uint32_t>(k % C::NSK) * C::TILE; };
+    auto v_st = [&](int k) { return sb + C::OFF_V + static_cast<uint32_t>(k % C::NSV) * C::TILE; };
+    auto s_col = [&](int k) { return (k & 1) ? C::C_S1 : C::C_S0; };
+    auto wait_k = [&](int k) {
+      return wait_bar(bar(C::B_KF + k % C::NSK), static_cast<uint32_t>(k / C::NSK) & 1u,
+                      abort_flag, &g_bwd_status, 0x53, lim);
+    };
+    auto wait_v = [&](int k) {
+      return wait_bar(bar(C::B_VF + k % C::NSV), static_cast<uint32_t>(k / C::NSV) & 1u,
+                      abort_flag, &g_bwd_status, 0x58, lim);
+    };
     bool ok = wait_bar(bar(C::B_R), 0, abort_flag, &g_bwd_status, 0x52, lim);
-    for (int k = 0; k < n && ok; ++k) {
-      const int st = k % C::NST;
-      ok = wait_bar(bar(C::B_F + st), static_cast<uint32_t>(k / C::NST) & 1u, abort_flag,
-                    &g_bwd_status, 0x53, lim);
-      if (!ok) break;
+    if (ok) ok = wait_k(0);
+    if (ok) ok = wait_v(0);
+    if (ok) {
       tc_fence_after();
-      const uint32_t sK = sb + C::OFF_ST + st * 2 * C::TILE;
-      const uint64_t kdesc = sdesc_sw128(sK, 16, 1024);
-      const uint64_t vdesc = sdesc_sw128(sK + C::TILE, 16, 1024);
-      mma_rows<D>(lead, tmem + C::C_S, qdesc, kdesc);   // S = Q K^T
-      mma_rows<D>(lead, tmem + C::C_DP, odesc, vdesc);  // dP = dO V^T
+      mma_rows<D>(lead, tmem + C::C_S0, qdesc, sdesc_sw128(k_st(0), 16, 1024));  // S = Q K^T
+      mma_rows<D>(lead, tmem + C::C_DP, odesc, sdesc_sw128(v_st(0), 16, 1024));  // dP = dO V^T
       tc_commit_lead(lead, bar(C::B_S));
+      tc_commit_lead(lead, bar(C::B_VE));
+    }
+    if (ok && n > 1) {
+      ok = wait_k(1);
+      if (ok) mma_rows<D>(lead, tmem + C::C_S1, qdesc, sdesc_sw128(k_st(1), 16, 1024));
+    }
+    for (int k = 0; k < n && ok; ++k) {
       ok = wait_bar(bar(C::B_P), static_cast<uint32_t>(k) & 1u, abort_flag, &g_bwd_status, 0x54,
                     lim);
       if (!ok) break;
       tc_fence_after();
-      mma_acc<D>(lead, tmem + C::C_A0, tmem + C::C_S, sdesc_sw128(sK, CHB, 1024));  // dQ += dS K
-      tc_commit_lead(lead, bar(C::B_E + st));
+      if (k + 1 < n) {
+        ok = wait_v(k + 1);
+        if (!ok) break;
+        mma_rows<D>(lead, tmem + C::C_DP, odesc, sdesc_sw128(v_st(k + 1), 16, 1024));
+        tc_commit_lead(lead, bar(C::B_S));  // covers S(k+1), issued earlier
+        tc_commit_lead(lead, bar(C::B_VE + (k + 1) % C::NSV));
+      }
+      mma_acc<D>(lead, tmem + C::C_A, tmem + s_col(k), sdesc_sw128(k_st(k), CHB, 1024));  // dQ += dS K
+      tc_commit_lead(lead, bar(C::B_KE + k % C::NSK));
       if (k + 1 == n) tc_commit_lead(lead, bar(C::B_O));
+      if (k + 2 < n) {
+        ok = wait_k(k + 2);
+        if (!ok) break;
+        mma_rows<D>(lead, tmem + s_col(k), qdesc, sdesc_sw128(k_st(k + 2), 16, 1024));
+      }
     }
     volatile int no_abort = 0;
     tc_commit_lead(lead, bar(C::B_DRAIN));
@@ -311,7 +396,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       row_lo = static_cast<int>(lo);
       row_hi = static_cast<int>(hi);
     }
-    acc_to_tmem<D>(tl + C::C_A0, b.dq + sidx * D, valid);
+    acc_to_tmem<D>(tl + C::C_A, b.dq + sidx * D, valid);
     tmem_wait_st();
     // Key tiles full_0 .. full_0 + n_full - 1 lie wholly inside the row's
     // interval and need no mask (one unsigned compare decides).
@@ -330,33 +415,41 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       const int t = t0 + k;
       const bool masked = static_cast<unsigned>(t - full_0) >= static_cast<unsigned>(n_full);
       const int lo_j = row_lo - t * BT, hi_j = row_hi - t * BT;
+      const uint32_t cs = tl + ((k & 1) ? C::C_S1 : C::C_S0);
 #pragma unroll
       for (int c = 0; c < BT / 32; ++c) {
         uint32_t s[32], dp[32], w[16];
-        tmem_ld32(tl + C::C_S + c * 32, s);
+        tmem_ld32(cs + c * 32, s);
         tmem_ld32(tl + C::C_DP + c * 32, dp);
         tmem_wait_ld();
         reg_fence32(s);
         reg_fence32(dp);
+        // Three branch-free passes (exponentials, mask, dS), so the 16
+        // column pairs of a pass are independent chains in one block.
+        float p[32];
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
           float x0, x1;
           f2unpack(ffma2(f2pack(__uint_as_float(s[j]), __uint_as_float(s[j + 1])), sl2x2, nlse2),
                    x0, x1);
-          float p0 = ex2(x0), p1 = ex2(x1);
-          if (masked) {
-            const int col = c * 32 + j;
-            if (!(col >= lo_j && col < hi_j)) p0 = 0.f;
-            if (!(col + 1 >= lo_j && col + 1 < hi_j)) p1 = 0.f;
-          }
+          p[j] = ex2(x0);
+          p[j + 1] = ex2(x1);
+        }
+        if (masked) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (!(c * 32 + j >= lo_j && c * 32 + j < hi_j)) p[j] = 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
           const uint64_t t2 =
               fadd2(f2pack(__uint_as_float(dp[j]), __uint_as_float(dp[j + 1])), ndr2);
           float d0, d1;
-          f2unpack(fmul2(fmul2(f2pack(p0, p1), t2), scx2), d0, d1);
+          f2unpack(fmul2(fmul2(f2pack(p[j], p[j + 1]), t2), scx2), d0, d1);
           w[j / 2] = bf16x2_rn(d0, d1);
         }
-        // dS pairs over columns [16c, 16c + 16): S columns already read.
-        tmem_st16(tl + C::C_S + c * 16, w);
+        // dS pairs over columns [16c, 16c + 16) of the S buffer: already read.
+        tmem_st16(cs + c * 16, w);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -368,7 +461,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     }
     if (ok) {
       tc_fence_after();
-      tmem_to_acc<D>(tl + C::C_A0, b.dq + sidx * D, valid);
+      tmem_to_acc<D>(tl + C::C_A, b.dq + sidx * D, valid);
     }
   }
   tc_fence_before();
@@ -538,7 +631,6 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       }
       if (!ok) continue;
       tc_fence_after();
-      const uint32_t nlb = smem_u32(nl + (it & 1) * BT);
       const int2* lb = lmt + (it & 1) * BT;
       // Rolled: the chunk loop body is large, and one copy keeps the
       // softmax warps' code in the instruction cache.
@@ -547,32 +639,41 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         uint32_t s[32], dp[32], wp[16], wd[16];
         tmem_ld32(tl + C::C_S + c * 32, s);
         tmem_ld32(tl + C::C_DP + c * 32, dp);
+        // (-lse2, -D) of the chunk's 32 queries, two per 16-byte load, all
+        // issued before the loops that use them.
+        float4 nv[16];
+        const float4* nlc = reinterpret_cast<const float4*>(nl + (it & 1) * BT + c * 32);
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) nv[jj] = nlc[jj];
         tmem_wait_ld();
         reg_fence32(s);
         reg_fence32(dp);
+        // Three branch-free passes (exponentials, mask, dS), so the 16
+        // column pairs of a pass are independent chains in one block.
+        float p[32];
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
-          // Columns q, q + 1: (-lse2, -D) of both in one 16-byte load.
-          uint32_t w0, w1, w2, w3;
-          asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                       : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
-                       : "r"(nlb + (c * 32 + j) * 8));
-          const uint64_t x2 = ffma2(f2pack(__uint_as_float(s[j]), __uint_as_float(s[j + 1])),
-                                    sl2x2, f2pack(__uint_as_float(w0), __uint_as_float(w2)));
           float x0, x1;
-          f2unpack(x2, x0, x1);
-          float p0 = ex2(x0), p1 = ex2(x1);
-          if (!full) {
-            const int2 m0 = lb[c * 32 + j], m1 = lb[c * 32 + j + 1];
-            if (!(kvalid && kidx >= m0.x && kidx < m0.y)) p0 = 0.f;
-            if (!(kvalid && kidx >= m1.x && kidx < m1.y)) p1 = 0.f;
+          f2unpack(ffma2(f2pack(__uint_as_float(s[j]), __uint_as_float(s[j + 1])), sl2x2,
+                         f2pack(nv[j / 2].x, nv[j / 2].z)),
+                   x0, x1);
+          p[j] = ex2(x0);
+          p[j + 1] = ex2(x1);
+        }
+        if (!full) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int2 m = lb[c * 32 + j];
+            if (!(kvalid && kidx >= m.x && kidx < m.y)) p[j] = 0.f;
           }
-          const uint64_t pp = f2pack(p0, p1);
+        }
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
           const uint64_t t2 = fadd2(f2pack(__uint_as_float(dp[j]), __uint_as_float(dp[j + 1])),
-                                    f2pack(__uint_as_float(w1), __uint_as_float(w3)));
+                                    f2pack(nv[j / 2].y, nv[j / 2].w));
           float d0, d1;
-          f2unpack(fmul2(fmul2(pp, t2), scx2), d0, d1);
-          wp[j / 2] = bf16x2_rn(p0, p1);
+          f2unpack(fmul2(fmul2(f2pack(p[j], p[j + 1]), t2), scx2), d0, d1);
+          wp[j / 2] = bf16x2_rn(p[j], p[j + 1]);
           wd[j / 2] = bf16x2_rn(d0, d1);
         }
         tmem_st16(tl + C::C_S + c * 16, wp);   // P^T pairs over read S^T columns
@@ -603,7 +704,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 template <int D>
 cudaError_t launch_dq_d(const BwdArgs& b, const CUtensorMap& tq, const CUtensorMap& tk,
                         const CUtensorMap& tv, const CUtensorMap& to, cudaStream_t st) {
-  using C = BCfg<D>;
+  using C = QCfg<D>;
   cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(C::SMEM));
   if (e != cudaSuccess) return e;
