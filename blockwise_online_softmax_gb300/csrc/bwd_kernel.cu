@@ -40,6 +40,18 @@
 
 namespace ra {
 
+// Integer bf16 packing (variant probe): both values rounded on the ALU pipe.
+__device__ __forceinline__ uint32_t pack_ta(float lo, float hi) {
+  const uint32_t a = __float_as_uint(lo) + 0x8000u, b = __float_as_uint(hi) + 0x8000u;
+  return __byte_perm(a, b, 0x7632);
+}
+__device__ __forceinline__ uint32_t pack_rne(float lo, float hi) {
+  uint32_t a = __float_as_uint(lo), b = __float_as_uint(hi);
+  a += 0x7fffu + ((a >> 16) & 1u);
+  b += 0x7fffu + ((b >> 16) & 1u);
+  return __byte_perm(a, b, 0x7632);
+}
+
 __device__ int g_bwd_status = 0;
 
 namespace {
@@ -64,8 +76,9 @@ struct BCfg {
   static constexpr int B_F = 1;             // NST: stage full
   static constexpr int B_E = B_F + NST;     // NST: stage free
   static constexpr int B_S = B_E + NST;     // S and dP (or their transposes) done
-  static constexpr int B_P = B_S + 1;       // softmax results in TMEM (128 arrivals)
-  static constexpr int B_O = B_P + 1;       // last accumulating MMA done
+  static constexpr int NPC = BT / 32;       // softmax chunks of 32 queries
+  static constexpr int B_P = B_S + 1;       // NPC: chunk c of P^T, dS^T in TMEM (128 arrivals)
+  static constexpr int B_O = B_P + NPC;     // last accumulating MMA done
   static constexpr int B_DRAIN = B_O + 1;
   static constexpr int NBAR = B_DRAIN + 1;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
@@ -100,6 +113,17 @@ __device__ __forceinline__ void mma_acc(uint32_t lead, uint32_t d_tmem, uint32_t
   constexpr uint32_t idesc = idesc_bf16(BT, D, 1);
 #pragma unroll
   for (int kk = 0; kk < BT / 16; ++kk)
+    mma_ts_lead(lead, d_tmem, a_tmem + kk * 8, bdesc_mn + static_cast<uint64_t>((kk * 2048) >> 4),
+                idesc, 1u);
+}
+
+// The same, over the 32 rows of B (two K-steps) starting at step kk0.
+template <int D>
+__device__ __forceinline__ void mma_acc_part(uint32_t lead, uint32_t d_tmem, uint32_t a_tmem,
+                                             uint64_t bdesc_mn, int kk0) {
+  constexpr uint32_t idesc = idesc_bf16(BT, D, 1);
+#pragma unroll
+  for (int kk = kk0; kk < kk0 + 2; ++kk)
     mma_ts_lead(lead, d_tmem, a_tmem + kk * 8, bdesc_mn + static_cast<uint64_t>((kk * 2048) >> 4),
                 idesc, 1u);
 }
@@ -403,7 +427,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const int full_0 = (row_lo + BT - 1) / BT;
     const int n_full = row_hi / BT - full_0 > 0 ? row_hi / BT - full_0 : 0;
     const uint64_t sl2x2 = f2pack(a.scale_log2, a.scale_log2);
-    const uint64_t nlse2 = f2pack(-lse2, -lse2), ndr2 = f2pack(-dr, -dr);
+    // dS = P * (dP * scale - D * scale): one FFMA2 and one FMUL2 per pair.
+    const uint64_t nlse2 = f2pack(-lse2, -lse2), ndr2 = f2pack(-dr * a.scale, -dr * a.scale);
     const uint64_t scx2 = f2pack(a.scale, a.scale);
     bool ok = true;
     for (int k = 0; k < n; ++k) {
@@ -443,9 +468,9 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
           const uint64_t t2 =
-              fadd2(f2pack(__uint_as_float(dp[j]), __uint_as_float(dp[j + 1])), ndr2);
+              ffma2(f2pack(__uint_as_float(dp[j]), __uint_as_float(dp[j + 1])), scx2, ndr2);
           float d0, d1;
-          f2unpack(fmul2(fmul2(f2pack(p[j], p[j + 1]), t2), scx2), d0, d1);
+          f2unpack(fmul2(f2pack(p[j], p[j + 1]), t2), d0, d1);
           w[j / 2] = bf16x2_rn(d0, d1);
         }
         // dS pairs over columns [16c, 16c + 16) of the S buffer: already read.
@@ -502,7 +527,8 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const long long lim = a.wait_limit;
 
   if (tid == 0) {
-    for (int i = 0; i < C::NBAR; ++i) mbar_init(bar(i), i == C::B_P ? 128u : 1u);
+    for (int i = 0; i < C::NBAR; ++i)
+      mbar_init(bar(i), (i >= C::B_P && i < C::B_P + C::NPC) ? 128u : 1u);
     *abort_flag = *reinterpret_cast<volatile int*>(&g_bwd_status) != 0 ? 1 : 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -569,12 +595,21 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       mma_rows<D>(lead, tmem + C::C_S, kdesc, sdesc_sw128(sQ, 16, 1024));   // S^T = K Q^T
       mma_rows<D>(lead, tmem + C::C_DP, vdesc, sdesc_sw128(sO, 16, 1024));  // dP^T = V dO^T
       tc_commit_lead(lead, bar(C::B_S));
-      ok = wait_bar(bar(C::B_P), static_cast<uint32_t>(it) & 1u, abort_flag, &g_bwd_status, 0x64,
-                    lim);
+      // dV += P^T dO and dK += dS^T Q, one 32-query chunk at a time as the
+      // softmax warps publish it, so these products overlap their later
+      // chunks.
+      const uint64_t odesc_mn = sdesc_sw128(sO, CHB, 1024);
+      const uint64_t qdesc_mn = sdesc_sw128(sQ, CHB, 1024);
+#pragma unroll
+      for (int c = 0; c < C::NPC; ++c) {
+        ok = wait_bar(bar(C::B_P + c), static_cast<uint32_t>(it) & 1u, abort_flag, &g_bwd_status,
+                      0x64, lim);
+        if (!ok) break;
+        tc_fence_after();
+        mma_acc_part<D>(lead, tmem + C::C_A0, tmem + C::C_S, odesc_mn, 2 * c);   // dV
+        mma_acc_part<D>(lead, tmem + C::C_A1, tmem + C::C_DP, qdesc_mn, 2 * c);  // dK
+      }
       if (!ok) break;
-      tc_fence_after();
-      mma_acc<D>(lead, tmem + C::C_A0, tmem + C::C_S, sdesc_sw128(sO, CHB, 1024));   // dV += P^T dO
-      mma_acc<D>(lead, tmem + C::C_A1, tmem + C::C_DP, sdesc_sw128(sQ, CHB, 1024));  // dK += dS^T Q
       tc_commit_lead(lead, bar(C::B_E + st));
       if (it + 1 == n) tc_commit_lead(lead, bar(C::B_O));
     }
@@ -593,9 +628,12 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     acc_to_tmem<D>(tl + C::C_A1, b.dk + kst * D, kvalid);
     tmem_wait_st();
     // Per-query data of the current tile, double-buffered in shared memory:
-    // nl = (-lse * log2(e), -D) and lim = the query's allowed key rows
-    // [lo, hi).  A tile whose every query sees every key of this key tile
-    // (the common case off the diagonal) skips the mask.
+    // nl = -lse * log2(e) and -D / sqrt(d), interleaved by query pairs
+    // (q, q+1) as {-lse2_q, -lse2_q+1, -D'_q, -D'_q+1} so that one 16-byte
+    // load gives both operands of the packed f32x2 math as aligned register
+    // pairs; and lim = the query's allowed key rows [lo, hi).  A tile whose
+    // every query sees every key of this key tile (the common case off the
+    // diagonal) skips the mask.
     float2* nl = reinterpret_cast<float2*>(smem + C::OFF_QV);
     int2* lmt = reinterpret_cast<int2*>(smem + C::OFF_QV + 2 * BT * 8);
     const float sl2 = a.scale_log2;
@@ -617,7 +655,9 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           lo = static_cast<int>(l);
           hi = static_cast<int>(hh2);
         }
-        nl[(it & 1) * BT + t] = make_float2(-l2, -dq);
+        float* nlf = reinterpret_cast<float*>(nl + (it & 1) * BT);
+        nlf[(t >> 1) * 4 + (t & 1)] = -l2;
+        nlf[(t >> 1) * 4 + 2 + (t & 1)] = -dq * a.scale;
         lmt[(it & 1) * BT + t] = make_int2(lo, hi);
         sees_all = r < a.cq && lo <= k0 && hi >= k0 + BT && k0 + BT <= a.ck;
       }
@@ -639,8 +679,8 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         uint32_t s[32], dp[32], wp[16], wd[16];
         tmem_ld32(tl + C::C_S + c * 32, s);
         tmem_ld32(tl + C::C_DP + c * 32, dp);
-        // (-lse2, -D) of the chunk's 32 queries, two per 16-byte load, all
-        // issued before the loops that use them.
+        // (-lse2, -D') of the chunk's 32 queries, one pair per 16-byte
+        // load, all issued before the loops that use them.
         float4 nv[16];
         const float4* nlc = reinterpret_cast<const float4*>(nl + (it & 1) * BT + c * 32);
 #pragma unroll
@@ -655,7 +695,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         for (int j = 0; j < 32; j += 2) {
           float x0, x1;
           f2unpack(ffma2(f2pack(__uint_as_float(s[j]), __uint_as_float(s[j + 1])), sl2x2,
-                         f2pack(nv[j / 2].x, nv[j / 2].z)),
+                         f2pack(nv[j / 2].x, nv[j / 2].y)),
                    x0, x1);
           p[j] = ex2(x0);
           p[j + 1] = ex2(x1);
@@ -669,19 +709,19 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
-          const uint64_t t2 = fadd2(f2pack(__uint_as_float(dp[j]), __uint_as_float(dp[j + 1])),
-                                    f2pack(nv[j / 2].y, nv[j / 2].w));
+          const uint64_t t2 = ffma2(f2pack(__uint_as_float(dp[j]), __uint_as_float(dp[j + 1])),
+                                    scx2, f2pack(nv[j / 2].z, nv[j / 2].w));
           float d0, d1;
-          f2unpack(fmul2(fmul2(f2pack(p[j], p[j + 1]), t2), scx2), d0, d1);
+          f2unpack(fmul2(f2pack(p[j], p[j + 1]), t2), d0, d1);
           wp[j / 2] = bf16x2_rn(p[j], p[j + 1]);
           wd[j / 2] = bf16x2_rn(d0, d1);
         }
         tmem_st16(tl + C::C_S + c * 16, wp);   // P^T pairs over read S^T columns
         tmem_st16(tl + C::C_DP + c * 16, wd);  // dS^T pairs over read dP^T columns
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(C::B_P + c));
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(C::B_P));
     }
     if (ok) {
       ok = wait_bar(bar(C::B_O), 0u, abort_flag, &g_bwd_status, 0x66, lim);
