@@ -66,16 +66,31 @@ struct BCfg {
   static constexpr int NCH = D / 64;
   static constexpr uint32_t TILE = BT * D * 2;
   static constexpr int NST = 2;  // stages of the streamed operand pair
-  // shared memory: two resident tiles, NST stages of two tiles, barriers
+  // Augmentation tiles: 128 rows x 16 bf16 (one K-step), K-major without
+  // swizzle: element (r, k) at (r / 8) * 256 + (k / 8) * 128 + (r % 8) * 16
+  // + (k % 8) * 2, i.e. 8x16-byte core matrices, LBO 128 (along K), SBO 256
+  // (along rows).
+  static constexpr uint32_t AUG = BT * 32;
+  // shared memory: K and V resident, NST stages of (Q, dO), the ones tile,
+  // NST stages of (lse, D) augmentation tiles, per-query key intervals
   static constexpr uint32_t OFF_R0 = 0;
   static constexpr uint32_t OFF_R1 = OFF_R0 + TILE;
   static constexpr uint32_t OFF_ST = OFF_R1 + TILE;  // stage s: tiles at OFF_ST + s*2*TILE
-  static constexpr uint32_t OFF_QV = OFF_ST + NST * 2 * TILE;  // per-query data (dK/dV kernel)
-  static constexpr uint32_t OFF_BAR = OFF_QV + 2 * BT * 16;
+  static constexpr uint32_t OFF_ONES = OFF_ST + NST * 2 * TILE;
+  static constexpr uint32_t OFF_AUG = OFF_ONES + AUG;      // stage s: lse at +s*2*AUG, D at +AUG
+  // int2 [3][BT]: three buffers, since the tile after next is staged while
+  // a lagging warp may still read the previous tile's intervals.
+  static constexpr uint32_t OFF_LM = OFF_AUG + NST * 2 * AUG;
+  static constexpr uint32_t OFF_BAR = OFF_LM + 3 * BT * 8;
   static constexpr int B_R = 0;             // resident tiles loaded
   static constexpr int B_F = 1;             // NST: stage full
   static constexpr int B_E = B_F + NST;     // NST: stage free
-  static constexpr int B_S = B_E + NST;     // S and dP (or their transposes) done
+  // 2: augmentation tiles of tile it written (128 arrivals), alternating by
+  // the parity of it: the softmax warps stage one tile ahead, so one
+  // barrier could complete two phases before the MMA thread waits for the
+  // first of them.
+  static constexpr int B_A = B_E + NST;
+  static constexpr int B_S = B_A + 2;       // S^T and dP^T done
   static constexpr int NPC = BT / 32;       // softmax chunks of 32 queries
   static constexpr int B_P = B_S + 1;       // NPC: chunk c of P^T, dS^T in TMEM (128 arrivals)
   static constexpr int B_O = B_P + NPC;     // last accumulating MMA done
@@ -85,12 +100,35 @@ struct BCfg {
   static constexpr uint32_t SMEM = OFF_MISC + 16 + 1024;
   static_assert(SMEM <= 232448, "shared memory budget");
   // TMEM columns
-  static constexpr uint32_t C_S = 0;       // S or S^T (then dS or P^T, bf16 pairs)
-  static constexpr uint32_t C_DP = BT;     // dP or dP^T (then dS^T, bf16 pairs)
-  static constexpr uint32_t C_A0 = 2 * BT; // dQ, or dV
+  static constexpr uint32_t C_S = 0;       // S^T (then P^T, bf16 pairs)
+  static constexpr uint32_t C_DP = BT;     // dP^T (then dS^T, bf16 pairs)
+  static constexpr uint32_t C_A0 = 2 * BT; // dV
   static constexpr uint32_t C_A1 = 2 * BT + D;  // dK
   static_assert(C_A1 + D <= TMEM_COLS, "TMEM budget");
 };
+
+// Descriptor of a K-major tile without swizzle (see BCfg::AUG).
+__device__ __forceinline__ uint64_t sdesc_noswz(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;  // descriptor version; swizzle field (61..63) = 0: none
+  return d;
+}
+
+// v as the sum of three bf16 (a + b + c within ~2^-24 |v|), packed for
+// row elements k = 0, 1 (first word) and 2 (second word).
+__device__ __forceinline__ uint2 bf16_split3(float v) {
+  const __nv_bfloat16 a = __float2bfloat16_rn(v);
+  const float r1 = v - __bfloat162float(a);
+  const __nv_bfloat16 b = __float2bfloat16_rn(r1);
+  const float r2 = r1 - __bfloat162float(b);
+  const __nv_bfloat16 c = __float2bfloat16_rn(r2);
+  return make_uint2(static_cast<uint32_t>(__bfloat16_as_ushort(a)) |
+                        (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16),
+                    static_cast<uint32_t>(__bfloat16_as_ushort(c)));
+}
 
 // ------------------------------------------------------------------ shared pieces
 // S-like tile product: D[tmem] = A B^T over d, both operands K-major in
@@ -498,6 +536,11 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 }
 
 // ------------------------------------------------------------------ dK/dV kernel
+// The per-query terms enter the products: S^T and dP^T each get one more
+// K-step, a ones column block of the keys against three bf16 terms of
+// -lse * sqrt(d) (resp. -D) per query, so TMEM holds S^T - lse * sqrt(d)
+// and dP^T - D.  The softmax warps then need no per-query data for full
+// tiles: P = 2^(x * log2(e) / sqrt(d)) and dS = P * (y / sqrt(d)).
 template <int D>
 __global__ void __launch_bounds__(NTH, 1)
 bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -528,11 +571,22 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
   if (tid == 0) {
     for (int i = 0; i < C::NBAR; ++i)
-      mbar_init(bar(i), (i >= C::B_P && i < C::B_P + C::NPC) ? 128u : 1u);
+      mbar_init(bar(i), ((i >= C::B_P && i < C::B_P + C::NPC) || i == C::B_A || i == C::B_A + 1)
+                            ? 128u
+                            : 1u);
     *abort_flag = *reinterpret_cast<volatile int*>(&g_bwd_status) != 0 ? 1 : 0;
     fence_mbar_init();
-    fence_proxy_async_smem();
   }
+  // Augmentation tiles: zero everywhere; the ones tile has 1 at k = 0, 1, 2
+  // of every row (k < 8 lies in the first core matrix of each row).
+  for (uint32_t off = static_cast<uint32_t>(tid) * 16; off < (1 + 2 * C::NST) * C::AUG;
+       off += NTH * 16)
+    *reinterpret_cast<uint4*>(smem + C::OFF_ONES + off) = make_uint4(0u, 0u, 0u, 0u);
+  __syncthreads();
+  if (tid < BT)
+    *reinterpret_cast<uint2*>(smem + C::OFF_ONES + (tid >> 3) * 256 + (tid & 7) * 16) =
+        make_uint2(0x3F803F80u, 0x00003F80u);
+  fence_proxy_async_smem();
   __syncthreads();
   if (*abort_flag) return;
   if (warp == 5) {
@@ -581,19 +635,27 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   } else if (warp == 5) {
     // ---------------------------------------------------------------- MMA issuer
     const uint32_t lead = lane == 0 ? 1u : 0u;
+    constexpr uint32_t idesc_s = idesc_bf16(BT, BT, 0);
     const uint64_t kdesc = sdesc_sw128(sK, 16, 1024);
     const uint64_t vdesc = sdesc_sw128(sV, 16, 1024);
+    const uint64_t ones = sdesc_noswz(sb + C::OFF_ONES, 128, 256);
     bool ok = wait_bar(bar(C::B_R), 0, abort_flag, &g_bwd_status, 0x62, lim);
     for (int it = 0; it < n && ok; ++it) {
       const int st = it % C::NST;
       ok = wait_bar(bar(C::B_F + st), static_cast<uint32_t>(it / C::NST) & 1u, abort_flag,
                     &g_bwd_status, 0x63, lim);
+      if (ok)
+        ok = wait_bar(bar(C::B_A + (it & 1)), static_cast<uint32_t>(it >> 1) & 1u, abort_flag,
+                      &g_bwd_status, 0x67, lim);
       if (!ok) break;
       tc_fence_after();
       const uint32_t sQ = sb + C::OFF_ST + st * 2 * C::TILE;
       const uint32_t sO = sQ + C::TILE;
+      const uint32_t sA = sb + C::OFF_AUG + st * 2 * C::AUG;
       mma_rows<D>(lead, tmem + C::C_S, kdesc, sdesc_sw128(sQ, 16, 1024));   // S^T = K Q^T
+      mma_ss_lead(lead, tmem + C::C_S, ones, sdesc_noswz(sA, 128, 256), idesc_s, 1u);  // - lse sqrt(d)
       mma_rows<D>(lead, tmem + C::C_DP, vdesc, sdesc_sw128(sO, 16, 1024));  // dP^T = V dO^T
+      mma_ss_lead(lead, tmem + C::C_DP, ones, sdesc_noswz(sA + C::AUG, 128, 256), idesc_s, 1u);  // - D
       tc_commit_lead(lead, bar(C::B_S));
       // dV += P^T dO and dK += dS^T Q, one 32-query chunk at a time as the
       // softmax warps publish it, so these products overlap their later
@@ -619,7 +681,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     __syncwarp();
   } else if (warp < 4) {
     // ---------------------------------------------------------------- softmax
-    const int t = warp * 32 + lane;  // key row of the tile = TMEM lane
+    const int t = warp * 32 + lane;  // key row of the tile = TMEM lane; query t when staging
     const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     const long long kidx = k0 + t;
     const bool kvalid = kidx < a.ck;
@@ -627,101 +689,103 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     acc_to_tmem<D>(tl + C::C_A0, b.dv + kst * D, kvalid);
     acc_to_tmem<D>(tl + C::C_A1, b.dk + kst * D, kvalid);
     tmem_wait_st();
-    // Per-query data of the current tile, double-buffered in shared memory:
-    // nl = -lse * log2(e) and -D / sqrt(d), interleaved by query pairs
-    // (q, q+1) as {-lse2_q, -lse2_q+1, -D'_q, -D'_q+1} so that one 16-byte
-    // load gives both operands of the packed f32x2 math as aligned register
-    // pairs; and lim = the query's allowed key rows [lo, hi).  A tile whose
-    // every query sees every key of this key tile (the common case off the
-    // diagonal) skips the mask.
-    float2* nl = reinterpret_cast<float2*>(smem + C::OFF_QV);
-    int2* lmt = reinterpret_cast<int2*>(smem + C::OFF_QV + 2 * BT * 8);
+    int2* lmt = reinterpret_cast<int2*>(smem + C::OFF_LM);
+    // Stages query t of tile `it`: its -lse * sqrt(d) and -D as three bf16
+    // terms into the augmentation tiles of stage it % NST, and its allowed
+    // key rows [lo, hi) for the mask.  Returns whether the query sees every
+    // key of this key tile.  Queries with no allowed key (or past the
+    // block) get zero terms; the mask covers them.
+    auto stage = [&](int it) -> bool {
+      const long long r = it_row(it) + t;
+      float vl = 0.f, vd = 0.f;
+      int lo = 0, hi = 0;
+      if (r < a.cq) {
+        const long long qi = (wk.state_base + r) * a.heads + it_head(it);
+        const float lse = b.lse[qi];
+        if (lse > -INFINITY) vl = -lse / a.scale;
+        vd = -b.dvec[qi];
+        long long l, h;
+        row_keys(a, wk, r, vb, &l, &h);
+        lo = static_cast<int>(l);
+        hi = static_cast<int>(h);
+      }
+      uint8_t* aug = smem + C::OFF_AUG + (it % C::NST) * 2 * C::AUG + (t >> 3) * 256 + (t & 7) * 16;
+      *reinterpret_cast<uint2*>(aug) = bf16_split3(vl);
+      *reinterpret_cast<uint2*>(aug + C::AUG) = bf16_split3(vd);
+      lmt[(it % 3) * BT + t] = make_int2(lo, hi);
+      return r < a.cq && lo <= k0 && hi >= k0 + BT && k0 + BT <= a.ck;
+    };
     const float sl2 = a.scale_log2;
     const uint64_t sl2x2 = f2pack(sl2, sl2), scx2 = f2pack(a.scale, a.scale);
+    // Tile 0 is staged here; tile it + 1 while the products of tile it run.
+    // The augmentation stage of tile it + 1 was last read by the products
+    // of tile it - 1, which finished before this group read their results.
+    // Every softmax thread passes named barrier 2 once per tile, aborted or
+    // not, so the warps are at most one tile apart.
+    bool full = named_bar_and(2, 128, stage(0));
+    fence_proxy_async_smem();
+    mbar_arrive(bar(C::B_A));  // tile 0: barrier B_A + 0, phase 0
     bool ok = true;
     for (int it = 0; it < n; ++it) {
-      bool sees_all;
-      {
-        const long long r = it_row(it) + t;
-        const int hh = it_head(it);
-        float l2 = -INFINITY, dq = 0.f;
-        int lo = 0, hi = 0;
-        if (r < a.cq) {
-          const long long qi = (wk.state_base + r) * a.heads + hh;
-          l2 = b.lse[qi] * kLog2e;
-          dq = b.dvec[qi];
-          long long l, hh2;
-          row_keys(a, wk, r, vb, &l, &hh2);
-          lo = static_cast<int>(l);
-          hi = static_cast<int>(hh2);
-        }
-        float* nlf = reinterpret_cast<float*>(nl + (it & 1) * BT);
-        nlf[(t >> 1) * 4 + (t & 1)] = -l2;
-        nlf[(t >> 1) * 4 + 2 + (t & 1)] = -dq * a.scale;
-        lmt[(it & 1) * BT + t] = make_int2(lo, hi);
-        sees_all = r < a.cq && lo <= k0 && hi >= k0 + BT && k0 + BT <= a.ck;
+      bool full_next = false;
+      if (it + 1 < n) {
+        full_next = named_bar_and(2, 128, stage(it + 1));
+        fence_proxy_async_smem();
+        mbar_arrive(bar(C::B_A + ((it + 1) & 1)));
       }
-      // Every softmax warp passes this barrier n times, aborted or not, so
-      // a warp that gave up a wait can never leave the others blocked here.
-      const bool full = named_bar_and(2, 128, sees_all);
       if (ok) {
         ok = wait_bar(bar(C::B_S), static_cast<uint32_t>(it) & 1u, abort_flag, &g_bwd_status,
                       0x65, lim);
         ok = __all_sync(0xffffffffu, ok);
       }
-      if (!ok) continue;
-      tc_fence_after();
-      const int2* lb = lmt + (it & 1) * BT;
-      // Rolled: the chunk loop body is large, and one copy keeps the
-      // softmax warps' code in the instruction cache.
+      if (ok) {
+        tc_fence_after();
+        const int2* lb = lmt + (it % 3) * BT;
+        // Rolled: the chunk loop body is large, and one copy keeps the
+        // softmax warps' code in the instruction cache.
 #pragma unroll 1
-      for (int c = 0; c < BT / 32; ++c) {
-        uint32_t s[32], dp[32], wp[16], wd[16];
-        tmem_ld32(tl + C::C_S + c * 32, s);
-        tmem_ld32(tl + C::C_DP + c * 32, dp);
-        // (-lse2, -D') of the chunk's 32 queries, one pair per 16-byte
-        // load, all issued before the loops that use them.
-        float4 nv[16];
-        const float4* nlc = reinterpret_cast<const float4*>(nl + (it & 1) * BT + c * 32);
+        for (int c = 0; c < BT / 32; ++c) {
+          uint32_t s[32], dp[32], wp[16], wd[16];
+          tmem_ld32(tl + C::C_S + c * 32, s);
+          tmem_ld32(tl + C::C_DP + c * 32, dp);
+          tmem_wait_ld();
+          reg_fence32(s);
+          reg_fence32(dp);
+          // Three branch-free passes (exponentials, mask, dS), so the 16
+          // column pairs of a pass are independent chains in one block.
+          float p[32];
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) nv[jj] = nlc[jj];
-        tmem_wait_ld();
-        reg_fence32(s);
-        reg_fence32(dp);
-        // Three branch-free passes (exponentials, mask, dS), so the 16
-        // column pairs of a pass are independent chains in one block.
-        float p[32];
-#pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          float x0, x1;
-          f2unpack(ffma2(f2pack(__uint_as_float(s[j]), __uint_as_float(s[j + 1])), sl2x2,
-                         f2pack(nv[j / 2].x, nv[j / 2].y)),
-                   x0, x1);
-          p[j] = ex2(x0);
-          p[j + 1] = ex2(x1);
-        }
-        if (!full) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int2 m = lb[c * 32 + j];
-            if (!(kvalid && kidx >= m.x && kidx < m.y)) p[j] = 0.f;
+          for (int j = 0; j < 32; j += 2) {
+            float x0, x1;
+            f2unpack(fmul2(f2pack(__uint_as_float(s[j]), __uint_as_float(s[j + 1])), sl2x2), x0,
+                     x1);
+            p[j] = ex2(x0);
+            p[j + 1] = ex2(x1);
           }
-        }
+          if (!full) {
 #pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          const uint64_t t2 = ffma2(f2pack(__uint_as_float(dp[j]), __uint_as_float(dp[j + 1])),
-                                    scx2, f2pack(nv[j / 2].z, nv[j / 2].w));
-          float d0, d1;
-          f2unpack(fmul2(f2pack(p[j], p[j + 1]), t2), d0, d1);
-          wp[j / 2] = bf16x2_rn(p[j], p[j + 1]);
-          wd[j / 2] = bf16x2_rn(d0, d1);
+            for (int j = 0; j < 32; ++j) {
+              const int2 m = lb[c * 32 + j];
+              if (!(kvalid && kidx >= m.x && kidx < m.y)) p[j] = 0.f;
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const uint64_t t2 =
+                fmul2(f2pack(__uint_as_float(dp[j]), __uint_as_float(dp[j + 1])), scx2);
+            float d0, d1;
+            f2unpack(fmul2(f2pack(p[j], p[j + 1]), t2), d0, d1);
+            wp[j / 2] = bf16x2_rn(p[j], p[j + 1]);
+            wd[j / 2] = bf16x2_rn(d0, d1);
+          }
+          tmem_st16(tl + C::C_S + c * 16, wp);   // P^T pairs over read S^T columns
+          tmem_st16(tl + C::C_DP + c * 16, wd);  // dS^T pairs over read dP^T columns
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(bar(C::B_P + c));
         }
-        tmem_st16(tl + C::C_S + c * 16, wp);   // P^T pairs over read S^T columns
-        tmem_st16(tl + C::C_DP + c * 16, wd);  // dS^T pairs over read dP^T columns
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar(C::B_P + c));
       }
+      full = full_next;
     }
     if (ok) {
       ok = wait_bar(bar(C::B_O), 0u, abort_flag, &g_bwd_status, 0x66, lim);

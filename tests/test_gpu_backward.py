@@ -161,6 +161,41 @@ def test_backward_gqa_128k_sampled():
 
 
 @pytest.mark.slow
+def test_backward_gqa_128k_window_sampled_keys():
+    """gqa-128k at full size, causal with a 1024-key window: dQ on sampled
+    rows, and dK, dV on sampled keys, element by element against the
+    oracle.  Key k is seen only by queries [k, k + W), so the oracle needs
+    their LSE and D alone; the other rows' entries are NaN, which would
+    poison any result that used them.  Every key tile of the dK/dV kernel
+    walks 32 query tiles (8 per query head of its group)."""
+    w = inputs.WORKLOADS["gqa-128k"]
+    W = 1024
+    q, k, v = inputs.make_workload(w)
+    g = inputs.randn_chunked((w.N, w.heads, w.d), w.seed, 3).to(torch.bfloat16)
+    qd, kd, vd, gd = q.to(DEV), k.to(DEV), v.to(DEV), g.to(DEV)
+    out, lse = ra.ra_ring_forward_masked(qd, kd, vd, P=w.P, causal=True, window=W)
+    dq, dk, dv = ra.ra_ring_backward_masked(qd, kd, vd, out, lse, gd, P=w.P, causal=True,
+                                            window=W)
+    ra.ra_device_status()
+    c = w.c
+    keys = np.array([0, 1, c - 1, c, 3 * c + 777, 8 * c - 1, 8 * c, 11 * c + 4000,
+                     w.N - W - 1, w.N - 1], dtype=np.int64)
+    need = np.unique(np.concatenate([np.arange(kk, min(w.N, kk + W)) for kk in keys]))
+    dq_ref, lse_rows, d_rows = oracle.grad_q(q, k, v, g, causal=True, rows=need, window=W)
+    lse_all = np.full((w.N, w.heads), np.nan)
+    d_all = np.full((w.N, w.heads), np.nan)
+    lse_all[need] = lse_rows
+    d_all[need] = d_rows
+    dk_ref, dv_ref = oracle.grad_kv(q, k, v, g, lse_all, d_all, causal=True, keys=keys, window=W)
+    sel = torch.from_numpy(keys).to(DEV)
+    check_grad(dk.index_select(0, sel).cpu(), dk_ref, "dk")
+    check_grad(dv.index_select(0, sel).cpu(), dv_ref, "dv")
+    rows = need[::97]
+    check_grad(dq.index_select(0, torch.from_numpy(rows).to(DEV)).cpu(),
+               dq_ref[::97], "dq")
+
+
+@pytest.mark.slow
 def test_backward_mha_8k_window_and_documents():
     w = inputs.WORKLOADS["mha-8k"]
     run(w.N, w.P, w.heads, w.kv_heads, w.d, True, layout="zigzag", window=2000,
