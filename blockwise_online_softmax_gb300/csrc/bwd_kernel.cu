@@ -15,21 +15,27 @@
 //                       and walks the K/V tiles they may see.  S and dP go
 //                       to TMEM; the softmax warpgroup turns them into dS
 //                       (bf16, written over S); dQ += dS K reads dS from
-//                       TMEM.  dQ stays in TMEM for the whole block.
+//                       TMEM.  S is double-buffered, so the softmax of one
+//                       tile overlaps dQ of the previous tile and S of the
+//                       next.  dQ stays in TMEM for the whole block.
 //   bwd_dkdv_kernel<D>  K/V-stationary: a CTA owns 128 keys of one KV head
 //                       and walks the query tiles, of every query head of
-//                       its group, that may see them.  S^T and dP^T go to
-//                       TMEM; the softmax warpgroup writes P^T over S^T and
-//                       dS^T over dP^T; dV += P^T dO and dK += dS^T Q read
-//                       them from TMEM.  No atomics: in one launch each K/V
+//                       its group, that may see them.  S^T - lse sqrt(d)
+//                       and dP^T - D go to TMEM (the per-query terms enter
+//                       as one extra K-step of each product); the softmax
+//                       warpgroup writes P^T over S^T and dS^T over dP^T,
+//                       32 queries at a time, and dV += P^T dO and
+//                       dK += dS^T Q read each chunk from TMEM as soon as
+//                       it is written.  No atomics: in one launch each K/V
 //                       block belongs to one rank, each key tile to one CTA.
 // The accumulators (dQ, dK, dV, fp32) live in HBM between ring steps, like
 // the forward's (m, l, O~) state.  Masks and layouts are the forward's: a
 // per-row interval of allowed key rows.
 //
 // Roles (256 threads): warps 0-3 the softmax warpgroup (one thread per
-// TMEM lane), warp 4 the TMA producer, warp 5 the MMA issuer (it also owns
-// the TMEM allocation), warps 6-7 idle.  Every wait is bounded.
+// TMEM lane), warp 4 the TMA producer (K ring in the dQ kernel), warp 5 the
+// MMA issuer (it also owns the TMEM allocation), warp 6 the V producer of
+// the dQ kernel.  Every wait is bounded.
 #include <cmath>
 #include <cstdint>
 
