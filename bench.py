@@ -211,6 +211,49 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sms)}
 
 
+def timed_warmup(step, warmup, dev):
+    """Run the warm-up steps; return their mean wall time in seconds."""
+    import torch
+
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    return (time.time() - t0) / max(1, warmup)
+
+
+CLOCK_WINDOW_S = 1.0  # shortest sampled window: five nvidia-smi samples
+CLOCK_PAD_S = 0.5
+
+
+def clock_pad(step, dev, seconds):
+    """Untimed steps of the same workload for about `seconds` of wall time,
+    run inside the clock sampler's window just before and just after a
+    timed region shorter than CLOCK_WINDOW_S, so the samples see the GPU
+    under the same load as the timed steps."""
+    import torch
+
+    if seconds <= 0:
+        return
+    t_end = time.time() + seconds
+    while time.time() < t_end:
+        step()
+        torch.cuda.synchronize(dev)
+
+
+def pad_seconds(est_step_s, steps):
+    return CLOCK_PAD_S if est_step_s * steps < CLOCK_WINDOW_S else 0.0
+
+
+def note_window(clk, pad):
+    if clk is not None:
+        clk["window"] = ("timed region" if pad == 0 else
+                         f"timed region with {pad:.1f} s of untimed steps of the same workload "
+                         "on each side (region shorter than the sampling needs)")
+    return clk
+
+
 # ------------------------------------------------------------------ traffic record
 def kernel_digest() -> str:
     h = hashlib.sha256()
@@ -359,8 +402,8 @@ def run_decode(args, ws, rank, local):
     def step():
         ra.ra_decode_forward(qd, kd, vd, P=w.P, out=out, lse=lse, stream=stream)
 
-    for _ in range(args.warmup):
-        step()
+    est = timed_warmup(step, args.warmup, dev)
+    pad = pad_seconds(est, args.steps)
     ra.ra_device_status(stream)
     gpu_index = local
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
@@ -368,6 +411,7 @@ def run_decode(args, ws, rank, local):
         gpu_index = int(vis)
     clocks = ClockSampler(gpu_index, args.clock_log)
     clocks.start()
+    clock_pad(step, dev, pad)
     ra.ra_trace_reset()
     ra.ra_trace_enable(True)
     ev0 = torch.cuda.Event(enable_timing=True)
@@ -381,7 +425,8 @@ def run_decode(args, ws, rank, local):
     torch.cuda.synchronize(dev)
     barrier(ws)
     ra.ra_trace_enable(False)
-    clk = clocks.stop()
+    clock_pad(step, dev, pad)
+    clk = note_window(clocks.stop(), pad)
     ra.ra_device_status(stream)
     ms_step = reduce_max(ev0.elapsed_time(ev1), ws) / args.steps
     kinds = ("decode_split", "decode_combine", "merge", "finalize", "state_init")
@@ -466,8 +511,8 @@ def run_backward(args, w, ws, rank, local):
         ra.ra_ring_backward(qd, kd, vd, out, lse, gd, P=w.P, causal=w.causal, dq=dq, dk=dk,
                             dv=dv, stream=stream)
 
-    for _ in range(args.warmup):
-        step()
+    est = timed_warmup(step, args.warmup, dev)
+    pad = pad_seconds(est, args.steps)
     ra.ra_device_status(stream)
     gpu_index = local
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
@@ -475,6 +520,7 @@ def run_backward(args, w, ws, rank, local):
         gpu_index = int(vis)
     clocks = ClockSampler(gpu_index, args.clock_log)
     clocks.start()
+    clock_pad(step, dev, pad)
     ra.ra_trace_reset()
     ra.ra_trace_enable(True)
     ev0 = torch.cuda.Event(enable_timing=True)
@@ -488,7 +534,8 @@ def run_backward(args, w, ws, rank, local):
     torch.cuda.synchronize(dev)
     barrier(ws)
     ra.ra_trace_enable(False)
-    clk = clocks.stop()
+    clock_pad(step, dev, pad)
+    clk = note_window(clocks.stop(), pad)
     ra.ra_device_status(stream)
     ms_step = reduce_max(ev0.elapsed_time(ev1), ws) / args.steps
     trace = {kd_: ra.ra_trace_query(kd_) for kd_ in ("bwd_pre", "bwd_dq", "bwd_dkdv")}
@@ -607,8 +654,8 @@ def run_ours(args, w, ws, rank, local):
                                       window=mask.window, n_valid=mask.n_valid, cu_seqlens=cu,
                                       out=out, lse=lse, stream=stream)
 
-    for _ in range(args.warmup):
-        step()
+    est = timed_warmup(step, args.warmup, dev)
+    pad = pad_seconds(est, args.steps)
     ra.ra_device_status(stream)
     torch.cuda.synchronize(dev)
     barrier(ws)
@@ -619,6 +666,7 @@ def run_ours(args, w, ws, rank, local):
         gpu_index = int(vis)
     clocks = ClockSampler(gpu_index, args.clock_log)
     clocks.start()
+    clock_pad(step, dev, pad)
     ra.ra_trace_reset()
     ra.ra_trace_enable(True)
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
@@ -631,7 +679,8 @@ def run_ours(args, w, ws, rank, local):
     torch.cuda.synchronize(dev)
     barrier(ws)
     ra.ra_trace_enable(False)
-    clk = clocks.stop()
+    clock_pad(step, dev, pad)
+    clk = note_window(clocks.stop(), pad)
     ra.ra_device_status(stream)
     ms_total = evs[0].elapsed_time(evs[-1])
     per_step = [evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps)]
