@@ -263,10 +263,11 @@ def kernel_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
-    """DRAM bytes per block-update launch from the committed ncu summary, if
-    it was taken on the current kernel source (digest match), else None."""
-    p = os.path.join(ROOT, "profiles", "block_update_bf16_traffic.md")
+def recorded_traffic(workload: str, profile: str = "block_update_bf16_traffic.md"):
+    """DRAM bytes per launch of the dominant kernel from its committed ncu
+    summary, if it was taken on the current kernel source (digest match),
+    else None."""
+    p = os.path.join(ROOT, "profiles", profile)
     try:
         text = open(p).read()
     except OSError:
@@ -686,9 +687,18 @@ def run_ours(args, w, ws, rank, local):
     per_step = [evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps)]
     n_upd, ms_upd = ra.ra_trace_query("block_update_bf16" if w.dtype == "bf16"
                                       else "block_update_f32")
+    n_fz, ms_fz = ra.ra_trace_query("ring_fused_bf16")
     n_init, ms_init = ra.ra_trace_query("state_init")
     n_fin, ms_fin = ra.ra_trace_query("finalize")
     ra.ra_trace_reset()
+    # The dominant kernel: the fused ring (bf16, one launch per forward) or
+    # the one-step block update (fp32, P launches per forward).
+    if n_fz > 0:
+        dom_ms, dom_name, dom_profile = ms_fz, "fused ring forward (tcgen05)", \
+            "ring_fused_bf16_traffic.md"
+    else:
+        dom_ms, dom_name, dom_profile = ms_upd, "block update (tcgen05)", \
+            "block_update_bf16_traffic.md"
 
     ms_max = reduce_max(ms_total, ws)
     ms_step = ms_max / args.steps
@@ -699,11 +709,11 @@ def run_ours(args, w, ws, rank, local):
         f_adj = f_exact = 4.0 * w.d * w.heads * mask.pairs
     value = ws * f_adj / (ms_step * 1e-3) / 1e12
 
-    # roofline of the dominant kernel (block update): algorithmic FLOPs of
-    # all its launches (exact allowed-pair count) over their summed time.
-    achieved = (f_exact * args.steps) / (ms_upd * 1e-3) / 1e12 if ms_upd > 0 else None
+    # roofline of the dominant kernel: algorithmic FLOPs of all its launches
+    # (exact allowed-pair count) over their summed time.
+    achieved = (f_exact * args.steps) / (dom_ms * 1e-3) / 1e12 if dom_ms > 0 else None
     peak = peaks["bf16_tflops_sustained"]
-    traffic = recorded_traffic(w.name)
+    traffic = recorded_traffic(w.name, dom_profile)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -730,13 +740,14 @@ def run_ours(args, w, ws, rank, local):
                            "recipe": w.recipe, "seed": w.seed, "mask": mask.describe(),
                            "parallelism": f"replicas{ws}", "flops_per_step": f_adj,
                            "l2": "inputs larger than L2 (Q alone exceeds 129 MB); no flush"},
-                "clocks": clk, "e2e": None, "gpu_launches": n_upd + n_init + n_fin,
-                "kernel_ms": {"block_update": ms_upd / args.steps,
+                "clocks": clk, "e2e": None, "gpu_launches": n_upd + n_fz + n_init + n_fin,
+                "kernel_ms": {"ring_fused": ms_fz / args.steps,
+                              "block_update": ms_upd / args.steps,
                               "state_init": ms_init / args.steps,
                               "finalize": ms_fin / args.steps},
                 "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
                              "unit": "TFLOP/s", "frac": (achieved / peak) if achieved else None,
-                             "traffic": None, "kernel": "block update (tcgen05)",
+                             "traffic": None, "kernel": dom_name,
                              "peak_kind": f"bf16_tflops_sustained ({peak_src})"},
                 "cpu_baseline": cpu,
             }
@@ -746,7 +757,7 @@ def run_ours(args, w, ws, rank, local):
     if w.dtype == "bf16":
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": (achieved / peak) if achieved else None, "traffic": traffic,
-                "kernel": "block update (tcgen05)",
+                "kernel": dom_name,
                 "peak_kind": f"bf16_tflops_sustained ({peak_src})",
                 "frac_of_burst": (achieved / peaks["bf16_tflops"]) if achieved else None}
     else:
@@ -806,8 +817,9 @@ def run_ours(args, w, ws, rank, local):
         "clocks": clk,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-        "gpu_launches": n_upd + n_init + n_fin,
-        "kernel_ms": {"block_update": ms_upd / args.steps, "state_init": ms_init / args.steps,
+        "gpu_launches": n_upd + n_fz + n_init + n_fin,
+        "kernel_ms": {"ring_fused": ms_fz / args.steps,
+                      "block_update": ms_upd / args.steps, "state_init": ms_init / args.steps,
                       "finalize": ms_fin / args.steps},
         "roofline": roof,
         "cpu_baseline": cpu,

@@ -37,6 +37,7 @@ KERNEL_KINDS = {
     "bwd_pre": 7,
     "bwd_dq": 8,
     "bwd_dkdv": 9,
+    "ring_fused_bf16": 10,
 }
 
 _lock = threading.Lock()

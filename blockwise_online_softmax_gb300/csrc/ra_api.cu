@@ -352,9 +352,50 @@ int ring_step_impl(const void* q, const void* k, const void* v, float* m, float*
   return run_update(a, d, dtype, st);
 }
 
+// The bf16 ring in one launch: every rank's state stays on chip for all P
+// steps, and the kernel writes out and lse itself (no scratch, no init or
+// finalize launch).
+constexpr int kFusedMaxSteps = 256;
+
+int ring_fused_impl(const void* q, const void* k, const void* v, float* out, float* lse,
+                    long long N, int P, const MaskSpec& mk, int d, int heads, int kv_heads,
+                    cudaStream_t st) {
+  ra::FwdArgs a{};
+  a.q = q; a.k = k; a.v = v; a.o = out; a.m = lse; a.l = nullptr;
+  a.cq = N / P;
+  a.ck = N / P;
+  a.q_rows = N;
+  a.kv_rows = N;
+  a.heads = heads;
+  a.kv_heads = kv_heads;
+  a.mode = 1;
+  a.P = P;
+  a.s = 0;
+  a.i0 = 0;
+  a.nwork = P;
+  put_mask(a, mk);
+  a.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
+  a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+  a.wait_limit = kWaitLimit;
+  if (a.cq == 0) return RA_OK;
+  int rc = get_encoder();
+  if (rc != RA_OK) return rc;
+  CUtensorMap tq, tk, tv;
+  if ((rc = encode_map(&tq, q, N, heads, d)) != RA_OK) return rc;
+  if ((rc = encode_map(&tk, k, N, kv_heads, d)) != RA_OK) return rc;
+  if ((rc = encode_map(&tv, v, N, kv_heads, d)) != RA_OK) return rc;
+  TraceScope ts(RA_KERNEL_RING_FUSED_BF16, st);
+  cudaError_t e = ra::launch_umma_ring(a, d, tq, tk, tv, st);
+  ts.done(e == cudaSuccess);
+  if (e != cudaSuccess) return cuda_fail(e, "fused ring launch");
+  return RA_OK;
+}
+
 int ring_forward_impl(const void* q, const void* k, const void* v, float* out, float* lse,
                       long long N, int P, const MaskSpec& mk, int d, int heads, int kv_heads,
                       int dtype, cudaStream_t st, float* l_scratch) {
+  if (dtype == RA_BF16 && P <= kFusedMaxSteps)
+    return ring_fused_impl(q, k, v, out, lse, N, P, mk, d, heads, kv_heads, st);
   const long long rows = N;
   TraceScope t0(RA_KERNEL_STATE_INIT, st);
   cudaError_t e = ra::launch_state_init(lse, l_scratch, out, rows, heads, d, st);
@@ -378,14 +419,16 @@ MaskSpec plain_mask(int causal) {
   return mk;
 }
 
-// ra_ring_forward and ra_ring_forward_masked: l scratch from the stream's
-// pool allocator.
+// ra_ring_forward and ra_ring_forward_masked: the fused launch for bf16,
+// else the step loop with the l scratch from the stream's pool allocator.
 int ring_forward_alloc(const void* q, const void* k, const void* v, float* out, float* lse,
                        long long N, int P, const MaskSpec& mk, int d, int heads, int kv_heads,
                        int dtype, void* stream) {
   int rc;
   if ((rc = check_ptrs({q, k, v, out, lse})) != RA_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (dtype == RA_BF16 && P <= kFusedMaxSteps)
+    return ring_fused_impl(q, k, v, out, lse, N, P, mk, d, heads, kv_heads, st);
   float* l_scratch = nullptr;
   const size_t l_bytes = static_cast<size_t>(N) * heads * sizeof(float);
   cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&l_scratch), l_bytes, st);
@@ -816,11 +859,16 @@ int ra_ring_forward_noalloc(const void* q, const void* k, const void* v, float* 
   if (rc != RA_OK) return rc;
   if (N == 0) return RA_OK;
   if ((rc = check_ptrs({q, k, v, out, lse})) != RA_OK) return rc;
+  // The documented limit holds for every dtype and is checked before any
+  // launch, although the bf16 ring (one fused launch) needs no scratch.
   if (N * heads > kNoAllocMaxRowsHeads)
     return fail(RA_ERR_UNSUPPORTED,
                 "N * heads = %lld exceeds the fixed scratch of ra_ring_forward_noalloc (%lld "
                 "rows x heads); use ra_ring_forward",
                 N * heads, kNoAllocMaxRowsHeads);
+  if (dtype == RA_BF16 && P <= kFusedMaxSteps)
+    return ring_fused_impl(q, k, v, out, lse, N, P, plain_mask(causal), d, heads, kv_heads,
+                           static_cast<cudaStream_t>(stream));
   float* l_scratch = nullptr;
   if ((rc = noalloc_scratch(&l_scratch)) != RA_OK) return rc;
   // The state-init kernel zeroes the l rows this call uses, so whatever a

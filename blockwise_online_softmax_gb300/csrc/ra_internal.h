@@ -250,6 +250,10 @@ cudaError_t launch_finalize(const float* m, const float* l, const float* o, floa
 cudaError_t launch_simt_update(const FwdArgs& a, int d, cudaStream_t st);
 cudaError_t launch_umma_update(const FwdArgs& a, int d, const CUtensorMap& tq,
                                const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st);
+// The whole ring forward of every rank in one launch (bf16): a.o is the
+// output [rows, heads, d] and a.m the LSE [rows, heads]; a.l is unused.
+cudaError_t launch_umma_ring(const FwdArgs& a, int d, const CUtensorMap& tq,
+                             const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st);
 cudaError_t launch_wait_selftest(long long limit_cycles, cudaStream_t st);
 cudaError_t launch_decode_tc(const DecArgs& a, int d, const CUtensorMap& tq, const CUtensorMap& tk,
                              const CUtensorMap& tv, cudaStream_t st);

@@ -340,6 +340,117 @@ __device__ __forceinline__ void control_roles(const FwdArgs& a, const Work& wk, 
   }
 }
 
+// One K/V tile of one softmax row (TMEM lane): wait for S (barrier b_s,
+// phase parity `parity`), mask the keys outside [row_lo, row_hi) on tiles
+// that cut that interval (tiles full_0 .. full_0 + n_full - 1 need no mask),
+// move the row max, rescale O~ in TMEM when it moved, write P over S and
+// arrive on b_p.  The running state is m_used / m_true (log2 units) and
+// l_run.  Returns false after an abort.
+template <int D>
+__device__ __forceinline__ bool softmax_tile(uint32_t tl, uint32_t s_col, uint32_t o_col, int t,
+                                             int row_lo, int row_hi, int full_0, int n_full,
+                                             float sl2, uint64_t sl2x2, uint32_t b_s,
+                                             uint32_t b_p, uint32_t parity,
+                                             volatile int* abort_flag, long long lim,
+                                             float& m_used, float& m_true, bool& m_moved,
+                                             float& l_run) {
+  bool ok = wait_bar(b_s, parity, abort_flag, &g_umma_status, 0x31, lim);
+  ok = __all_sync(0xffffffffu, ok);
+  if (!ok) return false;
+  tc_fence_after();
+  // S row: 128 fp32 scores, loaded once into registers.
+  uint32_t sr[BN / 32][32];
+#pragma unroll
+  for (int cc = 0; cc < BN / 32; ++cc) tmem_ld32(tl + s_col + cc * 32, sr[cc]);
+  tmem_wait_ld();
+#pragma unroll
+  for (int cc = 0; cc < BN / 32; ++cc) reg_fence32(sr[cc]);
+#define RA_S(j) __uint_as_float(sr[(j) >> 5][(j) & 31])
+  // Mask: key j of this tile is allowed iff lo_j <= j < hi_j.
+  if (static_cast<unsigned>(t - full_0) >= static_cast<unsigned>(n_full)) {
+    const int lo_j = row_lo - t * BN, hi_j = row_hi - t * BN;
+#pragma unroll
+    for (int j = 0; j < BN; ++j)
+      if (j < lo_j || j >= hi_j) sr[j >> 5][j & 31] = 0xff800000u;  // -inf
+  }
+  // Row max: four independent chains over columns 0..127, two new
+  // values per three-input max.
+  float mx0 = fmaxf(RA_S(0), RA_S(4)), mx1 = fmaxf(RA_S(1), RA_S(5));
+  float mx2 = fmaxf(RA_S(2), RA_S(6)), mx3 = fmaxf(RA_S(3), RA_S(7));
+#pragma unroll
+  for (int j = 8; j < BN; j += 8) {
+    mx0 = fmax3(mx0, RA_S(j + 0), RA_S(j + 4));
+    mx1 = fmax3(mx1, RA_S(j + 1), RA_S(j + 5));
+    mx2 = fmax3(mx2, RA_S(j + 2), RA_S(j + 6));
+    mx3 = fmax3(mx3, RA_S(j + 3), RA_S(j + 7));
+  }
+  static_assert(BN % 8 == 0, "the max loop covers columns in groups of 8");
+  const float m_tile = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
+  if (m_tile > m_true) {
+    m_true = m_tile;
+    m_moved = true;
+  }
+  const bool need = m_true > m_used + RESCALE_THRESHOLD;
+  float alpha = 1.f;
+  if (need) {
+    alpha = ex2(m_used - m_true);  // m_used = -inf gives 0
+    m_used = m_true;
+  }
+  // O~_g is stable here: S_g(t) comes from QK_g(t), which the MMA thread
+  // issued after PV_g(t-1), and the commit that signalled S_g(t)
+  // covers every earlier MMA.  Rescale it before any of P_g(t) is
+  // published, since PV_g(t) accumulates on top.
+  if (__any_sync(0xffffffffu, need)) {
+    // 32 columns at a time: the S row still occupies 128 registers.
+    const uint64_t al2 = f2pack(alpha, alpha);
+#pragma unroll
+    for (int cc = 0; cc < D / 32; ++cc) {
+      uint32_t r[32];
+      tmem_ld32(tl + o_col + cc * 32, r);
+      tmem_wait_ld();
+      reg_fence32(r);
+#pragma unroll
+      for (int j = 0; j < 32; j += 2) {
+        float y0, y1;
+        f2unpack(fmul2(f2pack(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), al2), y0,
+                 y1);
+        r[j] = __float_as_uint(y0);
+        r[j + 1] = __float_as_uint(y1);
+      }
+      tmem_st32(tl + o_col + cc * 32, r);
+    }
+  }
+  const float mref = (m_used == -INFINITY) ? 0.f : m_used;
+  const uint64_t nmref2 = f2pack(-mref, -mref);
+  // P = 2^(s * log2(e)/sqrt(d) - m), two lanes per FFMA2; row sum in
+  // two FADD2 accumulators; P rounded to bf16 in pairs, written over
+  // the first half of the same registers.
+  uint64_t acc0 = f2pack(0.f, 0.f), acc1 = acc0;
+#pragma unroll
+  for (int j = 0; j < BN; j += 4) {
+    float x0, x1, x2, x3;
+    f2unpack(ffma2(f2pack(RA_S(j), RA_S(j + 1)), sl2x2, nmref2), x0, x1);
+    f2unpack(ffma2(f2pack(RA_S(j + 2), RA_S(j + 3)), sl2x2, nmref2), x2, x3);
+    const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
+    acc0 = fadd2(acc0, f2pack(p0, p1));
+    acc1 = fadd2(acc1, f2pack(p2, p3));
+    // pair k = j/2 goes to word k; k < j, so the scores it overwrites
+    // have already been read.
+    sr[(j / 2) >> 5][(j / 2) & 31] = bf16x2_rn(p0, p1);
+    sr[(j / 2 + 1) >> 5][(j / 2 + 1) & 31] = bf16x2_rn(p2, p3);
+  }
+  tmem_st32(tl + s_col, sr[0]);
+  tmem_st32(tl + s_col + 32, sr[1]);
+  tmem_wait_st();
+  tc_fence_before();
+  mbar_arrive(b_p);
+#undef RA_S
+  float sa, sb;
+  f2unpack(fadd2(acc0, acc1), sa, sb);
+  l_run = l_run * alpha + (sa + sb);
+  return true;
+}
+
 // Softmax groups: warps 0..3 own the rows of Q0, warps 4..7 those of Q1.
 template <int D>
 __device__ __forceinline__ void softmax_role(const FwdArgs& a, const Work& wk, long long row0,
@@ -414,101 +525,11 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, const Work& wk, l
       bool ok = true;
 
       for (int t = t_first; t < t_end; ++t) {
-        ok = wait_bar(bar(C::B_SF + g), static_cast<uint32_t>(t - t_first) & 1u, abort_flag,
-                      &g_umma_status, 0x31, lim);
-        ok = __all_sync(0xffffffffu, ok);
+        ok = softmax_tile<D>(tl, s_col, o_col, t, row_lo, row_hi, full_0, n_full, sl2, sl2x2,
+                             bar(C::B_SF + g), bar(C::B_PF + g),
+                             static_cast<uint32_t>(t - t_first) & 1u, abort_flag, lim, m_used,
+                             m_true, m_moved, l_run);
         if (!ok) break;
-        tc_fence_after();
-        // S row: 128 fp32 scores, loaded once into registers.
-        uint32_t sr[BN / 32][32];
-#pragma unroll
-        for (int cc = 0; cc < BN / 32; ++cc) tmem_ld32(tl + s_col + cc * 32, sr[cc]);
-        tmem_wait_ld();
-#pragma unroll
-        for (int cc = 0; cc < BN / 32; ++cc) reg_fence32(sr[cc]);
-#define RA_S(j) __uint_as_float(sr[(j) >> 5][(j) & 31])
-        // Mask: key j of this tile is allowed iff lo_j <= j < hi_j.
-        if (static_cast<unsigned>(t - full_0) >= static_cast<unsigned>(n_full)) {
-          const int lo_j = row_lo - t * BN, hi_j = row_hi - t * BN;
-#pragma unroll
-          for (int j = 0; j < BN; ++j)
-            if (j < lo_j || j >= hi_j) sr[j >> 5][j & 31] = 0xff800000u;  // -inf
-        }
-        // Row max: four independent chains over columns 0..127, two new
-        // values per three-input max.
-        float mx0 = fmaxf(RA_S(0), RA_S(4)), mx1 = fmaxf(RA_S(1), RA_S(5));
-        float mx2 = fmaxf(RA_S(2), RA_S(6)), mx3 = fmaxf(RA_S(3), RA_S(7));
-#pragma unroll
-        for (int j = 8; j < BN; j += 8) {
-          mx0 = fmax3(mx0, RA_S(j + 0), RA_S(j + 4));
-          mx1 = fmax3(mx1, RA_S(j + 1), RA_S(j + 5));
-          mx2 = fmax3(mx2, RA_S(j + 2), RA_S(j + 6));
-          mx3 = fmax3(mx3, RA_S(j + 3), RA_S(j + 7));
-        }
-        static_assert(BN % 8 == 0, "the max loop covers columns in groups of 8");
-        const float m_tile = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
-        if (m_tile > m_true) {
-          m_true = m_tile;
-          m_moved = true;
-        }
-        const bool need = m_true > m_used + RESCALE_THRESHOLD;
-        float alpha = 1.f;
-        if (need) {
-          alpha = ex2(m_used - m_true);  // m_used = -inf gives 0
-          m_used = m_true;
-        }
-        // O~_g is stable here: S_g(t) comes from QK_g(t), which the MMA thread
-        // issued after PV_g(t-1), and the commit that signalled S_g(t)
-        // covers every earlier MMA.  Rescale it before any of P_g(t) is
-        // published, since PV_g(t) accumulates on top.
-        if (__any_sync(0xffffffffu, need)) {
-          // 32 columns at a time: the S row still occupies 128 registers.
-          const uint64_t al2 = f2pack(alpha, alpha);
-#pragma unroll
-          for (int cc = 0; cc < D / 32; ++cc) {
-            uint32_t r[32];
-            tmem_ld32(tl + o_col + cc * 32, r);
-            tmem_wait_ld();
-            reg_fence32(r);
-#pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              float y0, y1;
-              f2unpack(fmul2(f2pack(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), al2), y0,
-                       y1);
-              r[j] = __float_as_uint(y0);
-              r[j + 1] = __float_as_uint(y1);
-            }
-            tmem_st32(tl + o_col + cc * 32, r);
-          }
-        }
-        const float mref = (m_used == -INFINITY) ? 0.f : m_used;
-        const uint64_t nmref2 = f2pack(-mref, -mref);
-        // P = 2^(s * log2(e)/sqrt(d) - m), two lanes per FFMA2; row sum in
-        // two FADD2 accumulators; P rounded to bf16 in pairs, written over
-        // the first half of the same registers.
-        uint64_t acc0 = f2pack(0.f, 0.f), acc1 = acc0;
-#pragma unroll
-        for (int j = 0; j < BN; j += 4) {
-          float x0, x1, x2, x3;
-          f2unpack(ffma2(f2pack(RA_S(j), RA_S(j + 1)), sl2x2, nmref2), x0, x1);
-          f2unpack(ffma2(f2pack(RA_S(j + 2), RA_S(j + 3)), sl2x2, nmref2), x2, x3);
-          const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
-          acc0 = fadd2(acc0, f2pack(p0, p1));
-          acc1 = fadd2(acc1, f2pack(p2, p3));
-          // pair k = j/2 goes to word k; k < j, so the scores it overwrites
-          // have already been read.
-          sr[(j / 2) >> 5][(j / 2) & 31] = bf16x2_rn(p0, p1);
-          sr[(j / 2 + 1) >> 5][(j / 2 + 1) & 31] = bf16x2_rn(p2, p3);
-        }
-        tmem_st32(tl + s_col, sr[0]);
-        tmem_st32(tl + s_col + 32, sr[1]);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar(C::B_PF + g));
-#undef RA_S
-        float sa, sb;
-        f2unpack(fadd2(acc0, acc1), sa, sb);
-        l_run = l_run * alpha + (sa + sb);
       }
 
       if (ok) {
@@ -624,6 +645,462 @@ umma_update_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   }
 }
 
+// ====================================================================== fused ring
+// One launch runs the whole ring ("Ring Attention Paper Breakdown", section
+// 2: Q_i stays while the K/V blocks j = (i - s) mod P, s = 0 .. P-1, come
+// by).  A CTA owns 256 query rows of one head of block i and keeps them,
+// and their running state (m, l, O~), on chip for every step: the state
+// lives in registers and TMEM from the first K/V tile to the last, and the
+// CTA finalizes at the end (O = O~ / l, LSE).  The ring hop is the producer
+// moving on to the next block's rows: its first tiles load into the same
+// stage ring while the tensor pipe works on the previous block's last ones.
+// Every role walks the same visit: the steps in ring order, within a step
+// the union of the two query tiles' key-tile ranges (as in the one-step
+// kernel), skipping steps whose pair has no allowed key.
+
+// Rank i at ring step s: the same work item as the one-step launch.
+__device__ __forceinline__ Work ring_work(const FwdArgs& a, int i, int s) {
+  Work wk;
+  const int j = (i - s + a.P) % a.P;
+  wk.q_base = static_cast<long long>(i) * a.cq;
+  wk.kv_base = static_cast<long long>(j) * a.ck;
+  wk.state_base = wk.q_base;
+  wk.qmap = PosMap{a.layout, a.P, a.cq, i, wk.q_base};
+  wk.kmap = PosMap{a.layout, a.P, a.ck, j, wk.kv_base};
+  return wk;
+}
+
+// The visit of one step: the union of the groups' tile ranges, where each
+// group's run starts in it (ks) and its length (ne), and the K/V block's
+// first row.
+struct StepVisit {
+  long long kv_base;
+  TileSeq seq;
+  int ta[NQ], tb[NQ];  // the groups' tile ranges within the K/V block
+  int ks[NQ], ne[NQ];
+};
+
+// Steps of one fused launch at most (the visit table is in shared memory).
+constexpr int kRingMaxSteps = 256;
+
+__device__ __forceinline__ StepVisit step_visit(const FwdArgs& a, int i, int s, long long row0,
+                                                long long vb) {
+  const Work wk = ring_work(a, i, s);
+  int ta[NQ], tb[NQ];
+#pragma unroll
+  for (int g = 0; g < NQ; ++g)
+    tile_range(a, wk, row0 + g * BM, row0 + (g + 1) * BM, vb, BN, &ta[g], &tb[g]);
+  StepVisit v;
+  v.seq = make_seq(ta, tb);
+#pragma unroll
+  for (int g = 0; g < NQ; ++g) {
+    v.ta[g] = ta[g];
+    v.tb[g] = tb[g];
+    v.ne[g] = tb[g] > ta[g] ? tb[g] - ta[g] : 0;
+    v.ks[g] = ta[g] < v.seq.a0 + v.seq.na ? ta[g] - v.seq.a0 : v.seq.na + (ta[g] - v.seq.b0);
+  }
+  v.kv_base = wk.kv_base;
+  return v;
+}
+
+// The first step at or after s whose visit (in the table) is not empty, or
+// P if none.
+__device__ __forceinline__ int next_step(const StepVisit* rec, int P, int s) {
+  while (s < P && rec[s].seq.n == 0) ++s;
+  return s;
+}
+
+// Slot-ring producer over the whole visit: slot c takes visit tile c (K,
+// v_lag = 0) or c - 1 (V, v_lag = 1); a slot without a tile is a plain
+// arrival (slot 0 for V, the slot after the last tile for K).  Returns false
+// on an abort, after draining (bounded) the copies still in flight.
+template <int D, int NS>
+__device__ __forceinline__ bool produce_ring(const FwdArgs& a, const StepVisit* rec, int kh,
+                                             uint32_t sbase, uint32_t b_full,
+                                             uint32_t b_empty, const CUtensorMap* tm, int v_lag,
+                                             volatile int* abort_flag, int code, long long lim) {
+  using C = Cfg<D>;
+  tma_prefetch_desc(tm);
+  int c = 0;
+  auto fill = [&](long long kv_row, bool tile) -> bool {
+    const int st = c % NS;
+    if (c >= NS &&
+        !wait_bar(b_empty + 8u * st, (static_cast<uint32_t>(c / NS) & 1u) ^ 1u, abort_flag,
+                  &g_umma_status, code, lim))
+      return false;
+    if (tile) {
+      mbar_arrive_expect_tx(b_full + 8u * st, C::TILE_BYTES);
+#pragma unroll
+      for (int ch = 0; ch < C::NCH; ++ch)
+        tma_load_3d(sbase + st * C::TILE_BYTES + ch * CHUNK_BYTES, tm, b_full + 8u * st, ch * 64,
+                    kh, static_cast<int>(kv_row));
+    } else {
+      mbar_arrive(b_full + 8u * st);
+    }
+    ++c;
+    return true;
+  };
+  bool ok = true;
+  if (v_lag) ok = fill(0, false);
+  for (int s = next_step(rec, a.P, 0); s < a.P && ok; s = next_step(rec, a.P, s + 1)) {
+    const TileSeq seq = rec[s].seq;
+    const long long kv_base = rec[s].kv_base;
+    for (int k = 0; k < seq.n && ok; ++k)
+      ok = fill(kv_base + static_cast<long long>(seq.at(k)) * BN, true);
+  }
+  if (ok && !v_lag) ok = fill(0, false);
+  if (!ok) {
+    volatile int no_abort = 0;
+    for (int x = (c > NS ? c - NS : 0); x < c; ++x)
+      wait_bar(b_full + 8u * (x % NS), static_cast<uint32_t>(x / NS) & 1u, &no_abort, nullptr, 0,
+               lim);
+  }
+  return ok;
+}
+
+// Producers (warps 8 and 10) and MMA issuer (warp 9) of the fused ring; the
+// visit is not empty (the kernel returns early otherwise).
+template <int D>
+__device__ __forceinline__ void ring_control_roles(const FwdArgs& a, const StepVisit* rec, int i,
+                                                   long long row0, uint32_t tmem, uint32_t sQ,
+                                                   uint32_t sK, uint32_t sV, uint32_t bar0,
+                                                   volatile int* abort_flag,
+                                                   const CUtensorMap* tmQ,
+                                                   const CUtensorMap* tmK,
+                                                   const CUtensorMap* tmV) {
+  using C = Cfg<D>;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int h = blockIdx.y;
+  const int kh = h / (a.heads / a.kv_heads);
+  const long long lim = a.wait_limit;
+  auto bar = [&](int x) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(x); };
+  if (warp == 8 || warp == 10) {
+    // ------------------------------------------------------------ producers
+    if (lane == 0) {
+      if (warp == 8) {
+        tma_prefetch_desc(tmQ);
+        mbar_arrive_expect_tx(bar(C::B_Q), NQ * C::TILE_BYTES);
+#pragma unroll
+        for (int g = 0; g < NQ; ++g) {
+          const int q_row = static_cast<int>(static_cast<long long>(i) * a.cq + row0 + g * BM);
+#pragma unroll
+          for (int ch = 0; ch < C::NCH; ++ch)
+            tma_load_3d(sQ + g * C::TILE_BYTES + ch * CHUNK_BYTES, tmQ, bar(C::B_Q), ch * 64, h,
+                        q_row);
+        }
+        if (!produce_ring<D, C::NSK>(a, rec, kh, sK, bar(C::B_KF), bar(C::B_KE), tmK, 0,
+                                     abort_flag, 0x11, lim)) {
+          volatile int no_abort = 0;
+          wait_bar(bar(C::B_Q), 0, &no_abort, nullptr, 0, lim);
+        }
+      } else {
+        produce_ring<D, C::NSK>(a, rec, kh, sV, bar(C::B_KF), bar(C::B_KE), tmV, 1, abort_flag,
+                                0x12, lim);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    // As in the one-step kernel, with the visit index K running over every
+    // step: slot K + 1 holds V(K) and K(K + 1).  At the last tile of a step
+    // the look-ahead QK is the next step's first tile, whose groups are
+    // known from the next step's visit, computed when the step begins.
+    const uint32_t lead = lane == 0 ? 1u : 0u;
+    constexpr uint32_t idesc_qk = idesc_bf16(BM, BN, 0);
+    constexpr uint32_t idesc_pv = idesc_bf16(BM, D, 1);
+    const uint64_t qdesc = sdesc_sw128(sQ, 16, 1024);
+    const uint64_t kdesc = sdesc_sw128(sK, 16, 1024);
+    const uint64_t vdesc = sdesc_sw128(sV, CHUNK_BYTES, 1024);
+    constexpr uint64_t TILE16 = C::TILE_BYTES >> 4;
+    auto qk = [&](int g, int sk) {
+      const uint32_t d_tmem = tmem + C::S_COL + static_cast<uint32_t>(g) * BN;
+      const uint64_t a0 = qdesc + static_cast<uint64_t>(g) * TILE16;
+      const uint64_t b0 = kdesc + static_cast<uint64_t>(sk) * TILE16;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t off = ((kk >> 2) * CHUNK_BYTES + (kk & 3) * 32) >> 4;
+        mma_ss_lead(lead, d_tmem, a0 + off, b0 + off, idesc_qk, kk > 0 ? 1u : 0u);
+      }
+      tc_commit_lead(lead, bar(C::B_SF + g));
+    };
+    auto pv = [&](int g, int sv) {
+      const uint32_t p_tmem = tmem + C::S_COL + static_cast<uint32_t>(g) * BN;
+      const uint32_t o_tmem = tmem + C::O_COL + static_cast<uint32_t>(g) * D;
+      const uint64_t b0 = vdesc + static_cast<uint64_t>(sv) * TILE16;
+#pragma unroll
+      for (int kk = 0; kk < BN / 16; ++kk)
+        mma_ts_lead(lead, o_tmem, p_tmem + kk * 8, b0 + static_cast<uint64_t>((kk * 2048) >> 4),
+                    idesc_pv, 1u);
+    };
+    // The current step's visit in registers; of the next non-empty step
+    // only which groups its first tile has.
+    int s_cur = next_step(rec, a.P, 0);
+    int s_nxt = next_step(rec, a.P, s_cur + 1);
+    TileSeq seq = rec[s_cur].seq;
+    int ks[NQ], ne[NQ];
+#pragma unroll
+    for (int g = 0; g < NQ; ++g) {
+      ks[g] = rec[s_cur].ks[g];
+      ne[g] = rec[s_cur].ne[g];
+    }
+    bool ok = wait_bar(bar(C::B_Q), 0, abort_flag, &g_umma_status, 0x21, lim);
+    if (ok) ok = wait_bar(bar(C::B_KF), 0, abort_flag, &g_umma_status, 0x22, lim);
+    if (ok) {
+      tc_fence_after();
+      if (ks[0] == 0 && ne[0] > 0) qk(0, 0);
+      if (ks[1] == 0 && ne[1] > 0) qk(1, 0);
+      tc_commit_lead(lead, bar(C::B_KE));
+    }
+    int K = 0;            // visit index over all steps
+    int cnt[NQ] = {0, 0};  // tiles of each group so far (its P barrier's phase)
+    while (ok) {
+      bool nx[NQ];
+#pragma unroll
+      for (int g = 0; g < NQ; ++g)
+        nx[g] = s_nxt < a.P && rec[s_nxt].ks[g] == 0 && rec[s_nxt].ne[g] > 0;
+      for (int k = 0; k < seq.n && ok; ++k, ++K) {
+        const int sv = (K + 1) % C::NSK;  // slot K + 1: V(K) and K(K + 1)
+        ok = wait_bar(bar(C::B_KF + sv), static_cast<uint32_t>((K + 1) / C::NSK) & 1u, abort_flag,
+                      &g_umma_status, 0x24, lim);
+        if (!ok) break;
+        const bool last = k + 1 == seq.n;
+#pragma unroll
+        for (int g = 0; g < NQ; ++g) {
+          const int kg = k - ks[g];
+          if (static_cast<unsigned>(kg) < static_cast<unsigned>(ne[g])) {
+            ok = wait_bar(bar(C::B_PF + g), static_cast<uint32_t>(cnt[g]) & 1u, abort_flag,
+                          &g_umma_status, 0x23, lim);
+            if (!ok) break;
+            ++cnt[g];
+            tc_fence_after();
+            pv(g, sv);
+          }
+          const bool qn =
+              last ? nx[g] : static_cast<unsigned>(kg + 1) < static_cast<unsigned>(ne[g]);
+          if (qn) qk(g, sv);
+        }
+        if (!ok) break;
+        tc_commit_lead(lead, bar(C::B_KE + sv));
+      }
+      if (!ok || s_nxt >= a.P) break;
+      s_cur = s_nxt;
+      s_nxt = next_step(rec, a.P, s_cur + 1);
+      seq = rec[s_cur].seq;
+#pragma unroll
+      for (int g = 0; g < NQ; ++g) {
+        ks[g] = rec[s_cur].ks[g];
+        ne[g] = rec[s_cur].ne[g];
+      }
+    }
+    if (ok) {
+      // Both groups' epilogues wait for the last products of the visit.
+      tc_commit_lead(lead, bar(C::B_OD));
+      tc_commit_lead(lead, bar(C::B_OD + 1));
+    }
+    volatile int no_abort = 0;
+    tc_commit_lead(lead, bar(C::B_DRAIN));
+    wait_bar(bar(C::B_DRAIN), 0, &no_abort, nullptr, 0, lim);
+    __syncwarp();
+  }
+}
+
+// Softmax groups of the fused ring.  The state starts empty (m = -inf,
+// l = 0, O~ = 0 in TMEM) and never leaves the CTA; at the end each valid
+// row writes O = O~ / l and LSE = ln 2 * (m + log2 l) (m in log2 units; O~
+// and l are relative to the same m), or 0 and -inf for a row that saw no
+// key.  out is [rows, heads, d] and lse [rows, heads], like the state.
+template <int D>
+__device__ __forceinline__ void ring_softmax_role(const FwdArgs& a, const StepVisit* rec, int i,
+                                                  long long row0, long long vb, uint32_t tmem,
+                                                  uint32_t bar0,
+                                                  volatile int* abort_flag) {
+  using C = Cfg<D>;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int h = blockIdx.y;
+  const long long lim = a.wait_limit;
+  auto bar = [&](int x) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(x); };
+  const int g = warp >> 2;
+  const int quarter = warp & 3;
+  const int row = quarter * 32 + lane;
+  const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+  const uint32_t s_col = C::S_COL + static_cast<uint32_t>(g) * BN;
+  const uint32_t o_col = C::O_COL + static_cast<uint32_t>(g) * D;
+  const long long grow = row0 + g * BM + row;  // row within block i
+  const bool valid = grow < a.cq;
+  const long long oidx = (static_cast<long long>(i) * a.cq + grow) * a.heads + h;
+  const float sl2 = a.scale_log2;
+  const uint64_t sl2x2 = f2pack(sl2, sl2);
+  {
+    uint32_t z[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) z[j] = 0u;
+#pragma unroll
+    for (int cc = 0; cc < D / 32; ++cc) tmem_st32(tl + o_col + cc * 32, z);
+    tmem_wait_st();
+  }
+  float m_used = -INFINITY, m_true = -INFINITY, l_run = 0.f;
+  bool m_moved = false;
+  bool ok = true;
+  int cnt = 0;  // tiles so far: the phase of this group's S barrier
+  for (int s = 0; s < a.P && ok; ++s) {
+    // Select, not index: g is not a compile-time constant here.
+    const int t0 = g ? rec[s].ta[1] : rec[s].ta[0], t1 = g ? rec[s].tb[1] : rec[s].tb[0];
+    if (t1 <= t0) continue;
+    const Work wk = ring_work(a, i, s);
+    int row_lo = 0, row_hi = 0;
+    if (valid) {
+      long long lo, hi;
+      row_keys(a, wk, grow, vb, &lo, &hi);
+      row_lo = static_cast<int>(lo);
+      row_hi = static_cast<int>(hi);
+    }
+    const int full_0 = (row_lo + BN - 1) / BN;
+    const int n_full = row_hi / BN - full_0 > 0 ? row_hi / BN - full_0 : 0;
+    for (int t = t0; t < t1; ++t) {
+      ok = softmax_tile<D>(tl, s_col, o_col, t, row_lo, row_hi, full_0, n_full, sl2, sl2x2,
+                           bar(C::B_SF + g), bar(C::B_PF + g), static_cast<uint32_t>(cnt) & 1u,
+                           abort_flag, lim, m_used, m_true, m_moved, l_run);
+      ++cnt;
+      if (!ok) break;
+    }
+  }
+  if (ok && cnt > 0) {
+    ok = wait_bar(bar(C::B_OD + g), 0u, abort_flag, &g_umma_status, 0x33, lim);
+    ok = __all_sync(0xffffffffu, ok);
+  }
+  if (!ok) return;
+  const bool seen = l_run > 0.f;
+  const float inv = seen ? 1.f / l_run : 0.f;
+  float* dst = a.o + oidx * D;
+  if (cnt > 0) {
+    tc_fence_after();
+#pragma unroll
+    for (int cc = 0; cc < D / 32; ++cc) {
+      uint32_t r[32];
+      tmem_ld32(tl + o_col + cc * 32, r);
+      tmem_wait_ld();
+      reg_fence32(r);
+      if (valid) {
+        float4* d4 = reinterpret_cast<float4*>(dst + cc * 32);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          d4[j] = make_float4(__uint_as_float(r[4 * j + 0]) * inv,
+                              __uint_as_float(r[4 * j + 1]) * inv,
+                              __uint_as_float(r[4 * j + 2]) * inv,
+                              __uint_as_float(r[4 * j + 3]) * inv);
+      }
+    }
+  } else if (valid) {
+#pragma unroll
+    for (int j = 0; j < D / 4; ++j)
+      reinterpret_cast<float4*>(dst)[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  if (valid) a.m[oidx] = seen ? (m_used + log2f(l_run)) * kLn2 : -INFINITY;
+}
+
+// Grid (query-tile pairs, heads, P ranks).  Under causal masking with the
+// contiguous layout, rank i does i + 1 blocks of work and the later rows of
+// a block more than the earlier ones, so the heavy CTAs are launched first.
+template <int D>
+__global__ void __launch_bounds__(NTHREADS, 1)
+umma_ring_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                 const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t s_base = smem_u32(smem);
+  const uint32_t sQ = s_base + C::OFF_Q;
+  const uint32_t sK = s_base + C::OFF_K;
+  const uint32_t sV = s_base + C::OFF_V;
+  const uint32_t bar0 = s_base + C::OFF_BAR;
+  auto bar = [&](int x) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(x); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const bool heavy_first = a.mask.causal && a.layout == kContiguous;
+  const int i = heavy_first ? a.P - 1 - static_cast<int>(blockIdx.z)
+                            : static_cast<int>(blockIdx.z);
+  const int pair = a.mask.causal ? static_cast<int>(gridDim.x - 1 - blockIdx.x)
+                                 : static_cast<int>(blockIdx.x);
+  const long long row0 = static_cast<long long>(pair) * (NQ * BM);
+  const long long vb = valid_bound(a.mask);
+  // The visit table: every step's tile ranges, computed once by all threads
+  // before the roles split the registers.
+  StepVisit* rec = reinterpret_cast<StepVisit*>(smem + C::OFF_MISC + 16);
+  for (int s = tid; s < a.P; s += NTHREADS) rec[s] = step_visit(a, i, s, row0, vb);
+  if (tid == 0) {
+    for (int x = 0; x < C::NBAR; ++x) {
+      const bool pf = x >= C::B_PF && x < C::B_PF + NQ;
+      const bool kvf = x >= C::B_KF && x < C::B_KF + C::NSK;
+      mbar_init(bar(x), pf ? 128u : (kvf ? 2u : 1u));
+    }
+    *abort_flag = *reinterpret_cast<volatile int*>(&g_umma_status) != 0 ? 1 : 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  __syncthreads();
+  {
+    // Rows that see no key anywhere: O = 0 and LSE = -inf, and no pipeline.
+    if (next_step(rec, a.P, 0) == a.P) {
+      if (tid < NQ * BM) {
+        const long long grow = row0 + tid;
+        if (grow < a.cq) {
+          const long long oidx = (static_cast<long long>(i) * a.cq + grow) * a.heads + blockIdx.y;
+#pragma unroll
+          for (int j = 0; j < D / 4; ++j)
+            reinterpret_cast<float4*>(a.o + oidx * D)[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+          a.m[oidx] = -INFINITY;
+        }
+      }
+      return;
+    }
+  }
+  if (*abort_flag) return;
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (warp >= 8) {
+    regs_dec<C::REGS_CONTROL>();
+    ring_control_roles<D>(a, rec, i, row0, tmem, sQ, sK, sV, bar0, abort_flag, &tmQ, &tmK, &tmV);
+    tc_fence_before();
+    named_bar_sync(1, NTHREADS);
+    if (warp == 9) {
+      tc_fence_after();
+      tmem_dealloc(tmem, TMEM_COLS);
+    }
+  } else {
+    regs_inc<C::REGS_SOFTMAX>();
+    ring_softmax_role<D>(a, rec, i, row0, vb, tmem, bar0, abort_flag);
+    tc_fence_before();
+    named_bar_sync(1, NTHREADS);
+  }
+}
+
+template <int D>
+cudaError_t launch_ring_d(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, cudaStream_t st) {
+  using C = Cfg<D>;
+  constexpr uint32_t smem = C::SMEM_BYTES + kRingMaxSteps * sizeof(StepVisit);
+  static_assert(smem <= 232448, "shared memory budget of the fused ring");
+  if (a.P > kRingMaxSteps) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(umma_ring_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  dim3 grid(static_cast<unsigned>((a.cq + NQ * BM - 1) / (NQ * BM)), a.heads, a.P);
+  umma_ring_kernel<D><<<grid, NTHREADS, smem, st>>>(tq, tk, tv, a);
+  return cudaGetLastError();
+}
+
 // One CTA waits on an mbarrier nothing will arrive on.  Used to test that a
 // bounded wait gives up and reports instead of hanging.
 __global__ void wait_selftest_kernel(long long limit) {
@@ -658,6 +1135,11 @@ cudaError_t launch_d(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap&
 cudaError_t launch_umma_update(const FwdArgs& a, int d, const CUtensorMap& tq,
                                const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st) {
   return d == 128 ? launch_d<128>(a, tq, tk, tv, st) : launch_d<64>(a, tq, tk, tv, st);
+}
+
+cudaError_t launch_umma_ring(const FwdArgs& a, int d, const CUtensorMap& tq,
+                             const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st) {
+  return d == 128 ? launch_ring_d<128>(a, tq, tk, tv, st) : launch_ring_d<64>(a, tq, tk, tv, st);
 }
 
 cudaError_t launch_wait_selftest(long long limit_cycles, cudaStream_t st) {

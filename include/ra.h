@@ -115,7 +115,8 @@ typedef enum {
   RA_KERNEL_BWD_PRE = 7,        /* backward: D = rowsum(dO * O) */
   RA_KERNEL_BWD_DQ = 8,         /* backward: dQ (tcgen05, Q-stationary) */
   RA_KERNEL_BWD_DKDV = 9,       /* backward: dK, dV (tcgen05, K/V-stationary) */
-  RA_KERNEL_KINDS = 10
+  RA_KERNEL_RING_FUSED_BF16 = 10, /* the whole bf16 ring forward in one launch (tcgen05) */
+  RA_KERNEL_KINDS = 11
 } ra_kernel_kind;
 
 /*

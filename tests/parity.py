@@ -81,3 +81,17 @@ def check_grad(x, ref, name="grad"):
     assert err <= TOL["bf16"]["grad"] * max(scale, 1e-30), \
         f"{name}: max err {err:.3e} > {TOL['bf16']['grad']} x {scale:.3e}"
     return err / max(scale, 1e-30)
+
+
+def assert_fused_matches(out, lse, ref_out, ref_lse):
+    """The fused bf16 ring against the same ring run step by step: the same
+    products and the same state updates in the same order, so they differ
+    only in the last fp32 roundings of the finalize (out = O~ / l, and LSE
+    from the log2-unit max)."""
+    import torch
+
+    assert (out - ref_out).abs().max().item() <= 1e-6
+    fin = torch.isfinite(ref_lse)
+    assert torch.equal(torch.isfinite(lse), fin)
+    err = ((lse - ref_lse).abs() / ref_lse.abs().clamp(min=1.0))[fin]
+    assert err.numel() == 0 or err.max().item() <= 1e-6

@@ -16,7 +16,7 @@ import pytest
 import torch
 
 import oracle
-from parity import check_output, check_state
+from parity import check_output, check_state, assert_fused_matches
 
 import blockwise_online_softmax_gb300 as ra
 from blockwise_online_softmax_gb300 import binding, inputs
@@ -191,7 +191,9 @@ def test_masked_steps_equal_the_masked_forward():
         ra.ra_ring_step_masked(q, k, v, m, l, o, P=P, s=s, **kw)
     out, lse = ra.ra_finalize(m, l, o)
     torch.cuda.synchronize()
-    assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
+    # The masked forward (bf16) is one fused launch; the steps above do the
+    # same products and state updates, with the state in HBM between them.
+    assert_fused_matches(ref_out, ref_lse, out, lse)
 
 
 @pytest.mark.slow

@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import oracle
-from parity import TOL, check_output
+from parity import TOL, check_output, assert_fused_matches
 
 import blockwise_online_softmax_gb300 as ra
 from blockwise_online_softmax_gb300 import binding, inputs
@@ -121,21 +121,19 @@ def test_block_count_does_not_change_the_result():
         assert (x - outs[0]).abs().max().item() <= TOL["bf16"]["o"]
 
 
-@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-def test_ring_equals_its_steps_and_resumes_from_saved_state(dtype):
-    """ra_ring_forward equals init + ra_ring_step for s = 0..P-1 + finalize,
-    bit for bit.  Saving the (m, l, O~) state to the host after step k and
-    restoring it gives the same bits again (checkpoint and resume)."""
-    N, P, heads, kv_heads, d = 1024, 4, 2, 1, 64
-    q, k, v = (t.to(DEV) for t in inputs.make_random(N, heads, kv_heads, d, dtype=dtype, seed=13))
-    ref_out, ref_lse = ra.ra_ring_forward(q, k, v, P=P, causal=True)
+def stepwise_ring(q, k, v, P, causal, save_after=None):
+    """init + ra_ring_step for s = 0..P-1 + finalize.  With save_after = k,
+    the (m, l, O~) state goes to the host after step k, the device copies
+    are overwritten with NaN, and the state is restored (checkpoint and
+    resume)."""
+    N, heads, d = q.shape
     m = torch.empty(N, heads, device=DEV)
     l = torch.empty(N, heads, device=DEV)
     o = torch.empty(N, heads, d, device=DEV)
     ra.ra_state_init(m, l, o)
     for s in range(P):
-        ra.ra_ring_step(q, k, v, m, l, o, P=P, s=s, causal=True)
-        if s == 1:
+        ra.ra_ring_step(q, k, v, m, l, o, P=P, s=s, causal=causal)
+        if s == save_after:
             saved = [x.cpu() for x in (m, l, o)]
             for x in (m, l, o):
                 x.fill_(float("nan"))
@@ -143,16 +141,38 @@ def test_ring_equals_its_steps_and_resumes_from_saved_state(dtype):
                 x.copy_(y)
     out, lse = ra.ra_finalize(m, l, o)
     torch.cuda.synchronize()
-    assert torch.equal(out, ref_out)
-    assert torch.equal(lse, ref_lse)
+    return out, lse
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_ring_equals_its_steps_and_resumes_from_saved_state(dtype):
+    """init + ra_ring_step for s = 0..P-1 + finalize gives the same bits
+    when the (m, l, O~) state is saved to the host after step 1 and restored
+    (checkpoint and resume).  ra_ring_forward equals that composition bit
+    for bit in fp32 (it is that composition); in bf16 it is one fused launch
+    that keeps the state on chip, equal up to the finalize's roundings."""
+    N, P, heads, kv_heads, d = 1024, 4, 2, 1, 64
+    q, k, v = (t.to(DEV) for t in inputs.make_random(N, heads, kv_heads, d, dtype=dtype, seed=13))
+    ref_out, ref_lse = ra.ra_ring_forward(q, k, v, P=P, causal=True)
+    out0, lse0 = stepwise_ring(q, k, v, P, True)
+    out, lse = stepwise_ring(q, k, v, P, True, save_after=1)
+    assert torch.equal(out, out0) and torch.equal(lse, lse0)
+    if dtype == torch.float32:
+        assert torch.equal(out, ref_out)
+        assert torch.equal(lse, ref_lse)
+    else:
+        assert_fused_matches(ref_out, ref_lse, out, lse)
 
 
 def test_ring_equals_single_pair_calls():
     """The all-ranks ring step computes, for every rank, the same bits as
-    per-pair ra_block_update calls made in ring order."""
+    per-pair ra_block_update calls made in ring order (and the fused ring
+    matches both up to the finalize's roundings)."""
     N, P, heads, d = 768, 3, 2, 128
     q, k, v = (t.to(DEV) for t in inputs.make_random(N, heads, heads, d, seed=15))
-    ref_out, ref_lse = ra.ra_ring_forward(q, k, v, P=P, causal=True)
+    ref_out, ref_lse = stepwise_ring(q, k, v, P, True)
+    fused_out, fused_lse = ra.ra_ring_forward(q, k, v, P=P, causal=True)
+    assert_fused_matches(fused_out, fused_lse, ref_out, ref_lse)
     c = N // P
     for i in range(P):
         m = torch.empty(c, heads, device=DEV)
@@ -182,17 +202,31 @@ def test_host_buffer_entry_point():
     assert torch.equal(out_h, out_d.cpu()) and torch.equal(lse_h, lse_d.cpu())
 
 
-def test_trace_counts_launches():
-    q, k, v = (t.to(DEV) for t in inputs.make_random(1024, 2, 2, 128, seed=21))
+def trace_counts(run):
     ra.ra_trace_reset()
     ra.ra_trace_enable(True)
     try:
-        ra.ra_ring_forward(q, k, v, P=4, causal=True)
-        n_upd, ms_upd = ra.ra_trace_query("block_update_bf16")
-        n_init, _ = ra.ra_trace_query("state_init")
-        n_fin, _ = ra.ra_trace_query("finalize")
+        run()
+        got = {kind: ra.ra_trace_query(kind)
+               for kind in ("ring_fused_bf16", "block_update_bf16", "block_update_f32",
+                            "state_init", "finalize")}
     finally:
         ra.ra_trace_enable(False)
         ra.ra_trace_reset()
-    assert (n_upd, n_init, n_fin) == (4, 1, 1)
-    assert ms_upd > 0
+    return got
+
+
+def test_trace_counts_launches():
+    """bf16: the whole ring is one fused launch.  fp32: state init, one
+    block-update launch per ring step, finalize."""
+    q, k, v = (t.to(DEV) for t in inputs.make_random(1024, 2, 2, 128, seed=21))
+    got = trace_counts(lambda: ra.ra_ring_forward(q, k, v, P=4, causal=True))
+    assert [got[x][0] for x in ("ring_fused_bf16", "block_update_bf16", "state_init",
+                                "finalize")] == [1, 0, 0, 0]
+    assert got["ring_fused_bf16"][1] > 0
+    q, k, v = (t.to(DEV) for t in inputs.make_random(1024, 2, 2, 64, dtype=torch.float32,
+                                                     seed=21))
+    got = trace_counts(lambda: ra.ra_ring_forward(q, k, v, P=4, causal=True))
+    assert [got[x][0] for x in ("ring_fused_bf16", "block_update_f32", "state_init",
+                                "finalize")] == [0, 4, 1, 1]
+    assert got["block_update_f32"][1] > 0
