@@ -189,15 +189,20 @@ int ra_ring_step(const void* q, const void* k, const void* v, float* m, float* l
 
 /*
  * ra_ring_forward -- the whole per-device forward loop of [MATH]
- * "Accumulation math, step by step" for all P virtual ranks.  It runs the
- * state init, ring steps s = 0 .. P-1, then the finalize.
- *   out: [N, heads, d] fp32.  It is used as the O~ state during the ring,
- *        then finalized in place.
- *   lse: [N, heads] fp32.  It is used as the m state, then holds LSE =
- *        m + ln l.
- * Scratch: the l state ([N, heads] fp32) is the only scratch.  It is
- * allocated with cudaMallocAsync on `stream` and freed the same way.  A
- * failed allocation returns RA_ERR_ALLOC.
+ * "Accumulation math, step by step" for all P virtual ranks: every rank i
+ * folds the K/V blocks j = (i - s) mod P, s = 0 .. P-1, into the state of
+ * its queries, then finalizes ([PB] §2).
+ *   out: [N, heads, d] fp32: O = O~ / l (0 for a row that sees no key).
+ *   lse: [N, heads] fp32: LSE = m + ln l (-inf for such a row).
+ * bf16 with P <= 256: one fused launch.  Each rank's state stays on chip
+ * across all P steps and the kernel writes out and lse once; no scratch.
+ * fp32 (or P > 256): the state init, P ring-step launches with the O~ state
+ * in `out` and m in `lse`, then the finalize.  The l state ([N, heads]
+ * fp32) is then the only scratch, allocated with cudaMallocAsync on
+ * `stream` and freed the same way; a failed allocation returns
+ * RA_ERR_ALLOC.  Both give the results of init + ra_ring_step for
+ * s = 0..P-1 + ra_finalize, the fused launch up to the last roundings of
+ * the finalize.
  */
 int ra_ring_forward(const void* q, const void* k, const void* v, float* out, float* lse,
                     long long N, int P, int causal, int d, int heads, int kv_heads, int dtype,
