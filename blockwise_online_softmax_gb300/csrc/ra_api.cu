@@ -356,10 +356,12 @@ int ring_step_impl(const void* q, const void* k, const void* v, float* m, float*
 // steps, and the kernel writes out and lse itself (no scratch, no init or
 // finalize launch).
 constexpr int kFusedMaxSteps = 256;
+constexpr int kHostGroups = 8;  // KV-head groups of the pipelined host-buffer ring (8 measured best)
 
+// Query heads h0 .. h0 + nh - 1 only (nh = 0: all of them).
 int ring_fused_impl(const void* q, const void* k, const void* v, float* out, float* lse,
                     long long N, int P, const MaskSpec& mk, int d, int heads, int kv_heads,
-                    cudaStream_t st) {
+                    cudaStream_t st, int h0 = 0, int nh = 0) {
   ra::FwdArgs a{};
   a.q = q; a.k = k; a.v = v; a.o = out; a.m = lse; a.l = nullptr;
   a.cq = N / P;
@@ -373,6 +375,8 @@ int ring_fused_impl(const void* q, const void* k, const void* v, float* out, flo
   a.s = 0;
   a.i0 = 0;
   a.nwork = P;
+  a.h0 = h0;
+  a.nh = nh;
   put_mask(a, mk);
   a.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
   a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
@@ -799,6 +803,113 @@ int ra_ring_forward(const void* q, const void* k, const void* v, float* out, flo
                             dtype, stream);
 }
 
+// The bf16 host-buffer ring in pipelined groups of KV heads (heads never
+// interact): the inputs of group G + 1 copy in and the outputs of group
+// G - 1 copy out while group G runs.  Copies are pitched (a group is a
+// column range of every token row) on two helper streams, ordered against
+// the caller's stream, which runs the kernels, by events.  Device buffers
+// are allocated on the caller's stream and freed there once every copy
+// is done.
+static int ring_forward_host_pipelined(const void* q_host, const void* k_host,
+                                       const void* v_host, float* out_host, float* lse_host,
+                                       long long N, int P, int causal, int d, int heads,
+                                       int kv_heads, cudaStream_t st) {
+  const int g = heads / kv_heads;
+  int ng = kv_heads < kHostGroups ? kv_heads : kHostGroups;
+  while (kv_heads % ng) --ng;
+  const int gkv = kv_heads / ng, gq = gkv * g;
+  const size_t q_bytes = static_cast<size_t>(N) * heads * d * 2;
+  const size_t kv_bytes = static_cast<size_t>(N) * kv_heads * d * 2;
+  const size_t out_bytes = static_cast<size_t>(N) * heads * d * sizeof(float);
+  const size_t rh_bytes = static_cast<size_t>(N) * heads * sizeof(float);
+  void *dq = nullptr, *dk = nullptr, *dv = nullptr;
+  float *dout = nullptr, *dlse = nullptr;
+  cudaStream_t s_in = nullptr, s_out = nullptr;
+  cudaEvent_t ev_alloc = nullptr, ev_end = nullptr, ev_inall = nullptr;
+  cudaEvent_t ev_in[kHostGroups] = {}, ev_run[kHostGroups] = {};
+  cudaError_t e = cudaSuccess;
+  auto ok = [&](cudaError_t x) {
+    if (e == cudaSuccess) e = x;
+    return e == cudaSuccess;
+  };
+  auto alloc = [&](void** p, size_t n) { ok(cudaMallocAsync(p, n, st)); };
+  alloc(&dq, q_bytes);
+  alloc(&dk, kv_bytes);
+  alloc(&dv, kv_bytes);
+  alloc(reinterpret_cast<void**>(&dout), out_bytes);
+  alloc(reinterpret_cast<void**>(&dlse), rh_bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    int rc = fail(RA_ERR_ALLOC, "cudaMallocAsync of device staging failed: %s",
+                  cudaGetErrorString(e));
+    void* bufs[5] = {dq, dk, dv, dout, dlse};
+    for (void* p : bufs)
+      if (p) cudaFreeAsync(p, st);
+    return rc;
+  }
+  ok(cudaStreamCreateWithFlags(&s_in, cudaStreamNonBlocking));
+  ok(cudaStreamCreateWithFlags(&s_out, cudaStreamNonBlocking));
+  ok(cudaEventCreateWithFlags(&ev_alloc, cudaEventDisableTiming));
+  ok(cudaEventCreateWithFlags(&ev_end, cudaEventDisableTiming));
+  ok(cudaEventCreateWithFlags(&ev_inall, cudaEventDisableTiming));
+  for (int G = 0; G < ng; ++G) {
+    ok(cudaEventCreateWithFlags(&ev_in[G], cudaEventDisableTiming));
+    ok(cudaEventCreateWithFlags(&ev_run[G], cudaEventDisableTiming));
+  }
+  int rc = RA_OK;
+  if (e == cudaSuccess) {
+    ok(cudaEventRecord(ev_alloc, st));
+    ok(cudaStreamWaitEvent(s_in, ev_alloc, 0));
+    const size_t qrow = static_cast<size_t>(heads) * d * 2, kvrow = static_cast<size_t>(kv_heads) * d * 2;
+    for (int G = 0; G < ng && e == cudaSuccess; ++G) {
+      const size_t qo = static_cast<size_t>(G) * gq * d * 2, ko = static_cast<size_t>(G) * gkv * d * 2;
+      const size_t qw = static_cast<size_t>(gq) * d * 2, kw = static_cast<size_t>(gkv) * d * 2;
+      ok(cudaMemcpy2DAsync(static_cast<char*>(dq) + qo, qrow, static_cast<const char*>(q_host) + qo,
+                           qrow, qw, N, cudaMemcpyHostToDevice, s_in));
+      ok(cudaMemcpy2DAsync(static_cast<char*>(dk) + ko, kvrow, static_cast<const char*>(k_host) + ko,
+                           kvrow, kw, N, cudaMemcpyHostToDevice, s_in));
+      ok(cudaMemcpy2DAsync(static_cast<char*>(dv) + ko, kvrow, static_cast<const char*>(v_host) + ko,
+                           kvrow, kw, N, cudaMemcpyHostToDevice, s_in));
+      ok(cudaEventRecord(ev_in[G], s_in));
+    }
+    cudaEventRecord(ev_inall, s_in);  // after every copy that was enqueued
+    for (int G = 0; G < ng && e == cudaSuccess && rc == RA_OK; ++G) {
+      ok(cudaStreamWaitEvent(st, ev_in[G], 0));
+      if (e != cudaSuccess) break;
+      rc = ring_fused_impl(dq, dk, dv, dout, dlse, N, P, plain_mask(causal), d, heads, kv_heads,
+                           st, G * gq, gq);
+      ok(cudaEventRecord(ev_run[G], st));
+      ok(cudaStreamWaitEvent(s_out, ev_run[G], 0));
+      const size_t orow = static_cast<size_t>(heads) * d * 4, oo = static_cast<size_t>(G) * gq * d * 4;
+      ok(cudaMemcpy2DAsync(reinterpret_cast<char*>(out_host) + oo, orow,
+                           reinterpret_cast<const char*>(dout) + oo, orow,
+                           static_cast<size_t>(gq) * d * 4, N, cudaMemcpyDeviceToHost, s_out));
+    }
+    // LSE is small: one contiguous copy after the last group.
+    if (e == cudaSuccess && rc == RA_OK)
+      ok(cudaMemcpyAsync(lse_host, dlse, rh_bytes, cudaMemcpyDeviceToHost, s_out));
+    // The caller's stream, which frees the buffers, waits for every copy.
+    cudaEventRecord(ev_end, s_out);
+    cudaStreamWaitEvent(st, ev_end, 0);
+    cudaStreamWaitEvent(st, ev_inall, 0);
+  }
+  void* bufs[5] = {dq, dk, dv, dout, dlse};
+  for (void* p : bufs)
+    if (p) cudaFreeAsync(p, st);
+  if (s_in) cudaStreamDestroy(s_in);
+  if (s_out) cudaStreamDestroy(s_out);
+  if (ev_alloc) cudaEventDestroy(ev_alloc);
+  if (ev_end) cudaEventDestroy(ev_end);
+  if (ev_inall) cudaEventDestroy(ev_inall);
+  for (int G = 0; G < ng; ++G) {
+    if (ev_in[G]) cudaEventDestroy(ev_in[G]);
+    if (ev_run[G]) cudaEventDestroy(ev_run[G]);
+  }
+  if (rc != RA_OK) return rc;
+  if (e != cudaSuccess) return cuda_fail(e, "pipelined host-buffer ring");
+  return RA_OK;
+}
+
 int ra_ring_forward_host(const void* q_host, const void* k_host, const void* v_host,
                          float* out_host, float* lse_host, long long N, int P, int causal, int d,
                          int heads, int kv_heads, int dtype, void* stream) {
@@ -807,6 +918,13 @@ int ra_ring_forward_host(const void* q_host, const void* k_host, const void* v_h
   if (N == 0) return RA_OK;
   if (!q_host || !k_host || !v_host || !out_host || !lse_host)
     return fail(RA_ERR_INVALID, "a host pointer is NULL");
+  if (dtype == RA_BF16 && P <= kFusedMaxSteps) {
+    rc = ring_forward_host_pipelined(q_host, k_host, v_host, out_host, lse_host, N, P, causal, d,
+                                     heads, kv_heads, static_cast<cudaStream_t>(stream));
+    const int st_rc = ra_device_status(stream);
+    if (rc != RA_OK) return rc;
+    return st_rc;
+  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t esz = dtype == RA_BF16 ? 2 : 4;
   const size_t q_bytes = static_cast<size_t>(N) * heads * d * esz;

@@ -134,6 +134,8 @@ struct FwdArgs {
   float scale_log2;  // log2(e)/sqrt(d)
   long long wait_limit;  // SM cycles before a bounded wait gives up
   MaskArgs mask;
+  int h0;  // fused ring: first query head of the launch (grid.y runs h0 .. h0 + nh - 1)
+  int nh;  // fused ring: query heads in the launch (0: all `heads`)
 };
 
 // Decoded work item of grid.z index w.

@@ -771,7 +771,7 @@ __device__ __forceinline__ void ring_control_roles(const FwdArgs& a, const StepV
   using C = Cfg<D>;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int h = blockIdx.y;
+  const int h = a.h0 + static_cast<int>(blockIdx.y);
   const int kh = h / (a.heads / a.kv_heads);
   const long long lim = a.wait_limit;
   auto bar = [&](int x) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(x); };
@@ -918,7 +918,7 @@ __device__ __forceinline__ void ring_softmax_role(const FwdArgs& a, const StepVi
   using C = Cfg<D>;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int h = blockIdx.y;
+  const int h = a.h0 + static_cast<int>(blockIdx.y);
   const long long lim = a.wait_limit;
   auto bar = [&](int x) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(x); };
   const int g = warp >> 2;
@@ -1000,9 +1000,10 @@ __device__ __forceinline__ void ring_softmax_role(const FwdArgs& a, const StepVi
   if (valid) a.m[oidx] = seen ? (m_used + log2f(l_run)) * kLn2 : -INFINITY;
 }
 
-// Grid (query-tile pairs, heads, P ranks).  Under causal masking with the
-// contiguous layout, rank i does i + 1 blocks of work and the later rows of
-// a block more than the earlier ones, so the heavy CTAs are launched first.
+// Grid (query-tile pairs, query heads h0 .. h0 + nh - 1, P ranks).  Under
+// causal masking with the contiguous layout, rank i does i + 1 blocks of
+// work and the later rows of a block more than the earlier ones, so the
+// heavy CTAs are launched first.
 template <int D>
 __global__ void __launch_bounds__(NTHREADS, 1)
 umma_ring_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -1049,7 +1050,8 @@ umma_ring_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       if (tid < NQ * BM) {
         const long long grow = row0 + tid;
         if (grow < a.cq) {
-          const long long oidx = (static_cast<long long>(i) * a.cq + grow) * a.heads + blockIdx.y;
+          const long long oidx =
+              (static_cast<long long>(i) * a.cq + grow) * a.heads + a.h0 + blockIdx.y;
 #pragma unroll
           for (int j = 0; j < D / 4; ++j)
             reinterpret_cast<float4*>(a.o + oidx * D)[j] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1096,7 +1098,8 @@ cudaError_t launch_ring_d(const FwdArgs& a, const CUtensorMap& tq, const CUtenso
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  dim3 grid(static_cast<unsigned>((a.cq + NQ * BM - 1) / (NQ * BM)), a.heads, a.P);
+  dim3 grid(static_cast<unsigned>((a.cq + NQ * BM - 1) / (NQ * BM)), a.nh > 0 ? a.nh : a.heads,
+            a.P);
   umma_ring_kernel<D><<<grid, NTHREADS, smem, st>>>(tq, tk, tv, a);
   return cudaGetLastError();
 }

@@ -212,7 +212,11 @@ int ra_ring_forward(const void* q, const void* k, const void* v, float* out, flo
  * ra_ring_forward_host -- ra_ring_forward on HOST buffers.  It copies q, k
  * and v to stream-ordered device buffers, runs the ring, copies out and
  * lse back, frees the buffers, and synchronizes `stream` before it
- * returns.  Pinned host memory makes the copies asynchronous DMA.  Device
+ * returns.  Pinned host memory makes the copies asynchronous DMA.  In bf16
+ * the work is split into up to 8 groups of KV heads (heads never interact):
+ * group G runs on `stream` while group G + 1 copies in and group G - 1
+ * copies out on two streams the call creates and destroys, ordered by
+ * events.  The results are those of ra_ring_forward, bit for bit.  Device
  * wait timeouts are checked before return and give RA_ERR_TIMEOUT.
  */
 int ra_ring_forward_host(const void* q_host, const void* k_host, const void* v_host,

@@ -193,11 +193,22 @@ def test_ring_equals_single_pair_calls():
         assert torch.equal(lse, ref_lse[i * c:(i + 1) * c])
 
 
-def test_host_buffer_entry_point():
-    q, k, v = inputs.make_random(1024, 4, 2, 128, dtype=torch.bfloat16, seed=19)
-    qp, kp, vp = q.pin_memory(), k.pin_memory(), v.pin_memory()
-    out_h, lse_h = ra.ra_ring_forward_host(qp, kp, vp, P=4, causal=True)
-    out_d, lse_d = run_ring(q, k, v, 4, True)
+@pytest.mark.parametrize("shape", [
+    (1024, 4, 2, 128, True, True),     # 2 KV-head groups, pinned
+    (4096, 32, 8, 128, True, True),    # 4 groups of 2 KV heads (the gqa-128k grouping)
+    (2048, 6, 3, 64, False, True),     # 3 groups, pageable host memory
+    (1000, 8, 8, 64, True, False),     # 4 groups, non-causal, ragged last block
+])
+def test_host_buffer_entry_point(shape):
+    """The host-buffer ring (bf16: KV-head groups pipelined against their
+    copies) gives the device ring's bits."""
+    N, heads, kv_heads, d, pinned, causal = shape
+    q, k, v = inputs.make_random(N, heads, kv_heads, d, dtype=torch.bfloat16, seed=19)
+    if pinned:
+        q, k, v = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    P = 4 if N % 4 == 0 else 8
+    out_h, lse_h = ra.ra_ring_forward_host(q, k, v, P=P, causal=causal)
+    out_d, lse_d = run_ring(q, k, v, P, causal)
     assert not out_h.is_cuda
     assert torch.equal(out_h, out_d.cpu()) and torch.equal(lse_h, lse_d.cpu())
 
