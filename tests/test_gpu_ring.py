@@ -213,6 +213,26 @@ def test_host_buffer_entry_point(shape):
     assert torch.equal(out_h, out_d.cpu()) and torch.equal(lse_h, lse_d.cpu())
 
 
+def test_more_than_256_ranks_takes_the_step_path():
+    """bf16 with P > 256 (beyond the fused launch's visit table) runs one
+    launch per ring step; it gives the attention of the fused P = 256 ring
+    and of the oracle on sampled rows."""
+    N, heads, kv_heads, d = 10240, 2, 1, 64
+    q, k, v = inputs.make_random(N, heads, kv_heads, d, seed=29)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    got = trace_counts(lambda: ra.ra_ring_forward(qd, kd, vd, P=320, causal=True))
+    assert got["ring_fused_bf16"][0] == 0 and got["block_update_bf16"][0] == 320
+    out, lse = ra.ra_ring_forward(qd, kd, vd, P=320, causal=True)
+    out_f, lse_f = ra.ra_ring_forward(qd, kd, vd, P=256, causal=True)
+    ra.ra_device_status()
+    assert (out - out_f).abs().max().item() <= TOL["bf16"]["o"]
+    rows = np.array([0, 1, 31, 32, 5000, 10239])
+    idx = torch.from_numpy(rows).to(DEV)
+    ref_out, ref_lse = oracle.attention(q, k, v, causal=True, rows=rows)
+    check_output(out.index_select(0, idx).cpu(), lse.index_select(0, idx).cpu(), ref_out, ref_lse,
+                 "bf16")
+
+
 def trace_counts(run):
     ra.ra_trace_reset()
     ra.ra_trace_enable(True)
