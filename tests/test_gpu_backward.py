@@ -129,6 +129,25 @@ def test_backward_block_count_does_not_change_the_result():
             assert (x - y).abs().max().item() <= 2e-2 * y.abs().max().item()
 
 
+def test_backward_with_300_ranks():
+    """P = 300 ranks of two rows each: 300 ring steps of mostly empty or
+    one-tile work, the gradients accumulating in HBM across the steps.  They
+    are those of the P = 4 ring (the same attention) and of the oracle."""
+    N, P, heads, kv_heads, d = 600, 300, 2, 1, 64
+    q, k, v = inputs.make_random(N, heads, kv_heads, d, seed=41)
+    g = inputs.randn_chunked((N, heads, d), 41, 3).to(torch.bfloat16)
+    qd, kd, vd, gd = q.to(DEV), k.to(DEV), v.to(DEV), g.to(DEV)
+    grads = {}
+    for p in (P, 4):
+        out, lse = ra.ra_ring_forward(qd, kd, vd, P=p, causal=True)
+        grads[p] = ra.ra_ring_backward(qd, kd, vd, out, lse, gd, P=p, causal=True)
+    ra.ra_device_status()
+    refs = oracle.backward(q, k, v, g, causal=True)[:3]
+    for name, x, y, r in zip(("dq", "dk", "dv"), grads[P], grads[4], refs):
+        check_grad(x, r, name)
+        assert (x - y).abs().max().item() <= 2e-2 * float(np.abs(r).max())
+
+
 @pytest.mark.slow
 def test_backward_mha_8k():
     w = inputs.WORKLOADS["mha-8k"]
