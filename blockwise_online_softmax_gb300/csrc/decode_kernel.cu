@@ -9,9 +9,10 @@
 // g * n_q query rows of its KV head (g = heads / kv_heads).  The layout is
 // built around that read:
 //   * decode_tc_kernel: a CTA takes one KV head and one chunk of one
-//     shard's keys (split-K; the grid covers chunks x KV heads x shards, a
-//     few waves of the SMs).  The KV head's query rows sit in one 128-row
-//     tile, so tcgen05 products give S = Q K^T and O += P V for a whole
+//     shard's keys (split-K; the grid covers chunks x row tiles x KV heads
+//     x shards, a few waves of the SMs).  The KV head's query rows sit in
+//     128-row tiles (one for up to 128 rows, the usual case), so tcgen05
+//     products give S = Q K^T and O += P V for a whole
 //     128-key tile at a time; the unused rows of the tile cost tensor time,
 //     which the pipe has to spare, not bytes.  It writes one partial state
 //     (m, l, O~) per chunk.
@@ -34,9 +35,10 @@ __device__ int g_decode_status = 0;
 namespace {
 
 // ------------------------------------------------------------------ chunk kernel
-// The KV head's g * n_q query rows (up to 128) are gathered into one 128-row
-// query tile (a 3-D TMA box of g heads x n_q tokens; the rest of the tile
-// is zero), and the CTA walks its key chunk in 128-key tiles with
+// The KV head's g * n_q query rows are gathered into 128-row query tiles of
+// tq = floor(128 / g) tokens each (a 3-D TMA box of g heads x tq tokens,
+// row qi * g + hl; the rest of the tile is zero); a CTA takes one row tile
+// and walks its key chunk in 128-key tiles with
 // S = Q K^T and O += P V in TMEM and the online softmax of the forward
 // kernel on one thread per row.  S is double-buffered in
 // TMEM: the product S(k+2) runs while the softmax works on S(k), and the
@@ -81,9 +83,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int split = blockIdx.x, kh = blockIdx.y, shard = blockIdx.z;
+  const int split = static_cast<int>(blockIdx.x) % a.nsplit;
+  const int rt = static_cast<int>(blockIdx.x) / a.nsplit;  // row tile: tokens qa .. qa + qn - 1
+  const int kh = blockIdx.y, shard = blockIdx.z;
   const int g = a.heads / a.kv_heads;
-  const int R = g * static_cast<int>(a.n_q);
+  const long long qa = static_cast<long long>(rt) * a.tq;
+  const long long qn = a.tq < a.n_q - qa ? a.tq : a.n_q - qa;
+  const int R = g * static_cast<int>(qn);
   const long long sh0 = static_cast<long long>(shard) * a.shard_len;
   const long long sh1 = sh0 + a.shard_len < a.n_kv ? sh0 + a.shard_len : a.n_kv;
   const long long c0 = sh0 + static_cast<long long>(split) * a.chunk;
@@ -106,8 +112,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   // Rows grow in position with r (r = qi * g + hl), so the first and last
   // query tokens bound the key range of the tile.
   long long lo0, hi0, lo1, hi1;
-  keys_of(0, &lo0, &hi0);
-  keys_of(a.n_q - 1, &lo1, &hi1);
+  keys_of(qa, &lo0, &hi0);
+  keys_of(qa + qn - 1, &lo1, &hi1);
   const long long klo = lo0 < lo1 ? lo0 : lo1, khi = hi0 > hi1 ? hi0 : hi1;
   const long long kb = (klo / BT) * BT;
   const int n = khi > klo ? static_cast<int>((khi - kb + BT - 1) / BT) : 0;
@@ -116,7 +122,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   if (n == 0) {
     // No key of this chunk is allowed: an empty partial state.
     for (int i = tid; i < R * D; i += 256) {
-      const long long qi = (i / D) / g;
+      const long long qi = qa + (i / D) / g;
       const int h = kh * g + (i / D) % g;
       const long long pidx = (pbase + qi) * a.heads + h;
       a.po[pidx * D + i % D] = 0.f;
@@ -150,9 +156,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   if (warp == 4) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
-      mbar_arrive_expect_tx(bar(C::B_Q), static_cast<uint32_t>(R) * 128u * C::NCH);
+      // The box is g heads x tq tokens; tokens past n_q (a last partial
+      // tile) are filled with zeros and counted like the rest.
+      mbar_arrive_expect_tx(bar(C::B_Q),
+                            static_cast<uint32_t>(g * a.tq) * 128u * C::NCH);
       for (int ch = 0; ch < C::NCH; ++ch)
-        tma_load_3d(sb + C::OFF_Q + ch * CHB, &tmQ, bar(C::B_Q), ch * 64, kh * g, 0);
+        tma_load_3d(sb + C::OFF_Q + ch * CHB, &tmQ, bar(C::B_Q), ch * 64, kh * g,
+                    static_cast<int>(qa));
       int issued = 0;
       bool ok = true;
       for (int k = 0; k < n; ++k) {
@@ -246,7 +256,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     const bool valid = r < R;
     long long rlo = 0, rhi = 0;
-    if (valid) keys_of(r / g, &rlo, &rhi);
+    if (valid) keys_of(qa + r / g, &rlo, &rhi);
     const int row_lo = static_cast<int>(rlo - kb), row_hi = static_cast<int>(rhi - kb);
     {
       uint32_t z[32];
@@ -363,7 +373,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) reg_fence32(o[cc]);
       if (valid) {
-        const long long pidx = (pbase + r / g) * a.heads + kh * g + r % g;
+        const long long pidx = (pbase + qa + r / g) * a.heads + kh * g + r % g;
         float4* dst = reinterpret_cast<float4*>(a.po + pidx * D);
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc)
@@ -442,8 +452,8 @@ cudaError_t launch_tc_d(const DecArgs& a, const CUtensorMap& tq, const CUtensorM
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(C::SMEM));
   if (e != cudaSuccess) return e;
-  dim3 grid(static_cast<unsigned>(a.nsplit), static_cast<unsigned>(a.kv_heads),
-            static_cast<unsigned>(a.nshard));
+  dim3 grid(static_cast<unsigned>(a.nsplit) * static_cast<unsigned>(a.ntile),
+            static_cast<unsigned>(a.kv_heads), static_cast<unsigned>(a.nshard));
   tc::decode_tc_kernel<D><<<grid, 256, C::SMEM, st>>>(tq, tk, tv, a);
   return cudaGetLastError();
 }

@@ -129,16 +129,17 @@ int encode_map(CUtensorMap* map, const void* base, long long rows, int heads, in
   return RA_OK;
 }
 
-// 3-D map over the decode queries [n_q, heads, d] whose box is all n_q
-// tokens of g consecutive heads (one KV head's query rows), 64 columns
-// wide: the box lands in shared memory as g * n_q rows of 128 bytes, row
-// qi * g + hl, with 128-byte swizzle.
-int encode_q_group_map(CUtensorMap* map, const void* base, long long n_q, int heads, int g, int d) {
+// 3-D map over the decode queries [n_q, heads, d] whose box is tq tokens
+// of g consecutive heads (one row tile of a KV head's query rows), 64
+// columns wide: the box lands in shared memory as g * tq rows of 128 bytes,
+// row qi * g + hl, with 128-byte swizzle.
+int encode_q_group_map(CUtensorMap* map, const void* base, long long n_q, int heads, int g,
+                       long long tq, int d) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
                               static_cast<cuuint64_t>(n_q)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
                                  static_cast<cuuint64_t>(heads) * d * 2};
-  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(g), static_cast<cuuint32_t>(n_q)};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(g), static_cast<cuuint32_t>(tq)};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -548,7 +549,8 @@ int ring_backward_impl(const void* q, const void* k, const void* v, const float*
 }
 
 // ----------------------------------------------------------------- decode
-// Query rows per KV head (g * n_q) the decode path takes: one 128-row tile.
+// A decode row tile holds 128 query rows: floor(128 / g) tokens of the g
+// heads that share a KV head.
 constexpr int kDecodeMaxRows = 128;
 
 int decode_args_check(const void* q, const void* k, const void* v, long long n_q, long long n_kv,
@@ -560,11 +562,14 @@ int decode_args_check(const void* q, const void* k, const void* v, long long n_q
   if (n_q < 0 || n_kv < 0) return fail(RA_ERR_INVALID, "n_q=%lld or n_kv=%lld is negative", n_q, n_kv);
   if (n_kv > (1LL << 31) - 256) return fail(RA_ERR_UNSUPPORTED, "n_kv=%lld exceeds the 32-bit TMA row coordinate", n_kv);
   if (window < 0) return fail(RA_ERR_INVALID, "window=%lld is negative", window);
-  if (static_cast<long long>(heads / kv_heads) * n_q > kDecodeMaxRows)
+  if (heads / kv_heads > kDecodeMaxRows)
     return fail(RA_ERR_UNSUPPORTED,
-                "(heads / kv_heads) * n_q = %lld query rows per KV head exceeds %d; use "
-                "ra_block_update_masked for longer query blocks",
-                static_cast<long long>(heads / kv_heads) * n_q, kDecodeMaxRows);
+                "heads / kv_heads = %d query heads per KV head exceeds %d (one token's rows "
+                "must fit a %d-row tile)",
+                heads / kv_heads, kDecodeMaxRows, kDecodeMaxRows);
+  if (n_q > (1LL << 24))
+    return fail(RA_ERR_UNSUPPORTED, "n_q=%lld query tokens exceeds 2^24; use the ring forward",
+                n_q);
   (void)q; (void)k; (void)v;
   return RA_OK;
 }
@@ -578,6 +583,11 @@ int decode_run(const void* q, const void* k, const void* v, float* m, float* l, 
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // Row tiles: tq tokens of the g heads of a KV head, g * tq <= 128 rows.
+  const int g = heads / kv_heads;
+  long long tq = kDecodeMaxRows / g;
+  if (tq > n_q) tq = n_q;
+  const long long ntile = (n_q + tq - 1) / tq;
   // One CTA per SM at a time; about six waves; chunks of whole 128-key
   // tiles, at least one.  Each CTA pays a pipeline fill, so fewer, longer
   // chunks win up to the point where the last partial wave leaves SMs
@@ -585,8 +595,8 @@ int decode_run(const void* q, const void* k, const void* v, float* m, float* l, 
   // waves (two chunks per shard) measured 10% faster than three (one chunk,
   // 3.4 waves) and than ten or seventeen.
   const long long waves = 6, gran = 128;
-  long long want = (waves * sms + static_cast<long long>(kv_heads) * nshard - 1) /
-                   (static_cast<long long>(kv_heads) * nshard);
+  const long long units = static_cast<long long>(kv_heads) * nshard * ntile;
+  long long want = (waves * sms + units - 1) / units;
   if (want < 1) want = 1;
   long long chunk = (shard_len + want - 1) / want;
   chunk = ((chunk + gran - 1) / gran) * gran;
@@ -603,10 +613,10 @@ int decode_run(const void* q, const void* k, const void* v, float* m, float* l, 
                 cudaGetErrorString(e));
   }
   int rc = get_encoder();
-  CUtensorMap tk, tv, tq;
+  CUtensorMap tk, tv, tmq;
   if (rc == RA_OK) rc = encode_map(&tk, k, n_kv, kv_heads, d);
   if (rc == RA_OK) rc = encode_map(&tv, v, n_kv, kv_heads, d);
-  if (rc == RA_OK) rc = encode_q_group_map(&tq, q, n_q, heads, heads / kv_heads, d);
+  if (rc == RA_OK) rc = encode_q_group_map(&tmq, q, n_q, heads, g, tq, d);
   if (rc == RA_OK) {
     ra::DecArgs a{};
     a.q = q;
@@ -622,6 +632,8 @@ int decode_run(const void* q, const void* k, const void* v, float* m, float* l, 
     a.heads = heads;
     a.kv_heads = kv_heads;
     a.nsplit = static_cast<int>(nsplit);
+    a.tq = tq;
+    a.ntile = static_cast<int>(ntile);
     a.nshard = nshard;
     a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
     a.wait_limit = kWaitLimit;
@@ -629,7 +641,7 @@ int decode_run(const void* q, const void* k, const void* v, float* m, float* l, 
     a.mask.window = window > kAllValid ? kAllValid : window;
     a.mask.n_valid = kAllValid;
     TraceScope t0(RA_KERNEL_DECODE_SPLIT, st);
-    e = ra::launch_decode_tc(a, d, tq, tk, tv, st);
+    e = ra::launch_decode_tc(a, d, tmq, tk, tv, st);
     t0.done(e == cudaSuccess);
     if (e != cudaSuccess) {
       rc = cuda_fail(e, "decode split launch");

@@ -223,6 +223,8 @@ struct DecArgs {
   int kv_heads;
   int nsplit;
   int nshard;
+  long long tq;      // query tokens per row tile (g * tq <= 128 rows)
+  int ntile;         // row tiles: ceil(n_q / tq); grid.x = nsplit * ntile
   float scale_log2;  // log2(e)/sqrt(d)
   long long wait_limit;
   MaskArgs mask;

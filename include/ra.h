@@ -360,13 +360,16 @@ int ra_ring_backward_masked(const void* q, const void* k, const void* v, const f
  *   k, v: [n_kv, kv_heads, d] bf16, positions kv_off .. kv_off + n_kv - 1.
  *   m, l: [n_q, heads] fp32; o: [n_q, heads, d] fp32 (updated in place).
  *   causal and window: as in the masked calls (kp <= qp; |qp - kp| < window).
- *   (heads / kv_heads) * n_q must be <= 128: every KV head's query rows are
- *   held together, so each K/V byte is read once.  Longer query blocks
- *   belong to ra_block_update_masked.  dtype must be RA_BF16.
+ *   heads / kv_heads must be <= 128 and n_q <= 2^24.  A KV head's query
+ *   rows (token qi of its g heads is row qi * g + hl) go in 128-row tiles of
+ *   floor(128 / g) tokens; with (heads / kv_heads) * n_q <= 128, the decode
+ *   case, they are one tile and each K/V byte is read once.  Each further
+ *   tile reads the keys again: long query blocks belong to
+ *   ra_block_update_masked.  dtype must be RA_BF16.
  * The work is HBM-bound: the keys of each KV head are streamed in chunks
  * spread over the SMs (split-K), each chunk giving one partial state, and a
  * second kernel folds them into m, l, o.  A chunk runs on the tensor cores
- * with the KV head's query rows gathered into one 128-row tile.  The partial states
+ * with one row tile of the KV head's query rows.  The partial states
  * (chunks x n_q x heads x (d + 2) fp32) are allocated with cudaMallocAsync
  * on `stream`.
  */

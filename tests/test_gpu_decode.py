@@ -49,6 +49,11 @@ CASES = [
     (8, 64, 8, 128, 20000, 16, True, 2048),  # 64 rows, windowed
     (5, 8, 8, 128, 777, 2, False, 0),        # 5 rows, non-causal, ragged
     (3, 32, 8, 64, 130, 8, True, 0),         # 12 rows, shards shorter than a tile
+    # more than 128 rows per KV head: several 128-row tiles
+    (64, 32, 8, 128, 6000, 4, True, 0),      # 256 rows: two full tiles of 32 tokens
+    (50, 12, 4, 64, 4000, 3, True, 700),     # g = 3: tiles of 42 tokens, the last partial
+    (300, 2, 2, 128, 2000, 2, False, 0),     # MHA: three tiles of 128 tokens, non-causal
+    (20, 256, 2, 64, 1000, 2, True, 0),      # g = 128: one token per tile
 ]
 
 

@@ -130,7 +130,8 @@ def test_decode_rejects_bad_arguments(lib):
     def fwd(n_q=1, heads=32, kv_heads=8, d=128, dtype=1, P=4, window=0):
         return lib.ra_decode_forward(FAKE, FAKE, FAKE, FAKE, FAKE, n_q, 1000, P, 999, 1, window,
                                      d, heads, kv_heads, dtype, None)
-    assert fwd(n_q=33) == -2 and b"exceeds 128" in lib.ra_last_error()
+    assert fwd(heads=258, kv_heads=2) == -2 and b"exceeds 128" in lib.ra_last_error()
+    assert fwd(n_q=(1 << 24) + 1) == -2 and b"2^24" in lib.ra_last_error()
     assert fwd(dtype=0) == -2 and b"bf16" in lib.ra_last_error()
     assert fwd(P=0) == -1 and b"P=0" in lib.ra_last_error()
     assert fwd(window=-3) == -1 and b"window" in lib.ra_last_error()
