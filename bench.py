@@ -781,9 +781,12 @@ def run_ours(args, w, ws, rank, local):
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
     barrier(ws)
     t0 = time.perf_counter()
+    e2e_step_ms = []
     for _ in range(e2e_steps):
+        t1 = time.perf_counter()
         ra.ra_ring_forward_host(qp, kp, vp, P=w.P, causal=w.causal, out=out_h, lse=lse_h,
                                 stream=stream)
+        e2e_step_ms.append((time.perf_counter() - t1) * 1e3)
     e2e_s = reduce_max(time.perf_counter() - t0, ws) / e2e_steps
     h2d = sum(t.numel() * t.element_size() for t in (q, k, v))
     d2h = out_h.numel() * 4 + lse_h.numel() * 4
@@ -816,7 +819,8 @@ def run_ours(args, w, ws, rank, local):
         },
         "clocks": clk,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "step_ms": [round(t, 2) for t in e2e_step_ms]},
         "gpu_launches": n_upd + n_fz + n_init + n_fin,
         "kernel_ms": {"ring_fused": ms_fz / args.steps,
                       "block_update": ms_upd / args.steps, "state_init": ms_init / args.steps,
@@ -841,7 +845,7 @@ def main():
     ap.add_argument("--workload", default="gqa-128k", choices=sorted(WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-step-seconds", type=float, default=6.0)
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--clock-log", default=None,
                     help="directory for the raw nvidia-smi clock samples of the timed region")

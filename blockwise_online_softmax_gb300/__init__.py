@@ -12,11 +12,13 @@ from .binding import (  # noqa: E402,F401
     layout_positions,
     ra_block_update,
     ra_block_update_masked,
+    ra_cached_memory,
     ra_decode_forward,
     ra_decode_partial,
     ra_device_status,
     ra_finalize,
     ra_merge,
+    ra_release_cached_memory,
     ra_ring_forward,
     ra_ring_forward_host,
     ra_ring_forward_masked,

@@ -25,7 +25,7 @@ RA_ERR_ALLOC = -5
 RA_F32 = 0
 RA_BF16 = 1
 LAYOUTS = {"contiguous": 0, "zigzag": 1, "striped": 2}
-ABI_VERSION = 2
+ABI_VERSION = 3
 KERNEL_KINDS = {
     "state_init": 0,
     "block_update_bf16": 1,
@@ -69,6 +69,8 @@ _SIGNATURES = {
     "ra_decode_forward": ("PPPPPLLiLiLiiiiP", "i"),
     "ra_device_status": ("P", "i"),
     "ra_selftest_wait_timeout": ("LP", "i"),
+    "ra_cached_memory": ("P", "i"),
+    "ra_release_cached_memory": ("", "i"),
     "ra_trace_enable": ("i", "i"),
     "ra_trace_reset": ("", "i"),
     "ra_trace_query": ("iPP", "i"),
@@ -452,6 +454,17 @@ def ra_device_status(stream=None):
 
 def ra_selftest_wait_timeout(limit_cycles: int, stream=None) -> int:
     return lib().ra_selftest_wait_timeout(int(limit_cycles), _stream(stream))
+
+
+def ra_cached_memory() -> int:
+    """Bytes the library's scratch pool holds on the current device."""
+    n = ctypes.c_longlong(0)
+    _check(lib().ra_cached_memory(ctypes.addressof(n)))
+    return int(n.value)
+
+
+def ra_release_cached_memory():
+    _check(lib().ra_release_cached_memory())
 
 
 def ra_trace_enable(on: bool = True):

@@ -93,6 +93,50 @@ struct TraceScope {
   }
 };
 
+// ----------------------------------------------------------------- scratch
+// Scratch and staging buffers come from a memory pool the library owns on
+// each device.  Its release threshold is unlimited, so memory freed at the
+// end of a call stays mapped for the next one: a fresh multi-GB mapping
+// costs milliseconds per call, which the default pool (threshold 0) would
+// pay every time.  ra_release_cached_memory() trims the pools.
+constexpr int kMaxDevices = 64;
+std::mutex g_pool_mu;
+cudaMemPool_t g_pool[kMaxDevices] = {};
+
+cudaError_t scratch_pool(cudaMemPool_t* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> g(g_pool_mu);
+  if (!g_pool[dev]) {
+    cudaMemPoolProps props{};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.handleTypes = cudaMemHandleTypeNone;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool = nullptr;
+    if ((e = cudaMemPoolCreate(&pool, &props)) != cudaSuccess) return e;
+    uint64_t keep = UINT64_MAX;
+    if ((e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess) {
+      cudaMemPoolDestroy(pool);
+      return e;
+    }
+    g_pool[dev] = pool;
+  }
+  *out = g_pool[dev];
+  return cudaSuccess;
+}
+
+// Stream-ordered allocation from the current device's pool; the buffer is
+// returned with cudaFreeAsync like any other.
+cudaError_t scratch_alloc(void** p, size_t bytes, cudaStream_t st) {
+  cudaMemPool_t pool = nullptr;
+  cudaError_t e = scratch_pool(&pool);
+  if (e != cudaSuccess) return e;
+  return cudaMallocFromPoolAsync(p, bytes, pool, st);
+}
+
 // ----------------------------------------------------------------- TMA maps
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -436,10 +480,10 @@ int ring_forward_alloc(const void* q, const void* k, const void* v, float* out, 
     return ring_fused_impl(q, k, v, out, lse, N, P, mk, d, heads, kv_heads, st);
   float* l_scratch = nullptr;
   const size_t l_bytes = static_cast<size_t>(N) * heads * sizeof(float);
-  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&l_scratch), l_bytes, st);
+  cudaError_t e = scratch_alloc(reinterpret_cast<void**>(&l_scratch), l_bytes, st);
   if (e != cudaSuccess) {
     cudaGetLastError();
-    return fail(RA_ERR_ALLOC, "cudaMallocAsync of %zu bytes for the l state failed: %s", l_bytes,
+    return fail(RA_ERR_ALLOC, "pool allocation of %zu bytes for the l state failed: %s", l_bytes,
                 cudaGetErrorString(e));
   }
   rc = ring_forward_impl(q, k, v, out, lse, N, P, mk, d, heads, kv_heads, dtype, st, l_scratch);
@@ -456,7 +500,6 @@ int ring_forward_alloc(const void* q, const void* k, const void* v, float* out, 
 constexpr long long kNoAllocMaxRowsHeads = 1LL << 22;  // N * heads <= 4,194,304
 static __device__ __align__(256) float g_noalloc_l[kNoAllocMaxRowsHeads];
 
-constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mu;
 float* g_noalloc_ptr[kMaxDevices] = {};
 
@@ -485,11 +528,11 @@ int ring_backward_impl(const void* q, const void* k, const void* v, const float*
                        long long N, int P, const MaskSpec& mk, int d, int heads, int kv_heads,
                        cudaStream_t st) {
   float* dvec = nullptr;
-  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&dvec),
+  cudaError_t e = scratch_alloc(reinterpret_cast<void**>(&dvec),
                                   static_cast<size_t>(N) * heads * sizeof(float), st);
   if (e != cudaSuccess) {
     cudaGetLastError();
-    return fail(RA_ERR_ALLOC, "cudaMallocAsync of the D vector failed: %s", cudaGetErrorString(e));
+    return fail(RA_ERR_ALLOC, "pool allocation of the D vector failed: %s", cudaGetErrorString(e));
   }
   int rc = RA_OK;
   {
@@ -605,11 +648,11 @@ int decode_run(const void* q, const void* k, const void* v, float* m, float* l, 
   const long long rows = n_q * heads;  // state rows of one shard
   const size_t n_part = static_cast<size_t>(nshard) * nsplit * rows;
   float* part = nullptr;
-  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&part),
+  cudaError_t e = scratch_alloc(reinterpret_cast<void**>(&part),
                                   n_part * (2 + static_cast<size_t>(d)) * sizeof(float), st);
   if (e != cudaSuccess) {
     cudaGetLastError();
-    return fail(RA_ERR_ALLOC, "cudaMallocAsync of the decode partial states failed: %s",
+    return fail(RA_ERR_ALLOC, "pool allocation of the decode partial states failed: %s",
                 cudaGetErrorString(e));
   }
   int rc = get_encoder();
@@ -661,7 +704,7 @@ int decode_run(const void* q, const void* k, const void* v, float* m, float* l, 
 
 extern "C" {
 
-int ra_abi_version(void) { return 2; }
+int ra_abi_version(void) { return 3; }
 
 const char* ra_status_string(int status) {
   switch (status) {
@@ -818,10 +861,10 @@ int ra_ring_forward(const void* q, const void* k, const void* v, float* out, flo
 // The bf16 host-buffer ring in pipelined groups of KV heads (heads never
 // interact): the inputs of group G + 1 copy in and the outputs of group
 // G - 1 copy out while group G runs.  Copies are pitched (a group is a
-// column range of every token row) on two helper streams, ordered against
-// the caller's stream, which runs the kernels, by events.  Device buffers
-// are allocated on the caller's stream and freed there once every copy
-// is done.
+// column range of every token row) on two helper streams; the kernels run
+// on the caller's stream and a third helper stream in turn; events order
+// them all.  Device buffers are allocated on the caller's stream and freed
+// there once every copy and kernel is done.
 static int ring_forward_host_pipelined(const void* q_host, const void* k_host,
                                        const void* v_host, float* out_host, float* lse_host,
                                        long long N, int P, int causal, int d, int heads,
@@ -836,15 +879,15 @@ static int ring_forward_host_pipelined(const void* q_host, const void* k_host,
   const size_t rh_bytes = static_cast<size_t>(N) * heads * sizeof(float);
   void *dq = nullptr, *dk = nullptr, *dv = nullptr;
   float *dout = nullptr, *dlse = nullptr;
-  cudaStream_t s_in = nullptr, s_out = nullptr;
-  cudaEvent_t ev_alloc = nullptr, ev_end = nullptr, ev_inall = nullptr;
+  cudaStream_t s_in = nullptr, s_out = nullptr, s_c1 = nullptr;
+  cudaEvent_t ev_alloc = nullptr, ev_end = nullptr, ev_inall = nullptr, ev_c1 = nullptr;
   cudaEvent_t ev_in[kHostGroups] = {}, ev_run[kHostGroups] = {};
   cudaError_t e = cudaSuccess;
   auto ok = [&](cudaError_t x) {
     if (e == cudaSuccess) e = x;
     return e == cudaSuccess;
   };
-  auto alloc = [&](void** p, size_t n) { ok(cudaMallocAsync(p, n, st)); };
+  auto alloc = [&](void** p, size_t n) { ok(scratch_alloc(p, n, st)); };
   alloc(&dq, q_bytes);
   alloc(&dk, kv_bytes);
   alloc(&dv, kv_bytes);
@@ -852,7 +895,7 @@ static int ring_forward_host_pipelined(const void* q_host, const void* k_host,
   alloc(reinterpret_cast<void**>(&dlse), rh_bytes);
   if (e != cudaSuccess) {
     cudaGetLastError();
-    int rc = fail(RA_ERR_ALLOC, "cudaMallocAsync of device staging failed: %s",
+    int rc = fail(RA_ERR_ALLOC, "pool allocation of device staging failed: %s",
                   cudaGetErrorString(e));
     void* bufs[5] = {dq, dk, dv, dout, dlse};
     for (void* p : bufs)
@@ -861,7 +904,9 @@ static int ring_forward_host_pipelined(const void* q_host, const void* k_host,
   }
   ok(cudaStreamCreateWithFlags(&s_in, cudaStreamNonBlocking));
   ok(cudaStreamCreateWithFlags(&s_out, cudaStreamNonBlocking));
+  ok(cudaStreamCreateWithFlags(&s_c1, cudaStreamNonBlocking));
   ok(cudaEventCreateWithFlags(&ev_alloc, cudaEventDisableTiming));
+  ok(cudaEventCreateWithFlags(&ev_c1, cudaEventDisableTiming));
   ok(cudaEventCreateWithFlags(&ev_end, cudaEventDisableTiming));
   ok(cudaEventCreateWithFlags(&ev_inall, cudaEventDisableTiming));
   for (int G = 0; G < ng; ++G) {
@@ -872,6 +917,7 @@ static int ring_forward_host_pipelined(const void* q_host, const void* k_host,
   if (e == cudaSuccess) {
     ok(cudaEventRecord(ev_alloc, st));
     ok(cudaStreamWaitEvent(s_in, ev_alloc, 0));
+    ok(cudaStreamWaitEvent(s_c1, ev_alloc, 0));
     const size_t qrow = static_cast<size_t>(heads) * d * 2, kvrow = static_cast<size_t>(kv_heads) * d * 2;
     for (int G = 0; G < ng && e == cudaSuccess; ++G) {
       const size_t qo = static_cast<size_t>(G) * gq * d * 2, ko = static_cast<size_t>(G) * gkv * d * 2;
@@ -885,12 +931,16 @@ static int ring_forward_host_pipelined(const void* q_host, const void* k_host,
       ok(cudaEventRecord(ev_in[G], s_in));
     }
     cudaEventRecord(ev_inall, s_in);  // after every copy that was enqueued
+    // Groups alternate between two compute streams, so the CTAs of group
+    // G+1 fill the SMs that group G's last wave leaves idle.
+    cudaStream_t cs[2] = {st, s_c1};
     for (int G = 0; G < ng && e == cudaSuccess && rc == RA_OK; ++G) {
-      ok(cudaStreamWaitEvent(st, ev_in[G], 0));
+      cudaStream_t c = cs[G & 1];
+      ok(cudaStreamWaitEvent(c, ev_in[G], 0));
       if (e != cudaSuccess) break;
       rc = ring_fused_impl(dq, dk, dv, dout, dlse, N, P, plain_mask(causal), d, heads, kv_heads,
-                           st, G * gq, gq);
-      ok(cudaEventRecord(ev_run[G], st));
+                           c, G * gq, gq);
+      ok(cudaEventRecord(ev_run[G], c));
       ok(cudaStreamWaitEvent(s_out, ev_run[G], 0));
       const size_t orow = static_cast<size_t>(heads) * d * 4, oo = static_cast<size_t>(G) * gq * d * 4;
       ok(cudaMemcpy2DAsync(reinterpret_cast<char*>(out_host) + oo, orow,
@@ -902,15 +952,19 @@ static int ring_forward_host_pipelined(const void* q_host, const void* k_host,
       ok(cudaMemcpyAsync(lse_host, dlse, rh_bytes, cudaMemcpyDeviceToHost, s_out));
     // The caller's stream, which frees the buffers, waits for every copy.
     cudaEventRecord(ev_end, s_out);
+    cudaEventRecord(ev_c1, s_c1);
     cudaStreamWaitEvent(st, ev_end, 0);
     cudaStreamWaitEvent(st, ev_inall, 0);
+    cudaStreamWaitEvent(st, ev_c1, 0);
   }
   void* bufs[5] = {dq, dk, dv, dout, dlse};
   for (void* p : bufs)
     if (p) cudaFreeAsync(p, st);
   if (s_in) cudaStreamDestroy(s_in);
   if (s_out) cudaStreamDestroy(s_out);
+  if (s_c1) cudaStreamDestroy(s_c1);
   if (ev_alloc) cudaEventDestroy(ev_alloc);
+  if (ev_c1) cudaEventDestroy(ev_c1);
   if (ev_end) cudaEventDestroy(ev_end);
   if (ev_inall) cudaEventDestroy(ev_inall);
   for (int G = 0; G < ng; ++G) {
@@ -947,7 +1001,7 @@ int ra_ring_forward_host(const void* q_host, const void* k_host, const void* v_h
   float *dout = nullptr, *dlse = nullptr, *dl = nullptr;
   cudaError_t e = cudaSuccess;
   auto alloc = [&](void** p, size_t n) {
-    if (e == cudaSuccess) e = cudaMallocAsync(p, n, st);
+    if (e == cudaSuccess) e = scratch_alloc(p, n, st);
   };
   alloc(&dq, q_bytes);
   alloc(&dk, kv_bytes);
@@ -957,7 +1011,7 @@ int ra_ring_forward_host(const void* q_host, const void* k_host, const void* v_h
   alloc(reinterpret_cast<void**>(&dl), rh_bytes);
   if (e != cudaSuccess) {
     cudaGetLastError();
-    rc = fail(RA_ERR_ALLOC, "cudaMallocAsync of device staging failed: %s", cudaGetErrorString(e));
+    rc = fail(RA_ERR_ALLOC, "pool allocation of device staging failed: %s", cudaGetErrorString(e));
   } else {
     e = cudaMemcpyAsync(dq, q_host, q_bytes, cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) e = cudaMemcpyAsync(dk, k_host, kv_bytes, cudaMemcpyHostToDevice, st);
@@ -1057,10 +1111,10 @@ int ra_decode_forward(const void* q, const void* k, const void* v, float* out, f
   const long long rows = n_q * heads;
   if (n_kv == 0) {  // no key: every row is empty (out = 0, lse = -inf)
     float* l0 = nullptr;
-    cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&l0), rows * sizeof(float), st);
+    cudaError_t e = scratch_alloc(reinterpret_cast<void**>(&l0), rows * sizeof(float), st);
     if (e != cudaSuccess) {
       cudaGetLastError();
-      return fail(RA_ERR_ALLOC, "cudaMallocAsync of %lld floats failed", rows);
+      return fail(RA_ERR_ALLOC, "pool allocation of %lld floats failed", rows);
     }
     e = ra::launch_state_init(lse, l0, out, n_q, heads, d, st);
     if (e == cudaSuccess) e = ra::launch_finalize(lse, l0, out, out, lse, n_q, heads, d, st);
@@ -1074,11 +1128,11 @@ int ra_decode_forward(const void* q, const void* k, const void* v, float* out, f
   // Shard states: m, l [nshard][rows], o [nshard][rows][d].
   float* sstate = nullptr;
   const size_t n_rows = static_cast<size_t>(nshard) * rows;
-  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&sstate),
+  cudaError_t e = scratch_alloc(reinterpret_cast<void**>(&sstate),
                                   n_rows * (2 + static_cast<size_t>(d)) * sizeof(float), st);
   if (e != cudaSuccess) {
     cudaGetLastError();
-    return fail(RA_ERR_ALLOC, "cudaMallocAsync of the shard states failed: %s", cudaGetErrorString(e));
+    return fail(RA_ERR_ALLOC, "pool allocation of the shard states failed: %s", cudaGetErrorString(e));
   }
   float* so = sstate;
   float* sm = so + n_rows * d;
@@ -1138,6 +1192,34 @@ int ra_selftest_wait_timeout(long long limit_cycles, void* stream) {
 int ra_trace_enable(int on) {
   std::lock_guard<std::mutex> g(g_trace_mu);
   g_trace_on = on != 0;
+  return RA_OK;
+}
+
+int ra_cached_memory(long long* bytes) {
+  if (!bytes) return fail(RA_ERR_INVALID, "bytes is NULL");
+  *bytes = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return RA_OK;
+  std::lock_guard<std::mutex> g(g_pool_mu);
+  if (!g_pool[dev]) return RA_OK;
+  uint64_t held = 0;
+  e = cudaMemPoolGetAttribute(g_pool[dev], cudaMemPoolAttrReservedMemCurrent, &held);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemPoolGetAttribute");
+  *bytes = static_cast<long long>(held);
+  return RA_OK;
+}
+
+int ra_release_cached_memory(void) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return RA_OK;
+  std::lock_guard<std::mutex> g(g_pool_mu);
+  if (!g_pool[dev]) return RA_OK;
+  e = cudaMemPoolTrimTo(g_pool[dev], 0);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemPoolTrimTo");
   return RA_OK;
 }
 

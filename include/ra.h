@@ -416,6 +416,28 @@ int ra_device_status(void* stream);
  */
 int ra_selftest_wait_timeout(long long limit_cycles, void* stream);
 
+/*
+ * Cached scratch memory.  Every buffer the library allocates for itself
+ * (the l state of ra_ring_forward on the step path, the device staging of
+ * ra_ring_forward_host, the D vector of the backward, the partial states of
+ * decode) comes, stream-ordered, from a memory pool that the library
+ * creates on each device at first use.  The pool keeps what is freed into
+ * it mapped, so the next call of the same size maps nothing: a call that
+ * needs a few GB of staging does not pay milliseconds for a fresh mapping.
+ * Ownership stays with the library, and what the pool holds is bounded by
+ * the largest set of buffers one call (or concurrent calls) held.
+ *
+ * ra_cached_memory -- write to *bytes the memory the current device's pool
+ *   holds (in use or cached); 0 before any allocation.  RA_ERR_INVALID if
+ *   `bytes` is NULL.
+ * ra_release_cached_memory -- return to the driver what the current
+ *   device's pool holds and no call is using.  Memory that an enqueued call
+ *   will still free stays until the work before that free has completed:
+ *   synchronize the streams first to release everything.
+ */
+int ra_cached_memory(long long* bytes);
+int ra_release_cached_memory(void);
+
 /* Tracing.  When enabled, the library records a CUDA event pair on the
  * launching stream around every kernel it launches.  ra_trace_query then
  * synchronizes those events.  It returns the number of launches of `kind`

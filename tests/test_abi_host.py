@@ -45,7 +45,7 @@ def test_binding_covers_every_declared_symbol():
 
 
 def test_status_strings(lib):
-    assert lib.ra_abi_version() == 2
+    assert lib.ra_abi_version() == 3
     for code, name in ((0, b"RA_OK"), (-1, b"RA_ERR_INVALID"), (-2, b"RA_ERR_UNSUPPORTED"),
                        (-3, b"RA_ERR_CUDA"), (-4, b"RA_ERR_TIMEOUT"), (-5, b"RA_ERR_ALLOC")):
         assert lib.ra_status_string(code) == name

@@ -213,6 +213,26 @@ def test_host_buffer_entry_point(shape):
     assert torch.equal(out_h, out_d.cpu()) and torch.equal(lse_h, lse_d.cpu())
 
 
+def test_scratch_pool_keeps_and_releases_staging():
+    """The host-buffer call's device staging comes from the library's pool:
+    it stays cached after the call (a second call of the same size adds
+    nothing) and goes back to the driver on release."""
+    N, heads, kv_heads, d = 4096, 8, 2, 128
+    q, k, v = inputs.make_random(N, heads, kv_heads, d, dtype=torch.bfloat16, seed=23)
+    q, k, v = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    staging = N * heads * d * 2 + 2 * N * kv_heads * d * 2 + N * heads * (d + 1) * 4
+    out1, lse1 = ra.ra_ring_forward_host(q, k, v, P=4, causal=True)
+    torch.cuda.synchronize()
+    held = ra.ra_cached_memory()
+    assert held >= staging
+    out2, lse2 = ra.ra_ring_forward_host(q, k, v, P=4, causal=True)
+    torch.cuda.synchronize()
+    assert ra.ra_cached_memory() == held
+    assert torch.equal(out1, out2) and torch.equal(lse1, lse2)
+    ra.ra_release_cached_memory()
+    assert ra.ra_cached_memory() == 0
+
+
 def test_more_than_256_ranks_takes_the_step_path():
     """bf16 with P > 256 (beyond the fused launch's visit table) runs one
     launch per ring step; it gives the attention of the fused P = 256 ring
