@@ -104,6 +104,11 @@ def test_zero_size_work_is_a_no_op(lib):
     assert lib.ra_finalize(None, None, None, None, None, 0, 64, 1, None) == 0
 
 
+def test_cached_memory_arguments(lib):
+    assert lib.ra_cached_memory(None) == -1
+    assert b"NULL" in lib.ra_last_error()
+
+
 def test_trace_controls(lib):
     assert lib.ra_trace_enable(0) == 0
     assert lib.ra_trace_reset() == 0
