@@ -46,18 +46,6 @@
 
 namespace ra {
 
-// Integer bf16 packing (variant probe): both values rounded on the ALU pipe.
-__device__ __forceinline__ uint32_t pack_ta(float lo, float hi) {
-  const uint32_t a = __float_as_uint(lo) + 0x8000u, b = __float_as_uint(hi) + 0x8000u;
-  return __byte_perm(a, b, 0x7632);
-}
-__device__ __forceinline__ uint32_t pack_rne(float lo, float hi) {
-  uint32_t a = __float_as_uint(lo), b = __float_as_uint(hi);
-  a += 0x7fffu + ((a >> 16) & 1u);
-  b += 0x7fffu + ((b >> 16) & 1u);
-  return __byte_perm(a, b, 0x7632);
-}
-
 __device__ int g_bwd_status = 0;
 
 namespace {
