@@ -3,9 +3,10 @@
 
 It reports causal-adjusted attention TFLOP/s, and the fraction of dense
 BF16 tensor peak, for ``ra_ring_forward``.  One step is one full forward:
-state init, the P ring steps (every virtual rank folds its visiting K/V
-block), and the finalize.  A step runs over one batch of the workload, with
-the inputs resident in HBM.
+in bf16 a single launch runs all P ring steps (every virtual rank folds
+each visiting K/V block into its state, kept on chip) and the finalize; in
+fp32 it is the state init, one launch per ring step and the finalize.  A
+step runs over one batch of the workload, with the inputs resident in HBM.
 
 FLOP convention: 4*d FLOPs per allowed (query, key) pair per query head
 (QK^T and PV, two each).  The causal pair count is N^2/2 ("causal-adjusted").
@@ -15,9 +16,12 @@ The JSON line also carries:
   e2e           the same metric through ra_ring_forward_host.  That call
                 copies pinned host Q/K/V to the device, runs, and copies O
                 and LSE back, every step.
-  roofline      the block-update kernel's achieved TFLOP/s against the
-                measured dense BF16 peak, timed by the library's per-launch
-                CUDA events on the launching stream.
+  roofline      the dominant kernel's achieved TFLOP/s (the fused ring in
+                bf16, the block update in fp32) against the measured
+                dense BF16 peak, timed by the library's per-launch CUDA
+                events on the launching stream, with its DRAM bytes per
+                launch from the committed ncu record while the kernel's
+                source is the one recorded.
   cpu_baseline  the fp64 CPU oracle on a bounded sample of the same
                 workload, on this host's cores.
   clocks        SM clocks and throttle reasons sampled during the timed
@@ -27,9 +31,11 @@ The JSON line also carries:
 the same workload, metric and unit.
 
 Decode runs (--decode decode-1m | decode-1m-q4) time ra_decode_forward: a
-few query tokens against a 1M-token K/V history in P shards.  That path is
-HBM-bound, so its metric is the K/V bytes read per second, and its
-roofline is against the measured HBM copy bandwidth.
+few query tokens against a 1M-token K/V history in P shards: the split-K
+chunk kernel, then one launch that merges every partial state and
+finalizes.  That path is HBM-bound, so its metric is the K/V bytes read per
+second, and its roofline is the chunk kernel against the measured HBM copy
+bandwidth.
 
 Backward runs (--backward) time ra_ring_backward on the workload, given
 the forward's outputs: the pre-pass, then per ring step the dQ and the
@@ -255,18 +261,23 @@ def note_window(clk, pad):
 
 
 # ------------------------------------------------------------------ traffic record
-def kernel_digest() -> str:
+FORWARD_SOURCES = ("umma_kernel.cu", "ptx.cuh", "ra_internal.h")
+DECODE_SOURCES = ("decode_kernel.cu", "ptx.cuh", "ra_internal.h")
+
+
+def kernel_digest(files=FORWARD_SOURCES) -> str:
     h = hashlib.sha256()
-    for f in ("umma_kernel.cu", "ptx.cuh", "ra_internal.h"):
+    for f in files:
         with open(os.path.join(ROOT, "blockwise_online_softmax_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str, profile: str = "block_update_bf16_traffic.md"):
+def recorded_traffic(workload: str, profile: str = "block_update_bf16_traffic.md",
+                     files=FORWARD_SOURCES):
     """DRAM bytes per launch of the dominant kernel from its committed ncu
-    summary, if it was taken on the current kernel source (digest match),
-    else None."""
+    summary, if it was taken on the current source of that kernel (digest
+    of `files` matches), else None."""
     p = os.path.join(ROOT, "profiles", profile)
     try:
         text = open(p).read()
@@ -274,7 +285,7 @@ def recorded_traffic(workload: str, profile: str = "block_update_bf16_traffic.md
         return None
     dig = re.search(r"kernel_digest:\s*([0-9a-f]+)", text)
     val = re.search(rf"traffic_bytes_per_launch\[{re.escape(workload)}\]:\s*([0-9.eE+]+)", text)
-    if not dig or not val or dig.group(1) != kernel_digest():
+    if not dig or not val or dig.group(1) != kernel_digest(files):
         return None
     return float(val.group(1))
 
@@ -475,7 +486,8 @@ def run_decode(args, ws, rank, local):
         "kernel_ms": {kd_: t / args.steps for kd_, (n, t) in trace.items()},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": (achieved / peaks["hbm_gbs"]) if achieved else None,
-                     "traffic": None, "kernel": "decode split-K (CUDA cores, TMA)",
+                     "traffic": recorded_traffic(w.name, "decode_tc_traffic.md", DECODE_SOURCES),
+                     "kernel": "decode split-K chunks (tcgen05, TMA)",
                      "peak_kind": f"hbm_gbs ({peak_src})"},
         "cpu_baseline": cpu,
     }

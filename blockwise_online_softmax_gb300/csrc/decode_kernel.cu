@@ -17,9 +17,12 @@
 //     which the pipe has to spare, not bytes.  It writes one partial state
 //     (m, l, O~) per chunk.
 //   * decode_combine_kernel folds a shard's chunk states into that shard's
-//     running state, one warp per (shard, query row, head).
-// Across shards the host reduces with the merge kernel of ra_merge, in a
-// tree.
+//     running state, one warp per (shard, query row, head) (one shard's
+//     partial state, ra_decode_partial).
+//   * decode_reduce_kernel folds the chunk states of every shard and
+//     finalizes, one CTA per (query row, head) (the whole decode,
+//     ra_decode_forward): the global reduction of the merge operator and
+//     the normalization in one launch.
 #include <cmath>
 #include <cstdint>
 
@@ -444,6 +447,74 @@ __global__ void decode_combine_kernel(float* __restrict__ m, float* __restrict__
   }
 }
 
+// The global reduction and the finalize in one launch: for each (query row,
+// head), the chunk partial states of every shard are folded with the
+// online-softmax merge (one max, then the rescaled sums) and the result is
+// normalized, out = O / l and lse = m + ln l (out = 0 and lse = -inf where
+// no key is allowed).  One CTA per (row, head): its warps take every
+// RW-th partial, lanes hold D / 32 columns each, and the warps' sums meet
+// in shared memory.
+constexpr int RW = 8;  // warps per CTA of the reduction
+template <int D>
+__global__ void __launch_bounds__(RW * 32)
+decode_reduce_kernel(float* __restrict__ out, float* __restrict__ lse,
+                     const float* __restrict__ pm, const float* __restrict__ pl,
+                     const float* __restrict__ po, long long rows, int np) {
+  constexpr int CPL = D / 32;  // columns per lane
+  __shared__ float s_max[RW], s_l[RW];
+  __shared__ __align__(16) float s_o[RW][D];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const long long rh = blockIdx.x;
+  float mx = -INFINITY;
+  for (int p = tid; p < np; p += RW * 32) mx = fmaxf(mx, pm[p * rows + rh]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  if (lane == 0) s_max[warp] = mx;
+  __syncthreads();
+  mx = s_max[0];
+#pragma unroll
+  for (int w = 1; w < RW; ++w) mx = fmaxf(mx, s_max[w]);
+  float acc[CPL];
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
+  float lsum = 0.f;
+  if (mx > -INFINITY) {
+    for (int p = warp; p < np; p += RW) {
+      const float ms = pm[p * rows + rh];
+      if (ms == -INFINITY) continue;  // warp-uniform: an empty partial adds nothing
+      const float e = expf(ms - mx);
+      lsum = fmaf(e, pl[p * rows + rh], lsum);
+      const float* src = po + (p * rows + rh) * D + CPL * lane;
+      if constexpr (CPL == 4) {
+        const float4 x = *reinterpret_cast<const float4*>(src);
+        acc[0] = fmaf(e, x.x, acc[0]);
+        acc[1] = fmaf(e, x.y, acc[1]);
+        acc[2] = fmaf(e, x.z, acc[2]);
+        acc[3] = fmaf(e, x.w, acc[3]);
+      } else {
+        const float2 x = *reinterpret_cast<const float2*>(src);
+        acc[0] = fmaf(e, x.x, acc[0]);
+        acc[1] = fmaf(e, x.y, acc[1]);
+      }
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) s_o[warp][CPL * lane + c] = acc[c];
+  if (lane == 0) s_l[warp] = lsum;
+  __syncthreads();
+  float l = 0.f;
+#pragma unroll
+  for (int w = 0; w < RW; ++w) l += s_l[w];
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  for (int x = tid; x < D; x += RW * 32) {
+    float o = 0.f;
+#pragma unroll
+    for (int w = 0; w < RW; ++w) o += s_o[w][x];
+    out[rh * D + x] = o * inv;
+  }
+  if (tid == 0) lse[rh] = l > 0.f ? mx + logf(l) : -INFINITY;
+}
+
 template <int D>
 cudaError_t launch_tc_d(const DecArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                         const CUtensorMap& tv, cudaStream_t st) {
@@ -478,6 +549,18 @@ cudaError_t launch_decode_combine(float* m, float* l, float* o, const float* pm,
   else
     decode_combine_kernel<64><<<static_cast<unsigned>(blocks), threads, 0, st>>>(
         m, l, o, pm, pl, po, rows_per_shard, nsplit, n_rh);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_reduce(float* out, float* lse, const float* pm, const float* pl,
+                                 const float* po, long long rows, int np, int d, cudaStream_t st) {
+  if (rows == 0) return cudaSuccess;
+  if (d == 128)
+    decode_reduce_kernel<128><<<static_cast<unsigned>(rows), RW * 32, 0, st>>>(out, lse, pm, pl,
+                                                                               po, rows, np);
+  else
+    decode_reduce_kernel<64><<<static_cast<unsigned>(rows), RW * 32, 0, st>>>(out, lse, pm, pl,
+                                                                             po, rows, np);
   return cudaGetLastError();
 }
 

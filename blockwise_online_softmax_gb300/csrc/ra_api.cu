@@ -619,10 +619,14 @@ int decode_args_check(const void* q, const void* k, const void* v, long long n_q
 
 // Split-K launch over nshard shards of shard_len keys, then the combine of
 // each shard's partials into its state (m, l, o: [nshard][n_q][heads]).
+// The split-K chunk kernel over nshard shards of shard_len keys, then
+// either the fold of each shard's chunk states into that shard's state
+// (m, l, o: [nshard][rows]) or, with out and lse given, the reduction over
+// every shard and the finalize straight into out and lse.
 int decode_run(const void* q, const void* k, const void* v, float* m, float* l, float* o,
                long long n_q, long long n_kv, long long shard_len, int nshard, long long q_off,
                long long kv_off, int causal, long long window, int d, int heads, int kv_heads,
-               cudaStream_t st) {
+               cudaStream_t st, float* out = nullptr, float* lse = nullptr) {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -688,6 +692,11 @@ int decode_run(const void* q, const void* k, const void* v, float* m, float* l, 
     t0.done(e == cudaSuccess);
     if (e != cudaSuccess) {
       rc = cuda_fail(e, "decode split launch");
+    } else if (out) {
+      TraceScope t1(RA_KERNEL_DECODE_COMBINE, st);
+      e = ra::launch_decode_reduce(out, lse, a.pm, a.pl, a.po, rows, nshard * a.nsplit, d, st);
+      t1.done(e == cudaSuccess);
+      if (e != cudaSuccess) rc = cuda_fail(e, "decode reduce launch");
     } else {
       TraceScope t1(RA_KERNEL_DECODE_COMBINE, st);
       e = ra::launch_decode_combine(m, l, o, a.pm, a.pl, a.po, rows, a.nsplit, nshard, d, st);
@@ -1125,46 +1134,10 @@ int ra_decode_forward(const void* q, const void* k, const void* v, float* out, f
   if ((rc = check_ptrs({k, v})) != RA_OK) return rc;
   const long long shard_len = (n_kv + P - 1) / P;
   const int nshard = static_cast<int>((n_kv + shard_len - 1) / shard_len);
-  // Shard states: m, l [nshard][rows], o [nshard][rows][d].
-  float* sstate = nullptr;
-  const size_t n_rows = static_cast<size_t>(nshard) * rows;
-  cudaError_t e = scratch_alloc(reinterpret_cast<void**>(&sstate),
-                                  n_rows * (2 + static_cast<size_t>(d)) * sizeof(float), st);
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return fail(RA_ERR_ALLOC, "pool allocation of the shard states failed: %s", cudaGetErrorString(e));
-  }
-  float* so = sstate;
-  float* sm = so + n_rows * d;
-  float* sl = sm + n_rows;
-  {
-    TraceScope t0(RA_KERNEL_STATE_INIT, st);
-    e = ra::launch_state_init(sm, sl, so, static_cast<long long>(nshard) * n_q, heads, d, st);
-    t0.done(e == cudaSuccess);
-  }
-  rc = e == cudaSuccess ? RA_OK : cuda_fail(e, "state-init launch");
-  if (rc == RA_OK)
-    rc = decode_run(q, k, v, sm, sl, so, n_q, n_kv, shard_len, nshard, q_off, 0, causal, window,
-                    d, heads, kv_heads, st);
-  // Global reduction: a tree of merges, shard b into shard a.
-  for (int cnt = nshard; rc == RA_OK && cnt > 1;) {
-    const int half = cnt / 2, keep = cnt - half;
-    TraceScope tm(RA_KERNEL_MERGE, st);
-    e = ra::launch_merge(sm, sl, so, sm + keep * rows, sl + keep * rows, so + keep * rows * d,
-                         static_cast<long long>(half) * n_q, heads, d, st);
-    tm.done(e == cudaSuccess);
-    if (e != cudaSuccess) rc = cuda_fail(e, "merge launch");
-    cnt = keep;
-  }
-  if (rc == RA_OK) {
-    TraceScope tf(RA_KERNEL_FINALIZE, st);
-    e = ra::launch_finalize(sm, sl, so, out, lse, n_q, heads, d, st);
-    tf.done(e == cudaSuccess);
-    if (e != cudaSuccess) rc = cuda_fail(e, "finalize launch");
-  }
-  e = cudaFreeAsync(sstate, st);
-  if (rc == RA_OK && e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync");
-  return rc;
+  // Each shard's chunks give partial states; one launch then folds them all
+  // (the global reduction of the merge operator) and finalizes.
+  return decode_run(q, k, v, nullptr, nullptr, nullptr, n_q, n_kv, shard_len, nshard, q_off, 0,
+                    causal, window, d, heads, kv_heads, st, out, lse);
 }
 
 int ra_device_status(void* stream) {

@@ -264,6 +264,10 @@ cudaError_t launch_decode_tc(const DecArgs& a, int d, const CUtensorMap& tq, con
 cudaError_t launch_decode_combine(float* m, float* l, float* o, const float* pm, const float* pl,
                                   const float* po, long long rows_per_shard, int nsplit,
                                   int nshard, int d, cudaStream_t st);
+// Folds the np partial states of every (row, head) (partial p of row rh at
+// p * rows + rh) and finalizes into out [rows, d] and lse [rows].
+cudaError_t launch_decode_reduce(float* out, float* lse, const float* pm, const float* pl,
+                                 const float* po, long long rows, int np, int d, cudaStream_t st);
 
 // Device status words (one per kernel translation unit): read and clear.
 cudaError_t take_umma_status(int* code);

@@ -111,7 +111,9 @@ typedef enum {
   RA_KERNEL_MERGE = 3,
   RA_KERNEL_FINALIZE = 4,
   RA_KERNEL_DECODE_SPLIT = 5,   /* decode split-K chunk kernel (tcgen05, TMA) */
-  RA_KERNEL_DECODE_COMBINE = 6, /* folds a shard's split partial states */
+  RA_KERNEL_DECODE_COMBINE = 6, /* folds split partial states: into a shard's state
+                                   (ra_decode_partial) or over every shard with the
+                                   finalize (ra_decode_forward) */
   RA_KERNEL_BWD_PRE = 7,        /* backward: D = rowsum(dO * O) */
   RA_KERNEL_BWD_DQ = 8,         /* backward: dQ (tcgen05, Q-stationary) */
   RA_KERNEL_BWD_DKDV = 9,       /* backward: dK, dV (tcgen05, K/V-stationary) */
@@ -381,14 +383,14 @@ int ra_decode_partial(const void* q, const void* k, const void* v, float* m, flo
 /*
  * ra_decode_forward -- the whole decode attention of n_q query tokens
  * against a K/V history of n_kv tokens (positions 0 .. n_kv - 1) split into
- * P shards of ceil(n_kv / P) keys: the partial state of every shard (one
- * launch over all shards), then the global reduction as a tree of merges
- * (ceil(log2 P) launches of the ra_merge kernel), then the finalize.
+ * P shards of ceil(n_kv / P) keys: the partial states of every shard (one
+ * launch over all shards, each shard in a few key chunks), then one launch
+ * that folds all of them with the merge operator of ra_merge (the global
+ * reduction) and finalizes.
  *   out: [n_q, heads, d] fp32; lse: [n_q, heads] fp32 (written).
  * Query positions are q_off .. q_off + n_q - 1 (for decode after a history
  * of n_kv tokens that includes the new ones: q_off = n_kv - n_q).  With
- * n_kv = 0 every row gets out = 0 and lse = -inf.  Scratch as above, plus
- * the P shard states.
+ * n_kv = 0 every row gets out = 0 and lse = -inf.  Scratch as above.
  */
 int ra_decode_forward(const void* q, const void* k, const void* v, float* out, float* lse,
                       long long n_q, long long n_kv, int P, long long q_off, int causal,
