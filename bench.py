@@ -316,17 +316,25 @@ def cpu_model() -> str:
     return platform.processor() or platform.machine()
 
 
+FULL_PARITY_MAX_N = 8192  # up to this length every output row is compared
+
+
 def parity_check(w, q, k, v, out, lse, per_block: int = 2):
-    """Sampled-row parity of the timed run's own output against the fp64
-    oracle (rows {0, 1, 127, 128, c/2, c-1} and `per_block` random rows of
-    every block, all heads, each over its full key range)."""
+    """Parity of the timed run's own output against the fp64 oracle: every
+    row when N <= FULL_PARITY_MAX_N (the small workloads, a few seconds of
+    oracle time), else sampled rows ({0, 1, 127, 128, c/2, c-1} and
+    `per_block` random rows of every block); all heads, each row over its
+    full key range."""
     import numpy as np
     import torch
 
     import oracle
     from blockwise_online_softmax_gb300 import inputs
 
-    rows = inputs.sample_rows(w, random_per_block=per_block)
+    if w.N <= FULL_PARITY_MAX_N:
+        rows = np.arange(w.N, dtype=np.int64)
+    else:
+        rows = inputs.sample_rows(w, random_per_block=per_block)
     idx = torch.from_numpy(rows).to(out.device)
     got_o = out.index_select(0, idx).cpu().double().numpy()
     got_l = lse.index_select(0, idx).cpu().double().numpy()
@@ -337,7 +345,8 @@ def parity_check(w, q, k, v, out, lse, per_block: int = 2):
     e_o = float(np.abs(got_o - ref_o).max())
     e_l = float((np.abs(got_l[fin] - ref_l[fin]) / np.maximum(1.0, np.abs(ref_l[fin]))).max())
     tol_o, tol_l = (1e-2, 1e-3) if w.dtype == "bf16" else (1e-5, 1e-5)
-    return {"rows": int(len(rows)), "heads": w.heads, "max_abs_o": e_o, "max_rel_lse": e_l,
+    return {"rows": int(len(rows)), "all_rows": bool(len(rows) == w.N), "heads": w.heads,
+            "max_abs_o": e_o, "max_rel_lse": e_l,
             "tol_o": tol_o, "tol_lse": tol_l, "pass": bool(e_o <= tol_o and e_l <= tol_l),
             "oracle_s": dt}
 
