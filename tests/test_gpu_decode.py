@@ -106,6 +106,24 @@ def test_decode_without_keys():
     assert (out == 0).all() and torch.isneginf(lse).all()
 
 
+@pytest.mark.parametrize("window", [0, 3])
+def test_decode_rows_that_see_no_key(window):
+    """Query positions before the first key (q_off < 0, causal) see no key:
+    the reduction over the shards gives out = 0 and lse = -inf for them and
+    the plain result for the others."""
+    n_q, heads, kv_heads, d, n_kv = 6, 8, 2, 128, 700
+    q, k, v = qkv(n_q, heads, kv_heads, d, n_kv, seed=41)
+    q_off = -3  # positions -3 .. 2
+    out, lse = ra.ra_decode_forward(q.to(DEV), k.to(DEV), v.to(DEV), P=5, q_off=q_off,
+                                    causal=True, window=window)
+    ra.ra_device_status()
+    ref_out, ref_lse = oracle.attention(q, k, v, causal=True, window=window,
+                                        q_pos=q_off + np.arange(n_q), k_pos=np.arange(n_kv))
+    assert np.isneginf(ref_lse[:3]).all() and np.isfinite(ref_lse[3:]).all()
+    check_output(out, lse, ref_out, ref_lse, "bf16")
+    assert (out[:3].cpu() == 0).all()
+
+
 def test_decode_large_logits_stay_finite():
     q, k, v = qkv(1, 8, 8, 128, 4000, seed=11)
     k = (k.float() * 20).to(torch.bfloat16)
