@@ -200,9 +200,9 @@ int ra_ring_step(const void* q, const void* k, const void* v, float* m, float* l
  * across all P steps and the kernel writes out and lse once; no scratch.
  * fp32 (or P > 256): the state init, P ring-step launches with the O~ state
  * in `out` and m in `lse`, then the finalize.  The l state ([N, heads]
- * fp32) is then the only scratch, allocated with cudaMallocAsync on
- * `stream` and freed the same way; a failed allocation returns
- * RA_ERR_ALLOC.  Both give the results of init + ra_ring_step for
+ * fp32) is then the only scratch, allocated stream-ordered on `stream`
+ * from the library's scratch pool (see ra_cached_memory) and freed the
+ * same way; a failed allocation returns RA_ERR_ALLOC.  Both give the results of init + ra_ring_step for
  * s = 0..P-1 + ra_finalize, the fused launch up to the last roundings of
  * the finalize.
  */
@@ -234,8 +234,8 @@ int ra_ring_forward_host(const void* q_host, const void* k_host, const void* v_h
  * counterpart to this call; it is a deployment convenience.
  *   Arguments, layouts and results are those of ra_ring_forward.  The l
  *   state lives in a fixed 16 MiB device array that is part of the library
- *   (N * heads <= 4,194,304 fp32 entries), instead of memory from
- *   cudaMallocAsync.  Every GPU that loads the library holds that array until
+ *   (N * heads <= 4,194,304 fp32 entries), instead of memory from the
+ *   scratch pool.  Every GPU that loads the library holds that array until
  *   the process exits.  The call calls no cudaMalloc, cudaFree or other
  *   allocating routine.
  *   Larger problems return RA_ERR_UNSUPPORTED; use ra_ring_forward for them.
@@ -333,7 +333,7 @@ int ra_ring_forward_masked(const void* q, const void* k, const void* v, float* o
  * K/V-stationary one adding to dk, dv of block j; within a launch every
  * block has one writer, so nothing is atomic.  P and dS are rounded to bf16
  * for their products, as in the forward.  Scratch: D ([N, heads] fp32),
- * from cudaMallocAsync on `stream`.  dtype must be RA_BF16.
+ * stream-ordered on `stream` from the scratch pool.  dtype must be RA_BF16.
  */
 int ra_ring_backward(const void* q, const void* k, const void* v, const float* out,
                      const float* lse, const void* dout, float* dq, float* dk, float* dv,
@@ -372,8 +372,8 @@ int ra_ring_backward_masked(const void* q, const void* k, const void* v, const f
  * spread over the SMs (split-K), each chunk giving one partial state, and a
  * second kernel folds them into m, l, o.  A chunk runs on the tensor cores
  * with one row tile of the KV head's query rows.  The partial states
- * (chunks x n_q x heads x (d + 2) fp32) are allocated with cudaMallocAsync
- * on `stream`.
+ * (chunks x n_q x heads x (d + 2) fp32) are allocated stream-ordered on
+ * `stream` from the scratch pool.
  */
 int ra_decode_partial(const void* q, const void* k, const void* v, float* m, float* l, float* o,
                       long long n_q, long long n_kv, int d, int heads, int kv_heads,
