@@ -613,12 +613,13 @@ int decode_args_check(const void* q, const void* k, const void* v, long long n_q
   if (n_q > (1LL << 24))
     return fail(RA_ERR_UNSUPPORTED, "n_q=%lld query tokens exceeds 2^24; use the ring forward",
                 n_q);
+  // One reduction CTA per (query row, head): the count must fit a grid.
+  if (n_q * heads > 0x7FFFFFFFLL)
+    return fail(RA_ERR_UNSUPPORTED, "n_q * heads = %lld rows exceeds 2^31 - 1", n_q * heads);
   (void)q; (void)k; (void)v;
   return RA_OK;
 }
 
-// Split-K launch over nshard shards of shard_len keys, then the combine of
-// each shard's partials into its state (m, l, o: [nshard][n_q][heads]).
 // The split-K chunk kernel over nshard shards of shard_len keys, then
 // either the fold of each shard's chunk states into that shard's state
 // (m, l, o: [nshard][rows]) or, with out and lse given, the reduction over

@@ -132,6 +132,7 @@ def test_decode_rejects_bad_arguments(lib):
                                      d, heads, kv_heads, dtype, None)
     assert fwd(heads=258, kv_heads=2) == -2 and b"exceeds 128" in lib.ra_last_error()
     assert fwd(n_q=(1 << 24) + 1) == -2 and b"2^24" in lib.ra_last_error()
+    assert fwd(n_q=1 << 24, heads=256, kv_heads=2) == -2 and b"2^31" in lib.ra_last_error()
     assert fwd(dtype=0) == -2 and b"bf16" in lib.ra_last_error()
     assert fwd(P=0) == -1 and b"P=0" in lib.ra_last_error()
     assert fwd(window=-3) == -1 and b"window" in lib.ra_last_error()
