@@ -362,7 +362,8 @@ int ra_ring_backward_masked(const void* q, const void* k, const void* v, const f
  *   k, v: [n_kv, kv_heads, d] bf16, positions kv_off .. kv_off + n_kv - 1.
  *   m, l: [n_q, heads] fp32; o: [n_q, heads, d] fp32 (updated in place).
  *   causal and window: as in the masked calls (kp <= qp; |qp - kp| < window).
- *   heads / kv_heads must be <= 128 and n_q <= 2^24.  A KV head's query
+ *   heads / kv_heads must be <= 128, n_q <= 2^24 and n_q * heads <= 2^31 - 1
+ *   (RA_ERR_UNSUPPORTED otherwise).  A KV head's query
  *   rows (token qi of its g heads is row qi * g + hl) go in 128-row tiles of
  *   floor(128 / g) tokens; with (heads / kv_heads) * n_q <= 128, the decode
  *   case, they are one tile and each K/V byte is read once.  Each further
