@@ -1,0 +1,58 @@
+"""Host-side checks of bench.py's bookkeeping that need no GPU: the DRAM
+traffic records are reported only for the kernel source they were taken
+on, the clock window padding, and the parity check's row choice."""
+import numpy as np
+import pytest
+import torch
+
+import bench
+import oracle
+from blockwise_online_softmax_gb300 import inputs
+
+
+def test_traffic_records_match_the_current_sources():
+    # Both committed records were taken on the committed kernel sources.
+    fwd = bench.recorded_traffic("gqa-128k", "ring_fused_bf16_traffic.md")
+    dec = bench.recorded_traffic("decode-1m", "decode_tc_traffic.md", bench.DECODE_SOURCES)
+    assert fwd is not None and 8e9 < fwd < 2e10
+    # decode: K and V read once (4.295 GB) plus the small partial states
+    assert dec is not None and 4.29e9 < dec < 4.31e9
+
+
+def test_traffic_record_needs_its_own_digest():
+    # A record checked against another kernel's sources does not count, and
+    # a workload the record does not list gives nothing.
+    assert bench.recorded_traffic("gqa-128k", "ring_fused_bf16_traffic.md",
+                                  bench.DECODE_SOURCES) is None
+    assert bench.recorded_traffic("decode-1m", "decode_tc_traffic.md") is None
+    assert bench.recorded_traffic("mha-8k", "ring_fused_bf16_traffic.md") is None
+    assert bench.recorded_traffic("gqa-128k", "no_such_profile.md") is None
+
+
+def test_digests_differ_per_kernel():
+    assert bench.kernel_digest() != bench.kernel_digest(bench.DECODE_SOURCES)
+    assert len(bench.kernel_digest()) == 16
+
+
+def test_clock_padding_only_for_short_regions():
+    assert bench.pad_seconds(0.1, 5) == bench.CLOCK_PAD_S  # 0.5 s region
+    assert bench.pad_seconds(0.3, 5) == 0.0                # 1.5 s region
+    clk = bench.note_window({"sm_mhz": 2000.0}, 0.5)
+    assert "untimed steps" in clk["window"]
+    assert bench.note_window({"sm_mhz": 2000.0}, 0.0)["window"] == "timed region"
+
+
+def test_parity_check_takes_every_row_of_a_small_workload():
+    """On the fp32 exactness workload the check covers all 1024 rows, and
+    it catches one wrong output row that sampling could miss."""
+    w = inputs.WORKLOADS["tiny-exact"]
+    q, k, v = inputs.make_workload(w)
+    ref_o, ref_l = oracle.attention(q, k, v, causal=w.causal)
+    out = torch.from_numpy(ref_o).float()
+    lse = torch.from_numpy(ref_l).float()
+    good = bench.parity_check(w, q, k, v, out, lse)
+    assert good["all_rows"] and good["rows"] == w.N and good["pass"]
+    bad = out.clone()
+    bad[777, 0, 5] += 1e-3  # row 777 is none of the fixed rows {0, 1, 127, 128, c/2, c-1} of a block
+    res = bench.parity_check(w, q, k, v, bad, lse)
+    assert not res["pass"] and res["max_abs_o"] == pytest.approx(1e-3, rel=1e-2)
