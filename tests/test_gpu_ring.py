@@ -267,6 +267,29 @@ def trace_counts(run):
     return got
 
 
+@pytest.mark.parametrize("shape", [
+    # N, heads, kv_heads, d, P, layout, window
+    (16384, 8, 2, 128, 4, "contiguous", 0),
+    (8192, 8, 8, 64, 8, "contiguous", 0),
+    (12288, 4, 1, 128, 6, "zigzag", 3000),
+])
+def test_fused_ring_is_bitwise_repeatable(shape):
+    """The fused ring forward gives the same bits on every run: its order
+    of operations is fixed, so a difference would mean a race (an mbarrier
+    phase read two phases late, a TMEM buffer overwritten early)."""
+    N, heads, kv_heads, d, P, layout, window = shape
+    q, k, v = inputs.make_random(N, heads, kv_heads, d, seed=N + d)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    runs = []
+    for _ in range(4):
+        out, lse = ra.ra_ring_forward_masked(qd, kd, vd, P=P, layout=layout, causal=True,
+                                             window=window)
+        runs.append((out.clone(), lse.clone()))
+    ra.ra_device_status()
+    for out, lse in runs[1:]:
+        assert torch.equal(out, runs[0][0]) and torch.equal(lse, runs[0][1])
+
+
 def test_trace_counts_launches():
     """bf16: the whole ring is one fused launch.  fp32: state init, one
     block-update launch per ring step, finalize."""
