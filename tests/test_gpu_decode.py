@@ -124,6 +124,17 @@ def test_decode_rows_that_see_no_key(window):
     assert (out[:3].cpu() == 0).all()
 
 
+def test_decode_is_bitwise_repeatable():
+    """Chunk kernel and reduction have a fixed order of operations: every
+    run gives the same bits."""
+    q, k, v = qkv(4, 32, 8, 128, 50000, seed=17)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    runs = [ra.ra_decode_forward(qd, kd, vd, P=16, q_off=50000 - 4) for _ in range(4)]
+    ra.ra_device_status()
+    for out, lse in runs[1:]:
+        assert torch.equal(out, runs[0][0]) and torch.equal(lse, runs[0][1])
+
+
 def test_decode_large_logits_stay_finite():
     q, k, v = qkv(1, 8, 8, 128, 4000, seed=11)
     k = (k.float() * 20).to(torch.bfloat16)
