@@ -437,6 +437,8 @@ int ra_selftest_wait_timeout(long long limit_cycles, void* stream);
  *   device's pool holds and no call is using.  Memory that an enqueued call
  *   will still free stays until the work before that free has completed:
  *   synchronize the streams first to release everything.
+ * The pages have no counterpart to these two calls: they are the library's
+ * memory management, not part of the method.
  */
 int ra_cached_memory(long long* bytes);
 int ra_release_cached_memory(void);
