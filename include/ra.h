@@ -212,14 +212,18 @@ int ra_ring_forward(const void* q, const void* k, const void* v, float* out, flo
 
 /*
  * ra_ring_forward_host -- ra_ring_forward on HOST buffers.  It copies q, k
- * and v to stream-ordered device buffers, runs the ring, copies out and
- * lse back, frees the buffers, and synchronizes `stream` before it
- * returns.  Pinned host memory makes the copies asynchronous DMA.  In bf16
- * the work is split into up to 8 groups of KV heads (heads never interact):
- * group G runs on `stream` while group G + 1 copies in and group G - 1
- * copies out on two streams the call creates and destroys, ordered by
- * events.  The results are those of ra_ring_forward, bit for bit.  Device
- * wait timeouts are checked before return and give RA_ERR_TIMEOUT.
+ * and v to device buffers (stream-ordered, from the scratch pool), runs the
+ * ring, copies out and lse back, frees the buffers, and synchronizes
+ * `stream` before it returns.  Pinned host memory makes the copies
+ * asynchronous DMA.  In bf16 the work is split into up to 8 groups of KV
+ * heads (heads never interact): group G runs while group G + 1 copies in
+ * and group G - 1 copies out; the copies go on two streams the call
+ * creates and destroys, the groups' launches alternate between `stream`
+ * and a third such stream, and events order them all.  The results are
+ * those of ra_ring_forward, bit for bit.  Device wait timeouts are checked
+ * before return and give RA_ERR_TIMEOUT.  The pages have no counterpart:
+ * this is the host-to-host form of the call, for callers whose tensors
+ * live in host memory.
  */
 int ra_ring_forward_host(const void* q_host, const void* k_host, const void* v_host,
                          float* out_host, float* lse_host, long long N, int P, int causal, int d,
@@ -387,7 +391,9 @@ int ra_decode_partial(const void* q, const void* k, const void* v, float* m, flo
  * P shards of ceil(n_kv / P) keys: the partial states of every shard (one
  * launch over all shards, each shard in a few key chunks), then one launch
  * that folds all of them with the merge operator of ra_merge (the global
- * reduction) and finalizes.
+ * reduction; [SP] "训练与推理的适用方式不同": the query goes to every shard,
+ * each shard gives a local state, a global online-softmax reduction
+ * combines them) and finalizes.
  *   out: [n_q, heads, d] fp32; lse: [n_q, heads] fp32 (written).
  * Query positions are q_off .. q_off + n_q - 1 (for decode after a history
  * of n_kv tokens that includes the new ones: q_off = n_kv - n_q).  With
@@ -407,6 +413,8 @@ int ra_decode_forward(const void* q, const void* k, const void* v, float* out, f
  * a code is recorded, block-update CTAs that start do no work (so one
  * failed wait cannot turn into a long cascade).  Results of launches made
  * since the failure are therefore invalid until this call clears the code.
+ * The pages have no counterpart to this call or the next: they are the
+ * library's failure detection.
  */
 int ra_device_status(void* stream);
 
@@ -446,7 +454,8 @@ int ra_release_cached_memory(void);
 /* Tracing.  When enabled, the library records a CUDA event pair on the
  * launching stream around every kernel it launches.  ra_trace_query then
  * synchronizes those events.  It returns the number of launches of `kind`
- * and their summed device time in milliseconds since the last reset. */
+ * and their summed device time in milliseconds since the last reset.
+ * These and the status helpers below have no counterpart on the pages. */
 int ra_trace_enable(int on);
 int ra_trace_reset(void);
 int ra_trace_query(int kind, long long* launches, double* total_ms);
