@@ -1051,15 +1051,16 @@ int ra_ring_forward_noalloc(const void* q, const void* k, const void* v, float* 
                             int dtype, void* stream) {
   int rc = ring_args_check(N, P, 0, d, heads, kv_heads, dtype, RA_LAYOUT_CONTIGUOUS);
   if (rc != RA_OK) return rc;
-  if (N == 0) return RA_OK;
-  if ((rc = check_ptrs({q, k, v, out, lse})) != RA_OK) return rc;
-  // The documented limit holds for every dtype and is checked before any
-  // launch, although the bf16 ring (one fused launch) needs no scratch.
+  // The documented limit holds for every dtype, although the bf16 ring (one
+  // fused launch) needs no scratch.  It is checked before the pointers and
+  // before any launch, so an over-the-limit call never touches its buffers.
   if (N * heads > kNoAllocMaxRowsHeads)
     return fail(RA_ERR_UNSUPPORTED,
                 "N * heads = %lld exceeds the fixed scratch of ra_ring_forward_noalloc (%lld "
                 "rows x heads); use ra_ring_forward",
                 N * heads, kNoAllocMaxRowsHeads);
+  if (N == 0) return RA_OK;
+  if ((rc = check_ptrs({q, k, v, out, lse})) != RA_OK) return rc;
   if (dtype == RA_BF16 && P <= kFusedMaxSteps)
     return ring_fused_impl(q, k, v, out, lse, N, P, plain_mask(causal), d, heads, kv_heads,
                            static_cast<cudaStream_t>(stream));

@@ -246,10 +246,15 @@ int ra_ring_forward_host(const void* q_host, const void* k_host, const void* v_h
  *   The first call on a device looks up the array's device address once,
  *   with that device current.  Make that first call before any stream
  *   capture starts.
- *   All calls share the one array.  Each call clears the rows it uses
- *   first, so what an earlier call left there does not matter.  But two
- *   calls that overlap on the GPU (different streams, not ordered) race on
- *   the array and both results are undefined.
+ *   Only the calls that run the ring step by step use the array: fp32
+ *   inputs, and bf16 inputs with P > 256.  A bf16 call with P <= 256 runs
+ *   the one fused launch, which keeps its state on chip and never touches
+ *   the array.  Calls that use it share the one array.  Each clears the
+ *   rows it uses first, so what an earlier call left there does not
+ *   matter.  But two such calls that overlap on the GPU (different
+ *   streams, not ordered) race on the array and both results are
+ *   undefined.  The size limit is checked first, before the pointers and
+ *   before any launch, for every dtype.
  */
 int ra_ring_forward_noalloc(const void* q, const void* k, const void* v, float* out, float* lse,
                             long long N, int P, int causal, int d, int heads, int kv_heads,

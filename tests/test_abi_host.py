@@ -129,3 +129,17 @@ def test_binding_marshalling_errors():
         binding.ra_ring_forward(q, q, q, P=2, causal=True)  # CPU tensors are refused
     with pytest.raises(ValueError):
         binding._shapes(q, torch.zeros(8, 2, 32), torch.zeros(8, 2, 32))
+
+
+def test_noalloc_size_limit_is_checked_before_the_pointers(lib):
+    # ra_ring_forward_noalloc refuses N * heads above its fixed scratch
+    # (4,194,304 entries) before it looks at the pointers, so NULL pointers
+    # give the size error; at the limit they give the NULL-pointer error.
+    limit = 1 << 22
+    for dtype in (0, 1):
+        rc = lib.ra_ring_forward_noalloc(None, None, None, None, None, limit // 4 + 256, 1, 1, 64,
+                                         4, 4, dtype, None)
+        assert rc == -2 and b"fixed scratch" in lib.ra_last_error()
+        rc = lib.ra_ring_forward_noalloc(None, None, None, None, None, limit // 4, 1, 1, 64, 4, 4,
+                                         dtype, None)
+        assert rc == -1 and b"NULL" in lib.ra_last_error()
