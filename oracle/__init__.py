@@ -68,15 +68,15 @@ def _load():
             gq = lib.oracle_grad_q
             gq.argtypes = [P, P, P, P, ctypes.c_int, LL, LL, ctypes.c_int, ctypes.c_int,
                            ctypes.c_int, ctypes.c_double, ctypes.c_int, LL, P, P, P, P, P, LL,
-                           P, P, P, ctypes.c_int]
+                           P, P, P, P, P, ctypes.c_int]
             gq.restype = ctypes.c_int
             gkv = lib.oracle_grad_kv
             gkv.argtypes = [P, P, P, P, ctypes.c_int, LL, LL, ctypes.c_int, ctypes.c_int,
                             ctypes.c_int, ctypes.c_double, ctypes.c_int, LL, P, P, P, P, P, P,
-                            P, LL, P, P, ctypes.c_int]
+                            P, LL, P, P, P, P, P, ctypes.c_int]
             gkv.restype = ctypes.c_int
             lib.oracle_abi_version.restype = ctypes.c_int
-            if lib.oracle_abi_version() != 3:
+            if lib.oracle_abi_version() != 4:
                 raise RuntimeError("liboracle.so is stale; rebuild it")
             _lib = lib
     return _lib
@@ -217,10 +217,16 @@ def _ptr(a):
 
 
 def grad_q(q, k, v, dout, *, causal: bool, rows=None, q_pos=None, k_pos=None, window: int = 0,
-           q_doc=None, k_doc=None, scale: float | None = None, threads: int | None = None):
+           q_doc=None, k_doc=None, scale: float | None = None, threads: int | None = None,
+           absolute: bool = False):
     """dQ, LSE and D = sum_t P dP of the listed query rows (default: all),
     for the loss sum(dout * O).  Shapes [nrows, hq, d], [nrows, hq],
-    [nrows, hq]; fp64.  The definition is in ``attention.c``."""
+    [nrows, hq]; fp64.  The definition is in ``attention.c``.
+
+    With ``absolute=True`` two more arrays follow: the absolute-term sums
+    of dQ ([nrows, hq, d]) and of D ([nrows, hq]), the error scales defined
+    in ``attention.c`` (each sum with every term replaced by its absolute
+    value)."""
     qa, ka, va, ga, dt, nq, nk, hq, hkv, d, qp, kp, qd, kd, sc = _grad_inputs(
         q, k, v, dout, q_pos, k_pos, q_doc, k_doc, scale)
     rows = np.arange(nq, dtype=np.int64) if rows is None else np.ascontiguousarray(
@@ -229,20 +235,28 @@ def grad_q(q, k, v, dout, *, causal: bool, rows=None, q_pos=None, k_pos=None, wi
     dq = np.empty((nr, hq, d))
     lse = np.empty((nr, hq))
     dvec = np.empty((nr, hq))
+    dq_abs = np.empty((nr, hq, d)) if absolute else None
+    d_abs = np.empty((nr, hq)) if absolute else None
     rc = _load().oracle_grad_q(_ptr(qa), _ptr(ka), _ptr(va), _ptr(ga), dt, nq, nk, hq, hkv, d,
                                sc, int(bool(causal)), int(window), _ptr(qp), _ptr(kp), _ptr(qd),
                                _ptr(kd), _ptr(rows), nr, _ptr(dq), _ptr(lse), _ptr(dvec),
-                               int(threads or os.cpu_count() or 1))
+                               _ptr(dq_abs), _ptr(d_abs), int(threads or os.cpu_count() or 1))
     if rc != 0:
         raise ValueError(f"oracle_grad_q failed with code {rc}")
+    if absolute:
+        return dq, lse, dvec, dq_abs, d_abs
     return dq, lse, dvec
 
 
 def grad_kv(q, k, v, dout, lse_all, d_all, *, causal: bool, keys=None, q_pos=None, k_pos=None,
             window: int = 0, q_doc=None, k_doc=None, scale: float | None = None,
-            threads: int | None = None):
+            threads: int | None = None, d_abs_all=None):
     """dK and dV of the listed keys (default: all), [nkeys, hkv, d] fp64,
-    given LSE and D of every query row (from ``grad_q`` over all rows)."""
+    given LSE and D of every query row (from ``grad_q`` over all rows).
+
+    Given ``d_abs_all`` (the absolute-term sums of D of every query row,
+    from ``grad_q(absolute=True)``), two more arrays follow: the
+    absolute-term sums of dK and of dV."""
     qa, ka, va, ga, dt, nq, nk, hq, hkv, d, qp, kp, qd, kd, sc = _grad_inputs(
         q, k, v, dout, q_pos, k_pos, q_doc, k_doc, scale)
     lse_all = np.ascontiguousarray(np.asarray(lse_all, dtype=np.float64))
@@ -254,12 +268,22 @@ def grad_kv(q, k, v, dout, lse_all, d_all, *, causal: bool, keys=None, q_pos=Non
     nkk = keys.shape[0]
     dk = np.empty((nkk, hkv, d))
     dv = np.empty((nkk, hkv, d))
+    absolute = d_abs_all is not None
+    if absolute:
+        d_abs_all = np.ascontiguousarray(np.asarray(d_abs_all, dtype=np.float64))
+        if d_abs_all.shape != (nq, hq):
+            raise ValueError("d_abs_all must be [nq, hq]")
+    dk_abs = np.empty((nkk, hkv, d)) if absolute else None
+    dv_abs = np.empty((nkk, hkv, d)) if absolute else None
     rc = _load().oracle_grad_kv(_ptr(qa), _ptr(ka), _ptr(va), _ptr(ga), dt, nq, nk, hq, hkv, d,
                                 sc, int(bool(causal)), int(window), _ptr(qp), _ptr(kp), _ptr(qd),
                                 _ptr(kd), _ptr(lse_all), _ptr(d_all), _ptr(keys), nkk, _ptr(dk),
-                                _ptr(dv), int(threads or os.cpu_count() or 1))
+                                _ptr(dv), _ptr(d_abs_all), _ptr(dk_abs), _ptr(dv_abs),
+                                int(threads or os.cpu_count() or 1))
     if rc != 0:
         raise ValueError(f"oracle_grad_kv failed with code {rc}")
+    if absolute:
+        return dk, dv, dk_abs, dv_abs
     return dk, dv
 
 
@@ -268,3 +292,12 @@ def backward(q, k, v, dout, *, causal: bool, **kw):
     dq, lse, dvec = grad_q(q, k, v, dout, causal=causal, **kw)
     dk, dv = grad_kv(q, k, v, dout, lse, dvec, causal=causal, **kw)
     return dq, dk, dv, lse
+
+
+def backward_with_scales(q, k, v, dout, *, causal: bool, **kw):
+    """The gradients and their absolute-term sums (the error scales of
+    ``attention.c``): ((dq, dk, dv), (dq_abs, dk_abs, dv_abs), lse)."""
+    dq, lse, dvec, dq_abs, d_abs = grad_q(q, k, v, dout, causal=causal, absolute=True, **kw)
+    dk, dv, dk_abs, dv_abs = grad_kv(q, k, v, dout, lse, dvec, causal=causal, d_abs_all=d_abs,
+                                     **kw)
+    return (dq, dk, dv), (dq_abs, dk_abs, dv_abs), lse

@@ -220,6 +220,25 @@ int oracle_partial_state_masked(const void* q, const void* k, const void* v, int
  * oracle_grad_q: for the listed query rows and every head, LSE, D and dQ.
  * oracle_grad_kv: for the listed keys and every KV head, dK and dV; it
  * needs LSE and D of every query row (from oracle_grad_q over all rows).
+ *
+ * Absolute-term sums (optional outputs; NULL skips them).  These are not a
+ * step of the method and the pages have no counterpart: they are the
+ * magnitudes that bound rounding error in the standard forward error
+ * analysis of a sum (Higham, "Accuracy and Stability of Numerical
+ * Algorithms", ch. 3: fl(sum x_i) - sum x_i is at most a multiple of the
+ * unit roundoff times sum |x_i|).  Each is the same sum as above with
+ * every product and every term replaced by its absolute value:
+ *   |dP|_rt = sum_x |dO_rx| |v_tx|
+ *   A_D,r   = sum_t P_rt |dP|_rt
+ *   A_S,rt  = P_rt (|dP|_rt + A_D,r)
+ *   A_dQ,r  = scale * sum_t A_S,rt |k_t|
+ *   A_dK,t  = scale * sum over (r, query heads) A_S,rt |q_r|
+ *   A_dV,t  = sum over (r, query heads) P_rt |dO_r|
+ * A rounding of relative size u in any operand of a product (P or dS
+ * rounded to bf16, D taken from a rounded O) moves an output element by at
+ * most a small multiple of u times its A.  Elementwise A >= |gradient|.
+ * oracle_grad_q writes A_dQ and A_D; oracle_grad_kv takes A_D of every
+ * query row and writes A_dK and A_dV.
  */
 typedef struct {
   job_t base;  /* inputs, mask, positions, rows, threads */
@@ -231,6 +250,11 @@ typedef struct {
   double* dv;
   const long long* keys;
   long long nkeys;
+  /* absolute-term sums, NULL when not asked for */
+  double* dq_abs;   /* [nrows, hq, d] */
+  double* dvec_abs; /* [nrows, hq] (grad_q: out; grad_kv: in, all nq rows) */
+  double* dk_abs;   /* [nkeys, hkv, d] */
+  double* dv_abs;
 } gjob_t;
 
 static int pair_allowed(const job_t* J, long long r, long long t) {
@@ -245,6 +269,14 @@ static int pair_allowed(const job_t* J, long long r, long long t) {
 static double dot_rows(const job_t* J, const void* a, size_t ia, const void* b, size_t ib) {
   double s = 0.0;
   for (int x = 0; x < J->d; ++x) s += widen(a, J->dtype, ia + x) * widen(b, J->dtype, ib + x);
+  return s;
+}
+
+/* sum_x |a_x| |b_x| */
+static double dot_abs(const job_t* J, const void* a, size_t ia, const void* b, size_t ib) {
+  double s = 0.0;
+  for (int x = 0; x < J->d; ++x)
+    s += fabs(widen(a, J->dtype, ia + x)) * fabs(widen(b, J->dtype, ib + x));
   return s;
 }
 
@@ -268,27 +300,36 @@ static void grad_q_item(gjob_t* G, long long item, double* sc) {
       if (!isnan(sc[t])) l += exp(sc[t] - m);
   const double lse = l > 0.0 ? m + log(l) : -INFINITY;
   /* D = sum P dP, then dQ */
-  double D = 0.0;
+  double D = 0.0, Da = 0.0;
   double* dq = G->dq + ((size_t)ri * J->hq + h) * d;
+  double* dqa = G->dq_abs ? G->dq_abs + ((size_t)ri * J->hq + h) * d : NULL;
   for (int x = 0; x < d; ++x) dq[x] = 0.0;
+  if (dqa)
+    for (int x = 0; x < d; ++x) dqa[x] = 0.0;
   if (l > 0.0) {
     for (long long t = 0; t < J->nk; ++t) {
       if (isnan(sc[t])) continue;
       const double p = exp(sc[t] - lse);
-      const double dp = dot_rows(J, G->dout, qb, J->v, ((size_t)t * J->hkv + kh) * d);
-      D += p * dp;
+      const size_t vb = ((size_t)t * J->hkv + kh) * d;
+      D += p * dot_rows(J, G->dout, qb, J->v, vb);
+      if (dqa) Da += p * dot_abs(J, G->dout, qb, J->v, vb);
     }
     for (long long t = 0; t < J->nk; ++t) {
       if (isnan(sc[t])) continue;
       const double p = exp(sc[t] - lse);
-      const double dp = dot_rows(J, G->dout, qb, J->v, ((size_t)t * J->hkv + kh) * d);
-      const double ds = p * (dp - D);
       const size_t kb = ((size_t)t * J->hkv + kh) * d;
+      const double dp = dot_rows(J, G->dout, qb, J->v, kb);
+      const double ds = p * (dp - D);
       for (int x = 0; x < d; ++x) dq[x] += J->scale * ds * widen(J->k, J->dtype, kb + x);
+      if (dqa) {
+        const double dsa = p * (dot_abs(J, G->dout, qb, J->v, kb) + Da);
+        for (int x = 0; x < d; ++x) dqa[x] += J->scale * dsa * fabs(widen(J->k, J->dtype, kb + x));
+      }
     }
   }
   G->lse[ri * J->hq + h] = lse;
   G->dvec[ri * J->hq + h] = D;
+  if (G->dvec_abs) G->dvec_abs[ri * J->hq + h] = Da;
 }
 
 static void grad_kv_item(gjob_t* G, long long item) {
@@ -300,7 +341,11 @@ static void grad_kv_item(gjob_t* G, long long item) {
   const size_t kb = ((size_t)t * J->hkv + kh) * d;
   double* dk = G->dk + ((size_t)ti * J->hkv + kh) * d;
   double* dv = G->dv + ((size_t)ti * J->hkv + kh) * d;
+  double* dka = G->dk_abs ? G->dk_abs + ((size_t)ti * J->hkv + kh) * d : NULL;
+  double* dva = G->dv_abs ? G->dv_abs + ((size_t)ti * J->hkv + kh) * d : NULL;
   for (int x = 0; x < d; ++x) dk[x] = dv[x] = 0.0;
+  if (dka)
+    for (int x = 0; x < d; ++x) dka[x] = dva[x] = 0.0;
   for (int hl = 0; hl < g; ++hl) {
     const int h = kh * g + hl;
     for (long long r = 0; r < J->nq; ++r) {
@@ -314,6 +359,13 @@ static void grad_kv_item(gjob_t* G, long long item) {
       for (int x = 0; x < d; ++x) {
         dk[x] += J->scale * ds * widen(J->q, J->dtype, qb + x);
         dv[x] += p * widen(G->dout, J->dtype, qb + x);
+      }
+      if (dka) {
+        const double dsa = p * (dot_abs(J, G->dout, qb, J->v, kb) + G->dvec_abs[r * J->hq + h]);
+        for (int x = 0; x < d; ++x) {
+          dka[x] += J->scale * dsa * fabs(widen(J->q, J->dtype, qb + x));
+          dva[x] += p * fabs(widen(G->dout, J->dtype, qb + x));
+        }
       }
     }
   }
@@ -386,7 +438,7 @@ int oracle_grad_q(const void* q, const void* k, const void* v, const void* dout,
                   long long window, const long long* q_pos, const long long* k_pos,
                   const long long* q_doc, const long long* k_doc, const long long* rows,
                   long long nrows, double* dq_out, double* lse_out, double* d_out,
-                  int nthreads) {
+                  double* dq_abs_out, double* d_abs_out, int nthreads) {
   gjob_t G;
   int rc = grad_setup(&G, q, k, v, dout, dtype, nq, nk, hq, hkv, d, scale, causal, window, q_pos,
                       k_pos, q_doc, k_doc);
@@ -396,9 +448,12 @@ int oracle_grad_q(const void* q, const void* k, const void* v, const void* dout,
     if (rows[i] < 0 || rows[i] >= nq) return -1;
   G.base.rows = rows;
   G.base.nrows = nrows;
+  if ((!dq_abs_out) != (!d_abs_out)) return -1;
   G.dq = dq_out;
   G.lse = lse_out;
   G.dvec = d_out;
+  G.dq_abs = dq_abs_out;
+  G.dvec_abs = d_abs_out;
   if (run_threads(gq_worker, &G, nthreads < 1 ? 1 : nthreads) != 0) return -2;
   return G.base.failed ? -2 : 0;
 }
@@ -408,7 +463,8 @@ int oracle_grad_kv(const void* q, const void* k, const void* v, const void* dout
                    long long window, const long long* q_pos, const long long* k_pos,
                    const long long* q_doc, const long long* k_doc, const double* lse_all,
                    const double* d_all, const long long* keys, long long nkeys, double* dk_out,
-                   double* dv_out, int nthreads) {
+                   double* dv_out, const double* d_abs_all, double* dk_abs_out,
+                   double* dv_abs_out, int nthreads) {
   gjob_t G;
   int rc = grad_setup(&G, q, k, v, dout, dtype, nq, nk, hq, hkv, d, scale, causal, window, q_pos,
                       k_pos, q_doc, k_doc);
@@ -420,8 +476,12 @@ int oracle_grad_kv(const void* q, const void* k, const void* v, const void* dout
   G.dvec = (double*)d_all;
   G.keys = keys;
   G.nkeys = nkeys;
+  if ((!d_abs_all) != (!dk_abs_out) || (!d_abs_all) != (!dv_abs_out)) return -1;
   G.dk = dk_out;
   G.dv = dv_out;
+  G.dvec_abs = (double*)d_abs_all;
+  G.dk_abs = dk_abs_out;
+  G.dv_abs = dv_abs_out;
   if (run_threads(gkv_worker, &G, nthreads < 1 ? 1 : nthreads) != 0) return -2;
   return G.base.failed ? -2 : 0;
 }
@@ -438,4 +498,4 @@ int oracle_partial_state(const void* q, const void* k, const void* v, int dtype,
 }
 
 /* Version tag so the Python side can tell a stale build. */
-int oracle_abi_version(void) { return 3; }
+int oracle_abi_version(void) { return 4; }

@@ -14,17 +14,29 @@ exact running max:
 * |O~ - O~_ref| <= tol_o * l_ref, elementwise.  O~ is a weighted sum with
   total weight l, so its error scales with l.
 
-Gradients (bf16 inputs only) are compared per tensor against the largest
-reference magnitude: max |dX - dX_ref| <= 2e-2 * max |dX_ref|.  Each
-product in the backward rounds one operand to bf16 (P for dV, dS for dQ
-and dK), a relative error of at most 2^-9 per term; summed over the keys
-(or queries) with mixed signs, the error of an output element stays a few
-times 2^-9 of the largest |term| sums, which the bar covers with margin.
+Gradients (bf16 inputs only) are compared element by element against the
+oracle's absolute-term sum A of that element (the same sum with every term
+replaced by its absolute value; see oracle/attention.c):
+    |dX - dX_ref| <= 2^-7 * A + 1e-6 * max A.
+Why this form: every product of the backward rounds one operand to bf16
+(P for dV, dS for dQ and dK; D comes from the forward's O, whose P was
+rounded too), a relative error of at most 2^-9 per term.  The standard
+error bound of a sum is a multiple of the unit error times the sum of the
+|terms|, not times |sum|: elements whose terms cancel (a late causal key
+that few queries see, a query row whose dS nearly sums away) have a small
+|dX_ref| but not a small error.  A model of the kernel's roundings in fp64
+(P and dS rounded to bf16, O from bf16 P) stays below 3.3e-3 * A on every
+element of the test cases, so 2^-7 = 7.8e-3 leaves a 2.4x margin.  A wrong
+element is usually off by |dX_ref|, whose median is 4e-2 * A, and a key
+whose gradient is dropped is off by 0.1-0.9 of its A: both fail.  The
+1e-6 * max A floor only covers entries with no allowed pair (A = 0).
+tests/test_grad_bar_host.py plants such mistakes in the oracle's gradients
+on the CPU and checks that this bar rejects them.
 """
 import numpy as np
 
 TOL = {
-    "bf16": {"o": 1e-2, "lse": 1e-3, "l": 2e-3, "grad": 2e-2},
+    "bf16": {"o": 1e-2, "lse": 1e-3, "l": 2e-3, "grad": 2.0 ** -7, "grad_floor": 1e-6},
     "f32": {"o": 1e-5, "lse": 1e-5, "l": 1e-5},
 }
 
@@ -70,17 +82,37 @@ def check_state(m, l, o, ref, kind):
     assert (l[~fin] == 0).all() and (o[~fin] == 0).all()
 
 
-def check_grad(x, ref, name="grad"):
-    """max |x - ref| <= TOL["bf16"]["grad"] * max |ref| (the gradient bar)."""
+def grad_errors(x, ref, scale):
+    """|x - ref| / (2^-7 A + 1e-6 max A) per element: the gradient bar's
+    ratio (<= 1 passes), and the largest |x - ref| / A."""
+    t = TOL["bf16"]
     x = _np(x)
     ref = np.asarray(ref, dtype=np.float64)
-    assert x.shape == ref.shape, (x.shape, ref.shape)
-    assert np.isfinite(x).all(), f"non-finite {name}"
-    scale = np.abs(ref).max() if ref.size else 0.0
-    err = np.abs(x - ref).max() if ref.size else 0.0
-    assert err <= TOL["bf16"]["grad"] * max(scale, 1e-30), \
-        f"{name}: max err {err:.3e} > {TOL['bf16']['grad']} x {scale:.3e}"
-    return err / max(scale, 1e-30)
+    scale = np.asarray(scale, dtype=np.float64)
+    assert x.shape == ref.shape == scale.shape, (x.shape, ref.shape, scale.shape)
+    if not ref.size:
+        return np.zeros(0), 0.0
+    err = np.abs(x - ref)
+    bar = t["grad"] * scale + t["grad_floor"] * scale.max()
+    ratio = np.where(bar > 0, err / np.where(bar > 0, bar, 1.0), np.where(err > 0, np.inf, 0.0))
+    rel = (err / np.where(scale > 0, scale, np.inf)).max()
+    return ratio, float(rel)
+
+
+def check_grad(x, ref, scale, name="grad"):
+    """|x - ref| <= 2^-7 * scale + 1e-6 * max(scale), element by element,
+    where scale is the oracle's absolute-term sum of each element (the
+    gradient bar; see the module docstring).  Returns max |x - ref| / scale."""
+    xs = _np(x)
+    assert np.isfinite(xs).all(), f"non-finite {name}"
+    ratio, rel = grad_errors(xs, ref, scale)
+    if ratio.size and ratio.max() > 1.0:
+        i = np.unravel_index(int(ratio.argmax()), ratio.shape)
+        raise AssertionError(
+            f"{name}: element {i} off by {abs(xs[i] - ref[i]):.3e} (ref {ref[i]:.3e}, "
+            f"absolute-term sum {scale[i]:.3e}); bar 2^-7 of that sum; {int((ratio > 1).sum())} "
+            f"elements over")
+    return rel
 
 
 def assert_fused_matches(out, lse, ref_out, ref_lse):

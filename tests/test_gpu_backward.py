@@ -58,11 +58,10 @@ def run(N, P, heads, kv_heads, d, causal, layout="contiguous", window=0, n_valid
     if docs is not None or n_valid is not None:
         ids = doc_ids(N, docs, n_valid)[pos.numpy()]
         okw = dict(q_doc=ids, k_doc=ids)
-    rdq, rdk, rdv, _ = oracle.backward(ql, kl, vl, gl, causal=causal, window=window,
-                                       q_pos=pos.numpy(), k_pos=pos.numpy(), **okw)
-    check_grad(dq, rdq, "dq")
-    check_grad(dk, rdk, "dk")
-    check_grad(dv, rdv, "dv")
+    refs, scales, _ = oracle.backward_with_scales(ql, kl, vl, gl, causal=causal, window=window,
+                                                  q_pos=pos.numpy(), k_pos=pos.numpy(), **okw)
+    for name, x, r, a in zip(("dq", "dk", "dv"), (dq, dk, dv), refs, scales):
+        check_grad(x, r, a, name)
 
 
 CASES = [
@@ -115,9 +114,13 @@ def test_backward_is_deterministic():
 
 
 def test_backward_block_count_does_not_change_the_result():
+    # Each P is within the bar of the oracle, so two of them are within
+    # twice the bar of each other.
     N = 1024
-    q, k, v = (t.to(DEV) for t in inputs.make_random(N, 2, 1, 128, seed=13))
-    g = inputs.randn_chunked((N, 2, 128), 13, 3).to(torch.bfloat16).to(DEV)
+    qh, kh, vh = inputs.make_random(N, 2, 1, 128, seed=13)
+    gh = inputs.randn_chunked((N, 2, 128), 13, 3).to(torch.bfloat16)
+    q, k, v, g = (t.to(DEV) for t in (qh, kh, vh, gh))
+    _, scales, _ = oracle.backward_with_scales(qh, kh, vh, gh, causal=True)
     ref = None
     for P in (1, 2, 4, 8):
         out, lse = ra.ra_ring_forward(q, k, v, P=P, causal=True)
@@ -125,8 +128,10 @@ def test_backward_block_count_does_not_change_the_result():
         torch.cuda.synchronize()
         if ref is None:
             ref = res
-        for x, y in zip(res, ref):
-            assert (x - y).abs().max().item() <= 2e-2 * y.abs().max().item()
+        for x, y, a in zip(res, ref, scales):
+            a = torch.from_numpy(a)
+            bar = 2 * (2.0 ** -7 * a + 1e-6 * a.max())
+            assert ((x.cpu().double() - y.cpu().double()).abs() <= bar).all()
 
 
 def test_backward_with_300_ranks():
@@ -142,10 +147,10 @@ def test_backward_with_300_ranks():
         out, lse = ra.ra_ring_forward(qd, kd, vd, P=p, causal=True)
         grads[p] = ra.ra_ring_backward(qd, kd, vd, out, lse, gd, P=p, causal=True)
     ra.ra_device_status()
-    refs = oracle.backward(q, k, v, g, causal=True)[:3]
-    for name, x, y, r in zip(("dq", "dk", "dv"), grads[P], grads[4], refs):
-        check_grad(x, r, name)
-        assert (x - y).abs().max().item() <= 2e-2 * float(np.abs(r).max())
+    refs, scales, _ = oracle.backward_with_scales(q, k, v, g, causal=True)
+    for name, x, y, r, a in zip(("dq", "dk", "dv"), grads[P], grads[4], refs, scales):
+        check_grad(x, r, a, name)
+        check_grad(y, r, a, name + " (P = 4)")
 
 
 @pytest.mark.slow
@@ -168,8 +173,8 @@ def test_backward_gqa_128k_sampled():
     ra.ra_device_status()
     rows = inputs.sample_rows(w, random_per_block=2)
     got = dq.index_select(0, torch.from_numpy(rows).to(DEV)).cpu()
-    ref, _, _ = oracle.grad_q(q, k, v, g, causal=True, rows=rows)
-    check_grad(got, ref, "dq")
+    ref, _, _, ref_abs, _ = oracle.grad_q(q, k, v, g, causal=True, rows=rows, absolute=True)
+    check_grad(got, ref, ref_abs, "dq")
     gsum = g.double().view(w.N, w.kv_heads, w.heads // w.kv_heads, w.d).sum((0, 2))
     dv_sum = dv.double().sum(0).cpu()
     assert (dv_sum - gsum).abs().max().item() <= 2e-2 * gsum.abs().max().item()
@@ -200,18 +205,22 @@ def test_backward_gqa_128k_window_sampled_keys():
     keys = np.array([0, 1, c - 1, c, 3 * c + 777, 8 * c - 1, 8 * c, 11 * c + 4000,
                      w.N - W - 1, w.N - 1], dtype=np.int64)
     need = np.unique(np.concatenate([np.arange(kk, min(w.N, kk + W)) for kk in keys]))
-    dq_ref, lse_rows, d_rows = oracle.grad_q(q, k, v, g, causal=True, rows=need, window=W)
+    dq_ref, lse_rows, d_rows, dq_abs, d_abs_rows = oracle.grad_q(
+        q, k, v, g, causal=True, rows=need, window=W, absolute=True)
     lse_all = np.full((w.N, w.heads), np.nan)
     d_all = np.full((w.N, w.heads), np.nan)
+    d_abs_all = np.full((w.N, w.heads), np.nan)
     lse_all[need] = lse_rows
     d_all[need] = d_rows
-    dk_ref, dv_ref = oracle.grad_kv(q, k, v, g, lse_all, d_all, causal=True, keys=keys, window=W)
+    d_abs_all[need] = d_abs_rows
+    dk_ref, dv_ref, dk_abs, dv_abs = oracle.grad_kv(q, k, v, g, lse_all, d_all, causal=True,
+                                                    keys=keys, window=W, d_abs_all=d_abs_all)
     sel = torch.from_numpy(keys).to(DEV)
-    check_grad(dk.index_select(0, sel).cpu(), dk_ref, "dk")
-    check_grad(dv.index_select(0, sel).cpu(), dv_ref, "dv")
+    check_grad(dk.index_select(0, sel).cpu(), dk_ref, dk_abs, "dk")
+    check_grad(dv.index_select(0, sel).cpu(), dv_ref, dv_abs, "dv")
     rows = need[::97]
     check_grad(dq.index_select(0, torch.from_numpy(rows).to(DEV)).cpu(),
-               dq_ref[::97], "dq")
+               dq_ref[::97], dq_abs[::97], "dq")
 
 
 @pytest.mark.slow

@@ -553,3 +553,93 @@ def test_gradient_rows_and_keys_subsets():
     _, lse_a, d_a = oracle.grad_q(q, k, v, g, causal=True)
     dk_k, dv_k = oracle.grad_kv(q, k, v, g, lse_a, d_a, causal=True, keys=[3, 29], threads=3)
     assert np.array_equal(dk_k, dk[[3, 29]]) and np.array_equal(dv_k, dv[[3, 29]])
+
+
+# --- absolute-term sums of the gradients (error scales; Higham, "Accuracy and
+# Stability of Numerical Algorithms", ch. 3).  Each is a gradient's sum with
+# every term replaced by its absolute value.
+
+def _grad_case(seed, n=24, hq=4, hkv=2, d=8):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((n, hq, d)).astype(np.float32)
+    k = rng.standard_normal((n, hkv, d)).astype(np.float32)
+    v = rng.standard_normal((n, hkv, d)).astype(np.float32)
+    g = rng.standard_normal((n, hq, d)).astype(np.float32)
+    return q, k, v, g
+
+
+@pytest.mark.parametrize("kw", [dict(causal=False), dict(causal=True),
+                                dict(causal=True, window=5)])
+def test_abs_scales_bound_the_gradients(kw):
+    # Triangle inequality: |sum x_i| <= sum |x_i|, element by element; the
+    # gradients are the oracle's own (pinned above).
+    q, k, v, g = _grad_case(53)
+    grads, scales, _ = oracle.backward_with_scales(q, k, v, g, **kw)
+    plain = oracle.backward(q, k, v, g, **kw)[:3]
+    for x, y, a in zip(grads, plain, scales):
+        assert np.array_equal(x, y)
+        assert (np.abs(x) <= a * (1 + 1e-12)).all()
+        assert (a > 0).all()
+
+
+def test_abs_scales_equal_the_gradient_when_every_term_is_positive():
+    # dout >= 0: every term of dV_t (P_rt dO_r) is >= 0, so A_dV = dV.  With
+    # v >= 0 too, every dP and O is >= 0, so D's absolute sum is D.
+    q, k, v, g = _grad_case(55)
+    g, v = np.abs(g), np.abs(v)
+    dq, lse, dvec, dq_abs, d_abs = oracle.grad_q(q, k, v, g, causal=True, absolute=True)
+    dk, dv, dk_abs, dv_abs = oracle.grad_kv(q, k, v, g, lse, dvec, causal=True,
+                                            d_abs_all=d_abs)
+    assert np.abs(dv_abs - dv).max() <= 1e-13 * np.abs(dv).max()
+    assert np.abs(d_abs - dvec).max() <= 1e-13 * np.abs(dvec).max()
+
+
+def test_abs_scales_closed_form_with_one_key_per_row():
+    # Causal window 1: row r sees key r alone, so P = 1 and D = dP.  Then
+    # A_D,r = sum_x |dO_rx||v_rx| and A_S,rr = 2 A_D,r, so
+    # A_dQ,r = scale 2 A_D,r |k_r|, A_dK,t = scale sum_h 2 A_D,t,h |q_t,h|,
+    # A_dV,t = sum_h |dO_t,h| over the query heads h of t's KV head.
+    q, k, v, g = _grad_case(57, n=9, hq=4, hkv=2, d=8)
+    _, (aq, ak, av), _ = oracle.backward_with_scales(q, k, v, g, causal=True, window=1)
+    sc = 1.0 / math.sqrt(8)
+    q64, k64, v64, g64 = (x.astype(np.float64) for x in (q, k, v, g))
+    vh = np.repeat(v64, 2, axis=1)                  # value row of each query head
+    kh = np.repeat(k64, 2, axis=1)
+    a_d = (np.abs(g64) * np.abs(vh)).sum(-1)        # [n, hq]
+    want_q = sc * 2 * a_d[..., None] * np.abs(kh)
+    want_k = (sc * 2 * a_d[..., None] * np.abs(q64)).reshape(9, 2, 2, 8).sum(2)
+    want_v = np.abs(g64).reshape(9, 2, 2, 8).sum(2)
+    assert np.abs(aq - want_q).max() <= 1e-13 * want_q.max()
+    assert np.abs(ak - want_k).max() <= 1e-13 * want_k.max()
+    assert np.abs(av - want_v).max() <= 1e-13 * want_v.max()
+
+
+def test_abs_scales_ignore_coordinate_signs_and_scale_with_dout():
+    # Flipping the sign of coordinate x of dO in every row, or of v in every
+    # key, changes the gradients but none of the absolute sums (P depends on
+    # q and k only).  Scaling dO by -2 scales every absolute sum by 2.
+    q, k, v, g = _grad_case(59)
+    base_g, base_a, _ = oracle.backward_with_scales(q, k, v, g, causal=True)
+    rng = np.random.default_rng(61)
+    fg = np.where(rng.random(g.shape[-1]) < 0.5, -1, 1).astype(np.float32)
+    fv = np.where(rng.random(v.shape[-1]) < 0.5, -1, 1).astype(np.float32)
+    assert (fg < 0).any() and (fv < 0).any()
+    grads, scales, _ = oracle.backward_with_scales(q, k, v * fv, g * fg, causal=True)
+    for a, b in zip(scales, base_a):
+        assert np.abs(a - b).max() <= 1e-12 * b.max()
+    assert np.abs(grads[0] - base_g[0]).max() > 1e-3   # the gradients did change
+    _, scaled, _ = oracle.backward_with_scales(q, k, v, -2 * g, causal=True)
+    for a, b in zip(scaled, base_a):
+        assert np.abs(a - 2 * b).max() <= 1e-12 * b.max()
+
+
+def test_abs_scales_rows_and_keys_subsets():
+    q, k, v, g = _grad_case(63, n=30)
+    _, (aq, ak, av), _ = oracle.backward_with_scales(q, k, v, g, causal=True)
+    rows = np.array([29, 0, 7])
+    _, _, _, aq_r, _ = oracle.grad_q(q, k, v, g, causal=True, rows=rows, absolute=True)
+    assert np.array_equal(aq_r, aq[rows])
+    _, lse, dvec, _, d_abs = oracle.grad_q(q, k, v, g, causal=True, absolute=True)
+    _, _, ak_k, av_k = oracle.grad_kv(q, k, v, g, lse, dvec, causal=True, keys=[3, 29],
+                                      d_abs_all=d_abs, threads=3)
+    assert np.array_equal(ak_k, ak[[3, 29]]) and np.array_equal(av_k, av[[3, 29]])
