@@ -17,14 +17,16 @@ It follows the pages' own steps, in their order and notation:
   each side by exp(m_side - m_new), and adds.  The source is the
   xf_ring_attention page, section "The architecture: every piece explained"
   (the online softmax accumulator paragraph).
-* ``finalize`` is O = O~ / l, from "Ring Attention Math Deep", "After the
-  final block: out = o / l".  LSE = m + ln l is the row log-sum-exp that
+* ``finalize`` divides the accumulated O~ by l once the last block has been
+  folded in ("Ring Attention Math Deep", section "Accumulation math, step
+  by step").  LSE = m + ln l is the row log-sum-exp that
   "Ring Attention：把超长序列沿设备环流动", section "Backward
   需要让梯度也沿环传播", keeps for the backward pass.
 
 Readings where the pages are silent:
-* alpha = 0 when m = -inf.  The worked example prints "m' = 2, alpha = 0"
-  for the first block.
+* alpha = 0 when m = -inf.  In the worked example of "Ring Attention Math
+  Deep" ("Accumulation math, step by step") the first block sets the max
+  to 2 from an empty state and its rescale factor is zero.
 * A row with no allowed key so far (m' = -inf) keeps its state: alpha = 1
   and P = 0, so (-inf) - (-inf) is never formed.
 * finalize with l = 0 gives O = 0 and LSE = -inf.
