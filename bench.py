@@ -263,6 +263,15 @@ def note_window(clk, pad):
 # ------------------------------------------------------------------ traffic record
 FORWARD_SOURCES = ("umma_kernel.cu", "ptx.cuh", "ra_internal.h")
 DECODE_SOURCES = ("decode_kernel.cu", "ptx.cuh", "ra_internal.h")
+STATE_SOURCES = ("state_kernels.cu", "ra_internal.h")
+
+
+def gpu_index_of(local: int) -> int:
+    """The physical GPU index nvidia-smi knows this rank's device by."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    if vis and "," not in vis and vis.strip().isdigit():
+        return int(vis)
+    return local
 
 
 def kernel_digest(files=FORWARD_SOURCES) -> str:
@@ -426,11 +435,7 @@ def run_decode(args, ws, rank, local):
     est = timed_warmup(step, args.warmup, dev)
     pad = pad_seconds(est, args.steps)
     ra.ra_device_status(stream)
-    gpu_index = local
-    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
-    if vis and "," not in vis and vis.strip().isdigit():
-        gpu_index = int(vis)
-    clocks = ClockSampler(gpu_index, args.clock_log)
+    clocks = ClockSampler(gpu_index_of(local), args.clock_log)
     clocks.start()
     clock_pad(step, dev, pad)
     ra.ra_trace_reset()
@@ -503,6 +508,239 @@ def run_decode(args, ws, rank, local):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ state kernels
+METRIC_STATE = ("state kernels (init, merge, finalize): algorithmic HBM GB/s over one "
+                "init + two merges + one finalize of the workload's [N, heads] state")
+
+
+def state_bytes(d: int) -> dict:
+    """Algorithmic bytes per (row, head) of each state kernel: m and l are
+    fp32 scalars, O~ is d fp32 values; merge reads two states and writes
+    one; finalize reads one state and writes out (d values) and LSE."""
+    st = 8 + 4 * d
+    return {"state_init": st, "merge": 3 * st, "finalize": st + 4 + 4 * d}
+
+
+def run_state(args, w, ws, rank, local):
+    import numpy as np
+    import torch
+
+    import blockwise_online_softmax_gb300 as ra
+    from blockwise_online_softmax_gb300 import binding
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    binding.lib()
+    peaks, peak_src = load_peaks()
+    R, H, d = w.N, w.heads, w.d
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(w.seed)
+
+    def partial_state():
+        # A synthetic partial state: a running max near a typical LSE, a
+        # positive sum and O~ of that scale.
+        m = torch.randn((R, H), generator=gen, device=dev) * 2 + 5
+        l = torch.rand((R, H), generator=gen, device=dev) * 99 + 1
+        o = torch.randn((R, H, d), generator=gen, device=dev) * l[..., None]
+        return m, l, o
+
+    b, c = partial_state(), partial_state()
+    a = (torch.empty((R, H), device=dev), torch.empty((R, H), device=dev),
+         torch.empty((R, H, d), device=dev))
+    out = torch.empty((R, H, d), device=dev)
+    lse = torch.empty((R, H), device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ra.ra_state_init(*a, stream=stream)
+        ra.ra_merge(*a, *b, stream=stream)     # a = identity (+) b
+        ra.ra_merge(*a, *c, stream=stream)     # the general case
+        ra.ra_finalize(*a, out=out, lse=lse, stream=stream)
+
+    est = timed_warmup(step, args.warmup, dev)
+    pad = pad_seconds(est, args.steps)
+    ra.ra_device_status(stream)
+    clocks = ClockSampler(gpu_index_of(local), args.clock_log)
+    clocks.start()
+    clock_pad(step, dev, pad)
+    ra.ra_trace_reset()
+    ra.ra_trace_enable(True)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    ra.ra_trace_enable(False)
+    clock_pad(step, dev, pad)
+    clk = note_window(clocks.stop(), pad)
+    ra.ra_device_status(stream)
+    ms_step = reduce_max(ev0.elapsed_time(ev1), ws) / args.steps
+    per_rh = state_bytes(d)
+    trace = {kd_: ra.ra_trace_query(kd_) for kd_ in per_rh}
+    ra.ra_trace_reset()
+    kernels = {}
+    for kd_, (n, ms) in trace.items():
+        gbs = per_rh[kd_] * R * H * n / (ms * 1e-3) / 1e9 if ms > 0 else None
+        kernels[kd_] = {"launches_per_step": n / args.steps, "ms_per_launch": ms / max(n, 1),
+                        "bytes_per_launch": per_rh[kd_] * R * H, "achieved_gbs": gbs,
+                        "frac": gbs / peaks["hbm_gbs"] if gbs else None}
+    step_bytes = R * H * (per_rh["state_init"] + 2 * per_rh["merge"] + per_rh["finalize"])
+    value = ws * step_bytes / (ms_step * 1e-3) / 1e9
+    dom = kernels["merge"]
+    # parity of the run's own output on sampled rows: the oracle's merge and
+    # finalize (fp64 numpy) over the same three states
+    parity = None
+    cpu = None
+    if rank == 0:
+        import oracle.online as online
+
+        rows = np.random.default_rng(5).choice(R, size=min(R, 256), replace=False)
+        sel = torch.from_numpy(rows).to(dev)
+
+        def pick(st):
+            return tuple(x.index_select(0, sel).double().cpu().numpy() for x in st)
+
+        sb, sc_ = pick(b), pick(c)
+        t0 = time.perf_counter()
+        ref = online.merge(online.merge(online.identity_state(len(rows), H, d), sb), sc_)
+        ref_out, ref_lse = online.finalize(ref)
+        dt = time.perf_counter() - t0
+        got_o = out.index_select(0, sel).double().cpu().numpy()
+        got_l = lse.index_select(0, sel).double().cpu().numpy()
+        e_o = float(np.abs(got_o - ref_out).max())
+        e_l = float((np.abs(got_l - ref_lse) / np.maximum(1.0, np.abs(ref_lse))).max())
+        parity = {"rows": "256 seeded rows, all heads", "max_abs_out": e_o, "lse_rel": e_l,
+                  "bar_out": 1e-5, "bar_lse": 1e-5, "pass": e_o <= 1e-5 and e_l <= 1e-5}
+        if ws == 1 and not args.no_cpu_baseline:
+            cpu = {"value": step_bytes * (len(rows) / R) / dt / 1e9, "unit": "GB/s", "cores": 1,
+                   "kind": "oracle",
+                   "sample": f"merge, merge and finalize of {len(rows)} rows x {H} heads in "
+                             f"fp64 numpy ({dt * 1e3:.1f} ms)"}
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC_STATE, "value": value, "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "rows": R, "heads": H, "d": d, "seed": w.seed,
+                   "parallelism": f"replicas{ws}", "bytes_per_step": step_bytes,
+                   "bytes_per_row_head": per_rh,
+                   "l2": f"each state {R * H * (8 + 4 * d) / 1e9:.2f} GB, larger than L2; "
+                         "no flush"},
+        "clocks": clk, "e2e": None,
+        "gpu_launches": sum(n for n, _ in trace.values()),
+        "kernels": kernels,
+        "roofline": {"bound": "hbm", "achieved": dom["achieved_gbs"], "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": dom["frac"],
+                     "traffic": recorded_traffic(w.name, "state_kernels_traffic.md",
+                                                 STATE_SOURCES),
+                     "kernel": "merge", "peak_kind": f"hbm_gbs ({peak_src})"},
+        "cpu_baseline": cpu,
+        "parity": parity,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ ring steps
+METRIC_STEPS = ("causal-adjusted attention TFLOP/s of the step-by-step ring (state init, "
+                "one block-update launch per ring step with (m, l, O~) in HBM, finalize)")
+
+
+def run_steps(args, w, ws, rank, local):
+    import torch
+
+    import blockwise_online_softmax_gb300 as ra
+    from blockwise_online_softmax_gb300 import binding, inputs
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    binding.lib()
+    peaks, peak_src = load_peaks()
+    q, k, v = workload_inputs(w)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    m = torch.empty((w.N, w.heads), device=dev)
+    l = torch.empty((w.N, w.heads), device=dev)
+    o = torch.empty((w.N, w.heads, w.d), device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        # out and lse are written in place over o and m, as ra_ring_forward's
+        # own fp32 path does.
+        ra.ra_state_init(m, l, o, stream=stream)
+        for s_ in range(w.P):
+            ra.ra_ring_step(qd, kd, vd, m, l, o, P=w.P, s=s_, causal=w.causal, stream=stream)
+        ra.ra_finalize(m, l, o, out=o, lse=m, stream=stream)
+
+    est = timed_warmup(step, args.warmup, dev)
+    pad = pad_seconds(est, args.steps)
+    ra.ra_device_status(stream)
+    clocks = ClockSampler(gpu_index_of(local), args.clock_log)
+    clocks.start()
+    clock_pad(step, dev, pad)
+    ra.ra_trace_reset()
+    ra.ra_trace_enable(True)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    ra.ra_trace_enable(False)
+    clock_pad(step, dev, pad)
+    clk = note_window(clocks.stop(), pad)
+    ra.ra_device_status(stream)
+    ms_step = reduce_max(ev0.elapsed_time(ev1), ws) / args.steps
+    kinds = ("state_init", "block_update_bf16", "finalize")
+    trace = {kd_: ra.ra_trace_query(kd_) for kd_ in kinds}
+    ra.ra_trace_reset()
+    f_adj, f_exact = w.flops_causal_adjusted(), w.flops_exact()
+    value = ws * f_adj / (ms_step * 1e-3) / 1e12
+    n_upd, ms_upd = trace["block_update_bf16"]
+    achieved = f_exact * args.steps / (ms_upd * 1e-3) / 1e12 if ms_upd > 0 else None
+    peak = peaks["bf16_tflops_sustained"]
+    # Algorithmic bytes of one (rank, step) pair with a full block: Q_i and
+    # K_j, V_j read once, the state (m, l, O~ of block i) read and written.
+    el = 2
+    pair_bytes = (w.c * w.heads * w.d * el + 2 * w.c * w.kv_heads * w.d * el
+                  + 2 * w.c * w.heads * (8 + 4 * w.d))
+    parity = None
+    if rank == 0 and not args.no_check:
+        parity = parity_check(w, q, k, v, o, m)
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC_STEPS, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic",
+        "frac_of_dense_bf16_peak": value / ws / peaks["bf16_tflops"], "peak_source": peak_src,
+        "config": {**forward_config(w, ws), "path": "ra_state_init + P x ra_ring_step + "
+                   "ra_finalize", "algorithmic_bytes_per_full_pair": pair_bytes},
+        "clocks": clk, "e2e": None,
+        "gpu_launches": sum(n for n, _ in trace.values()),
+        "kernel_ms": {kd_: t / args.steps for kd_, (n, t) in trace.items()},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": (achieved / peak) if achieved else None,
+                     "traffic": recorded_traffic(w.name, "block_update_bf16_traffic.md"),
+                     "kernel": "block update (tcgen05), one launch per ring step",
+                     "peak_kind": f"bf16_tflops_sustained ({peak_src})",
+                     "frac_of_burst": (achieved / peaks["bf16_tflops"]) if achieved else None},
+        "cpu_baseline": None,
+        "parity": parity,
+    }
+    print(json.dumps(line), flush=True)
+
+
 # ------------------------------------------------------------------ backward
 METRIC_BWD = ("backward attention TFLOP/s (10*d FLOPs per allowed pair per query head, "
               "causal-adjusted) on 1 GB300")
@@ -520,7 +758,7 @@ def run_backward(args, w, ws, rank, local):
     torch.cuda.set_device(dev)
     binding.lib()
     peaks, peak_src = load_peaks()
-    q, k, v = inputs.make_workload(w)
+    q, k, v = workload_inputs(w)
     g = inputs.randn_chunked((w.N, w.heads, w.d), w.seed, 3).to(torch.bfloat16)
     qd, kd, vd, gd = q.to(dev), k.to(dev), v.to(dev), g.to(dev)
     stream = torch.cuda.current_stream(dev)
@@ -536,11 +774,7 @@ def run_backward(args, w, ws, rank, local):
     est = timed_warmup(step, args.warmup, dev)
     pad = pad_seconds(est, args.steps)
     ra.ra_device_status(stream)
-    gpu_index = local
-    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
-    if vis and "," not in vis and vis.strip().isdigit():
-        gpu_index = int(vis)
-    clocks = ClockSampler(gpu_index, args.clock_log)
+    clocks = ClockSampler(gpu_index_of(local), args.clock_log)
     clocks.start()
     clock_pad(step, dev, pad)
     ra.ra_trace_reset()
@@ -612,6 +846,34 @@ def run_backward(args, w, ws, rank, local):
 
 
 # ------------------------------------------------------------------ arms
+def head_slice(w, heads: int):
+    """The workload restricted to its first `heads` query heads and their KV
+    heads.  The inputs are the full workload's tensors cut to those heads
+    (the same values), so the slice is the same problem on fewer heads."""
+    import dataclasses
+
+    g = w.heads // w.kv_heads
+    if heads <= 0 or heads > w.heads or heads % g:
+        raise SystemExit(f"--heads must be a positive multiple of {g} up to {w.heads}")
+    return dataclasses.replace(w, name=f"{w.name}[:{heads} heads]", heads=heads,
+                               kv_heads=heads // g,
+                               extra={**w.extra, "full": w.name, "full_heads": w.heads,
+                                      "full_kv_heads": w.kv_heads})
+
+
+def workload_inputs(w):
+    """(q, k, v) of the workload; for a head slice, the full workload's
+    tensors cut to its heads."""
+    from blockwise_online_softmax_gb300 import inputs
+
+    full = w.extra.get("full")
+    if full is None:
+        return inputs.make_workload(w)
+    q, k, v = inputs.make_workload(inputs.WORKLOADS[full])
+    return (q[:, :w.heads].contiguous(), k[:, :w.kv_heads].contiguous(),
+            v[:, :w.kv_heads].contiguous())
+
+
 def forward_config(w, ws):
     """The workload description both arms print, key for key."""
     return {
@@ -646,7 +908,7 @@ def run_reference(args, w, ws, rank):
         return
     from blockwise_online_softmax_gb300 import inputs
 
-    q, k, v = inputs.make_workload(w)
+    q, k, v = workload_inputs(w)
     per_step = args.ref_step_seconds
     for _ in range(args.warmup):
         oracle_sample(w, q, k, v, per_step / 4)
@@ -682,7 +944,7 @@ def run_ours(args, w, ws, rank, local):
     binding.lib()
     peaks, peak_src = load_peaks()
 
-    q, k, v = inputs.make_workload(w)
+    q, k, v = workload_inputs(w)
     mask = args.mask
     if mask is not None:
         pos = binding.layout_positions(w.N, w.P, mask.layout)
@@ -709,11 +971,7 @@ def run_ours(args, w, ws, rank, local):
     torch.cuda.synchronize(dev)
     barrier(ws)
 
-    gpu_index = local
-    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
-    if vis and "," not in vis and vis.strip().isdigit():
-        gpu_index = int(vis)
-    clocks = ClockSampler(gpu_index, args.clock_log)
+    clocks = ClockSampler(gpu_index_of(local), args.clock_log)
     clocks.start()
     clock_pad(step, dev, pad)
     ra.ra_trace_reset()
@@ -909,11 +1167,20 @@ def main():
                     help="time the decode path on this workload instead")
     ap.add_argument("--backward", action="store_true",
                     help="time the backward ring (ra_ring_backward) instead")
+    ap.add_argument("--state", action="store_true",
+                    help="time the state kernels (init, merge, finalize) on the workload's state")
+    ap.add_argument("--ring-steps", action="store_true",
+                    help="time the step-by-step ring (init, P x ra_ring_step, finalize)")
+    ap.add_argument("--heads", type=int, default=0,
+                    help="run on the first H query heads (and their KV heads) of the workload "
+                         "only; for profiling a full-length slice in a few GB")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
     ws, rank, local = dist_info()
     w = WORKLOADS[args.workload]
+    if args.heads:
+        w = head_slice(w, args.heads)
     args.mask = MaskRun(w, args.layout, args.window, args.docs, args.n_valid, seed=w.seed)
     if not args.mask.active():
         args.mask = None
@@ -928,7 +1195,14 @@ def main():
             torch.cuda.set_device(local)
         dist.init_process_group(backend)
     try:
-        if args.backward:
+        if (args.state or args.ring_steps) and args.impl == "reference":
+            ap.error("state and ring-step runs have no reference arm; the oracle is the "
+                     "cpu_baseline or the parity check")
+        if args.state:
+            run_state(args, w, ws, rank, local)
+        elif args.ring_steps:
+            run_steps(args, w, ws, rank, local)
+        elif args.backward:
             if args.impl == "reference":
                 ap.error("backward runs have no reference arm; the oracle is the cpu_baseline")
             run_backward(args, w, ws, rank, local)

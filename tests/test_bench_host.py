@@ -63,3 +63,42 @@ def test_parity_check_takes_every_row_of_a_small_workload():
     bad[777, 0, 5] += 1e-3  # row 777 is none of the fixed rows {0, 1, 127, 128, c/2, c-1} of a block
     res = bench.parity_check(w, q, k, v, bad, lse)
     assert not res["pass"] and res["max_abs_o"] == pytest.approx(1e-3, rel=1e-2)
+
+
+def test_both_arms_describe_the_workload_identically():
+    # The reference arm and the GPU arm print the same config dict, key for
+    # key, so a reader (or a script) can tell they ran the same workload.
+    for name, w in inputs.WORKLOADS.items():
+        a, b = bench.forward_config(w, 1), bench.forward_config(w, 1)
+        assert a == b and a["workload"] == name
+        for key in ("N", "P", "c", "heads", "kv_heads", "d", "causal", "recipe", "seed"):
+            assert key in a
+
+
+def test_l2_flush_only_for_workloads_that_fit_in_l2():
+    W = inputs.WORKLOADS
+    assert bench.needs_l2_flush(W["tiny-exact"]) and bench.needs_l2_flush(W["mha-8k"])
+    for name in ("mha-32k-scaled-keys", "gqa-128k", "mha-1m-planted"):
+        assert not bench.needs_l2_flush(W[name])
+        assert bench.footprint_bytes(W[name]) > 2 * bench.L2_BYTES
+    assert bench.L2_FLUSH_BYTES > 2 * bench.L2_BYTES
+    assert "written between timed steps" in bench.forward_config(W["mha-8k"], 1)["l2"]
+
+
+def test_state_kernel_bytes():
+    # m and l (8 bytes) plus d fp32 values per state (row, head).
+    b = bench.state_bytes(128)
+    assert b == {"state_init": 520, "merge": 3 * 520, "finalize": 520 + 516}
+    assert bench.state_bytes(64)["merge"] == 3 * 264
+
+
+def test_head_slice_is_the_same_problem_on_fewer_heads():
+    w = bench.head_slice(inputs.WORKLOADS["mha-8k"], 2)
+    assert (w.heads, w.kv_heads, w.N, w.P) == (2, 2, 8192, 8)
+    q, k, v = bench.workload_inputs(w)
+    fq, fk, fv = inputs.make_workload(inputs.WORKLOADS["mha-8k"])
+    assert torch.equal(q, fq[:, :2]) and torch.equal(k, fk[:, :2]) and torch.equal(v, fv[:, :2])
+    g = bench.head_slice(inputs.WORKLOADS["gqa-128k"], 8)
+    assert (g.heads, g.kv_heads) == (8, 2)
+    with pytest.raises(SystemExit):
+        bench.head_slice(inputs.WORKLOADS["gqa-128k"], 6)
