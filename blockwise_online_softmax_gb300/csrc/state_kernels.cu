@@ -1,9 +1,7 @@
 // State kernels: identity init, log-sum-exp merge, finalize.  All three are
 // HBM-bound streams over [rows, heads] scalars and [rows, heads, d] fp32
-// vectors.  Merge and finalize give one warp to one (row, head): lane 0
-// reads the two scalars, and the per-row factors reach the other lanes by
-// warp shuffle.  The d-vector then moves as coalesced float4 (d = 128) or
-// float2 (d = 64) accesses, one 512- or 256-byte run per warp.
+// vectors, moved as coalesced float4 accesses by grid-stride loops sized to
+// fill every SM.
 #include <cmath>
 #include <cstdint>
 
@@ -36,71 +34,112 @@ __device__ __forceinline__ void merge_factors(float ma, float mb, float& m, floa
   eb = (mb == -INFINITY) ? (m == -INFINITY ? 1.f : 0.f) : expf(mb - mref);
 }
 
-template <int D>
-__global__ void merge_kernel(float* __restrict__ m_a, float* __restrict__ l_a,
-                             float* __restrict__ o_a, const float* __restrict__ m_b,
-                             const float* __restrict__ l_b, const float* __restrict__ o_b,
-                             long long n_rh) {
-  const int lane = threadIdx.x & 31;
-  const long long rh = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  if (rh >= n_rh) return;  // warp-uniform
-  float m = 0.f, ea = 0.f, eb = 0.f;
-  if (lane == 0) {
-    const float ma = m_a[rh], mb = m_b[rh];
-    merge_factors(ma, mb, m, ea, eb);
-    l_a[rh] = ea * l_a[rh] + eb * l_b[rh];
-    m_a[rh] = m;
-  }
-  ea = __shfl_sync(0xffffffffu, ea, 0);
-  eb = __shfl_sync(0xffffffffu, eb, 0);
-  if constexpr (D == 128) {
-    float4* pa = reinterpret_cast<float4*>(o_a + rh * D) + lane;
-    const float4 x = *pa;
-    const float4 y = reinterpret_cast<const float4*>(o_b + rh * D)[lane];
-    *pa = make_float4(ea * x.x + eb * y.x, ea * x.y + eb * y.y, ea * x.z + eb * y.z,
-                      ea * x.w + eb * y.w);
-  } else {
-    float2* pa = reinterpret_cast<float2*>(o_a + rh * D) + lane;
-    const float2 x = *pa;
-    const float2 y = reinterpret_cast<const float2*>(o_b + rh * D)[lane];
-    *pa = make_float2(ea * x.x + eb * y.x, ea * x.y + eb * y.y);
-  }
-}
+// Merge and finalize stream O~ as float4s: float4 e of the [rows * heads,
+// D] array belongs to (row, head) rh = e / (D / 4).  A thread takes kUnroll
+// float4s a grid stride apart and issues every load of all of them (O~, and
+// m and l of their (row, head), which the lanes sharing a (row, head) read
+// as one broadcast) before any arithmetic, so each thread keeps several
+// independent requests in flight.  The lane that holds the first float4 of
+// a (row, head) writes its scalars.  A (row, head) lies within one warp
+// (D / 4 = 32 or 16 consecutive float4s), and its scalars are read by the
+// warp's loads, which a __syncwarp puts before that lane's store, so the
+// in-place forms (merge into a; finalize with out = o, lse = m) are safe.
+// The loop runs over warp-aligned bases, so every lane of a warp takes the
+// same number of iterations and reaches each __syncwarp.
+constexpr int kUnroll = 4;
 
 template <int D>
-__global__ void finalize_kernel(const float* m, const float* l, const float* o, float* out,
-                                float* lse, long long n_rh) {
-  // `out` may alias `o` and `lse` may alias `m`: every element is read
-  // before it is written, by the same thread.
+__global__ void __launch_bounds__(kThreads) merge_kernel(
+    float* __restrict__ m_a, float* __restrict__ l_a, float4* __restrict__ o_a,
+    const float* __restrict__ m_b, const float* __restrict__ l_b,
+    const float4* __restrict__ o_b, long long n4) {
+  constexpr int V = D / 4;  // float4s per (row, head)
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   const int lane = threadIdx.x & 31;
-  const long long rh = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  if (rh >= n_rh) return;
-  float inv = 0.f;
-  if (lane == 0) {
-    const float mm = m[rh], ll = l[rh];
-    float val;
-    if (ll > 0.f) {
-      inv = 1.f / ll;
-      val = mm + logf(ll);
-    } else {
-      val = -INFINITY;
+  for (long long w0 = static_cast<long long>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
+       w0 < n4; w0 += kUnroll * stride) {
+    float4 x[kUnroll], y[kUnroll];
+    float ma[kUnroll], mb[kUnroll], la[kUnroll], lb[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const long long e = w0 + u * stride + lane;
+      if (e < n4) {
+        const long long rh = e / V;
+        x[u] = o_a[e];
+        y[u] = __ldg(&o_b[e]);
+        ma[u] = m_a[rh];
+        la[u] = l_a[rh];
+        mb[u] = __ldg(&m_b[rh]);
+        lb[u] = __ldg(&l_b[rh]);
+      }
     }
-    lse[rh] = val;
-  }
-  inv = __shfl_sync(0xffffffffu, inv, 0);
-  if constexpr (D == 128) {
-    const float4 x = reinterpret_cast<const float4*>(o + rh * D)[lane];
-    reinterpret_cast<float4*>(out + rh * D)[lane] =
-        make_float4(x.x * inv, x.y * inv, x.z * inv, x.w * inv);
-  } else {
-    const float2 x = reinterpret_cast<const float2*>(o + rh * D)[lane];
-    reinterpret_cast<float2*>(out + rh * D)[lane] = make_float2(x.x * inv, x.y * inv);
+    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const long long e = w0 + u * stride + lane;
+      if (e < n4) {
+        float m, ea, eb;
+        merge_factors(ma[u], mb[u], m, ea, eb);
+        o_a[e] = make_float4(ea * x[u].x + eb * y[u].x, ea * x[u].y + eb * y[u].y,
+                             ea * x[u].z + eb * y[u].z, ea * x[u].w + eb * y[u].w);
+        if (e % V == 0) {
+          const long long rh = e / V;
+          l_a[rh] = ea * la[u] + eb * lb[u];
+          m_a[rh] = m;
+        }
+      }
+    }
   }
 }
 
-int grid_for_warps(long long n_warps) {
-  const long long warps_per_block = kThreads / 32;
-  return static_cast<int>((n_warps + warps_per_block - 1) / warps_per_block);
+template <int D>
+__global__ void __launch_bounds__(kThreads) finalize_kernel(
+    const float* m, const float* l, const float4* o, float4* out, float* lse, long long n4) {
+  // `out` may alias `o` and `lse` may alias `m` (see above).
+  constexpr int V = D / 4;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  const int lane = threadIdx.x & 31;
+  for (long long w0 = static_cast<long long>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
+       w0 < n4; w0 += kUnroll * stride) {
+    float4 x[kUnroll];
+    float mm[kUnroll], ll[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const long long e = w0 + u * stride + lane;
+      if (e < n4) {
+        const long long rh = e / V;
+        x[u] = o[e];
+        mm[u] = m[rh];
+        ll[u] = l[rh];
+      }
+    }
+    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const long long e = w0 + u * stride + lane;
+      if (e < n4) {
+        const bool seen = ll[u] > 0.f;
+        const float inv = seen ? 1.f / ll[u] : 0.f;
+        out[e] = make_float4(x[u].x * inv, x[u].y * inv, x[u].z * inv, x[u].w * inv);
+        if (e % V == 0) lse[e / V] = seen ? mm[u] + logf(ll[u]) : -INFINITY;
+      }
+    }
+  }
+}
+
+// Grid of the streaming kernels: every SM holds as many CTAs of `kernel`
+// as fit, and no more CTAs than the work needs.
+template <typename K>
+int stream_grid(K kernel, long long n4) {
+  int dev = 0, sms = 148, per_sm = 1;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) != cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  const long long want = (n4 + kThreads - 1) / kThreads;
+  const long long cap = static_cast<long long>(sms) * per_sm;
+  return static_cast<int>(want < cap ? want : cap);
 }
 
 }  // namespace
@@ -123,25 +162,31 @@ cudaError_t launch_state_init(float* m, float* l, float* o, long long rows, int 
 
 cudaError_t launch_merge(float* m_a, float* l_a, float* o_a, const float* m_b, const float* l_b,
                          const float* o_b, long long rows, int heads, int d, cudaStream_t st) {
-  const long long n_rh = rows * heads;
-  if (n_rh == 0) return cudaSuccess;
-  const int grid = grid_for_warps(n_rh);
+  const long long n4 = rows * heads * d / 4;
+  if (n4 == 0) return cudaSuccess;
+  float4* oa = reinterpret_cast<float4*>(o_a);
+  const float4* ob = reinterpret_cast<const float4*>(o_b);
   if (d == 128)
-    merge_kernel<128><<<grid, kThreads, 0, st>>>(m_a, l_a, o_a, m_b, l_b, o_b, n_rh);
+    merge_kernel<128><<<stream_grid(merge_kernel<128>, n4), kThreads, 0, st>>>(m_a, l_a, oa, m_b,
+                                                                                l_b, ob, n4);
   else
-    merge_kernel<64><<<grid, kThreads, 0, st>>>(m_a, l_a, o_a, m_b, l_b, o_b, n_rh);
+    merge_kernel<64><<<stream_grid(merge_kernel<64>, n4), kThreads, 0, st>>>(m_a, l_a, oa, m_b,
+                                                                              l_b, ob, n4);
   return cudaGetLastError();
 }
 
 cudaError_t launch_finalize(const float* m, const float* l, const float* o, float* out,
                             float* lse, long long rows, int heads, int d, cudaStream_t st) {
-  const long long n_rh = rows * heads;
-  if (n_rh == 0) return cudaSuccess;
-  const int grid = grid_for_warps(n_rh);
+  const long long n4 = rows * heads * d / 4;
+  if (n4 == 0) return cudaSuccess;
+  const float4* o4 = reinterpret_cast<const float4*>(o);
+  float4* out4 = reinterpret_cast<float4*>(out);
   if (d == 128)
-    finalize_kernel<128><<<grid, kThreads, 0, st>>>(m, l, o, out, lse, n_rh);
+    finalize_kernel<128><<<stream_grid(finalize_kernel<128>, n4), kThreads, 0, st>>>(m, l, o4,
+                                                                                      out4, lse, n4);
   else
-    finalize_kernel<64><<<grid, kThreads, 0, st>>>(m, l, o, out, lse, n_rh);
+    finalize_kernel<64><<<stream_grid(finalize_kernel<64>, n4), kThreads, 0, st>>>(m, l, o4, out4,
+                                                                                    lse, n4);
   return cudaGetLastError();
 }
 
