@@ -261,7 +261,7 @@ def note_window(clk, pad):
 
 
 # ------------------------------------------------------------------ traffic record
-FORWARD_SOURCES = ("umma_kernel.cu", "ptx.cuh", "ra_internal.h")
+FORWARD_SOURCES = ("umma_kernel.cu", "fwd_tile.cuh", "ptx.cuh", "ra_internal.h")
 DECODE_SOURCES = ("decode_kernel.cu", "ptx.cuh", "ra_internal.h")
 STATE_SOURCES = ("state_kernels.cu", "ra_internal.h")
 
