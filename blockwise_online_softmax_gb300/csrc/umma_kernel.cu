@@ -508,6 +508,28 @@ umma_update_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 // the union of the two query tiles' key-tile ranges (as in the one-step
 // kernel), skipping steps whose pair has no allowed key.
 
+// The work item of a fused-ring CTA: rank i, query head h and query-tile
+// pair.  The grid is (query-tile pairs, P ranks, query heads): the launch
+// order (x fastest, then y, then z) is head-major, and the query heads of
+// one KV head are consecutive, so the CTAs that run at the same time read
+// the K/V blocks of one KV head, which stay in L2 for all of them.  Under
+// causal masking with the contiguous layout the ranks with the most
+// blocks, and within a rank the later query tiles, come first.  Everything
+// comes straight from the block index, which the compiler re-reads instead
+// of keeping live across the register split.
+struct RingItem {
+  int i, h, pair;
+};
+__device__ __forceinline__ RingItem ring_item(const FwdArgs& a) {
+  const bool heavy_first = a.mask.causal && a.layout == kContiguous;
+  RingItem it;
+  it.h = a.h0 + static_cast<int>(blockIdx.z);
+  it.i = heavy_first ? a.P - 1 - static_cast<int>(blockIdx.y) : static_cast<int>(blockIdx.y);
+  it.pair = a.mask.causal ? static_cast<int>(gridDim.x - 1 - blockIdx.x)
+                          : static_cast<int>(blockIdx.x);
+  return it;
+}
+
 // Slot-ring producer over the whole visit: slot c takes visit tile c (K,
 // v_lag = 0) or c - 1 (V, v_lag = 1); a slot without a tile is a plain
 // arrival (slot 0 for V, the slot after the last tile for K).  Returns false
@@ -569,7 +591,7 @@ __device__ __forceinline__ void ring_control_roles(const FwdArgs& a, const StepV
   using C = Cfg<D>;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int h = a.h0 + static_cast<int>(blockIdx.y);
+  const int h = ring_item(a).h;
   const int kh = h / (a.heads / a.kv_heads);
   const long long lim = a.wait_limit;
   auto bar = [&](int x) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(x); };
@@ -716,7 +738,6 @@ __device__ __forceinline__ void ring_softmax_role(const FwdArgs& a, const StepVi
   using C = Cfg<D>;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int h = a.h0 + static_cast<int>(blockIdx.y);
   const long long lim = a.wait_limit;
   auto bar = [&](int x) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(x); };
   const int g = warp >> 2;
@@ -727,7 +748,6 @@ __device__ __forceinline__ void ring_softmax_role(const FwdArgs& a, const StepVi
   const uint32_t o_col = C::O_COL + static_cast<uint32_t>(g) * D;
   const long long grow = row0 + g * BM + row;  // row within block i
   const bool valid = grow < a.cq;
-  const long long oidx = (static_cast<long long>(i) * a.cq + grow) * a.heads + h;
   const float sl2 = a.scale_log2;
   const uint64_t sl2x2 = f2pack(sl2, sl2);
   {
@@ -772,6 +792,7 @@ __device__ __forceinline__ void ring_softmax_role(const FwdArgs& a, const StepVi
   if (!ok) return;
   const bool seen = l_run > 0.f;
   const float inv = seen ? 1.f / l_run : 0.f;
+  const long long oidx = (static_cast<long long>(i) * a.cq + grow) * a.heads + ring_item(a).h;
   float* dst = a.o + oidx * D;
   if (cnt > 0) {
     tc_fence_after();
@@ -799,10 +820,8 @@ __device__ __forceinline__ void ring_softmax_role(const FwdArgs& a, const StepVi
   if (valid) a.m[oidx] = seen ? (m_used + log2f(l_run)) * kLn2 : -INFINITY;
 }
 
-// Grid (query-tile pairs, query heads h0 .. h0 + nh - 1, P ranks).  Under
-// causal masking with the contiguous layout, rank i does i + 1 blocks of
-// work and the later rows of a block more than the earlier ones, so the
-// heavy CTAs are launched first.
+// Grid (query-tile pairs, P ranks, query heads h0 .. h0 + nh - 1); see
+// ring_item for the order.
 template <int D>
 __global__ void __launch_bounds__(NTHREADS, 1)
 umma_ring_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -821,11 +840,10 @@ umma_ring_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
-  const bool heavy_first = a.mask.causal && a.layout == kContiguous;
-  const int i = heavy_first ? a.P - 1 - static_cast<int>(blockIdx.z)
-                            : static_cast<int>(blockIdx.z);
-  const int pair = a.mask.causal ? static_cast<int>(gridDim.x - 1 - blockIdx.x)
-                                 : static_cast<int>(blockIdx.x);
+  const RingItem it = ring_item(a);
+  const int i = it.i;
+  const int h = it.h;
+  const int pair = it.pair;
   const long long row0 = static_cast<long long>(pair) * (NQ * BM);
   const long long vb = valid_bound(a.mask);
   // The visit table: every step's tile ranges, computed once by all threads
@@ -850,7 +868,7 @@ umma_ring_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         const long long grow = row0 + tid;
         if (grow < a.cq) {
           const long long oidx =
-              (static_cast<long long>(i) * a.cq + grow) * a.heads + a.h0 + blockIdx.y;
+              (static_cast<long long>(i) * a.cq + grow) * a.heads + h;
 #pragma unroll
           for (int j = 0; j < D / 4; ++j)
             reinterpret_cast<float4*>(a.o + oidx * D)[j] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -897,8 +915,10 @@ cudaError_t launch_ring_d(const FwdArgs& a, const CUtensorMap& tq, const CUtenso
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  dim3 grid(static_cast<unsigned>((a.cq + NQ * BM - 1) / (NQ * BM)), a.nh > 0 ? a.nh : a.heads,
-            a.P);
+  const int nh = a.nh > 0 ? a.nh : a.heads;
+  dim3 grid(static_cast<unsigned>((a.cq + NQ * BM - 1) / (NQ * BM)), static_cast<unsigned>(a.P),
+            static_cast<unsigned>(nh));
+  if (grid.z > 65535u) return cudaErrorInvalidValue;
   umma_ring_kernel<D><<<grid, NTHREADS, smem, st>>>(tq, tk, tv, a);
   return cudaGetLastError();
 }
