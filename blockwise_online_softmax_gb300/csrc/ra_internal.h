@@ -136,6 +136,7 @@ struct FwdArgs {
   MaskArgs mask;
   int h0;  // fused ring: first query head of the launch (grid.y runs h0 .. h0 + nh - 1)
   int nh;  // fused ring: query heads in the launch (0: all `heads`)
+  int ring_lc;  // fused ring: log2 of the heads per chunk of the launch order (set by its launcher)
 };
 
 // Decoded work item of grid.z index w.

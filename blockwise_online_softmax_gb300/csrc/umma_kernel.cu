@@ -509,24 +509,35 @@ umma_update_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 // kernel), skipping steps whose pair has no allowed key.
 
 // The work item of a fused-ring CTA: rank i, query head h and query-tile
-// pair.  The grid is (query-tile pairs, P ranks, query heads): the launch
-// order (x fastest, then y, then z) is head-major, and the query heads of
-// one KV head are consecutive, so the CTAs that run at the same time read
-// the K/V blocks of one KV head, which stay in L2 for all of them.  Under
-// causal masking with the contiguous layout the ranks with the most
-// blocks, and within a rank the later query tiles, come first.  Everything
-// comes straight from the block index, which the compiler re-reads instead
-// of keeping live across the register split.
+// pair.  The query heads of a launch are taken in chunks of 2^a.ring_lc
+// consecutive heads (4 when the head count allows: one KV head's query heads
+// under GQA 4:1).  The grid is (query-tile pairs, 2^ring_lc x P, chunks):
+// the launch order (x fastest, then y, then z) runs one chunk after the
+// other, so the CTAs that run at the same time read the K/V blocks of a few
+// heads, which stay in L2 for all of them; within a chunk it is rank-major,
+// and under causal masking with the contiguous layout the ranks with the
+// most blocks, and within a rank the later query tiles, come first, so
+// that a launch of one or two waves still starts all its heaviest CTAs
+// first.  Shifts and masks of the block index only: cheap enough for the
+// compiler to recompute rather than keep live across the register split.
 struct RingItem {
   int i, h, pair;
 };
 __device__ __forceinline__ RingItem ring_item(const FwdArgs& a) {
+  // The block index is read with volatile moves so that every call
+  // recomputes the item where it is used instead of the compiler keeping
+  // one copy live through the roles.
+  uint32_t bx, by, bz;
+  asm volatile("mov.u32 %0, %%ctaid.x;" : "=r"(bx));
+  asm volatile("mov.u32 %0, %%ctaid.y;" : "=r"(by));
+  asm volatile("mov.u32 %0, %%ctaid.z;" : "=r"(bz));
   const bool heavy_first = a.mask.causal && a.layout == kContiguous;
+  const int y = static_cast<int>(by);
+  const int r = y >> a.ring_lc;
   RingItem it;
-  it.h = a.h0 + static_cast<int>(blockIdx.z);
-  it.i = heavy_first ? a.P - 1 - static_cast<int>(blockIdx.y) : static_cast<int>(blockIdx.y);
-  it.pair = a.mask.causal ? static_cast<int>(gridDim.x - 1 - blockIdx.x)
-                          : static_cast<int>(blockIdx.x);
+  it.h = a.h0 + (static_cast<int>(bz) << a.ring_lc) + (y & ((1 << a.ring_lc) - 1));
+  it.i = heavy_first ? a.P - 1 - r : r;
+  it.pair = a.mask.causal ? static_cast<int>(gridDim.x - 1 - bx) : static_cast<int>(bx);
   return it;
 }
 
@@ -581,7 +592,7 @@ __device__ __forceinline__ bool produce_ring(const FwdArgs& a, const StepVisit* 
 // Producers (warps 8 and 10) and MMA issuer (warp 9) of the fused ring; the
 // visit is not empty (the kernel returns early otherwise).
 template <int D>
-__device__ __forceinline__ void ring_control_roles(const FwdArgs& a, const StepVisit* rec, int i,
+__device__ __forceinline__ void ring_control_roles(const FwdArgs& a, const StepVisit* rec,
                                                    long long row0, uint32_t tmem, uint32_t sQ,
                                                    uint32_t sK, uint32_t sV, uint32_t bar0,
                                                    volatile int* abort_flag,
@@ -603,7 +614,8 @@ __device__ __forceinline__ void ring_control_roles(const FwdArgs& a, const StepV
         mbar_arrive_expect_tx(bar(C::B_Q), NQ * C::TILE_BYTES);
 #pragma unroll
         for (int g = 0; g < NQ; ++g) {
-          const int q_row = static_cast<int>(static_cast<long long>(i) * a.cq + row0 + g * BM);
+          const int q_row =
+              static_cast<int>(static_cast<long long>(ring_item(a).i) * a.cq + row0 + g * BM);
 #pragma unroll
           for (int ch = 0; ch < C::NCH; ++ch)
             tma_load_3d(sQ + g * C::TILE_BYTES + ch * CHUNK_BYTES, tmQ, bar(C::B_Q), ch * 64, h,
@@ -731,7 +743,7 @@ __device__ __forceinline__ void ring_control_roles(const FwdArgs& a, const StepV
 // and l are relative to the same m), or 0 and -inf for a row that saw no
 // key.  out is [rows, heads, d] and lse [rows, heads], like the state.
 template <int D>
-__device__ __forceinline__ void ring_softmax_role(const FwdArgs& a, const StepVisit* rec, int i,
+__device__ __forceinline__ void ring_softmax_role(const FwdArgs& a, const StepVisit* rec,
                                                   long long row0, long long vb, uint32_t tmem,
                                                   uint32_t bar0,
                                                   volatile int* abort_flag) {
@@ -746,7 +758,7 @@ __device__ __forceinline__ void ring_softmax_role(const FwdArgs& a, const StepVi
   const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
   const uint32_t s_col = C::S_COL + static_cast<uint32_t>(g) * BN;
   const uint32_t o_col = C::O_COL + static_cast<uint32_t>(g) * D;
-  const long long grow = row0 + g * BM + row;  // row within block i
+  const long long grow = row0 + g * BM + row;  // row within this CTA's query block
   const bool valid = grow < a.cq;
   const float sl2 = a.scale_log2;
   const uint64_t sl2x2 = f2pack(sl2, sl2);
@@ -766,7 +778,7 @@ __device__ __forceinline__ void ring_softmax_role(const FwdArgs& a, const StepVi
     // Select, not index: g is not a compile-time constant here.
     const int t0 = g ? rec[s].ta[1] : rec[s].ta[0], t1 = g ? rec[s].tb[1] : rec[s].tb[0];
     if (t1 <= t0) continue;
-    const Work wk = ring_work(a, i, s);
+    const Work wk = ring_work(a, ring_item(a).i, s);
     int row_lo = 0, row_hi = 0;
     if (valid) {
       long long lo, hi;
@@ -792,7 +804,8 @@ __device__ __forceinline__ void ring_softmax_role(const FwdArgs& a, const StepVi
   if (!ok) return;
   const bool seen = l_run > 0.f;
   const float inv = seen ? 1.f / l_run : 0.f;
-  const long long oidx = (static_cast<long long>(i) * a.cq + grow) * a.heads + ring_item(a).h;
+  const RingItem it = ring_item(a);
+  const long long oidx = (static_cast<long long>(it.i) * a.cq + grow) * a.heads + it.h;
   float* dst = a.o + oidx * D;
   if (cnt > 0) {
     tc_fence_after();
@@ -820,8 +833,8 @@ __device__ __forceinline__ void ring_softmax_role(const FwdArgs& a, const StepVi
   if (valid) a.m[oidx] = seen ? (m_used + log2f(l_run)) * kLn2 : -INFINITY;
 }
 
-// Grid (query-tile pairs, P ranks, query heads h0 .. h0 + nh - 1); see
-// ring_item for the order.
+// Grid (query-tile pairs, 2^ring_lc x P, head chunks); see ring_item for
+// the order.
 template <int D>
 __global__ void __launch_bounds__(NTHREADS, 1)
 umma_ring_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -889,7 +902,7 @@ umma_ring_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   const uint32_t tmem = *tmem_slot;
   if (warp >= 8) {
     regs_dec<C::REGS_CONTROL>();
-    ring_control_roles<D>(a, rec, i, row0, tmem, sQ, sK, sV, bar0, abort_flag, &tmQ, &tmK, &tmV);
+    ring_control_roles<D>(a, rec, row0, tmem, sQ, sK, sV, bar0, abort_flag, &tmQ, &tmK, &tmV);
     tc_fence_before();
     named_bar_sync(1, NTHREADS);
     if (warp == 9) {
@@ -898,7 +911,7 @@ umma_ring_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     }
   } else {
     regs_inc<C::REGS_SOFTMAX>();
-    ring_softmax_role<D>(a, rec, i, row0, vb, tmem, bar0, abort_flag);
+    ring_softmax_role<D>(a, rec, row0, vb, tmem, bar0, abort_flag);
     tc_fence_before();
     named_bar_sync(1, NTHREADS);
   }
@@ -916,10 +929,12 @@ cudaError_t launch_ring_d(const FwdArgs& a, const CUtensorMap& tq, const CUtenso
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int nh = a.nh > 0 ? a.nh : a.heads;
-  dim3 grid(static_cast<unsigned>((a.cq + NQ * BM - 1) / (NQ * BM)), static_cast<unsigned>(a.P),
-            static_cast<unsigned>(nh));
-  if (grid.z > 65535u) return cudaErrorInvalidValue;
-  umma_ring_kernel<D><<<grid, NTHREADS, smem, st>>>(tq, tk, tv, a);
+  FwdArgs b = a;
+  b.ring_lc = nh % 4 == 0 ? 2 : (nh % 2 == 0 ? 1 : 0);
+  dim3 grid(static_cast<unsigned>((a.cq + NQ * BM - 1) / (NQ * BM)),
+            static_cast<unsigned>(a.P << b.ring_lc), static_cast<unsigned>(nh >> b.ring_lc));
+  if (grid.y > 65535u || grid.z > 65535u) return cudaErrorInvalidValue;
+  umma_ring_kernel<D><<<grid, NTHREADS, smem, st>>>(tq, tk, tv, b);
   return cudaGetLastError();
 }
 
