@@ -1002,17 +1002,22 @@ def run_ours(args, w, ws, rank, local):
     n_upd, ms_upd = ra.ra_trace_query("block_update_bf16" if w.dtype == "bf16"
                                       else "block_update_f32")
     n_fz, ms_fz = ra.ra_trace_query("ring_fused_bf16")
+    n_fz32, ms_fz32 = ra.ra_trace_query("ring_fused_f32")
     n_init, ms_init = ra.ra_trace_query("state_init")
     n_fin, ms_fin = ra.ra_trace_query("finalize")
     ra.ra_trace_reset()
-    # The dominant kernel: the fused ring (bf16, one launch per forward) or
-    # the one-step block update (fp32, P launches per forward).
+    # The dominant kernel: the fused ring (one launch per forward: tcgen05 in
+    # bf16, FFMA in fp32), or the one-step block update (P launches).
     if n_fz > 0:
         dom_ms, dom_name, dom_profile = ms_fz, "fused ring forward (tcgen05)", \
             "ring_fused_bf16_traffic.md"
+    elif n_fz32 > 0:
+        dom_ms, dom_name, dom_profile = ms_fz32, "fused ring forward (fp32 FFMA)", None
     else:
         dom_ms, dom_name, dom_profile = ms_upd, "block update (tcgen05)", \
             "block_update_bf16_traffic.md"
+    n_fz += n_fz32
+    ms_fz += ms_fz32
 
     ms_max = reduce_max(ms_total, ws)
     ms_step = ms_max / args.steps
@@ -1027,7 +1032,7 @@ def run_ours(args, w, ws, rank, local):
     # (exact allowed-pair count) over their summed time.
     achieved = (f_exact * args.steps) / (dom_ms * 1e-3) / 1e12 if dom_ms > 0 else None
     peak = peaks["bf16_tflops_sustained"]
-    traffic = recorded_traffic(w.name, dom_profile)
+    traffic = recorded_traffic(w.name, dom_profile) if dom_profile else None
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -1083,7 +1088,7 @@ def run_ours(args, w, ws, rank, local):
         alu_peak = sms * 128 * 2 * 2.07e9 / 1e12
         roof = {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
                 "frac": (achieved / alu_peak) if achieved else None, "traffic": None,
-                "kernel": "block update (fp32 FFMA)",
+                "kernel": dom_name,
                 "peak_kind": f"{sms} SMs x 128 FP32 lanes x 2 FLOPs x 2070 MHz"}
 
     # end to end through the host-buffer entry point

@@ -38,6 +38,7 @@ KERNEL_KINDS = {
     "bwd_dq": 8,
     "bwd_dkdv": 9,
     "ring_fused_bf16": 10,
+    "ring_fused_f32": 11,
 }
 
 _lock = threading.Lock()

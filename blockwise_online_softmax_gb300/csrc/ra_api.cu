@@ -440,11 +440,46 @@ int ring_fused_impl(const void* q, const void* k, const void* v, float* out, flo
   return RA_OK;
 }
 
+// The fp32 ring in one launch (FFMA kernel, state on chip, finalized at
+// the end).
+int ring_fused_f32_impl(const void* q, const void* k, const void* v, float* out, float* lse,
+                        long long N, int P, const MaskSpec& mk, int d, int heads, int kv_heads,
+                        cudaStream_t st) {
+  ra::FwdArgs a{};
+  a.q = q; a.k = k; a.v = v; a.o = out; a.m = lse; a.l = nullptr;
+  a.cq = N / P;
+  a.ck = N / P;
+  a.q_rows = N;
+  a.kv_rows = N;
+  a.heads = heads;
+  a.kv_heads = kv_heads;
+  a.mode = 1;
+  a.P = P;
+  a.nwork = P;
+  put_mask(a, mk);
+  a.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
+  a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+  a.wait_limit = kWaitLimit;
+  if (a.cq == 0) return RA_OK;
+  TraceScope ts(RA_KERNEL_RING_FUSED_F32, st);
+  cudaError_t e = ra::launch_simt_ring(a, d, st);
+  ts.done(e == cudaSuccess);
+  if (e != cudaSuccess) return cuda_fail(e, "fused fp32 ring launch");
+  return RA_OK;
+}
+
+// Whether a ring forward runs as one fused launch (no state in HBM, no
+// scratch): bf16 with P <= kFusedMaxSteps, and fp32.
+bool ring_is_fused(int dtype, int P) {
+  return dtype == RA_F32 || (dtype == RA_BF16 && P <= kFusedMaxSteps);
+}
+
 int ring_forward_impl(const void* q, const void* k, const void* v, float* out, float* lse,
                       long long N, int P, const MaskSpec& mk, int d, int heads, int kv_heads,
                       int dtype, cudaStream_t st, float* l_scratch) {
   if (dtype == RA_BF16 && P <= kFusedMaxSteps)
     return ring_fused_impl(q, k, v, out, lse, N, P, mk, d, heads, kv_heads, st);
+  if (dtype == RA_F32) return ring_fused_f32_impl(q, k, v, out, lse, N, P, mk, d, heads, kv_heads, st);
   const long long rows = N;
   TraceScope t0(RA_KERNEL_STATE_INIT, st);
   cudaError_t e = ra::launch_state_init(lse, l_scratch, out, rows, heads, d, st);
@@ -468,16 +503,17 @@ MaskSpec plain_mask(int causal) {
   return mk;
 }
 
-// ra_ring_forward and ra_ring_forward_masked: the fused launch for bf16,
-// else the step loop with the l scratch from the stream's pool allocator.
+// ra_ring_forward and ra_ring_forward_masked: one fused launch (bf16 with
+// P <= 256, and fp32), else the step loop with the l scratch from the
+// stream's pool allocator.
 int ring_forward_alloc(const void* q, const void* k, const void* v, float* out, float* lse,
                        long long N, int P, const MaskSpec& mk, int d, int heads, int kv_heads,
                        int dtype, void* stream) {
   int rc;
   if ((rc = check_ptrs({q, k, v, out, lse})) != RA_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (dtype == RA_BF16 && P <= kFusedMaxSteps)
-    return ring_fused_impl(q, k, v, out, lse, N, P, mk, d, heads, kv_heads, st);
+  if (ring_is_fused(dtype, P))
+    return ring_forward_impl(q, k, v, out, lse, N, P, mk, d, heads, kv_heads, dtype, st, nullptr);
   float* l_scratch = nullptr;
   const size_t l_bytes = static_cast<size_t>(N) * heads * sizeof(float);
   cudaError_t e = scratch_alloc(reinterpret_cast<void**>(&l_scratch), l_bytes, st);
@@ -1061,9 +1097,9 @@ int ra_ring_forward_noalloc(const void* q, const void* k, const void* v, float* 
                 N * heads, kNoAllocMaxRowsHeads);
   if (N == 0) return RA_OK;
   if ((rc = check_ptrs({q, k, v, out, lse})) != RA_OK) return rc;
-  if (dtype == RA_BF16 && P <= kFusedMaxSteps)
-    return ring_fused_impl(q, k, v, out, lse, N, P, plain_mask(causal), d, heads, kv_heads,
-                           static_cast<cudaStream_t>(stream));
+  if (ring_is_fused(dtype, P))
+    return ring_forward_impl(q, k, v, out, lse, N, P, plain_mask(causal), d, heads, kv_heads,
+                             dtype, static_cast<cudaStream_t>(stream), nullptr);
   float* l_scratch = nullptr;
   if ((rc = noalloc_scratch(&l_scratch)) != RA_OK) return rc;
   // The state-init kernel zeroes the l rows this call uses, so whatever a

@@ -253,6 +253,9 @@ cudaError_t launch_merge(float* m_a, float* l_a, float* o_a, const float* m_b, c
 cudaError_t launch_finalize(const float* m, const float* l, const float* o, float* out,
                             float* lse, long long rows, int heads, int d, cudaStream_t st);
 cudaError_t launch_simt_update(const FwdArgs& a, int d, cudaStream_t st);
+// The whole fp32 ring forward in one launch: a.o is the output [rows,
+// heads, d] and a.m the LSE [rows, heads] (natural log); a.l is unused.
+cudaError_t launch_simt_ring(const FwdArgs& a, int d, cudaStream_t st);
 cudaError_t launch_umma_update(const FwdArgs& a, int d, const CUtensorMap& tq,
                                const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st);
 // The whole ring forward of every rank in one launch (bf16): a.o is the

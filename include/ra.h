@@ -118,7 +118,8 @@ typedef enum {
   RA_KERNEL_BWD_DQ = 8,         /* backward: dQ (tcgen05, Q-stationary) */
   RA_KERNEL_BWD_DKDV = 9,       /* backward: dK, dV (tcgen05, K/V-stationary) */
   RA_KERNEL_RING_FUSED_BF16 = 10, /* the whole bf16 ring forward in one launch (tcgen05) */
-  RA_KERNEL_KINDS = 11
+  RA_KERNEL_RING_FUSED_F32 = 11,  /* the whole fp32 ring forward in one launch (FFMA) */
+  RA_KERNEL_KINDS = 12
 } ra_kernel_kind;
 
 /*
@@ -196,14 +197,15 @@ int ra_ring_step(const void* q, const void* k, const void* v, float* m, float* l
  * its queries, then finalizes ([PB] §2).
  *   out: [N, heads, d] fp32: O = O~ / l (0 for a row that sees no key).
  *   lse: [N, heads] fp32: LSE = m + ln l (-inf for such a row).
- * bf16 with P <= 256: one fused launch.  Each rank's state stays on chip
- * across all P steps and the kernel writes out and lse once; no scratch.
- * fp32 (or P > 256): the state init, P ring-step launches with the O~ state
- * in `out` and m in `lse`, then the finalize.  The l state ([N, heads]
- * fp32) is then the only scratch, allocated stream-ordered on `stream`
- * from the library's scratch pool (see ra_cached_memory) and freed the
- * same way; a failed allocation returns RA_ERR_ALLOC.  Both give the results of init + ra_ring_step for
- * s = 0..P-1 + ra_finalize, the fused launch up to the last roundings of
+ * bf16 with P <= 256 (tcgen05), and fp32 (FFMA): one fused launch.  Each
+ * rank's state stays on chip across all P steps and the kernel writes out
+ * and lse once; no scratch.  bf16 with P > 256: the state init, P
+ * ring-step launches with the O~ state in `out` and m in `lse`, then the
+ * finalize.  The l state ([N, heads] fp32) is then the only scratch,
+ * allocated stream-ordered on `stream` from the library's scratch pool
+ * (see ra_cached_memory) and freed the same way; a failed allocation
+ * returns RA_ERR_ALLOC.  Both give the results of init + ra_ring_step for
+ * s = 0..P-1 + ra_finalize, the fused launches up to the last roundings of
  * the finalize.
  */
 int ra_ring_forward(const void* q, const void* k, const void* v, float* out, float* lse,
@@ -246,10 +248,10 @@ int ra_ring_forward_host(const void* q_host, const void* k_host, const void* v_h
  *   The first call on a device looks up the array's device address once,
  *   with that device current.  Make that first call before any stream
  *   capture starts.
- *   Only the calls that run the ring step by step use the array: fp32
- *   inputs, and bf16 inputs with P > 256.  A bf16 call with P <= 256 runs
- *   the one fused launch, which keeps its state on chip and never touches
- *   the array.  Calls that use it share the one array.  Each clears the
+ *   Only the calls that run the ring step by step use the array: bf16
+ *   inputs with P > 256.  fp32 calls, and bf16 calls with P <= 256, run one
+ *   fused launch, which keeps its state on chip and never touches the
+ *   array.  Calls that use it share the one array.  Each clears the
  *   rows it uses first, so what an earlier call left there does not
  *   matter.  But two such calls that overlap on the GPU (different
  *   streams, not ordered) race on the array and both results are

@@ -259,8 +259,8 @@ def trace_counts(run):
     try:
         run()
         got = {kind: ra.ra_trace_query(kind)
-               for kind in ("ring_fused_bf16", "block_update_bf16", "block_update_f32",
-                            "state_init", "finalize")}
+               for kind in ("ring_fused_bf16", "ring_fused_f32", "block_update_bf16",
+                            "block_update_f32", "state_init", "finalize")}
     finally:
         ra.ra_trace_enable(False)
         ra.ra_trace_reset()
@@ -291,8 +291,7 @@ def test_fused_ring_is_bitwise_repeatable(shape):
 
 
 def test_trace_counts_launches():
-    """bf16: the whole ring is one fused launch.  fp32: state init, one
-    block-update launch per ring step, finalize."""
+    """bf16 and fp32: the whole ring is one fused launch (tcgen05, FFMA)."""
     q, k, v = (t.to(DEV) for t in inputs.make_random(1024, 2, 2, 128, seed=21))
     got = trace_counts(lambda: ra.ra_ring_forward(q, k, v, P=4, causal=True))
     assert [got[x][0] for x in ("ring_fused_bf16", "block_update_bf16", "state_init",
@@ -301,6 +300,6 @@ def test_trace_counts_launches():
     q, k, v = (t.to(DEV) for t in inputs.make_random(1024, 2, 2, 64, dtype=torch.float32,
                                                      seed=21))
     got = trace_counts(lambda: ra.ra_ring_forward(q, k, v, P=4, causal=True))
-    assert [got[x][0] for x in ("ring_fused_bf16", "block_update_f32", "state_init",
-                                "finalize")] == [0, 4, 1, 1]
-    assert got["block_update_f32"][1] > 0
+    assert [got[x][0] for x in ("ring_fused_f32", "ring_fused_bf16", "block_update_f32",
+                                "state_init", "finalize")] == [1, 0, 0, 0, 0]
+    assert got["ring_fused_f32"][1] > 0

@@ -6,7 +6,8 @@ The call keeps its l state in a fixed device array inside the library.
 This file runs last (pytest collects it after the others).  It must pass
 on its own in a fresh process and after the rest of the suite.  It checks
 that two calls in a row, through the C ABI, match ra_ring_forward (and,
-for the fp32 case that uses the fixed array, the oracle directly), that
+for the fp32 case, the oracle directly), including a case with P > 256,
+the step-by-step ring that keeps its l state in the fixed array, that
 neither torch's allocator nor the library's scratch pool grows over those
 calls, and that sizes over the fixed limit are refused.
 """
@@ -44,6 +45,8 @@ def _call(L, q, k, v, out, lse, P, causal):
     (4096, 4, 8, 2, 128, torch.bfloat16, True),
     (1000, 5, 2, 2, 64, torch.bfloat16, False),
     (1536, 6, 3, 1, 64, torch.float32, True),
+    # P > 256: the step-by-step ring, the calls that use the fixed array
+    (600, 300, 2, 1, 64, torch.bfloat16, True),
 ])
 def test_two_calls_match_ring_forward(lib, shape):
     import blockwise_online_softmax_gb300 as ra
