@@ -35,19 +35,31 @@ import torch
 CHUNK = 1 << 22
 
 
-def randn_chunked(shape, seed: int, tensor_id: int, threads: int | None = None) -> torch.Tensor:
-    """fp32 standard normals, filled chunk by chunk (see the module recipe)."""
-    out = torch.empty(shape, dtype=torch.float32)
+def randn_chunked(shape, seed: int, tensor_id: int, threads: int | None = None, *,
+                  scale: float = 1.0, dtype=torch.float32) -> torch.Tensor:
+    """fp32 standard normals, filled chunk by chunk (see the module recipe).
+
+    With ``scale`` and ``dtype`` each chunk is multiplied in fp32 and cast
+    as it is drawn: the same values as ``(randn_chunked(...) * scale)
+    .to(dtype)``, without the whole fp32 tensor in memory at once."""
+    out = torch.empty(shape, dtype=dtype)
     flat = out.view(-1)
     n = flat.numel()
     nchunks = (n + CHUNK - 1) // CHUNK
     if nchunks >= (1 << 16) or not (0 <= tensor_id < 16) or seed < 0:
         raise ValueError("tensor too large or bad seed / tensor id for the chunked recipe")
+    direct = dtype == torch.float32 and scale == 1.0
 
     def fill(b):
         g = torch.Generator().manual_seed((seed << 20) | (tensor_id << 16) | b)
         part = flat[b * CHUNK:(b + 1) * CHUNK]
-        torch.randn(part.shape, generator=g, out=part)
+        if direct:
+            torch.randn(part.shape, generator=g, out=part)
+        else:
+            x = torch.randn(part.shape, generator=g)
+            if scale != 1.0:
+                x *= scale
+            part.copy_(x)
 
     if nchunks <= 1:
         for b in range(nchunks):
@@ -150,7 +162,8 @@ def make_workload(w: Workload | str):
     """Return (q, k, v) CPU tensors of the workload's dtype, token-major.
 
     Each tensor is drawn, modified and cast before the next one, so only
-    one fp32 tensor is alive at a time."""
+    one fp32 tensor (K, whose rows the recipe may scale) is alive at a
+    time; Q and V are cast chunk by chunk."""
     if isinstance(w, str):
         w = WORKLOADS[w]
     if w.recipe not in ("iid", "scaled_keys", "half", "planted"):
@@ -158,10 +171,7 @@ def make_workload(w: Workload | str):
     dt = w.torch_dtype
     half = w.recipe == "half"
 
-    q = randn_chunked((w.N, w.heads, w.d), w.seed, 0)
-    if half:
-        q *= 0.5
-    q = q.to(dt)
+    q = randn_chunked((w.N, w.heads, w.d), w.seed, 0, scale=0.5 if half else 1.0, dtype=dt)
     k = randn_chunked((w.N, w.kv_heads, w.d), w.seed, 1)
     if w.recipe == "scaled_keys":
         for _, h, rows in scaled_key_rows(w, pick_generator(w)):
@@ -172,20 +182,17 @@ def make_workload(w: Workload | str):
     elif half:
         k *= 0.5
     k = k.to(dt)
-    v = randn_chunked((w.N, w.kv_heads, w.d), w.seed, 2)
-    if half:
-        v *= 0.5
-    v = v.to(dt)
+    v = randn_chunked((w.N, w.kv_heads, w.d), w.seed, 2, scale=0.5 if half else 1.0, dtype=dt)
     return q, k, v
 
 
 def make_random(N: int, heads: int, kv_heads: int, d: int, *, dtype=torch.bfloat16,
                 seed: int = 0, scale: float = 1.0):
     """iid N(0,1)*scale case: Q [N,Hq,d], K and V [N,Hkv,d] (module recipe)."""
-    q = randn_chunked((N, heads, d), seed, 0) * scale
-    k = randn_chunked((N, kv_heads, d), seed, 1) * scale
-    v = randn_chunked((N, kv_heads, d), seed, 2) * scale
-    return q.to(dtype), k.to(dtype), v.to(dtype)
+    q = randn_chunked((N, heads, d), seed, 0, scale=scale, dtype=dtype)
+    k = randn_chunked((N, kv_heads, d), seed, 1, scale=scale, dtype=dtype)
+    v = randn_chunked((N, kv_heads, d), seed, 2, scale=scale, dtype=dtype)
+    return q, k, v
 
 
 def sample_rows(w: Workload | str, *, random_per_block: int = 16, seed: int = 12345,

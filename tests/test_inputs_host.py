@@ -95,3 +95,17 @@ def test_draws_do_not_depend_on_the_thread_count():
     # chunk 0 is torch.randn from its own generator
     g = torch.Generator().manual_seed((9 << 20) | (1 << 16) | 0)
     assert torch.equal(a.reshape(-1)[:inputs.CHUNK], torch.randn(inputs.CHUNK, generator=g))
+
+
+def test_chunkwise_cast_equals_the_whole_tensor_cast():
+    # Scale and cast per chunk (no whole fp32 tensor) give the recipe's
+    # values: the fp32 draw, times the scale in fp32, then the cast.
+    shape = (2 * inputs.CHUNK // 64 + 7, 64)
+    whole = inputs.randn_chunked(shape, 4, 2)
+    for scale, dtype in ((1.0, torch.bfloat16), (0.5, torch.bfloat16), (3.0, torch.float32)):
+        got = inputs.randn_chunked(shape, 4, 2, scale=scale, dtype=dtype)
+        assert got.dtype == dtype
+        assert torch.equal(got, (whole * scale).to(dtype))
+    q, k, v = inputs.make_random(300, 3, 1, 64, seed=6, scale=2.0)
+    assert torch.equal(q, (inputs.randn_chunked((300, 3, 64), 6, 0) * 2.0).to(torch.bfloat16))
+    assert torch.equal(v, (inputs.randn_chunked((300, 1, 64), 6, 2) * 2.0).to(torch.bfloat16))
