@@ -14,7 +14,7 @@ import torch
 
 import oracle
 from oracle import online
-from parity import check_output, check_state
+from parity import check_grad, check_output, check_state
 
 import blockwise_online_softmax_gb300 as ra
 from blockwise_online_softmax_gb300 import build, inputs
@@ -119,3 +119,42 @@ def test_merge_past_2_32_elements():
     assert not oa.isnan().any().item()
     got = tuple(t.index_select(0, idx).cpu() for t in (ma, la, oa))
     check_state(*got, online.merge(host[0], host[1]), "f32")
+
+
+def test_backward_past_2_32_elements():
+    # 131,072 tokens with 320 query heads over 8 KV heads: Q, dout, O and
+    # dQ hold 5.4e9 elements.  Causal with a 1024-key window (the offsets
+    # are what is tested, the window keeps it cheap).  dQ on the rows that
+    # straddle the marks, element by element; dK and dV through properties
+    # that hold at any size (sum of dV over keys = summed dout per KV head,
+    # sum of dK = 0).
+    build.build()
+    n, p, heads, kv_heads, w = 1 << 17, 16, 320, 8, 1024
+    assert n * heads * D > (1 << 32)
+    q, k, v = inputs.make_random(n, heads, kv_heads, D, seed=78)
+    g = inputs.randn_chunked((n, heads, D), 78, 3, dtype=torch.bfloat16)
+    qd, kd, vd, gd = q.to(DEV), k.to(DEV), v.to(DEV), g.to(DEV)
+    out, lse = ra.ra_ring_forward_masked(qd, kd, vd, P=p, causal=True, window=w)
+    dq = torch.full((n, heads, D), float("nan"), device=DEV)
+    dq, dk, dv = ra.ra_ring_backward_masked(qd, kd, vd, out, lse, gd, P=p, causal=True,
+                                            window=w, dq=dq)
+    ra.ra_device_status()
+    del qd, gd, out, lse
+    assert not dq.isnan().any().item()
+    rows = {0, n // p - 1, n // p, n - 1}
+    for mark in (1 << 31, 1 << 32):
+        r = mark // (heads * D)
+        rows |= {r - 1, r, r + 1}
+    rows = np.array(sorted(rows), dtype=np.int64)
+    got = dq.index_select(0, torch.from_numpy(rows).to(DEV)).cpu()
+    del dq
+    torch.cuda.empty_cache()
+    ref, _, _, ref_abs, _ = oracle.grad_q(q, k, v, g, causal=True, rows=rows, window=w,
+                                          absolute=True)
+    check_grad(got, ref, ref_abs, "dq")
+    gv = g.view(n, kv_heads, heads // kv_heads, D)
+    gsum = sum(gv[t:t + 8192].double().sum((0, 2)) for t in range(0, n, 8192))
+    dv_sum = dv.double().sum(0).cpu()
+    assert (dv_sum - gsum).abs().max().item() <= 2e-2 * gsum.abs().max().item()
+    dk_sum = dk.double().sum(0).cpu()
+    assert dk_sum.abs().max().item() <= 2.0 ** -8 * np.sqrt(n) * dk.abs().max().item()
