@@ -268,7 +268,8 @@ def make_decode(w: DecodeWorkload | str):
     """(q [n_q, heads, d], k, v [n_kv, kv_heads, d]) bf16 CPU tensors."""
     if isinstance(w, str):
         w = DECODE_WORKLOADS[w]
-    q = (randn_chunked((w.n_q, w.heads, w.d), w.seed, 0) * w.scale).to(torch.bfloat16)
-    k = (randn_chunked((w.n_kv, w.kv_heads, w.d), w.seed, 1) * w.scale).to(torch.bfloat16)
-    v = (randn_chunked((w.n_kv, w.kv_heads, w.d), w.seed, 2) * w.scale).to(torch.bfloat16)
+    bf = torch.bfloat16
+    q = randn_chunked((w.n_q, w.heads, w.d), w.seed, 0, scale=w.scale, dtype=bf)
+    k = randn_chunked((w.n_kv, w.kv_heads, w.d), w.seed, 1, scale=w.scale, dtype=bf)
+    v = randn_chunked((w.n_kv, w.kv_heads, w.d), w.seed, 2, scale=w.scale, dtype=bf)
     return q, k, v

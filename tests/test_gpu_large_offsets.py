@@ -7,7 +7,8 @@ computed in 64 bits.  Checked on the fused ring forward, on the one-step
 block update (which loads and stores its state in HBM) with the finalize
 in place, and on the merge: every output element written (outputs start
 as NaN), and the rows that straddle both marks, plus block edges and
-seeded random rows, against the oracle."""
+seeded random rows, against the oracle.  The backward (320 query heads)
+and decode (5M keys) get tensors of the same size their own way."""
 import numpy as np
 import pytest
 import torch
@@ -158,3 +159,19 @@ def test_backward_past_2_32_elements():
     assert (dv_sum - gsum).abs().max().item() <= 2e-2 * gsum.abs().max().item()
     dk_sum = dk.double().sum(0).cpu()
     assert dk_sum.abs().max().item() <= 2.0 ** -8 * np.sqrt(n) * dk.abs().max().item()
+
+
+def test_decode_past_2_32_elements():
+    # Two new tokens (32 query heads over 8 KV heads) after a history of
+    # 5,242,880 tokens in 80 shards: K and V hold 5.4e9 elements each.
+    build.build()
+    w = inputs.DecodeWorkload("decode-5m", seed=79, n_q=2, heads=32, kv_heads=8, d=D,
+                              n_kv=5 << 20, P=80)
+    assert w.n_kv * w.kv_heads * w.d > (1 << 32)
+    q, k, v = inputs.make_decode(w)
+    out, lse = ra.ra_decode_forward(q.to(DEV), k.to(DEV), v.to(DEV), P=w.P)
+    ra.ra_device_status()
+    torch.cuda.empty_cache()
+    ref_out, ref_lse = oracle.attention(q, k, v, causal=True,
+                                        q_pos=w.n_kv - w.n_q + np.arange(w.n_q))
+    check_output(out, lse, ref_out, ref_lse, "bf16")
