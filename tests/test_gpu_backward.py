@@ -72,6 +72,8 @@ CASES = [
     (600, 3, 2, 1, 128, True),   # c = 200: ragged tiles
     (256, 1, 2, 2, 64, True),    # one block
     (130, 2, 1, 1, 128, True),   # c = 65 < one tile
+    (768, 3, 6, 2, 64, True),    # GQA 3:1, six query heads
+    (512, 2, 3, 3, 128, False),  # odd head count
 ]
 
 

@@ -73,6 +73,12 @@ SHAPES = [
     (256, 1, 2, 2, 128, torch.bfloat16, True),    # P = 1: a single block
     (130, 2, 1, 1, 128, torch.bfloat16, True),    # c = 65 < one tile
     (8, 8, 1, 1, 64, torch.bfloat16, True),       # c = 1
+    # head counts for every grouping of the fused launch order (chunks of
+    # 4, 2 or 1 heads), including chunks that straddle two KV heads
+    (1024, 4, 3, 1, 128, torch.bfloat16, True),   # odd: chunks of 1, GQA 3:1
+    (1536, 3, 6, 2, 64, torch.bfloat16, True),    # chunks of 2, three of them
+    (1024, 4, 12, 4, 128, torch.bfloat16, True),  # chunks of 4 over groups of 3
+    (768, 2, 5, 5, 64, torch.bfloat16, False),    # odd, non-causal
     (1536, 6, 3, 1, 64, torch.float32, True),     # fp32 path, GQA 3:1
     (768, 2, 2, 2, 128, torch.float32, False),    # fp32, d = 128
 ]
