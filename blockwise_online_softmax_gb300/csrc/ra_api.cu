@@ -173,6 +173,25 @@ int encode_map(CUtensorMap* map, const void* base, long long rows, int heads, in
   return RA_OK;
 }
 
+// 3-D map over an fp32 output [rows, heads, d] for tile stores: dims (d,
+// heads, rows), box 32 elements (128 B, one swizzle span) x 1 head x 128
+// rows, 128-byte swizzle.  Returns false, and leaves the error state alone,
+// when the driver cannot map the tensor (the kernel then stores row by
+// row).
+bool encode_out_map(CUtensorMap* map, float* base, long long rows, int heads, int d) {
+  if (reinterpret_cast<uintptr_t>(base) % 16 != 0) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
+                              static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
+                                 static_cast<cuuint64_t>(heads) * d * 4};
+  const cuuint32_t box[3] = {32, 1, 128};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 3-D map over the decode queries [n_q, heads, d] whose box is tq tokens
 // of g consecutive heads (one row tile of a KV head's query rows), 64
 // columns wide: the box lands in shared memory as g * tq rows of 128 bytes,
@@ -433,8 +452,11 @@ int ring_fused_impl(const void* q, const void* k, const void* v, float* out, flo
   if ((rc = encode_map(&tq, q, N, heads, d)) != RA_OK) return rc;
   if ((rc = encode_map(&tk, k, N, kv_heads, d)) != RA_OK) return rc;
   if ((rc = encode_map(&tv, v, N, kv_heads, d)) != RA_OK) return rc;
+  CUtensorMap to;
+  std::memset(&to, 0, sizeof(to));
+  a.o_tma = encode_out_map(&to, out, N, heads, d) ? 1 : 0;
   TraceScope ts(RA_KERNEL_RING_FUSED_BF16, st);
-  cudaError_t e = ra::launch_umma_ring(a, d, tq, tk, tv, st);
+  cudaError_t e = ra::launch_umma_ring(a, d, tq, tk, tv, to, st);
   ts.done(e == cudaSuccess);
   if (e != cudaSuccess) return cuda_fail(e, "fused ring launch");
   return RA_OK;

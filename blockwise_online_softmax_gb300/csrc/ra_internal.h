@@ -137,6 +137,7 @@ struct FwdArgs {
   int h0;  // fused ring: first query head of the launch (grid.y runs h0 .. h0 + nh - 1)
   int nh;  // fused ring: query heads in the launch (0: all `heads`)
   int ring_lc;  // fused ring: log2 of the heads per chunk of the launch order (set by its launcher)
+  int o_tma;    // fused ring: 1 when the launch has a tensor map over o for its tile stores
 };
 
 // Decoded work item of grid.z index w.
@@ -260,8 +261,11 @@ cudaError_t launch_umma_update(const FwdArgs& a, int d, const CUtensorMap& tq,
                                const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st);
 // The whole ring forward of every rank in one launch (bf16): a.o is the
 // output [rows, heads, d] and a.m the LSE [rows, heads]; a.l is unused.
+// With a.o_tma set, `to` maps a.o (fp32, dims (d, heads, rows), box 32 x 1
+// x 128, 128-byte swizzle) and the kernel stores whole output tiles with it.
 cudaError_t launch_umma_ring(const FwdArgs& a, int d, const CUtensorMap& tq,
-                             const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st);
+                             const CUtensorMap& tk, const CUtensorMap& tv,
+                             const CUtensorMap& to, cudaStream_t st);
 cudaError_t launch_wait_selftest(long long limit_cycles, cudaStream_t st);
 cudaError_t launch_decode_tc(const DecArgs& a, int d, const CUtensorMap& tq, const CUtensorMap& tk,
                              const CUtensorMap& tv, cudaStream_t st);

@@ -596,7 +596,6 @@ __device__ __forceinline__ void ring_control_roles(const FwdArgs& a, const StepV
                                                    long long row0, uint32_t tmem, uint32_t sQ,
                                                    uint32_t sK, uint32_t sV, uint32_t bar0,
                                                    volatile int* abort_flag,
-                                                   const CUtensorMap* tmQ,
                                                    const CUtensorMap* tmK,
                                                    const CUtensorMap* tmV) {
   using C = Cfg<D>;
@@ -610,17 +609,7 @@ __device__ __forceinline__ void ring_control_roles(const FwdArgs& a, const StepV
     // ------------------------------------------------------------ producers
     if (lane == 0) {
       if (warp == 8) {
-        tma_prefetch_desc(tmQ);
-        mbar_arrive_expect_tx(bar(C::B_Q), NQ * C::TILE_BYTES);
-#pragma unroll
-        for (int g = 0; g < NQ; ++g) {
-          const int q_row =
-              static_cast<int>(static_cast<long long>(ring_item(a).i) * a.cq + row0 + g * BM);
-#pragma unroll
-          for (int ch = 0; ch < C::NCH; ++ch)
-            tma_load_3d(sQ + g * C::TILE_BYTES + ch * CHUNK_BYTES, tmQ, bar(C::B_Q), ch * 64, h,
-                        q_row);
-        }
+        // The Q tiles were requested in the kernel prologue.
         if (!produce_ring<D, C::NSK>(a, rec, kh, sK, bar(C::B_KF), bar(C::B_KE), tmK, 0,
                                      abort_flag, 0x11, lim)) {
           volatile int no_abort = 0;
@@ -745,7 +734,8 @@ __device__ __forceinline__ void ring_control_roles(const FwdArgs& a, const StepV
 template <int D>
 __device__ __forceinline__ void ring_softmax_role(const FwdArgs& a, const StepVisit* rec,
                                                   long long row0, long long vb, uint32_t tmem,
-                                                  uint32_t bar0,
+                                                  uint32_t bar0, uint32_t sK, uint32_t sV,
+                                                  const CUtensorMap* tmO,
                                                   volatile int* abort_flag) {
   using C = Cfg<D>;
   const int warp = threadIdx.x >> 5;
@@ -807,7 +797,51 @@ __device__ __forceinline__ void ring_softmax_role(const FwdArgs& a, const StepVi
   const RingItem it = ring_item(a);
   const long long oidx = (static_cast<long long>(it.i) * a.cq + grow) * a.heads + it.h;
   float* dst = a.o + oidx * D;
-  if (cnt > 0) {
+  if (cnt > 0 && a.o_tma && row0 + (g + 1) * BM <= a.cq) {
+    // Every row of the tile lies in this block: stage O in shared memory
+    // and store the tile with the tensor map.  The K/V stages are free once
+    // the last products are done (every MMA has completed when B_OD
+    // fires): group 0 stages in the K stages, group 1 in the V stages.
+    // The layout is the map's box, D / 32 boxes of 128 rows x 128 bytes,
+    // with the 16-byte chunks of row r XOR-permuted by r % 8 (the 128-byte
+    // swizzle), so that the eight lanes of a store phase hit distinct banks.
+    // Row by row from registers, each thread would write its own 512-byte
+    // row, every store instruction of a warp touching 32 rows.
+    static_assert(BM * D * 4 <= C::NSK * C::TILE_BYTES, "O tile staging fits in the K/V stages");
+    const uint32_t stage = g == 0 ? sK : sV;
+    tc_fence_after();
+#pragma unroll
+    for (int cc = 0; cc < D / 32; ++cc) {
+      uint32_t r[32];
+      tmem_ld32(tl + o_col + cc * 32, r);
+      tmem_wait_ld();
+      reg_fence32(r);
+      const uint32_t rb = stage + static_cast<uint32_t>(cc * BM * 128 + row * 128);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        st_shared_v4(rb + (static_cast<uint32_t>(j ^ (row & 7)) << 4),
+                     __float_as_uint(__uint_as_float(r[4 * j + 0]) * inv),
+                     __float_as_uint(__uint_as_float(r[4 * j + 1]) * inv),
+                     __float_as_uint(__uint_as_float(r[4 * j + 2]) * inv),
+                     __float_as_uint(__uint_as_float(r[4 * j + 3]) * inv));
+    }
+    // The group's P barrier, whose cnt phases are all done (the MMA warp
+    // waited for the last one before the last P.V), gathers the 128 rows:
+    // one more phase, waited for (bounded) by the thread that issues the
+    // stores.  A wait that gives up skips the stores; the status word has
+    // the error.
+    fence_proxy_async_smem();
+    mbar_arrive(bar(C::B_PF + g));
+    if (row == 0 && wait_bar(bar(C::B_PF + g), static_cast<uint32_t>(cnt) & 1u, abort_flag,
+                             &g_umma_status, 0x34, lim)) {
+      const int q_row = static_cast<int>(static_cast<long long>(it.i) * a.cq + row0 + g * BM);
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc)
+        tma_store_3d(tmO, stage + static_cast<uint32_t>(cc * BM * 128), cc * 32, it.h, q_row);
+      bulk_commit_group();
+      bulk_wait_group_read0();
+    }
+  } else if (cnt > 0) {
     tc_fence_after();
 #pragma unroll
     for (int cc = 0; cc < D / 32; ++cc) {
@@ -838,7 +872,8 @@ __device__ __forceinline__ void ring_softmax_role(const FwdArgs& a, const StepVi
 template <int D>
 __global__ void __launch_bounds__(NTHREADS, 1)
 umma_ring_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                 const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
+                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                 const FwdArgs a) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -853,6 +888,10 @@ umma_ring_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
+  // The launch's status word, read first so that its latency passes under
+  // the set-up below.
+  int launch_status = 0;
+  if (tid == 0) launch_status = *reinterpret_cast<volatile int*>(&g_umma_status);
   const RingItem it = ring_item(a);
   const int i = it.i;
   const int h = it.h;
@@ -869,7 +908,7 @@ umma_ring_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       const bool kvf = x >= C::B_KF && x < C::B_KF + C::NSK;
       mbar_init(bar(x), pf ? 128u : (kvf ? 2u : 1u));
     }
-    *abort_flag = *reinterpret_cast<volatile int*>(&g_umma_status) != 0 ? 1 : 0;
+    *abort_flag = launch_status != 0 ? 1 : 0;
     fence_mbar_init();
     fence_proxy_async_smem();
   }
@@ -892,6 +931,20 @@ umma_ring_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     }
   }
   if (*abort_flag) return;
+  if (tid == 8 * 32) {
+    // The Q tiles, requested before the tensor-memory allocation so that
+    // their load overlaps it.  From here on every path waits for B_Q before
+    // the CTA exits (the MMA warp, or the K producer when it gives up).
+    mbar_arrive_expect_tx(bar(C::B_Q), NQ * C::TILE_BYTES);
+#pragma unroll
+    for (int g = 0; g < NQ; ++g) {
+      const int q_row = static_cast<int>(static_cast<long long>(i) * a.cq + row0 + g * BM);
+#pragma unroll
+      for (int ch = 0; ch < C::NCH; ++ch)
+        tma_load_3d(sQ + g * C::TILE_BYTES + ch * CHUNK_BYTES, &tmQ, bar(C::B_Q), ch * 64, h,
+                    q_row);
+    }
+  }
   if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
     tmem_relinquish();
@@ -902,7 +955,7 @@ umma_ring_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   const uint32_t tmem = *tmem_slot;
   if (warp >= 8) {
     regs_dec<C::REGS_CONTROL>();
-    ring_control_roles<D>(a, rec, row0, tmem, sQ, sK, sV, bar0, abort_flag, &tmQ, &tmK, &tmV);
+    ring_control_roles<D>(a, rec, row0, tmem, sQ, sK, sV, bar0, abort_flag, &tmK, &tmV);
     tc_fence_before();
     named_bar_sync(1, NTHREADS);
     if (warp == 9) {
@@ -911,7 +964,7 @@ umma_ring_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     }
   } else {
     regs_inc<C::REGS_SOFTMAX>();
-    ring_softmax_role<D>(a, rec, row0, vb, tmem, bar0, abort_flag);
+    ring_softmax_role<D>(a, rec, row0, vb, tmem, bar0, sK, sV, &tmO, abort_flag);
     tc_fence_before();
     named_bar_sync(1, NTHREADS);
   }
@@ -919,7 +972,7 @@ umma_ring_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 
 template <int D>
 cudaError_t launch_ring_d(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
-                          const CUtensorMap& tv, cudaStream_t st) {
+                          const CUtensorMap& tv, const CUtensorMap& to, cudaStream_t st) {
   using C = Cfg<D>;
   constexpr uint32_t smem = C::SMEM_BYTES + kRingMaxSteps * sizeof(StepVisit);
   static_assert(smem <= 232448, "shared memory budget of the fused ring");
@@ -934,7 +987,7 @@ cudaError_t launch_ring_d(const FwdArgs& a, const CUtensorMap& tq, const CUtenso
   dim3 grid(static_cast<unsigned>((a.cq + NQ * BM - 1) / (NQ * BM)),
             static_cast<unsigned>(a.P << b.ring_lc), static_cast<unsigned>(nh >> b.ring_lc));
   if (grid.y > 65535u || grid.z > 65535u) return cudaErrorInvalidValue;
-  umma_ring_kernel<D><<<grid, NTHREADS, smem, st>>>(tq, tk, tv, b);
+  umma_ring_kernel<D><<<grid, NTHREADS, smem, st>>>(tq, tk, tv, to, b);
   return cudaGetLastError();
 }
 
@@ -975,8 +1028,10 @@ cudaError_t launch_umma_update(const FwdArgs& a, int d, const CUtensorMap& tq,
 }
 
 cudaError_t launch_umma_ring(const FwdArgs& a, int d, const CUtensorMap& tq,
-                             const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st) {
-  return d == 128 ? launch_ring_d<128>(a, tq, tk, tv, st) : launch_ring_d<64>(a, tq, tk, tv, st);
+                             const CUtensorMap& tk, const CUtensorMap& tv,
+                             const CUtensorMap& to, cudaStream_t st) {
+  return d == 128 ? launch_ring_d<128>(a, tq, tk, tv, to, st)
+                  : launch_ring_d<64>(a, tq, tk, tv, to, st);
 }
 
 cudaError_t launch_wait_selftest(long long limit_cycles, cudaStream_t st) {
