@@ -250,8 +250,11 @@ int run_update(ra::FwdArgs& a, int d, int dtype, cudaStream_t st) {
     if ((rc = encode_map(&tq, a.q, a.q_rows, a.heads, d)) != RA_OK) return rc;
     if ((rc = encode_map(&tk, a.k, a.kv_rows, a.kv_heads, d)) != RA_OK) return rc;
     if ((rc = encode_map(&tv, a.v, a.kv_rows, a.kv_heads, d)) != RA_OK) return rc;
+    CUtensorMap to;
+    std::memset(&to, 0, sizeof(to));
+    a.o_tma = encode_out_map(&to, a.o, a.q_rows, a.heads, d) ? 1 : 0;
     TraceScope ts(RA_KERNEL_BLOCK_UPDATE_BF16, st);
-    e = ra::launch_umma_update(a, d, tq, tk, tv, st);
+    e = ra::launch_umma_update(a, d, tq, tk, tv, to, st);
     ts.done(e == cudaSuccess);
   } else {
     TraceScope ts(RA_KERNEL_BLOCK_UPDATE_F32, st);

@@ -137,7 +137,7 @@ struct FwdArgs {
   int h0;  // fused ring: first query head of the launch (grid.y runs h0 .. h0 + nh - 1)
   int nh;  // fused ring: query heads in the launch (0: all `heads`)
   int ring_lc;  // fused ring: log2 of the heads per chunk of the launch order (set by its launcher)
-  int o_tma;    // fused ring: 1 when the launch has a tensor map over o for its tile stores
+  int o_tma;    // 1 when the launch has a tensor map over o for its tile stores (bf16 kernels)
 };
 
 // Decoded work item of grid.z index w.
@@ -257,8 +257,12 @@ cudaError_t launch_simt_update(const FwdArgs& a, int d, cudaStream_t st);
 // The whole fp32 ring forward in one launch: a.o is the output [rows,
 // heads, d] and a.m the LSE [rows, heads] (natural log); a.l is unused.
 cudaError_t launch_simt_ring(const FwdArgs& a, int d, cudaStream_t st);
+// One block-update launch (bf16).  With a.o_tma set, `to` maps the state
+// a.o like launch_umma_ring's output map (rows: a.q_rows) and the kernel
+// stores whole state tiles with it.
 cudaError_t launch_umma_update(const FwdArgs& a, int d, const CUtensorMap& tq,
-                               const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st);
+                               const CUtensorMap& tk, const CUtensorMap& tv,
+                               const CUtensorMap& to, cudaStream_t st);
 // The whole ring forward of every rank in one launch (bf16): a.o is the
 // output [rows, heads, d] and a.m the LSE [rows, heads]; a.l is unused.
 // With a.o_tma set, `to` maps a.o (fp32, dims (d, heads, rows), box 32 x 1

@@ -283,15 +283,19 @@ __device__ __forceinline__ void control_roles(const FwdArgs& a, const Work& wk, 
             if (!ok) break;
             tc_fence_after();
             pv(g, sv);
-            // Only the epilogue waits for PV_g: each tile's softmax already
-            // knows PV_g(t-1) is done from S_g(t).  So only the last product
-            // of the group is signalled.
-            if (kg + 1 == ne[g]) tc_commit_lead(lead, bar(C::B_OD + g));
           }
           if (static_cast<unsigned>(kg + 1) < static_cast<unsigned>(ne[g])) qk(g, sk1);
         }
         if (!ok) break;
         tc_commit_lead(lead, bar(C::B_KE + sv));
+      }
+      if (ok) {
+        // Only the epilogues wait for the P.V products (each tile's softmax
+        // knows PV_g(t-1) is done from S_g(t)).  Both groups' epilogues wait
+        // for every product of the CTA: they stage the state in the K/V
+        // stages, which the other group's last products may still read.
+        tc_commit_lead(lead, bar(C::B_OD));
+        tc_commit_lead(lead, bar(C::B_OD + 1));
       }
       // Drain every MMA issued so far before TMEM can be freed.
       volatile int no_abort = 0;
@@ -306,6 +310,7 @@ template <int D>
 __device__ __forceinline__ void softmax_role(const FwdArgs& a, const Work& wk, long long row0,
                                              const int (&ta)[NQ], const int (&tb)[NQ],
                                              long long vb, uint32_t tmem, uint32_t bar0,
+                                             uint32_t sK, uint32_t sV, const CUtensorMap* tmO,
                                              volatile int* abort_flag) {
   using C = Cfg<D>;
   const int warp = threadIdx.x >> 5;
@@ -383,11 +388,52 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, const Work& wk, l
       }
 
       if (ok) {
-        // The one commit on B_OD + g follows PV_g(t_end-1), the last product.
+        // The one commit on B_OD + g follows the CTA's last product.
         ok = wait_bar(bar(C::B_OD + g), 0u, abort_flag, &g_umma_status, 0x33, lim);
         ok = __all_sync(0xffffffffu, ok);
       }
-      if (ok) {
+      if (ok && a.o_tma && row0 + (g + 1) * BM <= a.cq) {
+        // Every row of the tile lies in the block: O~ goes back to HBM
+        // through shared memory and TMA tensor stores, as in the fused
+        // ring's epilogue (group 0 stages in the K stages, group 1 in the V
+        // stages, 128-byte swizzle; the group's P barrier, with all its
+        // phases done, gathers the 128 rows for one more phase).
+        static_assert(BM * D * 4 <= C::NSK * C::TILE_BYTES, "state tile staging fits");
+        tc_fence_after();
+        const float fin = (m_used == m_true) ? 1.f : ex2(m_used - m_true);
+        const uint32_t stage = g == 0 ? sK : sV;
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t r[32];
+          tmem_ld32(tl + o_col + cc * 32, r);
+          tmem_wait_ld();
+          reg_fence32(r);
+          const uint32_t rb = stage + static_cast<uint32_t>(cc * BM * 128 + row * 128);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            st_shared_v4(rb + (static_cast<uint32_t>(j ^ (row & 7)) << 4),
+                         __float_as_uint(__uint_as_float(r[4 * j + 0]) * fin),
+                         __float_as_uint(__uint_as_float(r[4 * j + 1]) * fin),
+                         __float_as_uint(__uint_as_float(r[4 * j + 2]) * fin),
+                         __float_as_uint(__uint_as_float(r[4 * j + 3]) * fin));
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar(C::B_PF + g));
+        if (row == 0 &&
+            wait_bar(bar(C::B_PF + g), static_cast<uint32_t>(t_end - t_first) & 1u, abort_flag,
+                     &g_umma_status, 0x34, lim)) {
+          const int s_row = static_cast<int>(wk.state_base + row0 + g * BM);
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc)
+            tma_store_3d(tmO, stage + static_cast<uint32_t>(cc * BM * 128), cc * 32, h, s_row);
+          bulk_commit_group();
+          bulk_wait_group_read0();
+        }
+        if (valid) {
+          a.l[sidx] = l_run * fin;
+          a.m[sidx] = m_moved ? m_true * kLn2 : m_ld;
+        }
+      } else if (ok) {
         tc_fence_after();
         // Canonical state: rescale once from m_used to the exact running max.
         const float fin = (m_used == m_true) ? 1.f : ex2(m_used - m_true);
@@ -421,7 +467,8 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, const Work& wk, l
 template <int D>
 __global__ void __launch_bounds__(NTHREADS, 1)
 umma_update_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                   const FwdArgs a) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -489,7 +536,7 @@ umma_update_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     }
   } else {
     regs_inc<C::REGS_SOFTMAX>();
-    softmax_role<D>(a, wk, row0, ta, tb, vb, tmem, bar0, abort_flag);
+    softmax_role<D>(a, wk, row0, ta, tb, vb, tmem, bar0, sK, sV, &tmO, abort_flag);
     tc_fence_before();
     named_bar_sync(1, NTHREADS);
   }
@@ -1009,22 +1056,23 @@ __global__ void wait_selftest_kernel(long long limit) {
 
 template <int D>
 cudaError_t launch_d(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
-                     const CUtensorMap& tv, cudaStream_t st) {
+                     const CUtensorMap& tv, const CUtensorMap& to, cudaStream_t st) {
   using C = Cfg<D>;
   cudaError_t e = cudaFuncSetAttribute(umma_update_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(C::SMEM_BYTES));
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>((a.cq + NQ * BM - 1) / (NQ * BM)), a.heads, a.nwork);
-  umma_update_kernel<D><<<grid, NTHREADS, C::SMEM_BYTES, st>>>(tq, tk, tv, a);
+  umma_update_kernel<D><<<grid, NTHREADS, C::SMEM_BYTES, st>>>(tq, tk, tv, to, a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_umma_update(const FwdArgs& a, int d, const CUtensorMap& tq,
-                               const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st) {
-  return d == 128 ? launch_d<128>(a, tq, tk, tv, st) : launch_d<64>(a, tq, tk, tv, st);
+                               const CUtensorMap& tk, const CUtensorMap& tv,
+                               const CUtensorMap& to, cudaStream_t st) {
+  return d == 128 ? launch_d<128>(a, tq, tk, tv, to, st) : launch_d<64>(a, tq, tk, tv, to, st);
 }
 
 cudaError_t launch_umma_ring(const FwdArgs& a, int d, const CUtensorMap& tq,
