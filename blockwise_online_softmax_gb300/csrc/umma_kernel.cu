@@ -945,43 +945,20 @@ umma_ring_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   const int pair = it.pair;
   const long long row0 = static_cast<long long>(pair) * (NQ * BM);
   const long long vb = valid_bound(a.mask);
-  // The visit table: every step's tile ranges, computed once by all threads
-  // before the roles split the registers.
-  StepVisit* rec = reinterpret_cast<StepVisit*>(smem + C::OFF_MISC + 16);
-  for (int s = tid; s < a.P; s += NTHREADS) rec[s] = step_visit(a, i, s, row0, vb);
-  if (tid == 0) {
+  // Barriers, the Q request and the tensor-memory allocation come first:
+  // they need only the work item, so the Q load and the allocation run
+  // under the visit computation below (about 3,000 cycles per CTA).
+  if (tid == 8 * 32) {
     for (int x = 0; x < C::NBAR; ++x) {
       const bool pf = x >= C::B_PF && x < C::B_PF + NQ;
       const bool kvf = x >= C::B_KF && x < C::B_KF + C::NSK;
       mbar_init(bar(x), pf ? 128u : (kvf ? 2u : 1u));
     }
-    *abort_flag = launch_status != 0 ? 1 : 0;
     fence_mbar_init();
     fence_proxy_async_smem();
-  }
-  __syncthreads();
-  {
-    // Rows that see no key anywhere: O = 0 and LSE = -inf, and no pipeline.
-    if (next_step(rec, a.P, 0) == a.P) {
-      if (tid < NQ * BM) {
-        const long long grow = row0 + tid;
-        if (grow < a.cq) {
-          const long long oidx =
-              (static_cast<long long>(i) * a.cq + grow) * a.heads + h;
-#pragma unroll
-          for (int j = 0; j < D / 4; ++j)
-            reinterpret_cast<float4*>(a.o + oidx * D)[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-          a.m[oidx] = -INFINITY;
-        }
-      }
-      return;
-    }
-  }
-  if (*abort_flag) return;
-  if (tid == 8 * 32) {
-    // The Q tiles, requested before the tensor-memory allocation so that
-    // their load overlaps it.  From here on every path waits for B_Q before
-    // the CTA exits (the MMA warp, or the K producer when it gives up).
+    // From here on every path waits for B_Q before the CTA exits (the MMA
+    // warp, the K producer when it gives up, or this thread on the early
+    // exits below).
     mbar_arrive_expect_tx(bar(C::B_Q), NQ * C::TILE_BYTES);
 #pragma unroll
     for (int g = 0; g < NQ; ++g) {
@@ -996,10 +973,36 @@ umma_ring_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
     tmem_relinquish();
   }
+  // The visit table: every step's tile ranges, computed once by all threads
+  // before the roles split the registers.
+  StepVisit* rec = reinterpret_cast<StepVisit*>(smem + C::OFF_MISC + 16);
+  for (int s = tid; s < a.P; s += NTHREADS) rec[s] = step_visit(a, i, s, row0, vb);
+  if (tid == 0) *abort_flag = launch_status != 0 ? 1 : 0;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const bool no_keys = next_step(rec, a.P, 0) == a.P;
+  if (no_keys || *abort_flag) {  // uniform across the CTA: read after the barrier
+    // Rows that see no key anywhere: O = 0 and LSE = -inf, and no pipeline.
+    if (no_keys && tid < NQ * BM) {
+      const long long grow = row0 + tid;
+      if (grow < a.cq) {
+        const long long oidx = (static_cast<long long>(i) * a.cq + grow) * a.heads + h;
+#pragma unroll
+        for (int j = 0; j < D / 4; ++j)
+          reinterpret_cast<float4*>(a.o + oidx * D)[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        a.m[oidx] = -INFINITY;
+      }
+    }
+    // The Q tiles land in shared memory before the CTA may exit.
+    if (tid == 8 * 32) {
+      volatile int no_abort = 0;
+      wait_bar(bar(C::B_Q), 0, &no_abort, nullptr, 0, a.wait_limit);
+    }
+    if (warp == 9) tmem_dealloc(tmem, TMEM_COLS);
+    return;
+  }
   if (warp >= 8) {
     regs_dec<C::REGS_CONTROL>();
     ring_control_roles<D>(a, rec, row0, tmem, sQ, sK, sV, bar0, abort_flag, &tmK, &tmV);
