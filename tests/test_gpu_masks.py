@@ -92,6 +92,12 @@ CASES = [
     (2048, 4, "contiguous", True, 0, 2048 - 77, None, 2, 2, 128, torch.bfloat16),
     (2048, 4, "striped", False, 0, 1500, None, 2, 2, 64, torch.bfloat16),
     (2048, 4, "zigzag", True, 256, 2000, [900, 3, 1000, 97], 4, 1, 128, torch.bfloat16),
+    # d = 64, causal: a document starts inside query tile 0 of a pair, so
+    # query tile 1 sees keys in the first ring step only and tile 0 runs
+    # alone through the later steps (the fused ring rotates three score
+    # buffers between the two tiles at d = 64).
+    (4096, 4, "contiguous", True, 0, None, [1000, 17, 2355, 724], 2, 2, 64, torch.bfloat16),
+    (4096, 4, "zigzag", True, 1500, None, [1000, 17, 2355, 724], 2, 1, 64, torch.bfloat16),
     (1024, 4, "zigzag", True, 100, 1000, [500, 11, 489], 2, 1, 64, torch.float32),
     (1024, 4, "contiguous", False, 64, 999, None, 2, 2, 128, torch.float32),
     (1024, 4, "striped", True, 0, None, [512, 512], 2, 2, 64, torch.float32),
