@@ -204,12 +204,11 @@ __device__ __forceinline__ void control_roles(const FwdArgs& a, const Work& wk, 
     __syncwarp();
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    // The whole warp runs this loop in step; the MMAs and commits are
-    // predicated on lane 0 inside their asm, so the warp never diverges.
-    // Every wait below reads the same barrier state on all lanes, so the
-    // outcome is warp-uniform.
-    const uint32_t lead = lane == 0 ? 1u : 0u;
-    if (seq.n > 0) {
+    // Lane 0 runs the whole loop alone; the other lanes wait at the end.
+    // Measured against the whole warp running it with every MMA and commit
+    // predicated on lane 0: +1.5% on a fused ring (the per-product issue
+    // cost is lower from one lane).
+    if (lane == 0 && seq.n > 0) {
       constexpr uint32_t idesc_qk = idesc_bf16(BM, BN, 0);
       constexpr uint32_t idesc_pv = idesc_bf16(BM, D, 1);
       // All shared-memory descriptors are built once.  Moving a descriptor's
@@ -228,9 +227,9 @@ __device__ __forceinline__ void control_roles(const FwdArgs& a, const Work& wk, 
           // K-major, 128-byte swizzle: 16 elements = 32 bytes along a row;
           // every 4 steps move to the next 64-wide column chunk.
           const uint64_t off = ((kk >> 2) * CHUNK_BYTES + (kk & 3) * 32) >> 4;
-          mma_ss_lead(lead, d_tmem, a0 + off, b0 + off, idesc_qk, kk > 0 ? 1u : 0u);
+          mma_ss(d_tmem, a0 + off, b0 + off, idesc_qk, kk > 0 ? 1u : 0u);
         }
-        tc_commit_lead(lead, bar(C::B_SF + g));
+        tc_commit(bar(C::B_SF + g));
       };
       // O_g += P_g V over the 128 keys of the tile.
       auto pv = [&](int g, int sv) {
@@ -242,8 +241,8 @@ __device__ __forceinline__ void control_roles(const FwdArgs& a, const Work& wk, 
           // P: two bf16 per 32-bit TMEM column, 8 columns per 16 keys.
           // V (MN-major, 128-byte swizzle): 16 keys = two 8-row groups of
           // 1024 B (SBO); the 64-wide column chunks sit CHUNK_BYTES apart (LBO).
-          mma_ts_lead(lead, o_tmem, p_tmem + kk * 8,
-                      b0 + static_cast<uint64_t>((kk * 2048) >> 4), idesc_pv, 1u);
+          mma_ts(o_tmem, p_tmem + kk * 8, b0 + static_cast<uint64_t>((kk * 2048) >> 4), idesc_pv,
+                 1u);
         }
       };
       bool ok = wait_bar(bar(C::B_Q), 0, abort_flag, &g_umma_status, 0x21, lim);
@@ -263,7 +262,7 @@ __device__ __forceinline__ void control_roles(const FwdArgs& a, const Work& wk, 
         tc_fence_after();
         if (ks[0] == 0 && ne[0] > 0) qk(0, 0);
         if (ks[1] == 0 && ne[1] > 0) qk(1, 0);
-        tc_commit_lead(lead, bar(C::B_KE));
+        tc_commit(bar(C::B_KE));
       }
       for (int k = 0; k < seq.n && ok; ++k) {
         // Slot k + 1: V(k) and K(k + 1), both in stage (k + 1) % NSK.
@@ -287,19 +286,19 @@ __device__ __forceinline__ void control_roles(const FwdArgs& a, const Work& wk, 
           if (static_cast<unsigned>(kg + 1) < static_cast<unsigned>(ne[g])) qk(g, sk1);
         }
         if (!ok) break;
-        tc_commit_lead(lead, bar(C::B_KE + sv));
+        tc_commit(bar(C::B_KE + sv));
       }
       if (ok) {
         // Only the epilogues wait for the P.V products (each tile's softmax
         // knows PV_g(t-1) is done from S_g(t)).  Both groups' epilogues wait
         // for every product of the CTA: they stage the state in the K/V
         // stages, which the other group's last products may still read.
-        tc_commit_lead(lead, bar(C::B_OD));
-        tc_commit_lead(lead, bar(C::B_OD + 1));
+        tc_commit(bar(C::B_OD));
+        tc_commit(bar(C::B_OD + 1));
       }
       // Drain every MMA issued so far before TMEM can be freed.
       volatile int no_abort = 0;
-      tc_commit_lead(lead, bar(C::B_DRAIN));
+      tc_commit(bar(C::B_DRAIN));
       wait_bar(bar(C::B_DRAIN), 0, &no_abort, nullptr, 0, lim);
     }
     __syncwarp();
@@ -670,105 +669,107 @@ __device__ __forceinline__ void ring_control_roles(const FwdArgs& a, const StepV
     __syncwarp();
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    // As in the one-step kernel, with the visit index K running over every
-    // step: slot K + 1 holds V(K) and K(K + 1).  At the last tile of a step
-    // the look-ahead QK is the next step's first tile, whose groups are
-    // known from the next step's visit, computed when the step begins.
-    const uint32_t lead = lane == 0 ? 1u : 0u;
-    constexpr uint32_t idesc_qk = idesc_bf16(BM, BN, 0);
-    constexpr uint32_t idesc_pv = idesc_bf16(BM, D, 1);
-    const uint64_t qdesc = sdesc_sw128(sQ, 16, 1024);
-    const uint64_t kdesc = sdesc_sw128(sK, 16, 1024);
-    const uint64_t vdesc = sdesc_sw128(sV, CHUNK_BYTES, 1024);
-    constexpr uint64_t TILE16 = C::TILE_BYTES >> 4;
-    auto qk = [&](int g, int sk) {
-      const uint32_t d_tmem = tmem + C::S_COL + static_cast<uint32_t>(g) * BN;
-      const uint64_t a0 = qdesc + static_cast<uint64_t>(g) * TILE16;
-      const uint64_t b0 = kdesc + static_cast<uint64_t>(sk) * TILE16;
+    // As in the one-step kernel (lane 0 alone), with the visit index K
+    // running over every step: slot K + 1 holds V(K) and K(K + 1).  At the
+    // last tile of a step the look-ahead QK is the next step's first tile,
+    // whose groups are known from the next step's visit, computed when the
+    // step begins.
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16(BM, BN, 0);
+      constexpr uint32_t idesc_pv = idesc_bf16(BM, D, 1);
+      const uint64_t qdesc = sdesc_sw128(sQ, 16, 1024);
+      const uint64_t kdesc = sdesc_sw128(sK, 16, 1024);
+      const uint64_t vdesc = sdesc_sw128(sV, CHUNK_BYTES, 1024);
+      constexpr uint64_t TILE16 = C::TILE_BYTES >> 4;
+      auto qk = [&](int g, int sk) {
+        const uint32_t d_tmem = tmem + C::S_COL + static_cast<uint32_t>(g) * BN;
+        const uint64_t a0 = qdesc + static_cast<uint64_t>(g) * TILE16;
+        const uint64_t b0 = kdesc + static_cast<uint64_t>(sk) * TILE16;
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint64_t off = ((kk >> 2) * CHUNK_BYTES + (kk & 3) * 32) >> 4;
-        mma_ss_lead(lead, d_tmem, a0 + off, b0 + off, idesc_qk, kk > 0 ? 1u : 0u);
-      }
-      tc_commit_lead(lead, bar(C::B_SF + g));
-    };
-    auto pv = [&](int g, int sv) {
-      const uint32_t p_tmem = tmem + C::S_COL + static_cast<uint32_t>(g) * BN;
-      const uint32_t o_tmem = tmem + C::O_COL + static_cast<uint32_t>(g) * D;
-      const uint64_t b0 = vdesc + static_cast<uint64_t>(sv) * TILE16;
-#pragma unroll
-      for (int kk = 0; kk < BN / 16; ++kk)
-        mma_ts_lead(lead, o_tmem, p_tmem + kk * 8, b0 + static_cast<uint64_t>((kk * 2048) >> 4),
-                    idesc_pv, 1u);
-    };
-    // The current step's visit in registers; of the next non-empty step
-    // only which groups its first tile has.
-    int s_cur = next_step(rec, a.P, 0);
-    int s_nxt = next_step(rec, a.P, s_cur + 1);
-    TileSeq seq = rec[s_cur].seq;
-    int ks[NQ], ne[NQ];
-#pragma unroll
-    for (int g = 0; g < NQ; ++g) {
-      ks[g] = rec[s_cur].ks[g];
-      ne[g] = rec[s_cur].ne[g];
-    }
-    bool ok = wait_bar(bar(C::B_Q), 0, abort_flag, &g_umma_status, 0x21, lim);
-    if (ok) ok = wait_bar(bar(C::B_KF), 0, abort_flag, &g_umma_status, 0x22, lim);
-    if (ok) {
-      tc_fence_after();
-      if (ks[0] == 0 && ne[0] > 0) qk(0, 0);
-      if (ks[1] == 0 && ne[1] > 0) qk(1, 0);
-      tc_commit_lead(lead, bar(C::B_KE));
-    }
-    int K = 0;            // visit index over all steps
-    int cnt[NQ] = {0, 0};  // tiles of each group so far (its P barrier's phase)
-    while (ok) {
-      bool nx[NQ];
-#pragma unroll
-      for (int g = 0; g < NQ; ++g)
-        nx[g] = s_nxt < a.P && rec[s_nxt].ks[g] == 0 && rec[s_nxt].ne[g] > 0;
-      for (int k = 0; k < seq.n && ok; ++k, ++K) {
-        const int sv = (K + 1) % C::NSK;  // slot K + 1: V(K) and K(K + 1)
-        ok = wait_bar(bar(C::B_KF + sv), static_cast<uint32_t>((K + 1) / C::NSK) & 1u, abort_flag,
-                      &g_umma_status, 0x24, lim);
-        if (!ok) break;
-        const bool last = k + 1 == seq.n;
-#pragma unroll
-        for (int g = 0; g < NQ; ++g) {
-          const int kg = k - ks[g];
-          if (static_cast<unsigned>(kg) < static_cast<unsigned>(ne[g])) {
-            ok = wait_bar(bar(C::B_PF + g), static_cast<uint32_t>(cnt[g]) & 1u, abort_flag,
-                          &g_umma_status, 0x23, lim);
-            if (!ok) break;
-            ++cnt[g];
-            tc_fence_after();
-            pv(g, sv);
-          }
-          const bool qn =
-              last ? nx[g] : static_cast<unsigned>(kg + 1) < static_cast<unsigned>(ne[g]);
-          if (qn) qk(g, sv);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t off = ((kk >> 2) * CHUNK_BYTES + (kk & 3) * 32) >> 4;
+          mma_ss(d_tmem, a0 + off, b0 + off, idesc_qk, kk > 0 ? 1u : 0u);
         }
-        if (!ok) break;
-        tc_commit_lead(lead, bar(C::B_KE + sv));
-      }
-      if (!ok || s_nxt >= a.P) break;
-      s_cur = s_nxt;
-      s_nxt = next_step(rec, a.P, s_cur + 1);
-      seq = rec[s_cur].seq;
+        tc_commit(bar(C::B_SF + g));
+      };
+      auto pv = [&](int g, int sv) {
+        const uint32_t p_tmem = tmem + C::S_COL + static_cast<uint32_t>(g) * BN;
+        const uint32_t o_tmem = tmem + C::O_COL + static_cast<uint32_t>(g) * D;
+        const uint64_t b0 = vdesc + static_cast<uint64_t>(sv) * TILE16;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts(o_tmem, p_tmem + kk * 8, b0 + static_cast<uint64_t>((kk * 2048) >> 4), idesc_pv,
+                 1u);
+      };
+      // The current step's visit in registers; of the next non-empty step
+      // only which groups its first tile has.
+      int s_cur = next_step(rec, a.P, 0);
+      int s_nxt = next_step(rec, a.P, s_cur + 1);
+      TileSeq seq = rec[s_cur].seq;
+      int ks[NQ], ne[NQ];
 #pragma unroll
       for (int g = 0; g < NQ; ++g) {
         ks[g] = rec[s_cur].ks[g];
         ne[g] = rec[s_cur].ne[g];
       }
+      bool ok = wait_bar(bar(C::B_Q), 0, abort_flag, &g_umma_status, 0x21, lim);
+      if (ok) ok = wait_bar(bar(C::B_KF), 0, abort_flag, &g_umma_status, 0x22, lim);
+      if (ok) {
+        tc_fence_after();
+        if (ks[0] == 0 && ne[0] > 0) qk(0, 0);
+        if (ks[1] == 0 && ne[1] > 0) qk(1, 0);
+        tc_commit(bar(C::B_KE));
+      }
+      int K = 0;            // visit index over all steps
+      int cnt[NQ] = {0, 0};  // tiles of each group so far (its P barrier's phase)
+      while (ok) {
+        bool nx[NQ];
+#pragma unroll
+        for (int g = 0; g < NQ; ++g)
+          nx[g] = s_nxt < a.P && rec[s_nxt].ks[g] == 0 && rec[s_nxt].ne[g] > 0;
+        for (int k = 0; k < seq.n && ok; ++k, ++K) {
+          const int sv = (K + 1) % C::NSK;  // slot K + 1: V(K) and K(K + 1)
+          ok = wait_bar(bar(C::B_KF + sv), static_cast<uint32_t>((K + 1) / C::NSK) & 1u, abort_flag,
+                        &g_umma_status, 0x24, lim);
+          if (!ok) break;
+          const bool last = k + 1 == seq.n;
+#pragma unroll
+          for (int g = 0; g < NQ; ++g) {
+            const int kg = k - ks[g];
+            if (static_cast<unsigned>(kg) < static_cast<unsigned>(ne[g])) {
+              ok = wait_bar(bar(C::B_PF + g), static_cast<uint32_t>(cnt[g]) & 1u, abort_flag,
+                            &g_umma_status, 0x23, lim);
+              if (!ok) break;
+              ++cnt[g];
+              tc_fence_after();
+              pv(g, sv);
+            }
+            const bool qn =
+                last ? nx[g] : static_cast<unsigned>(kg + 1) < static_cast<unsigned>(ne[g]);
+            if (qn) qk(g, sv);
+          }
+          if (!ok) break;
+          tc_commit(bar(C::B_KE + sv));
+        }
+        if (!ok || s_nxt >= a.P) break;
+        s_cur = s_nxt;
+        s_nxt = next_step(rec, a.P, s_cur + 1);
+        seq = rec[s_cur].seq;
+#pragma unroll
+        for (int g = 0; g < NQ; ++g) {
+          ks[g] = rec[s_cur].ks[g];
+          ne[g] = rec[s_cur].ne[g];
+        }
+      }
+      if (ok) {
+        // Both groups' epilogues wait for the last products of the visit.
+        tc_commit(bar(C::B_OD));
+        tc_commit(bar(C::B_OD + 1));
+      }
+      volatile int no_abort = 0;
+      tc_commit(bar(C::B_DRAIN));
+      wait_bar(bar(C::B_DRAIN), 0, &no_abort, nullptr, 0, lim);
     }
-    if (ok) {
-      // Both groups' epilogues wait for the last products of the visit.
-      tc_commit_lead(lead, bar(C::B_OD));
-      tc_commit_lead(lead, bar(C::B_OD + 1));
-    }
-    volatile int no_abort = 0;
-    tc_commit_lead(lead, bar(C::B_DRAIN));
-    wait_bar(bar(C::B_DRAIN), 0, &no_abort, nullptr, 0, lim);
     __syncwarp();
   }
 }
